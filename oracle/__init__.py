@@ -1,0 +1,191 @@
+"""CPU oracle for the tensor-core GEMM -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product library never loads it and
+shares no code with it; the two meet only on the stored bit patterns of the
+seeded inputs.
+
+The arithmetic lives in ``oracle.c`` (plain C, binary64, natural k order).
+This wrapper only marshals numpy arrays of stored codes into it, plus the
+acceptance bound that compares a tensor-core result with the fp64 reference.
+
+Sources of the definitions (page titles and sections):
+
+* GEMM ``D = A B + C``: "NVIDIA MMA", section "从 FMA 到 MMA，再到 GEMM".
+* A row-major / B column-major: "CUDA 014 - MMA 指令的用法详解", section
+  "MMA 指令的格式" (the ``.row.col`` modifier).
+* Input / accumulator / output stages and the epilogue
+  (scale / bias / cast): "NVIDIA MMA", section "输入/累加/输出".
+* 2:4 sparse A with ordered position metadata: "NVIDIA MMA", sections
+  "稠密乘法与 2:4 结构化稀疏乘法" and "Ampere：FP16/BF16 与整数 MMA 基线".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+# The oracle's own format codes (mirrors the enum in oracle.c only).
+FMT = {"bf16": 0, "f16": 1, "f32": 2, "e4m3": 3, "e5m2": 4}
+ELEM_BYTES = {"bf16": 2, "f16": 2, "f32": 4, "e4m3": 1, "e5m2": 1}
+CODE_DTYPE = {1: np.uint8, 2: np.uint16, 4: np.uint32}
+# significand precision p (bits incl. the implicit one) and the smallest
+# positive subnormal of each output format; an RNE cast to the format is
+# within 2^-p relative (half an ulp) of its argument, plus the subnormal step.
+PRECISION = {"bf16": 8, "f16": 11, "f32": 24}
+MIN_SUBNORMAL = {"bf16": 2.0 ** -133, "f16": 2.0 ** -24, "f32": 2.0 ** -149}
+# Accumulation allowance relative to sum_k |a*b|, the tolerance the GEMM is
+# held to for fp32 accumulation of any K.
+ACC_REL = 1e-5
+
+
+def build(force: bool = False) -> str:
+    """Compile ``oracle.c`` into ``liboracle.so`` beside it (gcc, OpenMP).
+
+    ``-ffp-contract=off`` keeps gcc from fusing a*b+c into fma on any host
+    architecture, so the oracle does the same roundings on x86 and Arm.
+    """
+    with _lock:
+        stale = (not os.path.exists(_LIB)) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC)
+        if force or stale:
+            tmp = _LIB + f".tmp{os.getpid()}"
+            cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+                   "-ffp-contract=off", "-Wall", "-o", tmp, _SRC, "-lm"]
+            subprocess.run(cmd, check=True)
+            os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    build()
+    lib = ctypes.CDLL(_LIB)
+    i64, i32, dbl, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_double, ctypes.c_void_p
+    lib.orc_decode.restype = dbl
+    lib.orc_decode.argtypes = [ctypes.c_uint32, i32]
+    lib.orc_decode_array.restype = i32
+    lib.orc_decode_array.argtypes = [vp, i32, i64, vp]
+    lib.orc_gemm.restype = i32
+    lib.orc_gemm.argtypes = [i64, i64, i64, i32, vp, i64, i32, vp, i64, i32, vp, i64,
+                             i32, vp, dbl, dbl, dbl, dbl, i64, vp, vp, vp, vp]
+    lib.orc_sp_compress.restype = i32
+    lib.orc_sp_compress.argtypes = [i64, i64, i32, vp, i64, vp, vp]
+    lib.orc_sp_decompress.restype = i32
+    lib.orc_sp_decompress.argtypes = [i64, i64, i32, vp, vp, vp, i64]
+    _lib = lib
+    return lib
+
+
+def _codes(x: np.ndarray, fmt: str) -> np.ndarray:
+    want = CODE_DTYPE[ELEM_BYTES[fmt]]
+    x = np.ascontiguousarray(x)
+    if x.dtype.itemsize != ELEM_BYTES[fmt]:
+        raise ValueError(f"{fmt} codes need {ELEM_BYTES[fmt]}-byte elements, got {x.dtype}")
+    return x.view(want)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def decode(codes: np.ndarray, fmt: str) -> np.ndarray:
+    """Exact real values (float64) of an array of stored codes of ``fmt``."""
+    c = _codes(codes, fmt)
+    out = np.empty(c.shape, dtype=np.float64)
+    if _load().orc_decode_array(_ptr(c), FMT[fmt], c.size, _ptr(out)) != 0:
+        raise ValueError("bad format")
+    return out
+
+
+def gemm(A, B, a_fmt, b_fmt, *, C=None, c_fmt="f32", bias=None, bias_fmt="bf16",
+         alpha=1.0, beta=0.0, sa=1.0, sb=1.0, rows=None, cols=None, K=None):
+    """fp64 reference ``alpha*sa*sb*sum_k a[m,k] b[n,k] + beta*C[m,n] + bias[n]``.
+
+    ``A`` is M x lda codes (row-major, the first K columns used), ``B`` is
+    N x ldb codes (B stored K-major), ``C`` M x ldc codes or None, ``bias``
+    N codes or None.  With ``rows``/``cols`` (equal-length index arrays) only
+    those outputs are computed.  Returns ``(ref, S)`` with
+    ``S = sum_k |a b|``: shaped M x N, or like ``rows`` when sampling.
+    """
+    A = _codes(A, a_fmt)
+    B = _codes(B, b_fmt)
+    M, lda = A.shape
+    N, ldb = B.shape
+    K = lda if K is None else K
+    if K > lda or K > ldb:
+        raise ValueError("K exceeds a leading dimension")
+    Cc = None if C is None else _codes(C, c_fmt)
+    ldc = 0 if Cc is None else Cc.shape[1]
+    bc = None if bias is None else _codes(bias, bias_fmt)
+    if rows is None:
+        nsamp = -1
+        r = c = None
+        ref = np.empty((M, N), dtype=np.float64)
+    else:
+        r = np.ascontiguousarray(rows, dtype=np.int64)
+        c = np.ascontiguousarray(cols, dtype=np.int64)
+        if r.shape != c.shape:
+            raise ValueError("rows and cols differ in shape")
+        nsamp = r.size
+        ref = np.empty(r.shape, dtype=np.float64)
+    S = np.empty_like(ref)
+    rc = _load().orc_gemm(M, N, K, FMT[a_fmt], _ptr(A), lda, FMT[b_fmt], _ptr(B), ldb,
+                          FMT[c_fmt], _ptr(Cc), ldc, FMT[bias_fmt], _ptr(bc),
+                          float(alpha), float(beta), float(sa), float(sb),
+                          nsamp, _ptr(r), _ptr(c), _ptr(ref), _ptr(S))
+    if rc != 0:
+        raise ValueError("orc_gemm rejected its arguments")
+    return ref, S
+
+
+def sp_compress(A, fmt):
+    """2:4 prune+compress of logical A (M x K codes) -> (Ac M x K/2, meta M x K/32 uint32)."""
+    A = _codes(A, fmt)
+    M, K = A.shape
+    Ac = np.zeros((M, K // 2), dtype=A.dtype)
+    meta = np.zeros((M, K // 32), dtype=np.uint32)
+    if _load().orc_sp_compress(M, K, FMT[fmt], _ptr(A), K, _ptr(Ac), _ptr(meta)) != 0:
+        raise ValueError("orc_sp_compress rejected its arguments (K % 32 != 0?)")
+    return Ac, meta
+
+
+def sp_decompress(Ac, meta, fmt):
+    """Inverse of :func:`sp_compress`: logical M x K codes with zeros restored."""
+    Ac = _codes(Ac, fmt)
+    meta = np.ascontiguousarray(meta, dtype=np.uint32)
+    M, Kh = Ac.shape
+    K = 2 * Kh
+    A = np.zeros((M, K), dtype=Ac.dtype)
+    if _load().orc_sp_decompress(M, K, FMT[fmt], _ptr(Ac), _ptr(meta), _ptr(A), K) != 0:
+        raise ValueError("orc_sp_decompress rejected its arguments")
+    return A
+
+
+def bound(ref, S, out_fmt, scale=1.0):
+    """Per-element acceptance bound for a result cast to ``out_fmt``.
+
+    ``ACC_REL * |scale| * S`` allows for fp32 accumulation over K in any order;
+    ``2^-p |ref|`` is the round-to-nearest cast of the output;
+    the smallest subnormal covers results that underflow.
+    """
+    p = PRECISION[out_fmt]
+    return ACC_REL * abs(scale) * np.asarray(S) + 2.0 ** -p * np.abs(ref) + MIN_SUBNORMAL[out_fmt]
+
+
+def err_over_bound(D_codes, out_fmt, ref, S, scale=1.0):
+    """max over elements of |D - ref| / bound (must be <= 1); NaN in D gives inf."""
+    d = decode(D_codes, out_fmt)
+    e = np.abs(d - ref) / bound(ref, S, out_fmt, scale)
+    e = np.where(np.isnan(e), np.inf, e)
+    return float(e.max()) if e.size else 0.0

@@ -1,0 +1,124 @@
+"""Seeded synthetic inputs for the GEMM workloads.
+
+This module is shared by the CUDA path's tests/bench and by the CPU oracle,
+and therefore holds none of the GEMM's arithmetic: it only draws random
+numbers with a seeded ``torch.Generator`` on the CPU and stores them in the
+input formats with torch's own round-to-nearest-even casts.  Everything is
+returned as CPU tensors; callers move them to the device.
+
+Workloads (shapes, value distributions, seeds):
+
+* ``small``       512^3 bf16, A/B ~ U[-1,1], C fp32 ~ U[-1,1], alpha=beta=1, seed 0
+* ``square``      4096^3 fp16 (or bf16), A/B ~ N(0,1)/sqrt(K), beta=0, seed 1
+* ``llm``         bf16 activations ~ N(0,1) (M x K), weights ~ N(0,0.02) (N x K), seed 2
+* ``fp8``         8192^3 E4M3 (x E4M3 or E5M2), N(0,1) scaled so amax lands
+                  on the format's largest finite value, bias bf16 ~ N(0,1), seed 3
+* ``sparse``      logical A ~ N(0,1) bf16 (pruned by the method), B ~ N(0,1), seed 4
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+FP8_MAX = {"e4m3": 448.0, "e5m2": 57344.0}
+TORCH_DTYPE = {
+    "bf16": torch.bfloat16,
+    "f16": torch.float16,
+    "f32": torch.float32,
+    "e4m3": torch.float8_e4m3fn,
+    "e5m2": torch.float8_e5m2,
+}
+
+
+def generator(seed: int) -> torch.Generator:
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    return g
+
+
+def uniform(shape, g, lo=-1.0, hi=1.0, dtype="bf16"):
+    x = torch.rand(shape, generator=g, dtype=torch.float32) * (hi - lo) + lo
+    return x.to(TORCH_DTYPE[dtype])
+
+
+def normal(shape, g, std=1.0, dtype="bf16"):
+    x = torch.randn(shape, generator=g, dtype=torch.float32) * std
+    return x.to(TORCH_DTYPE[dtype])
+
+
+def integers(shape, g, lo=-8, hi=8, dtype="bf16"):
+    """Integer-valued inputs in [lo, hi]; exactly representable in every format here."""
+    x = torch.randint(lo, hi + 1, shape, generator=g, dtype=torch.int32).to(torch.float32)
+    return x.to(TORCH_DTYPE[dtype])
+
+
+def fp8_per_tensor(x: torch.Tensor, fmt: str):
+    """Store fp32 ``x`` in ``fmt`` with one per-tensor factor chosen so that the
+    largest |x| lands on the format's largest finite value.
+
+    Returns ``(q, scale)``: the fp8 tensor and the fp32 dequantisation factor
+    (real value ~= q * scale).
+    """
+    amax = float(x.abs().max())
+    s_quant = FP8_MAX[fmt] / amax if amax > 0 else 1.0
+    q = (x * s_quant).clamp(-FP8_MAX[fmt], FP8_MAX[fmt]).to(TORCH_DTYPE[fmt])
+    return q, float(torch.tensor(1.0 / s_quant, dtype=torch.float32))
+
+
+def small_case(M=512, N=512, K=512, seed=0):
+    g = generator(seed)
+    A = uniform((M, K), g)
+    B = uniform((N, K), g)
+    C = uniform((M, N), g, dtype="f32")
+    return dict(A=A, B=B, C=C, alpha=1.0, beta=1.0, in_fmt="bf16", out_fmt="f32")
+
+
+def square_case(n=4096, fmt="f16", seed=1):
+    g = generator(seed)
+    A = normal((n, n), g, std=1.0 / math.sqrt(n), dtype=fmt)
+    B = normal((n, n), g, std=1.0 / math.sqrt(n), dtype=fmt)
+    return dict(A=A, B=B, C=None, alpha=1.0, beta=0.0, in_fmt=fmt, out_fmt="bf16")
+
+
+def llm_case(M, N, K, seed=2):
+    g = generator(seed)
+    A = normal((M, K), g, std=1.0)
+    B = normal((N, K), g, std=0.02)
+    return dict(A=A, B=B, C=None, alpha=1.0, beta=0.0, in_fmt="bf16", out_fmt="bf16")
+
+
+def fp8_case(M=8192, N=8192, K=8192, b_fmt="e4m3", seed=3):
+    g = generator(seed)
+    xa = torch.randn((M, K), generator=g, dtype=torch.float32)
+    xb = torch.randn((N, K), generator=g, dtype=torch.float32)
+    bias = normal((N,), g, std=1.0)
+    A, sa = fp8_per_tensor(xa, "e4m3")
+    B, sb = fp8_per_tensor(xb, b_fmt)
+    return dict(A=A, B=B, C=None, bias=bias, sa=sa, sb=sb, alpha=1.0, beta=0.0,
+                a_fmt="e4m3", b_fmt=b_fmt, out_fmt="bf16")
+
+
+def sparse_case(M=8192, N=8192, K=8192, seed=4):
+    g = generator(seed)
+    A = normal((M, K), g, std=1.0)
+    B = normal((N, K), g, std=1.0)
+    return dict(A_logical=A, B=B, C=None, alpha=1.0, beta=0.0, in_fmt="bf16", out_fmt="bf16")
+
+
+def codes(t: torch.Tensor):
+    """Stored bit patterns of a CPU tensor as a numpy unsigned-integer array."""
+    import numpy as np
+    size = t.element_size()
+    view = {1: torch.uint8, 2: torch.int16, 4: torch.int32}[size]
+    arr = t.contiguous().view(view).numpy()
+    return arr.view({1: np.uint8, 2: np.uint16, 4: np.uint32}[size])
+
+
+def from_codes(arr, fmt: str) -> torch.Tensor:
+    """CPU tensor of format ``fmt`` holding the given stored bit patterns."""
+    import numpy as np
+    size = {"bf16": 2, "f16": 2, "f32": 4, "e4m3": 1, "e5m2": 1}[fmt]
+    signed = {1: np.uint8, 2: np.int16, 4: np.int32}[size]
+    t = torch.from_numpy(np.ascontiguousarray(arr).view(signed).copy())
+    return t.view(TORCH_DTYPE[fmt])

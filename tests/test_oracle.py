@@ -1,0 +1,334 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle itself.
+
+Each test checks the oracle against one of: the published format definitions
+(closed-form special values), an independent decoder (numpy / torch casts),
+an exact rational brute force, numpy's fp64 matmul, closed forms (identity,
+permutation, rank-1, beta-only, bias-only), integer-exact products, and the
+pages' worked 2:4 example.  A dropped term, a wrong sign, a transposed B or a
+wrong tie rule in the oracle fails at least one of them.
+"""
+import itertools
+import json
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth_inputs as si
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------- decoders
+
+def _all_codes(bits):
+    return np.arange(1 << bits, dtype={8: np.uint8, 16: np.uint16}[bits])
+
+
+def _same(a, b):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    return np.array_equal(np.isnan(a), np.isnan(b)) and np.array_equal(
+        np.nan_to_num(a, nan=0.0), np.nan_to_num(b, nan=0.0)) and np.array_equal(
+        np.signbit(a[~np.isnan(a)]), np.signbit(b[~np.isnan(b)]))
+
+
+def test_decode_bf16_exhaustive_matches_torch():
+    c = _all_codes(16)
+    ours = oracle.decode(c, "bf16")
+    theirs = torch.from_numpy(c.view(np.int16).copy()).view(torch.bfloat16).to(torch.float64).numpy()
+    assert _same(ours, theirs)
+
+
+def test_decode_f16_exhaustive_matches_numpy():
+    c = _all_codes(16)
+    ours = oracle.decode(c, "f16")
+    theirs = c.view(np.float16).astype(np.float64)
+    assert _same(ours, theirs)
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_decode_fp8_exhaustive_matches_torch(fmt):
+    c = _all_codes(8)
+    ours = oracle.decode(c, fmt)
+    theirs = torch.from_numpy(c.copy()).view(si.TORCH_DTYPE[fmt]).to(torch.float64).numpy()
+    assert _same(ours, theirs)
+
+
+def test_decode_f32_roundtrip():
+    g = np.random.default_rng(5)
+    v = g.standard_normal(1000).astype(np.float32)
+    assert np.array_equal(oracle.decode(v.view(np.uint32), "f32"), v.astype(np.float64))
+
+
+@pytest.mark.parametrize("fmt,code,value", [
+    # closed forms from the format definitions
+    ("bf16", 0x3F80, 1.0), ("bf16", 0xC000, -2.0), ("bf16", 0x0001, 2.0 ** -133),
+    ("bf16", 0x7F7F, (2 - 2.0 ** -7) * 2.0 ** 127), ("bf16", 0x7F80, np.inf),
+    ("f16", 0x3C00, 1.0), ("f16", 0x0001, 2.0 ** -24), ("f16", 0x7BFF, 65504.0),
+    ("f16", 0x0400, 2.0 ** -14), ("f16", 0xFC00, -np.inf),
+    ("e4m3", 0x7E, 448.0), ("e4m3", 0x01, 2.0 ** -9), ("e4m3", 0x08, 2.0 ** -6),
+    ("e4m3", 0x78, 256.0), ("e4m3", 0x38, 1.0), ("e4m3", 0xB8, -1.0), ("e4m3", 0x7F, np.nan),
+    ("e5m2", 0x7B, 57344.0), ("e5m2", 0x7C, np.inf), ("e5m2", 0x01, 2.0 ** -16),
+    ("e5m2", 0x3C, 1.0), ("e5m2", 0x7D, np.nan), ("e5m2", 0x04, 2.0 ** -14),
+])
+def test_decode_closed_forms(fmt, code, value):
+    width = np.uint8 if fmt in ("e4m3", "e5m2") else np.uint16
+    got = oracle.decode(np.array([code], dtype=width), fmt)[0]
+    if np.isnan(value):
+        assert np.isnan(got)
+    else:
+        assert got == value
+
+
+# ---------------------------------------------------------------- GEMM
+
+def _rand_codes(shape, fmt, seed, kind="normal"):
+    g = si.generator(seed)
+    if kind == "normal":
+        t = si.normal(shape, g, dtype=fmt)
+    elif kind == "int":
+        t = si.integers(shape, g, dtype=fmt)
+    else:
+        t = si.uniform(shape, g, dtype=fmt)
+    return si.codes(t)
+
+
+def test_single_tile_m16n8k16_exact_bruteforce():
+    """One 16x8x16 tile (the m16n8k16 MMA shape) against exact rationals."""
+    spec = json.load(open(os.path.join(GOLDEN, "m16n8k16_tile.json")))
+    M, N, K = spec["M"], spec["N"], spec["K"]
+    A = _rand_codes((M, K), "bf16", 11)
+    B = _rand_codes((N, K), "bf16", 12)
+    C = _rand_codes((M, N), "f32", 13, kind="uniform")
+    ref, S = oracle.gemm(A, B, "bf16", "bf16", C=C, c_fmt="f32", alpha=1.0, beta=1.0)
+    a = torch.from_numpy(A.view(np.int16).copy()).view(torch.bfloat16).float().tolist()
+    b = torch.from_numpy(B.view(np.int16).copy()).view(torch.bfloat16).float().tolist()
+    c = C.view(np.float32).tolist()
+    positions = 0
+    for m in range(M):
+        for n in range(N):
+            exact = sum(Fraction(a[m][k]) * Fraction(b[n][k]) for k in range(K)) + Fraction(c[m][n])
+            sabs = sum(abs(Fraction(a[m][k]) * Fraction(b[n][k])) for k in range(K))
+            positions += K
+            assert abs(Fraction(ref[m, n]) - exact) <= Fraction(2.0 ** -50) * (sabs + abs(Fraction(c[m][n])))
+            assert abs(Fraction(S[m, n]) - sabs) <= Fraction(2.0 ** -50) * sabs
+    assert positions == spec["multiply_add_positions"]
+    # all-ones tile: every output counts exactly K multiply-adds
+    ones_a = si.codes(torch.ones((M, K), dtype=torch.bfloat16))
+    ones_b = si.codes(torch.ones((N, K), dtype=torch.bfloat16))
+    r1, _ = oracle.gemm(ones_a, ones_b, "bf16", "bf16")
+    assert r1.sum() == spec["multiply_add_positions"]
+
+
+@pytest.mark.parametrize("M,N,K,fa,fb", [
+    (37, 53, 71, "bf16", "bf16"), (128, 96, 256, "f16", "f16"), (256, 256, 256, "bf16", "bf16"),
+    (64, 40, 96, "e4m3", "e5m2"), (33, 17, 128, "e5m2", "e4m3"),
+])
+def test_gemm_matches_numpy_fp64(M, N, K, fa, fb):
+    A = _rand_codes((M, K), fa, 21) if fa in ("bf16", "f16") else si.codes(
+        si.fp8_per_tensor(torch.randn((M, K), generator=si.generator(21)), fa)[0])
+    B = _rand_codes((N, K), fb, 22) if fb in ("bf16", "f16") else si.codes(
+        si.fp8_per_tensor(torch.randn((N, K), generator=si.generator(22)), fb)[0])
+    ref, S = oracle.gemm(A, B, fa, fb)
+    Ad = oracle.decode(A, fa)
+    Bd = oracle.decode(B, fb)
+    np_ref = Ad @ Bd.T
+    assert np.all(np.abs(ref - np_ref) <= 1e-12 * S + 1e-300)
+    assert np.allclose(S, np.abs(Ad) @ np.abs(Bd).T, rtol=1e-12, atol=0)
+
+
+def test_identity_pins_k_major_b():
+    """A = I gives D[m, n] = B_stored[n, m]: pins B stored as N rows of K."""
+    K = 48
+    N = 40
+    A = si.codes(torch.eye(K, dtype=torch.bfloat16))
+    B = _rand_codes((N, K), "bf16", 31)
+    ref, _ = oracle.gemm(A, B, "bf16", "bf16")
+    Bd = oracle.decode(B, "bf16")
+    assert np.array_equal(ref, Bd.T)
+    assert not np.array_equal(ref[:N, :N], Bd[:, :N]) or np.array_equal(Bd[:, :N], Bd[:, :N].T)
+
+
+def test_permutation_rows():
+    K, N = 32, 24
+    perm = np.random.default_rng(7).permutation(K)
+    P = torch.zeros((K, K), dtype=torch.bfloat16)
+    P[torch.arange(K), torch.from_numpy(perm)] = 1.0
+    B = _rand_codes((N, K), "bf16", 32)
+    ref, _ = oracle.gemm(si.codes(P), B, "bf16", "bf16")
+    Bd = oracle.decode(B, "bf16")
+    assert np.array_equal(ref, Bd.T[perm, :])
+
+
+def test_rank1_closed_form_with_scales():
+    """a[m,k] = u_m, b[n,k] = v_n (powers of two): D = alpha*sa*sb*K*u_m*v_n exactly."""
+    M, N, K = 12, 10, 96
+    g = np.random.default_rng(3)
+    u = 2.0 ** g.integers(-4, 4, M) * g.choice([-1, 1], M)
+    v = 2.0 ** g.integers(-4, 4, N) * g.choice([-1, 1], N)
+    A = si.codes(torch.tensor(np.repeat(u[:, None], K, 1), dtype=torch.bfloat16))
+    B = si.codes(torch.tensor(np.repeat(v[:, None], K, 1), dtype=torch.bfloat16))
+    ref, S = oracle.gemm(A, B, "bf16", "bf16", alpha=0.5, sa=4.0, sb=0.125)
+    expect = 0.5 * 4.0 * 0.125 * K * np.outer(u, v)
+    assert np.array_equal(ref, expect)
+    assert np.array_equal(S, K * np.abs(np.outer(u, v)))
+
+
+def test_beta_only_and_bias_only():
+    M, N, K = 9, 14, 16
+    zA = si.codes(torch.zeros((M, K), dtype=torch.bfloat16))
+    B = _rand_codes((N, K), "bf16", 41)
+    C = _rand_codes((M, N), "f32", 42, kind="uniform")
+    ref, S = oracle.gemm(zA, B, "bf16", "bf16", C=C, c_fmt="f32", alpha=3.0, beta=-0.75)
+    assert np.array_equal(ref, -0.75 * C.view(np.float32).astype(np.float64))
+    assert np.all(S == 0)
+    bias = _rand_codes((N,), "bf16", 43)
+    ref2, _ = oracle.gemm(zA, B, "bf16", "bf16", bias=bias, bias_fmt="bf16")
+    assert np.array_equal(ref2, np.broadcast_to(oracle.decode(bias, "bf16"), (M, N)))
+    # the sign of beta and the C term must enter, and the bias must add (not replace)
+    ref3, _ = oracle.gemm(zA, B, "bf16", "bf16", C=C, c_fmt="f32", beta=1.0, bias=bias)
+    assert np.array_equal(ref3, C.view(np.float32).astype(np.float64) + oracle.decode(bias, "bf16")[None, :])
+
+
+@pytest.mark.parametrize("fa,fb", [("bf16", "bf16"), ("f16", "f16"), ("e4m3", "e4m3"), ("e4m3", "e5m2")])
+def test_integer_inputs_exact(fa, fb):
+    M, N, K = 40, 24, 200
+    A = _rand_codes((M, K), fa, 51, kind="int")
+    B = _rand_codes((N, K), fb, 52, kind="int")
+    ref, _ = oracle.gemm(A, B, fa, fb)
+    ai = oracle.decode(A, fa).astype(np.int64)
+    bi = oracle.decode(B, fb).astype(np.int64)
+    assert np.array_equal(ref, (ai @ bi.T).astype(np.float64))
+
+
+def test_leading_dimension_padding_ignored():
+    M, N, K, pad = 20, 12, 64, 16
+    A = _rand_codes((M, K + pad), "bf16", 61)
+    B = _rand_codes((N, K + pad), "bf16", 62)
+    ref, _ = oracle.gemm(A, B, "bf16", "bf16", K=K)
+    ref2, _ = oracle.gemm(np.ascontiguousarray(A[:, :K]), np.ascontiguousarray(B[:, :K]), "bf16", "bf16")
+    assert np.array_equal(ref, ref2)
+
+
+def test_sampled_equals_full():
+    M, N, K = 70, 50, 64
+    A = _rand_codes((M, K), "bf16", 71)
+    B = _rand_codes((N, K), "bf16", 72)
+    C = _rand_codes((M, N), "f32", 73, kind="uniform")
+    full, Sf = oracle.gemm(A, B, "bf16", "bf16", C=C, beta=0.5)
+    g = np.random.default_rng(0)
+    r = g.integers(0, M, 300)
+    c = g.integers(0, N, 300)
+    samp, Ss = oracle.gemm(A, B, "bf16", "bf16", C=C, beta=0.5, rows=r, cols=c)
+    assert np.array_equal(samp, full[r, c]) and np.array_equal(Ss, Sf[r, c])
+
+
+def test_bad_arguments_rejected():
+    A = _rand_codes((4, 32), "bf16", 1)
+    with pytest.raises(ValueError):
+        oracle.gemm(A, A, "bf16", "bf16", rows=[0, 9], cols=[0, 0])
+    with pytest.raises(ValueError):
+        oracle.sp_compress(_rand_codes((4, 24), "bf16", 1), "bf16")
+
+
+# ---------------------------------------------------------------- tolerance
+
+def test_bound_accepts_exact_and_rejects_outside():
+    ref = np.array([1.0, -3.0, 1e-3])
+    S = np.array([10.0, 20.0, 0.0])
+    b = oracle.bound(ref, S, "bf16")
+    exact = si.codes(torch.tensor(ref, dtype=torch.bfloat16))
+    assert oracle.err_over_bound(exact, "bf16", ref, S) <= 1.0
+    far = si.codes(torch.tensor(ref + 2.5 * b, dtype=torch.float32))
+    assert oracle.err_over_bound(far, "f32", ref, S) > 1.0
+    nan = si.codes(torch.tensor([np.nan, 0, 0], dtype=torch.float32))
+    assert oracle.err_over_bound(nan, "f32", ref, S) == np.inf
+
+
+# ---------------------------------------------------------------- 2:4 sparsity
+
+def _bf16_codes(vals):
+    return si.codes(torch.tensor(vals, dtype=torch.bfloat16))
+
+
+def test_sparse_worked_example_from_page():
+    spec = json.load(open(os.path.join(GOLDEN, "sp24_worked_example.json")))
+    for case in spec["cases"]:
+        logical = case["logical"] * 8  # K = 32: the example repeated over 8 groups
+        Ac, meta = oracle.sp_compress(_bf16_codes([logical]), "bf16")
+        assert oracle.decode(Ac, "bf16")[0, :2].tolist() == case["values"]
+        i0, i1 = case["positions"]
+        assert meta[0, 0] == sum((i0 | (i1 << 2)) << (4 * g) for g in range(8))
+        back = oracle.sp_decompress(Ac, meta, "bf16")
+        assert oracle.decode(back, "bf16")[0].tolist() == logical
+
+
+def _brute_keep(vals):
+    """Top two positions by (|v| descending, index ascending), returned ascending."""
+    order = sorted(range(4), key=lambda q: (-abs(vals[q]), q))
+    return sorted(order[:2])
+
+
+def test_sparse_selection_exhaustive_small_alphabet():
+    alphabet = [0.0, -0.0, 1.0, -1.0, 2.0, -2.0]
+    groups = list(itertools.product(alphabet, repeat=4))
+    while len(groups) % 8:
+        groups.append((0.0, 0.0, 0.0, 0.0))
+    row = [v for grp in groups for v in grp]
+    Ac, meta = oracle.sp_compress(_bf16_codes([row]), "bf16")
+    vals = oracle.decode(Ac, "bf16")[0]
+    for g, grp in enumerate(groups):
+        nib = (int(meta[0, g // 8]) >> (4 * (g % 8))) & 0xF
+        i0, i1 = nib & 3, nib >> 2
+        assert [i0, i1] == _brute_keep(grp), (grp, i0, i1)
+        assert i0 < i1
+        assert vals[2 * g] == grp[i0] and vals[2 * g + 1] == grp[i1]
+
+
+def test_sparse_roundtrip_random():
+    M, K = 64, 256
+    A = _rand_codes((M, K), "bf16", 81)
+    Ac, meta = oracle.sp_compress(A, "bf16")
+    Ap = oracle.sp_decompress(Ac, meta, "bf16")
+    # every group of the pruned matrix keeps exactly the brute-force pair
+    Ad = oracle.decode(A, "bf16")
+    Apd = oracle.decode(Ap, "bf16")
+    for m in range(0, M, 7):
+        for g in range(K // 4):
+            keep = _brute_keep(Ad[m, 4 * g:4 * g + 4].tolist())
+            for q in range(4):
+                want = Ad[m, 4 * g + q] if q in keep else 0.0
+                assert Apd[m, 4 * g + q] == want
+    # compress of an already-pruned matrix reproduces values and metadata
+    Ac2, meta2 = oracle.sp_compress(Ap, "bf16")
+    assert np.array_equal(Ac2, Ac) and np.array_equal(meta2, meta)
+
+
+def test_sparse_gemm_from_compressed_definition():
+    """D = sum over kept values only (compressed form) == dense GEMM of decompressed A."""
+    M, N, K = 6, 5, 64
+    A = _rand_codes((M, K), "bf16", 91)
+    B = _rand_codes((N, K), "bf16", 92)
+    Ac, meta = oracle.sp_compress(A, "bf16")
+    ref, _ = oracle.gemm(oracle.sp_decompress(Ac, meta, "bf16"), B, "bf16", "bf16")
+    acd = oracle.decode(Ac, "bf16")
+    bd = oracle.decode(B, "bf16")
+    for m in range(M):
+        for n in range(N):
+            total = Fraction(0)
+            for g in range(K // 4):
+                nib = (int(meta[m, g // 8]) >> (4 * (g % 8))) & 0xF
+                for t, q in enumerate((nib & 3, nib >> 2)):
+                    total += Fraction(acd[m, 2 * g + t]) * Fraction(bd[n, 4 * g + q])
+            assert abs(Fraction(ref[m, n]) - total) <= Fraction(2.0 ** -45) * (1 + abs(total))
+
+
+def test_sparse_decompress_rejects_unordered_metadata():
+    Ac = np.zeros((1, 16), dtype=np.uint16)
+    meta = np.array([[0x33333333]], dtype=np.uint32)  # i0 = i1 = 3: not ascending
+    with pytest.raises(ValueError):
+        oracle.sp_decompress(Ac, meta, "bf16")
