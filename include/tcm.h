@@ -1,0 +1,191 @@
+/*
+ * tcm.h -- C ABI of the GB300 (sm_103a) tensor-core GEMM library (libtcm.so).
+ *
+ * The library computes the tiled tensor-core GEMM of the pages
+ *   "NVIDIA MMA" (rainlin-net.pages.dev/llm-inference/nvidia-mma), section
+ *   "从 FMA 到 MMA，再到 GEMM":  D[m,n] = sum_k A[m,k] B[k,n] + C[m,n],
+ * with the input / accumulator / output stages of section "输入/累加/输出"
+ * (narrow inputs, fp32 accumulator, epilogue scale / bias / cast), and the
+ * 2:4 structured-sparse-A form of section "稠密乘法与 2:4 结构化稀疏乘法".
+ * Layout follows the ".row.col" convention of "CUDA 014 - MMA 指令的用法详解"
+ * (blog-9y3.pages.dev/posts/cuda/mma/), section "MMA 指令的格式": A is
+ * row-major, B is column-major -- stored as N rows of K contiguous elements
+ * ("K-major"), the N x K storage that the same page's ldmatrix section
+ * loads without a transpose.
+ *
+ * General conventions (every entry point):
+ *  - All matrix / vector pointers are CALLER-OWNED DEVICE memory on the
+ *    current CUDA device.  The library never frees or retains them.
+ *  - Work is enqueued asynchronously on `stream` (NULL = legacy default
+ *    stream).  A return of TCM_OK means "validated and launched"; results
+ *    are ready once the stream reaches that point.
+ *  - Argument errors are detected on the host BEFORE anything is launched
+ *    and return TCM_ERR_INVALID_ARG / TCM_ERR_UNSUPPORTED /
+ *    TCM_ERR_MISALIGNED; in that case no device memory is touched.
+ *  - Device-side failures (a pipeline wait that exceeded its time limit) do
+ *    not trap: the kernel records a code and returns; read it with
+ *    tcm_get_device_status().
+ *  - Element codes: bf16, f16 (IEEE binary16), f32 (IEEE binary32),
+ *    e4m3 (OCP FP8 E4M3, finite max 448), e5m2 (OCP FP8 E5M2).
+ *  - Base pointers must be 16-byte aligned and every leading dimension, in
+ *    bytes, a multiple of 16 (tensor-memory-accelerator rule), otherwise
+ *    TCM_ERR_MISALIGNED.
+ *  - The library allocates no device memory on any call path.
+ */
+#ifndef TCM_H
+#define TCM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; declared here so this header needs no CUDA include. */
+typedef struct CUstream_st *tcm_stream_t;
+
+typedef enum {
+    TCM_OK = 0,
+    TCM_ERR_INVALID_ARG = 1, /* null pointer, negative size, ld < row length, ... */
+    TCM_ERR_UNSUPPORTED = 2, /* dtype combination or shape class not implemented */
+    TCM_ERR_MISALIGNED = 3,  /* base pointer or leading dimension not 16-byte aligned */
+    TCM_ERR_CUDA = 4,        /* a CUDA runtime / driver call failed (launch, attribute, ...) */
+    TCM_ERR_TIMEOUT = 5      /* a device-side wait exceeded its limit (see tcm_get_device_status) */
+} tcm_status;
+
+typedef enum {
+    TCM_BF16 = 0,
+    TCM_F16 = 1,
+    TCM_F32 = 2,
+    TCM_E4M3 = 3,
+    TCM_E5M2 = 4
+} tcm_dtype;
+
+/*
+ * tcm_gemm -- D = alpha * (A . B) + beta * C
+ *
+ * Definition: "NVIDIA MMA", section "从 FMA 到 MMA，再到 GEMM"
+ * (D_{m,n} = sum_k A_{m,k} B_{k,n} + C_{m,n}); accumulation in fp32 as in
+ * section "输入/累加/输出"; the output cast is round-to-nearest-even.
+ *
+ *  M, N, K    problem size; M, N >= 1, K >= 0 (K == 0 gives beta*C).
+ *  in_dtype   TCM_BF16 or TCM_F16 for both A and B (the FP8 types go
+ *             through tcm_gemm_ex, which carries their scales).
+ *  A          M x K, row-major, leading dimension K (densely packed).
+ *  B          K x N column-major == N rows of K, leading dimension K.
+ *  C          M x N row-major, leading dimension N, dtype = out_dtype;
+ *             may be NULL iff beta == 0.  C may alias D exactly.
+ *  D          M x N row-major, leading dimension N, dtype out_dtype
+ *             (TCM_BF16, TCM_F16 or TCM_F32).
+ *  Results are within 1e-5 * |alpha| * sum_k |a_mk b_kn| + one rounding of the
+ *  output type of the exact value.
+ */
+tcm_status tcm_gemm(int64_t M, int64_t N, int64_t K, tcm_dtype in_dtype,
+                    const void *A, const void *B, const void *C, void *D,
+                    float alpha, float beta, tcm_dtype out_dtype, tcm_stream_t stream);
+
+/*
+ * tcm_gemm_ex -- D = alpha * sA * sB * (A . B) + beta * C + bias
+ *
+ * The epilogue chain of "NVIDIA MMA", section "输入/累加/输出"
+ * (FP8 A x FP8 B -> FP32 accumulator -> scale / bias / cast -> output),
+ * read as: scale, then + beta*C, then + bias[n], then one RNE cast.
+ *
+ *  a_dtype, b_dtype  (bf16,bf16), (f16,f16), or any pair of {e4m3, e5m2}
+ *                    (section "Blackwell ... SM100" table: kind::f8f6f4
+ *                    lets A and B differ).  Other pairs: TCM_ERR_UNSUPPORTED.
+ *  lda, ldb          row pitches in ELEMENTS of A (M x K) and of B (N x K);
+ *                    lda, ldb >= K.
+ *  ldc, ldd          row pitches in elements of C and D; >= N.
+ *  a_scale, b_scale  DEVICE pointers to one fp32 each (per-tensor
+ *                    dequantisation factors: real value = stored value *
+ *                    scale), or NULL for 1.0.
+ *  bias              DEVICE pointer to N elements of out_dtype, or NULL.
+ *  out_dtype         TCM_BF16, TCM_F16 or TCM_F32; C has the same dtype.
+ */
+tcm_status tcm_gemm_ex(int64_t M, int64_t N, int64_t K,
+                       tcm_dtype a_dtype, const void *A, int64_t lda,
+                       tcm_dtype b_dtype, const void *B, int64_t ldb,
+                       const void *C, int64_t ldc, void *D, int64_t ldd,
+                       tcm_dtype out_dtype, float alpha, float beta,
+                       const float *a_scale, const float *b_scale, const void *bias,
+                       tcm_stream_t stream);
+
+/*
+ * tcm_sp_compress -- prune a logical M x K matrix to 2:4 along K and compress it.
+ *
+ * Format: "NVIDIA MMA", section "稠密乘法与 2:4 结构化稀疏乘法" (each group of
+ * 4 logical positions along K keeps 2 values plus their positions; the
+ * worked example [a0,0,0,a3] -> values [a0,a3], metadata [0,3]) and
+ * section "Ampere ..." (ordered metadata: positions ascending).
+ * Selection: the two largest |v| of each group, ties to the lower position.
+ *
+ *  dtype      TCM_BF16 or TCM_F16.
+ *  A          logical M x K row-major, pitch lda elements (lda >= K); K % 32 == 0.
+ *  A_comp     output, M x K/2 row-major (pitch K/2): group g's kept values
+ *             at columns 2g (lower position) and 2g+1.
+ *  meta       output, M x K/32 uint32 row-major: group g's nibble
+ *             (i0 | i1 << 2, i0 < i1) at bits 4*(g % 8) of word g/8.
+ * Bit-exact: a pure selection, no arithmetic on the values.
+ */
+tcm_status tcm_sp_compress(int64_t M, int64_t K, tcm_dtype dtype,
+                           const void *A, int64_t lda, void *A_comp, uint32_t *meta,
+                           tcm_stream_t stream);
+
+/*
+ * tcm_sp_decompress -- inverse of tcm_sp_compress: writes the logical M x K
+ * matrix (pitch lda) with +0 at the two dropped positions of every group.
+ * `meta` must hold ascending nibbles as written by tcm_sp_compress.
+ */
+tcm_status tcm_sp_decompress(int64_t M, int64_t K, tcm_dtype dtype,
+                             const void *A_comp, const uint32_t *meta, void *A, int64_t lda,
+                             tcm_stream_t stream);
+
+/*
+ * tcm_gemm_sp -- D = alpha * (A' . B) + beta * C with A' the 2:4-sparse
+ * logical matrix given by (A_comp, meta) in the tcm_sp_compress format.
+ *
+ * "NVIDIA MMA", section "稠密乘法与 2:4 结构化稀疏乘法": only A is compressed;
+ * B, C and D are dense; shapes are stated on the logical K.
+ *  dtype      TCM_BF16 or TCM_F16 (A_comp and B); K % 32 == 0.
+ *  A_comp     M x K/2 row-major, meta M x K/32 uint32 (as tcm_sp_compress).
+ *  B, C, D    as in tcm_gemm.
+ */
+tcm_status tcm_gemm_sp(int64_t M, int64_t N, int64_t K, tcm_dtype dtype,
+                       const void *A_comp, const uint32_t *meta, const void *B,
+                       const void *C, void *D, float alpha, float beta,
+                       tcm_dtype out_dtype, tcm_stream_t stream);
+
+/*
+ * tcm_get_device_status -- synchronise `stream`, then report the first
+ * device-side failure recorded since the last tcm_clear_device_status():
+ * *code = TCM_OK or TCM_ERR_TIMEOUT, *site = which pipeline wait gave up
+ * (1 = loader waiting for a free stage, 2 = MMA issuer waiting for data,
+ * 3 = MMA issuer waiting for a free accumulator, 4 = epilogue waiting for
+ * an accumulator, 5 = drain at exit).  Returns TCM_ERR_CUDA if the
+ * synchronisation itself failed.  Either output pointer may be NULL.
+ */
+tcm_status tcm_get_device_status(tcm_stream_t stream, int32_t *code, int32_t *site);
+
+/* Reset the recorded device status of the current device to TCM_OK (synchronous). */
+tcm_status tcm_clear_device_status(void);
+
+/*
+ * Limit, in nanoseconds of the GPU's global timer, for any single pipeline
+ * wait inside the kernels of this library (default 2e9, i.e. 2 s; also read
+ * from the environment variable TCM_TIMEOUT_NS at first use).  0 restores
+ * the default.  Affects launches made after the call.
+ */
+void tcm_set_timeout_ns(uint64_t ns);
+
+/* Human-readable name of a status code (static storage). */
+const char *tcm_status_string(tcm_status status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int tcm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TCM_H */

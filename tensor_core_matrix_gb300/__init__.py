@@ -1,0 +1,203 @@
+"""Python binding of libtcm.so, the GB300 (sm_103a) tensor-core GEMM library.
+
+Argument marshalling only: every step of the computation runs in the
+library's CUDA kernels.  Functions carry the C ABI's names (``tcm_gemm``,
+``tcm_gemm_ex``, ``tcm_sp_compress``, ...) and take torch CUDA tensors, whose
+device pointers, shapes and row pitches are passed straight through; torch
+supplies device memory and the current stream, nothing else.
+
+There is no fallback: if ``libtcm.so`` is missing or cannot be loaded, every
+call raises.  Build it with ``python -m tensor_core_matrix_gb300.build`` (or
+``__graft_entry__.build()``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtcm.so")
+
+TCM_OK = 0
+STATUS_NAMES = {0: "TCM_OK", 1: "TCM_ERR_INVALID_ARG", 2: "TCM_ERR_UNSUPPORTED",
+                3: "TCM_ERR_MISALIGNED", 4: "TCM_ERR_CUDA", 5: "TCM_ERR_TIMEOUT"}
+DTYPE_CODE = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2,
+              torch.float8_e4m3fn: 3, torch.float8_e5m2: 4}
+# Symbols the C ABI (include/tcm.h) exports.
+EXPORTS = ("tcm_gemm", "tcm_gemm_ex", "tcm_sp_compress", "tcm_sp_decompress", "tcm_gemm_sp",
+           "tcm_get_device_status", "tcm_clear_device_status", "tcm_set_timeout_ns",
+           "tcm_status_string", "tcm_version")
+
+
+class TcmError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)}")
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libtcm.so and declare its signatures (raises if it is absent)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build the CUDA library first "
+                          "(python -m tensor_core_matrix_gb300.build)")
+    lib = ctypes.CDLL(path)
+    i64, i32, f32, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_void_p
+    lib.tcm_gemm.restype = i32
+    lib.tcm_gemm.argtypes = [i64, i64, i64, i32, vp, vp, vp, vp, f32, f32, i32, vp]
+    lib.tcm_gemm_ex.restype = i32
+    lib.tcm_gemm_ex.argtypes = [i64, i64, i64, i32, vp, i64, i32, vp, i64, vp, i64, vp, i64,
+                                i32, f32, f32, vp, vp, vp, vp]
+    lib.tcm_sp_compress.restype = i32
+    lib.tcm_sp_compress.argtypes = [i64, i64, i32, vp, i64, vp, vp, vp]
+    lib.tcm_sp_decompress.restype = i32
+    lib.tcm_sp_decompress.argtypes = [i64, i64, i32, vp, vp, vp, i64, vp]
+    lib.tcm_gemm_sp.restype = i32
+    lib.tcm_gemm_sp.argtypes = [i64, i64, i64, i32, vp, vp, vp, vp, vp, f32, f32, i32, vp]
+    lib.tcm_get_device_status.restype = i32
+    lib.tcm_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
+    lib.tcm_clear_device_status.restype = i32
+    lib.tcm_clear_device_status.argtypes = []
+    lib.tcm_set_timeout_ns.restype = None
+    lib.tcm_set_timeout_ns.argtypes = [ctypes.c_uint64]
+    lib.tcm_status_string.restype = ctypes.c_char_p
+    lib.tcm_status_string.argtypes = [i32]
+    lib.tcm_version.restype = i32
+    lib.tcm_version.argtypes = []
+    _lib = lib
+    return lib
+
+
+def _check(status: int, what: str):
+    if status != TCM_OK:
+        raise TcmError(status, what)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _row_pitch(t, name):
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError(f"{name} must be a 2-D tensor with unit column stride")
+    return t.stride(0)
+
+
+def _code(t, name):
+    try:
+        return DTYPE_CODE[t.dtype]
+    except KeyError:
+        raise ValueError(f"{name}: unsupported dtype {t.dtype}") from None
+
+
+def tcm_gemm_ex(A, B, D, *, C=None, alpha=1.0, beta=0.0, a_scale=None, b_scale=None, bias=None, stream=None):
+    """D = alpha * a_scale * b_scale * (A @ B_stored.T) + beta * C + bias.
+
+    A: M x K (row-major, pitch = A.stride(0)); B: N x K (K-major storage of
+    the K x N operand); C, D: M x N; bias: N; a_scale, b_scale: one-element
+    fp32 CUDA tensors or None.
+    """
+    lib = load_library()
+    M, K = A.shape
+    N = B.shape[0]
+    if B.shape[1] != K or tuple(D.shape) != (M, N):
+        raise ValueError("shape mismatch")
+    st = lib.tcm_gemm_ex(M, N, K, _code(A, "A"), _ptr(A), _row_pitch(A, "A"), _code(B, "B"), _ptr(B),
+                         _row_pitch(B, "B"), _ptr(C), _row_pitch(C, "C") if C is not None else 0,
+                         _ptr(D), _row_pitch(D, "D"), _code(D, "D"), float(alpha), float(beta),
+                         _ptr(a_scale), _ptr(b_scale), _ptr(bias), _stream(stream))
+    _check(st, "tcm_gemm_ex")
+    return D
+
+
+def tcm_gemm(A, B, D, *, C=None, alpha=1.0, beta=0.0, stream=None):
+    """D = alpha * (A @ B_stored.T) + beta * C for bf16/fp16 A, B (densely packed)."""
+    lib = load_library()
+    M, K = A.shape
+    N = B.shape[0]
+    for t, n in ((A, "A"), (B, "B"), (D, "D")):
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    if C is not None and not C.is_contiguous():
+        raise ValueError("C must be contiguous")
+    st = lib.tcm_gemm(M, N, K, _code(A, "A"), _ptr(A), _ptr(B), _ptr(C), _ptr(D), float(alpha),
+                      float(beta), _code(D, "D"), _stream(stream))
+    _check(st, "tcm_gemm")
+    return D
+
+
+def tcm_sp_compress(A, A_comp=None, meta=None, *, stream=None):
+    """2:4 prune + compress of logical A (M x K, K % 32 == 0) -> (A_comp M x K/2, meta M x K/32 int32)."""
+    lib = load_library()
+    M, K = A.shape
+    if A_comp is None:
+        A_comp = torch.empty((M, K // 2), dtype=A.dtype, device=A.device)
+    if meta is None:
+        meta = torch.empty((M, K // 32), dtype=torch.int32, device=A.device)
+    st = lib.tcm_sp_compress(M, K, _code(A, "A"), _ptr(A), _row_pitch(A, "A"), _ptr(A_comp), _ptr(meta),
+                             _stream(stream))
+    _check(st, "tcm_sp_compress")
+    return A_comp, meta
+
+
+def tcm_sp_decompress(A_comp, meta, A=None, *, stream=None):
+    """Logical M x K matrix from (A_comp, meta) with zeros at the dropped positions."""
+    lib = load_library()
+    M, Kh = A_comp.shape
+    K = 2 * Kh
+    if A is None:
+        A = torch.empty((M, K), dtype=A_comp.dtype, device=A_comp.device)
+    st = lib.tcm_sp_decompress(M, K, _code(A_comp, "A_comp"), _ptr(A_comp), _ptr(meta), _ptr(A),
+                               _row_pitch(A, "A"), _stream(stream))
+    _check(st, "tcm_sp_decompress")
+    return A
+
+
+def tcm_gemm_sp(A_comp, meta, B, D, *, C=None, alpha=1.0, beta=0.0, stream=None):
+    """D = alpha * (A' @ B_stored.T) + beta * C, A' the 2:4 matrix held by (A_comp, meta)."""
+    lib = load_library()
+    M, Kh = A_comp.shape
+    K = 2 * Kh
+    N = B.shape[0]
+    st = lib.tcm_gemm_sp(M, N, K, _code(A_comp, "A_comp"), _ptr(A_comp), _ptr(meta), _ptr(B), _ptr(C),
+                         _ptr(D), float(alpha), float(beta), _code(D, "D"), _stream(stream))
+    _check(st, "tcm_gemm_sp")
+    return D
+
+
+def tcm_get_device_status(stream=None):
+    """Synchronise the stream and return (code, site) of the first recorded device failure."""
+    lib = load_library()
+    code, site = ctypes.c_int32(0), ctypes.c_int32(0)
+    _check(lib.tcm_get_device_status(_stream(stream), ctypes.byref(code), ctypes.byref(site)),
+           "tcm_get_device_status")
+    return code.value, site.value
+
+
+def tcm_clear_device_status():
+    _check(load_library().tcm_clear_device_status(), "tcm_clear_device_status")
+
+
+def tcm_set_timeout_ns(ns: int):
+    load_library().tcm_set_timeout_ns(int(ns))
+
+
+def tcm_status_string(status: int) -> str:
+    return load_library().tcm_status_string(int(status)).decode()
+
+
+def tcm_version() -> int:
+    return load_library().tcm_version()

@@ -1,0 +1,306 @@
+// tcm_api.cu -- the extern "C" boundary of libtcm.so (declared in include/tcm.h).
+//
+// Validates arguments on the host, encodes the TMA tensor maps (through the
+// driver entry point cuTensorMapEncodeTiled, fetched at run time so the
+// library does not link libcuda directly), picks a kernel configuration and
+// launches it on the caller's stream.  No device memory is allocated here:
+// the device status words are a file-scope __device__ array.
+#include <atomic>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/tcm.h"
+#include "tcm_internal.h"
+#include "tcm_ptx.cuh"
+
+namespace tcm {
+
+__device__ int g_device_status[2]; // {code, site}, one copy per device
+
+static constexpr int kMaxDevices = 64;
+
+int *device_status_ptr()
+{
+    static int *ptrs[kMaxDevices] = {};
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ptrs[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+        ptrs[dev] = static_cast<int *>(p);
+    }
+    return ptrs[dev];
+}
+
+static int sm_count()
+{
+    static int counts[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    if (counts[dev] == 0) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        counts[dev] = n;
+    }
+    return counts[dev];
+}
+
+static std::atomic<unsigned long long> g_timeout_ns{0};
+
+static unsigned long long timeout_ns()
+{
+    unsigned long long t = g_timeout_ns.load();
+    if (t == 0) {
+        t = 2000000000ull;
+        if (const char *env = std::getenv("TCM_TIMEOUT_NS")) {
+            const unsigned long long v = std::strtoull(env, nullptr, 10);
+            if (v > 0) t = v;
+        }
+        g_timeout_ns.store(t);
+    }
+    return t;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// Tensor map of a K-major operand: `rows` rows of `inner` elements, pitch `ld`
+// elements; tiles of box_rows x 128 bytes with 128-byte swizzling; reads
+// outside the matrix return zeros.
+static bool encode_kmajor(CUtensorMap *map, const void *base, int elem_bytes, uint64_t inner, uint64_t rows,
+                          uint64_t ld, uint32_t box_rows)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const CUtensorMapDataType dt = elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+    const cuuint64_t dims[2] = {inner, rows};
+    const cuuint64_t strides[1] = {ld * static_cast<uint64_t>(elem_bytes)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / elem_bytes), box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static int elem_bytes(tcm_dtype t)
+{
+    switch (t) {
+    case TCM_BF16: case TCM_F16: return 2;
+    case TCM_F32: return 4;
+    case TCM_E4M3: case TCM_E5M2: return 1;
+    default: return 0;
+    }
+}
+
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+} // namespace tcm
+
+using namespace tcm;
+
+extern "C" {
+
+const char *tcm_status_string(tcm_status s)
+{
+    switch (s) {
+    case TCM_OK: return "TCM_OK";
+    case TCM_ERR_INVALID_ARG: return "TCM_ERR_INVALID_ARG";
+    case TCM_ERR_UNSUPPORTED: return "TCM_ERR_UNSUPPORTED";
+    case TCM_ERR_MISALIGNED: return "TCM_ERR_MISALIGNED";
+    case TCM_ERR_CUDA: return "TCM_ERR_CUDA";
+    case TCM_ERR_TIMEOUT: return "TCM_ERR_TIMEOUT";
+    default: return "TCM_UNKNOWN_STATUS";
+    }
+}
+
+int tcm_version(void) { return 100; }
+
+void tcm_set_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns); }
+
+tcm_status tcm_gemm_ex(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const void *A, int64_t lda,
+                       tcm_dtype b_dtype, const void *B, int64_t ldb, const void *C, int64_t ldc, void *D,
+                       int64_t ldd, tcm_dtype out_dtype, float alpha, float beta, const float *a_scale,
+                       const float *b_scale, const void *bias, tcm_stream_t stream)
+{
+    // ---- argument checks (nothing is launched on failure)
+    const bool a16 = a_dtype == TCM_BF16 || a_dtype == TCM_F16;
+    const bool a8 = a_dtype == TCM_E4M3 || a_dtype == TCM_E5M2;
+    const bool b8 = b_dtype == TCM_E4M3 || b_dtype == TCM_E5M2;
+    int kind;
+    if (a16 && b_dtype == a_dtype) kind = 0;
+    else if (a8 && b8) kind = 1;
+    else return TCM_ERR_UNSUPPORTED;
+    if (out_dtype != TCM_BF16 && out_dtype != TCM_F16 && out_dtype != TCM_F32) return TCM_ERR_UNSUPPORTED;
+    if (M < 1 || N < 1 || K < 0) return TCM_ERR_INVALID_ARG;
+    if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2) return TCM_ERR_UNSUPPORTED;
+    if (!D) return TCM_ERR_INVALID_ARG;
+    if (K > 0 && (!A || !B)) return TCM_ERR_INVALID_ARG;
+    if (beta != 0.f && !C) return TCM_ERR_INVALID_ARG;
+    if (lda < K || ldb < K || ldd < N || (C && ldc < N)) return TCM_ERR_INVALID_ARG;
+    const int ea = elem_bytes(a_dtype), eb = elem_bytes(b_dtype), eo = elem_bytes(out_dtype);
+    if ((A && !aligned16(A)) || (B && !aligned16(B)) || !aligned16(D) || (C && !aligned16(C)) ||
+        (bias && !aligned16(bias)))
+        return TCM_ERR_MISALIGNED;
+    if ((lda * ea) % 16 || (ldb * eb) % 16 || (ldd * eo) % 16 || (C && (ldc * eo) % 16)) return TCM_ERR_MISALIGNED;
+
+    // ---- configuration: swap A and B for skinny M so the weight fills the 128-row MMA
+    const bool swap = M <= 64 && N >= 128;
+    const int64_t kM = swap ? N : M, kN = swap ? M : N;
+    GemmConfig cfg{};
+    cfg.kind = kind;
+    if (swap) cfg.bn = kN <= 32 ? 32 : 64;
+    else if (kN <= 32) cfg.bn = 32;
+    else if (kN <= 64) cfg.bn = 64;
+    else if (kN <= 128) cfg.bn = 128;
+    else {
+        // prefer 256-wide tiles unless 128-wide ones fill clearly more of the GPU
+        const int64_t sms = sm_count();
+        const int64_t t256 = ((kM + 127) / 128) * ((kN + 255) / 256);
+        const int64_t t128 = ((kM + 127) / 128) * ((kN + 127) / 128);
+        cfg.bn = (t256 < sms / 2 && t128 > t256) ? 128 : 256;
+    }
+    cfg.stages = 0;
+
+    // ---- tensor maps (the kernel's "A" operand is the swapped one when swap)
+    const int k_elems_stage = kind == 1 ? 128 : 64;
+    const uint64_t kdim = K > 0 ? static_cast<uint64_t>(K) : static_cast<uint64_t>(k_elems_stage);
+    const void *opA = swap ? B : A;
+    const void *opB = swap ? A : B;
+    const int eA = swap ? eb : ea, eB = swap ? ea : eb;
+    const int64_t ldA = swap ? ldb : lda, ldB = swap ? lda : ldb;
+    CUtensorMap tmA, tmB;
+    std::memset(&tmA, 0, sizeof tmA);
+    std::memset(&tmB, 0, sizeof tmB);
+    if (K > 0) {
+        if (!encode_kmajor(&tmA, opA, eA, kdim, static_cast<uint64_t>(kM), static_cast<uint64_t>(ldA), 128))
+            return TCM_ERR_CUDA;
+        if (!encode_kmajor(&tmB, opB, eB, kdim, static_cast<uint64_t>(kN), static_cast<uint64_t>(ldB),
+                           static_cast<uint32_t>(cfg.bn)))
+            return TCM_ERR_CUDA;
+    }
+
+    // ---- parameters and launch
+    GemmParams p{};
+    p.kM = static_cast<int>(kM);
+    p.kN = static_cast<int>(kN);
+    p.K = static_cast<int>(K);
+    p.num_kb = static_cast<int>((K + k_elems_stage - 1) / k_elems_stage);
+    p.tiles_m = static_cast<int>((kM + 127) / 128);
+    p.tiles_n = static_cast<int>((kN + cfg.bn - 1) / cfg.bn);
+    p.num_tiles = p.tiles_m * p.tiles_n;
+    p.group_m = 16;
+    p.tile_begin = 0;
+    p.tile_end = p.num_tiles;
+    p.D = D;
+    p.ldd = ldd;
+    p.C = beta != 0.f ? C : nullptr;
+    p.ldc = ldc;
+    p.bias = bias;
+    p.a_scale = swap ? b_scale : a_scale;
+    p.b_scale = swap ? a_scale : b_scale;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.out_fmt = static_cast<int>(out_dtype);
+    p.swap_ab = swap ? 1 : 0;
+    const uint32_t fa = static_cast<uint32_t>(swap ? b_dtype : a_dtype);
+    const uint32_t fb = static_cast<uint32_t>(swap ? a_dtype : b_dtype);
+    // kind::f16: 0 = f16, 1 = bf16; kind::f8f6f4: 0 = E4M3, 1 = E5M2
+    const uint32_t codeA = kind == 0 ? (fa == TCM_BF16 ? 1u : 0u) : (fa == TCM_E5M2 ? 1u : 0u);
+    const uint32_t codeB = kind == 0 ? (fb == TCM_BF16 ? 1u : 0u) : (fb == TCM_E5M2 ? 1u : 0u);
+    p.idesc = make_idesc(codeA, codeB, 128, static_cast<uint32_t>(cfg.bn));
+    p.timeout_ns = timeout_ns();
+    p.status = device_status_ptr();
+    if (!p.status) return TCM_ERR_CUDA;
+
+    const int sms = sm_count();
+    if (sms <= 0) return TCM_ERR_CUDA;
+    const int grid = p.num_tiles < sms ? p.num_tiles : sms;
+    const cudaError_t e = launch_gemm(cfg, tmA, tmB, nullptr, p, grid, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TCM_OK : TCM_ERR_CUDA;
+}
+
+tcm_status tcm_gemm(int64_t M, int64_t N, int64_t K, tcm_dtype in_dtype, const void *A, const void *B,
+                    const void *C, void *D, float alpha, float beta, tcm_dtype out_dtype, tcm_stream_t stream)
+{
+    if (in_dtype != TCM_BF16 && in_dtype != TCM_F16) return TCM_ERR_UNSUPPORTED;
+    return tcm_gemm_ex(M, N, K, in_dtype, A, K, in_dtype, B, K, C, N, D, N, out_dtype, alpha, beta, nullptr, nullptr,
+                       nullptr, stream);
+}
+
+static tcm_status check_sparse_shape(int64_t M, int64_t K, tcm_dtype dtype, const void *x, const void *y,
+                                     const uint32_t *meta, int64_t lda)
+{
+    if (dtype != TCM_BF16 && dtype != TCM_F16) return TCM_ERR_UNSUPPORTED;
+    if (M < 0 || K < 0 || K % 32 != 0 || lda < K) return TCM_ERR_INVALID_ARG;
+    if (M > 0 && K > 0 && (!x || !y || !meta)) return TCM_ERR_INVALID_ARG;
+    if ((x && !aligned16(x)) || (y && !aligned16(y)) || (meta && !aligned16(meta))) return TCM_ERR_MISALIGNED;
+    if ((lda * 2) % 16) return TCM_ERR_MISALIGNED;
+    return TCM_OK;
+}
+
+tcm_status tcm_sp_compress(int64_t M, int64_t K, tcm_dtype dtype, const void *A, int64_t lda, void *A_comp,
+                           uint32_t *meta, tcm_stream_t stream)
+{
+    const tcm_status s = check_sparse_shape(M, K, dtype, A, A_comp, meta, lda);
+    if (s != TCM_OK) return s;
+    return launch_sp_compress(M, K, 2, A, lda, A_comp, meta, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? TCM_OK
+               : TCM_ERR_CUDA;
+}
+
+tcm_status tcm_sp_decompress(int64_t M, int64_t K, tcm_dtype dtype, const void *A_comp, const uint32_t *meta, void *A,
+                             int64_t lda, tcm_stream_t stream)
+{
+    const tcm_status s = check_sparse_shape(M, K, dtype, A, A_comp, meta, lda);
+    if (s != TCM_OK) return s;
+    return launch_sp_decompress(M, K, 2, A_comp, meta, A, lda, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? TCM_OK
+               : TCM_ERR_CUDA;
+}
+
+tcm_status tcm_gemm_sp(int64_t M, int64_t N, int64_t K, tcm_dtype dtype, const void *A_comp, const uint32_t *meta,
+                       const void *B, const void *C, void *D, float alpha, float beta, tcm_dtype out_dtype,
+                       tcm_stream_t stream)
+{
+    (void)M; (void)N; (void)K; (void)dtype; (void)A_comp; (void)meta; (void)B; (void)C; (void)D;
+    (void)alpha; (void)beta; (void)out_dtype; (void)stream;
+    return TCM_ERR_UNSUPPORTED;
+}
+
+tcm_status tcm_get_device_status(tcm_stream_t stream, int32_t *code, int32_t *site)
+{
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return TCM_ERR_CUDA;
+    int host[2] = {0, 0};
+    if (cudaMemcpyFromSymbol(host, g_device_status, sizeof host) != cudaSuccess) return TCM_ERR_CUDA;
+    if (code) *code = host[0];
+    if (site) *site = host[1];
+    return TCM_OK;
+}
+
+tcm_status tcm_clear_device_status(void)
+{
+    const int zero[2] = {0, 0};
+    if (cudaMemcpyToSymbol(g_device_status, zero, sizeof zero) != cudaSuccess) return TCM_ERR_CUDA;
+    return TCM_OK;
+}
+
+} // extern "C"

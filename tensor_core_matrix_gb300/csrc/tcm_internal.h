@@ -1,0 +1,67 @@
+// tcm_internal.h -- declarations shared by the library's translation units
+// (kernel launchers and the C-ABI layer).  Not installed; not part of the ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace tcm {
+
+// Output / C / bias element formats; values equal the public tcm_dtype codes.
+enum OutFmt : int { OUT_BF16 = 0, OUT_F16 = 1, OUT_F32 = 2 };
+
+// Device-status codes and the wait sites that can record a timeout.
+enum DevCode : int { DEV_OK = 0, DEV_TIMEOUT = 5 };
+enum WaitSite : int {
+    SITE_LOAD_EMPTY = 1,
+    SITE_MMA_FULL = 2,
+    SITE_MMA_ACC_EMPTY = 3,
+    SITE_EPI_ACC_FULL = 4,
+    SITE_DRAIN = 5,
+};
+
+// Everything a GEMM kernel needs besides its tensor maps.  "Kernel" rows and
+// columns (kM x kN) are the rows of the TMA "A" operand and of the "B"
+// operand; with swap_ab the kernel computes D^T (kernel row = D column).
+struct GemmParams {
+    int kM, kN, K;            // kernel-space problem (K = logical K)
+    int num_kb;               // number of K blocks of the tile loop
+    int tiles_m, tiles_n, num_tiles;
+    int group_m;              // rasterisation: tiles of this many row blocks share B in L2
+    int tile_begin, tile_end; // the linear tile range this launch covers
+    void *D;
+    long long ldd;
+    const void *C;
+    long long ldc;
+    const void *bias;
+    const float *a_scale;
+    const float *b_scale;
+    float alpha, beta;
+    int out_fmt;
+    int swap_ab;
+    uint32_t idesc;
+    unsigned long long timeout_ns;
+    int *status;              // device status word pair {code, site}
+};
+
+// Which kernel variant a launch uses.
+struct GemmConfig {
+    int kind;    // 0 = kind::f16, 1 = kind::f8f6f4, 2 = sparse kind::f16
+    int bn;      // N tile (columns of the accumulator)
+    int stages;  // shared-memory ring depth
+};
+
+cudaError_t launch_gemm(const GemmConfig &cfg, const CUtensorMap &tmA, const CUtensorMap &tmB,
+                        const CUtensorMap *tmMeta, const GemmParams &p, int grid, cudaStream_t stream);
+
+size_t gemm_smem_bytes(const GemmConfig &cfg);
+
+cudaError_t launch_sp_compress(int64_t M, int64_t K, int elem_bytes, const void *A, int64_t lda, void *Ac,
+                               uint32_t *meta, cudaStream_t stream);
+cudaError_t launch_sp_decompress(int64_t M, int64_t K, int elem_bytes, const void *Ac, const uint32_t *meta, void *A,
+                                 int64_t lda, cudaStream_t stream);
+
+int *device_status_ptr(); // address of this device's status words (per current device)
+
+} // namespace tcm

@@ -1,0 +1,207 @@
+"""GPU parity of the dense tcgen05 GEMM against the CPU oracle, through the C ABI.
+
+Bars: integer-valued inputs (exact in fp32 as long as |partial sums| < 2^24)
+must match bit for bit; everything else must satisfy
+|D - ref| <= 1e-5 * |alpha sA sB| * sum_k |a b| + 2^-p |ref| + min_subnormal
+element by element (oracle.bound).  D is pre-filled with NaN so an unwritten
+output fails.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth_inputs as si
+from parity import dev, oracle_ref, ratio, run_gemm_ex, sample_indices
+
+pytestmark = pytest.mark.gpu
+
+F8 = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _build():
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    import tensor_core_matrix_gb300 as tcm
+    tcm.tcm_clear_device_status()
+
+
+# ------------------------------------------------------------------ exact cases
+
+@pytest.mark.parametrize("M,N,K", [
+    (128, 32, 16), (128, 64, 64), (128, 128, 64), (128, 256, 64), (256, 512, 256),
+    (300, 520, 136), (1000, 260, 1024), (129, 257, 72),
+])
+@pytest.mark.parametrize("fmt", ["bf16", "f16"])
+def test_integer_inputs_bit_exact(M, N, K, fmt):
+    g = si.generator(100 + M + N + K)
+    A = si.integers((M, K), g, dtype=fmt)
+    B = si.integers((N, K), g, dtype=fmt)
+    D = run_gemm_ex(A, B, torch.float32)
+    ref, _ = oracle_ref(A, B)
+    assert np.array_equal(D.double().numpy(), ref)
+
+
+@pytest.mark.parametrize("fa,fb", [("e4m3", "e4m3"), ("e4m3", "e5m2"), ("e5m2", "e4m3"), ("e5m2", "e5m2")])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 128), (200, 136, 400)])
+def test_fp8_integer_inputs_bit_exact(fa, fb, M, N, K):
+    g = si.generator(7 + M)
+    A = si.integers((M, K), g, dtype=fa)
+    B = si.integers((N, K), g, dtype=fb)
+    D = run_gemm_ex(A, B, torch.float32)
+    ref, _ = oracle_ref(A, B)
+    assert np.array_equal(D.double().numpy(), ref)
+
+
+def test_identity_gives_b_transposed():
+    K, N = 256, 384
+    A = torch.eye(K, dtype=torch.bfloat16)
+    B = si.normal((N, K), si.generator(5))
+    D = run_gemm_ex(A, B, torch.float32)
+    assert torch.equal(D, B.float().t())
+
+
+def test_permutation_permutes_rows():
+    K, N = 192, 160
+    perm = torch.randperm(K, generator=si.generator(6))
+    P = torch.zeros((K, K), dtype=torch.bfloat16)
+    P[torch.arange(K), perm] = 1.0
+    B = si.normal((N, K), si.generator(7))
+    D = run_gemm_ex(P, B, torch.float32)
+    assert torch.equal(D, B.float().t()[perm])
+
+
+def test_rank1_closed_form():
+    M, N, K = 256, 256, 512
+    u = 2.0 ** torch.randint(-3, 3, (M,), generator=si.generator(8)).float()
+    v = -(2.0 ** torch.randint(-3, 3, (N,), generator=si.generator(9)).float())
+    A = u[:, None].expand(M, K).to(torch.bfloat16).contiguous()
+    B = v[:, None].expand(N, K).to(torch.bfloat16).contiguous()
+    D = run_gemm_ex(A, B, torch.float32, alpha=0.5)
+    assert torch.equal(D, 0.5 * K * torch.outer(u, v))
+
+
+# ------------------------------------------------------------------ configured workloads
+
+def test_small_config_512_bf16_with_c_and_16x8x16_tile():
+    case = si.small_case()
+    D = run_gemm_ex(case["A"], case["B"], torch.float32, C=case["C"], alpha=1.0, beta=1.0)
+    ref, S = oracle_ref(case["A"], case["B"], C=case["C"], alpha=1.0, beta=1.0)
+    assert ratio(D, ref, S) <= 1.0
+    # the single m16n8k16 tile: A 16x16, B 16x8 (stored 8 x 16), C/D 16x8
+    A, B, C = case["A"][:16, :16].contiguous(), case["B"][:8, :16].contiguous(), case["C"][:16, :8].contiguous()
+    D1 = run_gemm_ex(A, B, torch.float32, C=C, alpha=1.0, beta=1.0)
+    ref1, S1 = oracle_ref(A, B, C=C, alpha=1.0, beta=1.0)
+    assert ratio(D1, ref1, S1) <= 1.0
+
+
+@pytest.mark.parametrize("M,N,K,fmt,out", [
+    (777, 1000, 520, "bf16", torch.bfloat16), (130, 300, 8, "f16", torch.float16),
+    (64, 96, 4096, "bf16", torch.float32), (1536, 1280, 320, "f16", torch.bfloat16),
+    (96, 40, 200, "bf16", torch.bfloat16),
+])
+def test_ragged_shapes_with_beta(M, N, K, fmt, out):
+    g = si.generator(M * 7 + N)
+    A = si.normal((M, K), g, dtype=fmt)
+    B = si.normal((N, K), g, dtype=fmt)
+    C = si.normal((M, N), g, dtype={torch.bfloat16: "bf16", torch.float16: "f16", torch.float32: "f32"}[out])
+    D = run_gemm_ex(A, B, out, C=C, alpha=1.25, beta=-0.5)
+    ref, S = oracle_ref(A, B, C=C, alpha=1.25, beta=-0.5)
+    assert ratio(D, ref, S, scale=1.25) <= 1.0
+
+
+@pytest.mark.parametrize("fb", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("M,N,K", [(512, 512, 512), (333, 700, 1040)])
+def test_fp8_scales_and_bias(fb, M, N, K):
+    case = si.fp8_case(M, N, K, b_fmt=fb, seed=3)
+    D = run_gemm_ex(case["A"], case["B"], torch.bfloat16, sa=case["sa"], sb=case["sb"], bias=case["bias"])
+    ref, S = oracle_ref(case["A"], case["B"], sa=case["sa"], sb=case["sb"], bias=case["bias"])
+    assert ratio(D, ref, S, scale=case["sa"] * case["sb"]) <= 1.0
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 256, 512), (16, 1024, 1024), (64, 384, 256), (16, 200, 64)])
+def test_skinny_m_swaps_operands(M, N, K):
+    g = si.generator(M + 3 * N)
+    A = si.normal((M, K), g)
+    B = si.normal((N, K), g, std=0.02)
+    C = si.normal((M, N), g)
+    bias = si.normal((N,), g)
+    D = run_gemm_ex(A, B, torch.bfloat16, C=C, beta=1.0, bias=bias)
+    ref, S = oracle_ref(A, B, C=C, beta=1.0, bias=bias)
+    assert ratio(D, ref, S) <= 1.0
+
+
+def test_k_zero_gives_beta_c():
+    M, N = 100, 72
+    C = si.normal((M, N), si.generator(1), dtype="f32")
+    A = torch.zeros((M, 8), dtype=torch.bfloat16)[:, :0]
+    B = torch.zeros((N, 8), dtype=torch.bfloat16)[:, :0]
+    d = dev()
+    D = torch.full((M, N), float("nan"), dtype=torch.float32, device=d)
+    import tensor_core_matrix_gb300 as tcm
+    Ad = torch.zeros((M, 8), dtype=torch.bfloat16, device=d)
+    Bd = torch.zeros((N, 8), dtype=torch.bfloat16, device=d)
+    tcm.tcm_gemm_ex(Ad[:, :0], Bd[:, :0], D, C=C.to(d), beta=2.0)
+    assert torch.equal(D.cpu(), 2.0 * C)
+    del A, B
+
+
+def test_tcm_gemm_packed_entry_point():
+    import tensor_core_matrix_gb300 as tcm
+    d = dev()
+    g = si.generator(12)
+    A = si.normal((256, 384), g)
+    B = si.normal((320, 384), g)
+    C = si.normal((256, 320), g)
+    D = torch.empty((256, 320), dtype=torch.bfloat16, device=d)
+    tcm.tcm_gemm(A.to(d), B.to(d), D, C=C.to(d), alpha=2.0, beta=1.0)
+    ref, S = oracle_ref(A, B, C=C, alpha=2.0, beta=1.0)
+    assert ratio(D.cpu(), ref, S, scale=2.0) <= 1.0
+
+
+def test_c_aliasing_d_in_place():
+    import tensor_core_matrix_gb300 as tcm
+    d = dev()
+    g = si.generator(13)
+    A = si.normal((384, 256), g)
+    B = si.normal((512, 256), g)
+    C = si.normal((384, 512), g, dtype="f32")
+    Dd = C.to(d).clone()
+    tcm.tcm_gemm_ex(A.to(d), B.to(d), Dd, C=Dd, beta=1.0)
+    ref, S = oracle_ref(A, B, C=C, beta=1.0)
+    assert ratio(Dd.cpu(), ref, S) <= 1.0
+
+
+# ------------------------------------------------------------------ full-size workloads
+
+@pytest.mark.parametrize("fmt", ["f16", "bf16"])
+def test_square_4096_full_oracle(fmt):
+    case = si.square_case(4096, fmt=fmt)
+    D = run_gemm_ex(case["A"], case["B"], torch.bfloat16)
+    ref, S = oracle_ref(case["A"], case["B"])
+    assert ratio(D, ref, S) <= 1.0
+
+
+@pytest.mark.parametrize("M,N,K", [(8192, 28672, 8192), (8192, 8192, 28672), (8192, 24576, 8192),
+                                   (16, 28672, 8192)])
+def test_llm_shapes_sampled(M, N, K):
+    case = si.llm_case(M, N, K)
+    D = run_gemm_ex(case["A"], case["B"], torch.bfloat16)
+    rows, cols = sample_indices(M, N)
+    ref, S = oracle_ref(case["A"], case["B"], rows=rows, cols=cols)
+    assert ratio(D, ref, S, rows=rows, cols=cols) <= 1.0
+    assert not torch.isnan(D).any()
+
+
+@pytest.mark.parametrize("fb", ["e4m3", "e5m2"])
+def test_fp8_8192_sampled(fb):
+    case = si.fp8_case(b_fmt=fb)
+    D = run_gemm_ex(case["A"], case["B"], torch.bfloat16, sa=case["sa"], sb=case["sb"], bias=case["bias"])
+    rows, cols = sample_indices(8192, 8192)
+    ref, S = oracle_ref(case["A"], case["B"], sa=case["sa"], sb=case["sb"], bias=case["bias"], rows=rows, cols=cols)
+    assert ratio(D, ref, S, scale=case["sa"] * case["sb"], rows=rows, cols=cols) <= 1.0
+    assert not torch.isnan(D).any()
