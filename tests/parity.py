@@ -14,14 +14,26 @@ def dev():
     return torch.device("cuda:0")
 
 
+def padded(t, device):
+    """Copy of 2-D ``t`` on ``device`` whose row pitch is rounded up to 16 bytes (a view of a wider buffer)."""
+    rows, cols = t.shape
+    per = max(1, 16 // t.element_size())
+    pitch = max(per, -(-cols // per) * per)
+    if pitch == cols:
+        return t.to(device).contiguous()
+    buf = torch.zeros((rows, pitch), dtype=t.dtype, device=device)
+    buf[:, :cols] = t.to(device)
+    return buf[:, :cols]
+
+
 def run_gemm_ex(A, B, out_dtype, *, C=None, alpha=1.0, beta=0.0, sa=None, sb=None, bias=None,
                 fill=float("nan")):
     """Run tcm_gemm_ex on CPU tensors moved to the GPU; D is pre-filled with NaN."""
     d = dev()
-    Ad, Bd = A.to(d), B.to(d)
+    Ad, Bd = padded(A, d), padded(B, d)
     M, N = A.shape[0], B.shape[0]
-    D = torch.full((M, N), fill, dtype=out_dtype, device=d)
-    Cd = None if C is None else C.to(d)
+    D = padded(torch.full((M, N), fill, dtype=out_dtype), d)
+    Cd = None if C is None else padded(C, d)
     sad = None if sa is None else torch.tensor([sa], dtype=torch.float32, device=d)
     sbd = None if sb is None else torch.tensor([sb], dtype=torch.float32, device=d)
     biasd = None if bias is None else bias.to(d)
