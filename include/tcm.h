@@ -178,6 +178,27 @@ tcm_status tcm_clear_device_status(void);
  */
 void tcm_set_timeout_ns(uint64_t ns);
 
+/*
+ * Tuning / testing knob: force the CTA group (1 = one CTA per 128-row tile,
+ * 2 = a CTA pair per 256-row tile) and the tile width (32, 64, 128 or 256
+ * columns) of later dense GEMM launches in this process.  0 keeps the
+ * automatic choice; combinations the kernels do not provide fall back to it
+ * (a CTA pair needs 256-wide tiles).  Results are the same either way, up to
+ * the order of the fp32 accumulation.
+ */
+void tcm_set_config_override(int cta_group, int tile_n);
+
+/*
+ * Test hook for the device-side failure path: with mask bit 1 set, the next
+ * dense GEMM launch (only that one) has its loader skip the first shared-
+ * memory stage, so the waits for that stage run out after the time limit
+ * (tcm_set_timeout_ns): the kernel records TCM_ERR_TIMEOUT at the site of the
+ * first wait to give up (2, the MMA issuer, or 4, the epilogue waiting for
+ * the same tile), winds down and returns.  D is left partly unwritten.  No memory outside
+ * the kernel's own buffers is touched.
+ */
+void tcm_debug_fail_next_launch(int mask);
+
 /* Human-readable name of a status code (static storage). */
 const char *tcm_status_string(tcm_status status);
 

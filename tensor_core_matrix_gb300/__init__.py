@@ -28,7 +28,7 @@ DTYPE_CODE = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2,
 # Symbols the C ABI (include/tcm.h) exports.
 EXPORTS = ("tcm_gemm", "tcm_gemm_ex", "tcm_sp_compress", "tcm_sp_decompress", "tcm_gemm_sp",
            "tcm_get_device_status", "tcm_clear_device_status", "tcm_set_timeout_ns",
-           "tcm_status_string", "tcm_version")
+           "tcm_status_string", "tcm_version", "tcm_set_config_override", "tcm_debug_fail_next_launch")
 
 
 class TcmError(RuntimeError):
@@ -67,6 +67,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.tcm_clear_device_status.argtypes = []
     lib.tcm_set_timeout_ns.restype = None
     lib.tcm_set_timeout_ns.argtypes = [ctypes.c_uint64]
+    lib.tcm_set_config_override.restype = None
+    lib.tcm_set_config_override.argtypes = [i32, i32]
+    lib.tcm_debug_fail_next_launch.restype = None
+    lib.tcm_debug_fail_next_launch.argtypes = [i32]
     lib.tcm_status_string.restype = ctypes.c_char_p
     lib.tcm_status_string.argtypes = [i32]
     lib.tcm_version.restype = i32
@@ -193,6 +197,16 @@ def tcm_clear_device_status():
 
 def tcm_set_timeout_ns(ns: int):
     load_library().tcm_set_timeout_ns(int(ns))
+
+
+def tcm_set_config_override(cta_group: int = 0, tile_n: int = 0):
+    """Force the CTA group (1 or 2) and tile width of later GEMMs; 0, 0 restores the automatic choice."""
+    load_library().tcm_set_config_override(int(cta_group), int(tile_n))
+
+
+def tcm_debug_fail_next_launch(mask: int = 1):
+    """Test hook: the next GEMM launch skips its first load and times out (see include/tcm.h)."""
+    load_library().tcm_debug_fail_next_launch(int(mask))
 
 
 def tcm_status_string(status: int) -> str:

@@ -49,6 +49,9 @@ static int sm_count()
 }
 
 static std::atomic<unsigned long long> g_timeout_ns{0};
+static std::atomic<int> g_force_cta_group{0};
+static std::atomic<int> g_force_bn{0};
+static std::atomic<int> g_fault_once{0};
 
 static unsigned long long timeout_ns()
 {
@@ -136,6 +139,14 @@ int tcm_version(void) { return 100; }
 
 void tcm_set_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns); }
 
+void tcm_set_config_override(int cta_group, int tile_n)
+{
+    g_force_cta_group.store(cta_group);
+    g_force_bn.store(tile_n);
+}
+
+void tcm_debug_fail_next_launch(int mask) { g_fault_once.store(mask); }
+
 tcm_status tcm_gemm_ex(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const void *A, int64_t lda,
                        tcm_dtype b_dtype, const void *B, int64_t ldb, const void *C, int64_t ldc, void *D,
                        int64_t ldd, tcm_dtype out_dtype, float alpha, float beta, const float *a_scale,
@@ -165,20 +176,27 @@ tcm_status tcm_gemm_ex(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const
     // ---- configuration: swap A and B for skinny M so the weight fills the 128-row MMA
     const bool swap = M <= 64 && N >= 128;
     const int64_t kM = swap ? N : M, kN = swap ? M : N;
+    const int64_t sms = sm_count();
+    if (sms <= 0) return TCM_ERR_CUDA;
     GemmConfig cfg{};
     cfg.kind = kind;
+    cfg.cta_group = 1;
     if (swap) cfg.bn = kN <= 32 ? 32 : 64;
     else if (kN <= 32) cfg.bn = 32;
     else if (kN <= 64) cfg.bn = 64;
     else if (kN <= 128) cfg.bn = 128;
     else {
-        // prefer 256-wide tiles unless 128-wide ones fill clearly more of the GPU
-        const int64_t sms = sm_count();
-        const int64_t t256 = ((kM + 127) / 128) * ((kN + 255) / 256);
+        cfg.bn = 256;
+        // 256 x 256 pair tiles when they still give every CTA pair work
+        const int64_t pair_tiles = ((kM + 255) / 256) * ((kN + 255) / 256);
         const int64_t t128 = ((kM + 127) / 128) * ((kN + 127) / 128);
-        cfg.bn = (t256 < sms / 2 && t128 > t256) ? 128 : 256;
+        if (kM > 128 && pair_tiles >= sms / 2) cfg.cta_group = 2;
+        else if (((kM + 127) / 128) * ((kN + 255) / 256) < sms / 2 && t128 > pair_tiles) cfg.bn = 128;
     }
-    cfg.stages = 0;
+    const int force_cg = g_force_cta_group.load(), force_bn = g_force_bn.load();
+    if (force_cg == 1 || force_cg == 2) cfg.cta_group = force_cg;
+    if (force_bn == 32 || force_bn == 64 || force_bn == 128 || force_bn == 256) cfg.bn = force_bn;
+    if (cfg.cta_group == 2 && (cfg.bn != 256 || swap)) cfg.cta_group = 1;
 
     // ---- tensor maps (the kernel's "A" operand is the swapped one when swap)
     const int k_elems_stage = kind == 1 ? 128 : 64;
@@ -194,7 +212,7 @@ tcm_status tcm_gemm_ex(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const
         if (!encode_kmajor(&tmA, opA, eA, kdim, static_cast<uint64_t>(kM), static_cast<uint64_t>(ldA), 128))
             return TCM_ERR_CUDA;
         if (!encode_kmajor(&tmB, opB, eB, kdim, static_cast<uint64_t>(kN), static_cast<uint64_t>(ldB),
-                           static_cast<uint32_t>(cfg.bn)))
+                           static_cast<uint32_t>(cfg.bn / cfg.cta_group)))
             return TCM_ERR_CUDA;
     }
 
@@ -204,7 +222,7 @@ tcm_status tcm_gemm_ex(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const
     p.kN = static_cast<int>(kN);
     p.K = static_cast<int>(K);
     p.num_kb = static_cast<int>((K + k_elems_stage - 1) / k_elems_stage);
-    p.tiles_m = static_cast<int>((kM + 127) / 128);
+    p.tiles_m = static_cast<int>((kM + 128 * cfg.cta_group - 1) / (128 * cfg.cta_group));
     p.tiles_n = static_cast<int>((kN + cfg.bn - 1) / cfg.bn);
     p.num_tiles = p.tiles_m * p.tiles_n;
     p.group_m = 16;
@@ -226,14 +244,14 @@ tcm_status tcm_gemm_ex(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const
     // kind::f16: 0 = f16, 1 = bf16; kind::f8f6f4: 0 = E4M3, 1 = E5M2
     const uint32_t codeA = kind == 0 ? (fa == TCM_BF16 ? 1u : 0u) : (fa == TCM_E5M2 ? 1u : 0u);
     const uint32_t codeB = kind == 0 ? (fb == TCM_BF16 ? 1u : 0u) : (fb == TCM_E5M2 ? 1u : 0u);
-    p.idesc = make_idesc(codeA, codeB, 128, static_cast<uint32_t>(cfg.bn));
+    p.idesc = make_idesc(codeA, codeB, 128u * static_cast<uint32_t>(cfg.cta_group), static_cast<uint32_t>(cfg.bn));
     p.timeout_ns = timeout_ns();
     p.status = device_status_ptr();
     if (!p.status) return TCM_ERR_CUDA;
 
-    const int sms = sm_count();
-    if (sms <= 0) return TCM_ERR_CUDA;
-    const int grid = p.num_tiles < sms ? p.num_tiles : sms;
+    p.fault_inject = g_fault_once.exchange(0);
+    const int64_t clusters = sms / cfg.cta_group;
+    const int grid = static_cast<int>((p.num_tiles < clusters ? p.num_tiles : clusters) * cfg.cta_group);
     const cudaError_t e = launch_gemm(cfg, tmA, tmB, nullptr, p, grid, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TCM_OK : TCM_ERR_CUDA;
 }
@@ -281,9 +299,72 @@ tcm_status tcm_gemm_sp(int64_t M, int64_t N, int64_t K, tcm_dtype dtype, const v
                        const void *B, const void *C, void *D, float alpha, float beta, tcm_dtype out_dtype,
                        tcm_stream_t stream)
 {
-    (void)M; (void)N; (void)K; (void)dtype; (void)A_comp; (void)meta; (void)B; (void)C; (void)D;
-    (void)alpha; (void)beta; (void)out_dtype; (void)stream;
-    return TCM_ERR_UNSUPPORTED;
+    if (dtype != TCM_BF16 && dtype != TCM_F16) return TCM_ERR_UNSUPPORTED;
+    if (out_dtype != TCM_BF16 && out_dtype != TCM_F16 && out_dtype != TCM_F32) return TCM_ERR_UNSUPPORTED;
+    if (M < 1 || N < 1 || K < 0 || K % 32 != 0) return TCM_ERR_INVALID_ARG;
+    if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2) return TCM_ERR_UNSUPPORTED;
+    if (!D || (K > 0 && (!A_comp || !meta || !B)) || (beta != 0.f && !C)) return TCM_ERR_INVALID_ARG;
+    const int eo = elem_bytes(out_dtype);
+    if ((A_comp && !aligned16(A_comp)) || (B && !aligned16(B)) || (meta && !aligned16(meta)) || !aligned16(D) ||
+        (C && !aligned16(C)))
+        return TCM_ERR_MISALIGNED;
+    if ((N * eo) % 16) return TCM_ERR_MISALIGNED;
+    const int64_t sms = sm_count();
+    if (sms <= 0) return TCM_ERR_CUDA;
+
+    GemmConfig cfg{};
+    cfg.kind = 2;
+    const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
+    cfg.cta_group = (M > 128 && N > 128 && pair_tiles >= sms / 2) ? 2 : 1;
+    const int force_cg = g_force_cta_group.load();
+    if (force_cg == 1 || force_cg == 2) cfg.cta_group = force_cg;
+    cfg.bn = cfg.cta_group == 2 ? 256 : 128;
+
+    CUtensorMap tmA, tmB;
+    std::memset(&tmA, 0, sizeof tmA);
+    std::memset(&tmB, 0, sizeof tmB);
+    if (K > 0) {
+        if (!encode_kmajor(&tmA, A_comp, 2, static_cast<uint64_t>(K / 2), static_cast<uint64_t>(M),
+                           static_cast<uint64_t>(K / 2), 128))
+            return TCM_ERR_CUDA;
+        if (!encode_kmajor(&tmB, B, 2, static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(K),
+                           static_cast<uint32_t>(cfg.bn / cfg.cta_group)))
+            return TCM_ERR_CUDA;
+    }
+    GemmParams p{};
+    p.kM = static_cast<int>(M);
+    p.kN = static_cast<int>(N);
+    p.K = static_cast<int>(K);
+    p.num_kb = static_cast<int>((K + 127) / 128);
+    p.tiles_m = static_cast<int>((M + 128 * cfg.cta_group - 1) / (128 * cfg.cta_group));
+    p.tiles_n = static_cast<int>((N + cfg.bn - 1) / cfg.bn);
+    p.num_tiles = p.tiles_m * p.tiles_n;
+    p.group_m = 16;
+    p.tile_begin = 0;
+    p.tile_end = p.num_tiles;
+    p.D = D;
+    p.ldd = N;
+    p.C = beta != 0.f ? C : nullptr;
+    p.ldc = N;
+    p.bias = nullptr;
+    p.a_scale = p.b_scale = nullptr;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.out_fmt = static_cast<int>(out_dtype);
+    p.swap_ab = 0;
+    const uint32_t code = dtype == TCM_BF16 ? 1u : 0u;
+    p.idesc = make_idesc(code, code, 128u * static_cast<uint32_t>(cfg.cta_group), static_cast<uint32_t>(cfg.bn)) |
+              (1u << 2); // sparsity enabled
+    p.timeout_ns = timeout_ns();
+    p.status = device_status_ptr();
+    if (!p.status) return TCM_ERR_CUDA;
+    p.fault_inject = 0;
+    p.meta = meta;
+    p.meta_ld = K / 32;
+    const int64_t clusters = sms / cfg.cta_group;
+    const int grid = static_cast<int>((p.num_tiles < clusters ? p.num_tiles : clusters) * cfg.cta_group);
+    const cudaError_t e = launch_gemm_sp(cfg, tmA, tmB, p, grid, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TCM_OK : TCM_ERR_CUDA;
 }
 
 tcm_status tcm_get_device_status(tcm_stream_t stream, int32_t *code, int32_t *site)

@@ -19,6 +19,8 @@ enum WaitSite : int {
     SITE_MMA_ACC_EMPTY = 3,
     SITE_EPI_ACC_FULL = 4,
     SITE_DRAIN = 5,
+    SITE_MMA_META = 6,   // sparse: issuer waiting for a stage's metadata in TMEM
+    SITE_META_EMPTY = 7, // sparse: metadata warps waiting for a free stage
 };
 
 // Everything a GEMM kernel needs besides its tensor maps.  "Kernel" rows and
@@ -43,19 +45,30 @@ struct GemmParams {
     uint32_t idesc;
     unsigned long long timeout_ns;
     int *status;              // device status word pair {code, site}
+    int fault_inject;         // test hook (FaultBits); 0 in normal launches
+    const uint32_t *meta;     // sparse: 2:4 metadata, kM x meta_ld words (library layout)
+    long long meta_ld;        // sparse: words per metadata row (K / 32)
+};
+
+// Test hook bits: make a pipeline wait run out without touching memory.
+enum FaultBits : int {
+    FAULT_SKIP_FIRST_LOAD = 1, // the loader never issues (nor announces) its first stage
 };
 
 // Which kernel variant a launch uses.
 struct GemmConfig {
-    int kind;    // 0 = kind::f16, 1 = kind::f8f6f4, 2 = sparse kind::f16
-    int bn;      // N tile (columns of the accumulator)
-    int stages;  // shared-memory ring depth
+    int kind;      // 0 = kind::f16, 1 = kind::f8f6f4, 2 = sparse kind::f16
+    int bn;        // N tile (columns of the accumulator)
+    int cta_group; // 1 = one CTA per 128-row tile, 2 = CTA pair per 256-row tile
 };
 
 cudaError_t launch_gemm(const GemmConfig &cfg, const CUtensorMap &tmA, const CUtensorMap &tmB,
                         const CUtensorMap *tmMeta, const GemmParams &p, int grid, cudaStream_t stream);
 
-size_t gemm_smem_bytes(const GemmConfig &cfg);
+int gemm_stages(const GemmConfig &cfg);
+
+cudaError_t launch_gemm_sp(const GemmConfig &cfg, const CUtensorMap &tmA, const CUtensorMap &tmB,
+                           const GemmParams &p, int grid, cudaStream_t stream);
 
 cudaError_t launch_sp_compress(int64_t M, int64_t K, int elem_bytes, const void *A, int64_t lda, void *Ac,
                                uint32_t *meta, cudaStream_t stream);

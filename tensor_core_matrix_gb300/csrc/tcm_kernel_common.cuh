@@ -1,0 +1,207 @@
+// tcm_kernel_common.cuh -- pieces shared by the dense and the 2:4-sparse
+// tcgen05 GEMM kernels: shared-memory ring layout, bounded mbarrier waits
+// that record a device status instead of hanging, the grouped tile order,
+// and the epilogue (alpha*sA*sB*acc + beta*C + bias, RNE cast, stores).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "tcm_internal.h"
+#include "tcm_ptx.cuh"
+
+namespace tcm {
+
+constexpr int BM = 128;
+constexpr int TILE_K_BYTES = 128; // one 128-byte swizzle atom of K per stage
+constexpr int A_STAGE_BYTES = BM * TILE_K_BYTES;
+constexpr int NUM_THREADS = 192;
+constexpr int EPI_WARPS = 4;
+constexpr unsigned long long kMaxSpin = 1ull << 34;
+
+template <int BN, int STAGES>
+struct Smem {
+    static constexpr int B_STAGE = BN * TILE_K_BYTES;
+    static constexpr int A_OFF = 0;
+    static constexpr int B_OFF = STAGES * A_STAGE_BYTES;
+    static constexpr int BAR_OFF = B_OFF + STAGES * B_STAGE;
+    static constexpr int NUM_BARS = 2 * STAGES + 5; // full, empty, tfull[2], tempty[2], drain
+    static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
+    static constexpr int BYTES = MISC_OFF + 16;
+    static constexpr int ALLOC = BYTES + 1024; // slack to align the base to 1024
+};
+
+struct Waiter {
+    volatile int *abort_flag;
+    unsigned long long timeout_ns;
+    int *status;
+};
+
+__device__ __forceinline__ void record_timeout(const Waiter &w, int site)
+{
+    *w.abort_flag = 1;
+    if (atomicCAS(w.status, DEV_OK, DEV_TIMEOUT) == DEV_OK) atomicExch(w.status + 1, site);
+}
+
+// Wait for phase `parity` of `bar`; false if the CTA is aborting or the limit expired.
+template <int CG>
+__device__ __noinline__ bool bounded_wait(uint64_t *bar, uint32_t parity, const Waiter &w, int site, bool honour_abort)
+{
+    const uint32_t addr = smem_u32(bar);
+    auto try_once = [&]() { return CG == 2 ? mbar_try_wait_cluster(addr, parity) : mbar_try_wait(addr, parity); };
+    if (try_once()) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (unsigned long long it = 1; it < kMaxSpin; ++it) {
+        if (try_once()) return true;
+        if ((it & 31ull) == 0) {
+            if (honour_abort && *w.abort_flag) return false;
+            if (globaltimer_ns() - t0 > w.timeout_ns) break;
+        }
+    }
+    record_timeout(w, site);
+    return false;
+}
+
+__device__ __forceinline__ void tile_coords(const GemmParams &p, int t, int &mb, int &nb)
+{
+    const int group = p.group_m * p.tiles_n;
+    const int gid = t / group;
+    const int first = gid * p.group_m;
+    const int gm = min(p.tiles_m - first, p.group_m);
+    const int r = t - gid * group;
+    mb = first + r % gm;
+    nb = r / gm;
+}
+
+__device__ __forceinline__ float ld_elem(const void *base, long long i, int fmt)
+{
+    if (fmt == OUT_BF16) return __bfloat162float(static_cast<const __nv_bfloat16 *>(base)[i]);
+    if (fmt == OUT_F16) return __half2float(static_cast<const __half *>(base)[i]);
+    return static_cast<const float *>(base)[i];
+}
+
+__device__ __forceinline__ void st_elem(void *base, long long i, int fmt, float v)
+{
+    if (fmt == OUT_BF16) static_cast<__nv_bfloat16 *>(base)[i] = __float2bfloat16_rn(v);
+    else if (fmt == OUT_F16) static_cast<__half *>(base)[i] = __float2half_rn(v);
+    else static_cast<float *>(base)[i] = v;
+}
+
+// 32 consecutive elements starting at a 16-byte-aligned address.
+__device__ __forceinline__ void ld32(const void *base, long long i, int fmt, float (&v)[32])
+{
+    if (fmt == OUT_F32) {
+        const float4 *q = reinterpret_cast<const float4 *>(static_cast<const float *>(base) + i);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float4 x = q[j];
+            v[4 * j] = x.x, v[4 * j + 1] = x.y, v[4 * j + 2] = x.z, v[4 * j + 3] = x.w;
+        }
+    } else {
+        const uint4 *q = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(base) + i);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint4 x = q[j];
+            const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                if (fmt == OUT_BF16) {
+                    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&w[h]);
+                    v[8 * j + 2 * h] = __low2float(b), v[8 * j + 2 * h + 1] = __high2float(b);
+                } else {
+                    const __half2 b = *reinterpret_cast<const __half2 *>(&w[h]);
+                    v[8 * j + 2 * h] = __low2float(b), v[8 * j + 2 * h + 1] = __high2float(b);
+                }
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void st32(void *base, long long i, int fmt, const float (&v)[32])
+{
+    if (fmt == OUT_F32) {
+        float4 *q = reinterpret_cast<float4 *>(static_cast<float *>(base) + i);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) q[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    } else {
+        uint4 *q = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(base) + i);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint32_t w[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                if (fmt == OUT_BF16) {
+                    const __nv_bfloat162 b = __floats2bfloat162_rn(v[8 * j + 2 * h], v[8 * j + 2 * h + 1]);
+                    w[h] = *reinterpret_cast<const uint32_t *>(&b);
+                } else {
+                    const __half2 b = __floats2half2_rn(v[8 * j + 2 * h], v[8 * j + 2 * h + 1]);
+                    w[h] = *reinterpret_cast<const uint32_t *>(&b);
+                }
+            }
+            q[j] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+}
+
+// Epilogue of 32 accumulator columns of one kernel row: out = scale*acc + beta*C + bias.
+__device__ __forceinline__ void epilogue_row32(const GemmParams &p, float scale, int row, int col0,
+                                               const uint32_t (&r)[32])
+{
+    if (row >= p.kM) return;
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = scale * __uint_as_float(r[j]);
+    if (!p.swap_ab) {
+        const long long doff = static_cast<long long>(row) * p.ldd + col0;
+        if (col0 + 32 <= p.kN) {
+            if (p.beta != 0.f) {
+                float c[32];
+                ld32(p.C, static_cast<long long>(row) * p.ldc + col0, p.out_fmt, c);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = fmaf(p.beta, c[j], v[j]);
+            }
+            if (p.bias) {
+                float b[32];
+                ld32(p.bias, col0, p.out_fmt, b);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] += b[j];
+            }
+            st32(p.D, doff, p.out_fmt, v);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int col = col0 + j;
+                if (col < p.kN) {
+                    float x = v[j];
+                    if (p.beta != 0.f)
+                        x = fmaf(p.beta, ld_elem(p.C, static_cast<long long>(row) * p.ldc + col, p.out_fmt), x);
+                    if (p.bias) x += ld_elem(p.bias, col, p.out_fmt);
+                    st_elem(p.D, doff + j, p.out_fmt, x);
+                }
+            }
+        }
+    } else {
+        // kernel row = column n of D, kernel column = row m of D
+        const float b = p.bias ? ld_elem(p.bias, row, p.out_fmt) : 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const int m = col0 + j;
+            if (m < p.kN) {
+                float x = v[j];
+                if (p.beta != 0.f) x = fmaf(p.beta, ld_elem(p.C, static_cast<long long>(m) * p.ldc + row, p.out_fmt), x);
+                x += b;
+                st_elem(p.D, static_cast<long long>(m) * p.ldd + row, p.out_fmt, x);
+            }
+        }
+    }
+}
+
+// Wait on a barrier of this CTA; pair kernels use cluster-scope acquire
+// because the arrivals can come from the peer CTA.
+template <int CG>
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, const Waiter &w, int site, bool honour_abort)
+{
+    return bounded_wait<CG>(bar, parity, w, site, honour_abort);
+}
+
+} // namespace tcm

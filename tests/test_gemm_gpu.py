@@ -85,6 +85,66 @@ def test_rank1_closed_form():
     assert torch.equal(D, 0.5 * K * torch.outer(u, v))
 
 
+# ------------------------------------------------------------------ every kernel variant
+
+@pytest.fixture
+def override():
+    import tensor_core_matrix_gb300 as tcm
+    yield tcm
+    tcm.tcm_set_config_override(0, 0)
+
+
+@pytest.mark.parametrize("cg,bn", [(1, 256), (1, 128), (1, 64), (1, 32), (2, 256)])
+@pytest.mark.parametrize("M,N,K", [(256, 256, 64), (512, 768, 320), (300, 520, 136), (1000, 1030, 1024)])
+def test_each_variant_integer_exact(override, cg, bn, M, N, K):
+    override.tcm_set_config_override(cg, bn)
+    g = si.generator(M + N + K + cg + bn)
+    A = si.integers((M, K), g)
+    B = si.integers((N, K), g)
+    D = run_gemm_ex(A, B, torch.float32)
+    ref, _ = oracle_ref(A, B)
+    assert np.array_equal(D.double().numpy(), ref)
+
+
+@pytest.mark.parametrize("cg,bn", [(1, 256), (2, 256), (1, 128)])
+@pytest.mark.parametrize("fb", ["e4m3", "e5m2"])
+def test_each_variant_fp8_bound(override, cg, bn, fb):
+    override.tcm_set_config_override(cg, bn)
+    case = si.fp8_case(640, 768, 1024, b_fmt=fb, seed=3)
+    D = run_gemm_ex(case["A"], case["B"], torch.bfloat16, sa=case["sa"], sb=case["sb"], bias=case["bias"])
+    ref, S = oracle_ref(case["A"], case["B"], sa=case["sa"], sb=case["sb"], bias=case["bias"])
+    assert ratio(D, ref, S, scale=case["sa"] * case["sb"]) <= 1.0
+
+
+@pytest.mark.parametrize("cg", [1, 2])
+def test_pipeline_timeout_is_reported_and_context_stays_usable(override, cg):
+    """A wait that nothing will satisfy runs out, is reported, and the next launch is correct."""
+    tcm = override
+    override.tcm_set_config_override(cg, 256)
+    d = dev()
+    g = si.generator(77)
+    A = si.integers((512, 256), g)
+    B = si.integers((512, 256), g)
+    Ad, Bd = A.to(d), B.to(d)
+    D = torch.zeros((512, 512), dtype=torch.float32, device=d)
+    tcm.tcm_clear_device_status()
+    tcm.tcm_set_timeout_ns(50_000_000)
+    try:
+        tcm.tcm_debug_fail_next_launch(1)
+        tcm.tcm_gemm_ex(Ad, Bd, D)
+        code, site = tcm.tcm_get_device_status()
+        # whichever wait on the starved stage gives up first: the issuer's (2)
+        # or the epilogue's, which waits for the same tile (4)
+        assert code == 5 and site in (2, 4)
+    finally:
+        tcm.tcm_set_timeout_ns(0)
+        tcm.tcm_clear_device_status()
+    tcm.tcm_gemm_ex(Ad, Bd, D)
+    assert tcm.tcm_get_device_status() == (0, 0)
+    ref, _ = oracle_ref(A, B)
+    assert np.array_equal(D.cpu().double().numpy(), ref)
+
+
 # ------------------------------------------------------------------ configured workloads
 
 def test_small_config_512_bf16_with_c_and_16x8x16_tile():
