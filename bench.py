@@ -5,9 +5,10 @@ input at M = N = K = 8192:
   * bf16 x bf16 -> fp32 accumulate -> bf16 D (alpha = 1, beta = 0)
   * E4M3 x E4M3 with per-tensor fp32 dequantisation scales and a bf16 bias
     -> bf16 D
-  * 2:4 structured-sparse bf16 A: compress of the logical A plus the sparse
-    GEMM (logical FLOPs), once that path is available in the library
-value = sum of 2*M*N*K over the step's GEMMs / step time (TFLOP/s).
+  * 2:4 structured-sparse bf16 A: compress of the logical A (keep the two
+    largest of every four along K, ordered metadata) plus the sparse GEMM,
+    counted at its logical 2*M*N*K
+value = sum of 2*M*N*K over the step's three GEMMs / step time (TFLOP/s).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tcm|reference]
 
@@ -53,6 +54,9 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--shapes", action="store_true",
+                    help="instead of the step, time every configured workload shape (one JSON line each)")
+    ap.add_argument("--shape-iters", type=int, default=20)
     return ap.parse_args()
 
 
@@ -158,65 +162,85 @@ def make_inputs(device):
     """Resident device inputs of one step plus their pinned host copies (for the end-to-end leg)."""
     dense = si.llm_case(SIZE, SIZE, SIZE, seed=2)  # bf16 A ~ N(0,1), B ~ N(0, 0.02)
     f8 = si.fp8_case(SIZE, SIZE, SIZE, b_fmt="e4m3", seed=3)
+    sp = si.sparse_case(SIZE, SIZE, SIZE, seed=4)
     host = {
         "A": dense["A"], "B": dense["B"],
         "A8": f8["A"], "B8": f8["B"], "bias": f8["bias"],
         "sa": torch.tensor([f8["sa"]], dtype=torch.float32), "sb": torch.tensor([f8["sb"]], dtype=torch.float32),
+        "Asp": sp["A_logical"], "Bsp": sp["B"],
     }
     pinned = {k: v.pin_memory() for k, v in host.items()}
     dev = {k: v.to(device) for k, v in host.items()}
-    dev["D"] = torch.empty((SIZE, SIZE), dtype=torch.bfloat16, device=device)
-    dev["D8"] = torch.empty((SIZE, SIZE), dtype=torch.bfloat16, device=device)
+    for k in ("D", "D8", "Dsp"):
+        dev[k] = torch.empty((SIZE, SIZE), dtype=torch.bfloat16, device=device)
+    dev["Ac"] = torch.empty((SIZE, SIZE // 2), dtype=torch.bfloat16, device=device)
+    dev["meta"] = torch.empty((SIZE, SIZE // 32), dtype=torch.int32, device=device)
     return host, pinned, dev
 
 
 def run_step(tcm, dev, stream, events=None):
-    """One pass of the hot path; events = (e0, e1, e2) brackets the two GEMMs on `stream`."""
-    if events:
-        events[0].record(stream)
+    """One pass of the hot path; events[0..4] bracket the four launches on `stream`."""
+    def mark(i):
+        if events:
+            events[i].record(stream)
+    mark(0)
     tcm.tcm_gemm_ex(dev["A"], dev["B"], dev["D"], stream=stream)
-    if events:
-        events[1].record(stream)
+    mark(1)
     tcm.tcm_gemm_ex(dev["A8"], dev["B8"], dev["D8"], a_scale=dev["sa"], b_scale=dev["sb"], bias=dev["bias"],
                     stream=stream)
-    if events:
-        events[2].record(stream)
+    mark(2)
+    tcm.tcm_sp_compress(dev["Asp"], dev["Ac"], dev["meta"], stream=stream)
+    mark(3)
+    tcm.tcm_gemm_sp(dev["Ac"], dev["meta"], dev["Bsp"], dev["Dsp"], stream=stream)
+    mark(4)
 
 
-KERNELS_PER_STEP = 2
+KERNELS_PER_STEP = 4
+GEMMS_PER_STEP = 3
+COMPRESS_BYTES = SIZE * SIZE * 2 + SIZE * (SIZE // 2) * 2 + SIZE * (SIZE // 32) * 4
+
+
+class OracleSample:
+    """The CPU oracle on whole output rows of the step's three GEMMs (and the 2:4 compress of those rows)."""
+
+    def __init__(self, host):
+        import oracle
+        self.oracle = oracle
+        oracle.build()
+        self.a, self.b = si.codes(host["A"]), si.codes(host["B"])
+        self.a8, self.b8, self.bias = si.codes(host["A8"]), si.codes(host["B8"]), si.codes(host["bias"])
+        self.sa, self.sb = float(host["sa"][0]), float(host["sb"][0])
+        self.asp, self.bsp = si.codes(host["Asp"]), si.codes(host["Bsp"])
+
+    def rows(self, r):
+        import numpy as np
+        o = self.oracle
+        rows = np.repeat(np.arange(r, dtype=np.int64), SIZE)
+        cols = np.tile(np.arange(SIZE, dtype=np.int64), r)
+        o.gemm(self.a, self.b, "bf16", "bf16", rows=rows, cols=cols)
+        o.gemm(self.a8, self.b8, "e4m3", "e4m3", bias=self.bias, sa=self.sa, sb=self.sb, rows=rows, cols=cols)
+        ac, meta = o.sp_compress(np.ascontiguousarray(self.asp[:r]), "bf16")
+        o.gemm(o.sp_decompress(ac, meta, "bf16"), self.bsp, "bf16", "bf16", rows=rows, cols=cols)
+        return GEMMS_PER_STEP * 2.0 * r * SIZE * SIZE
+
+    def calibrate(self, seconds):
+        t0 = time.perf_counter()
+        self.rows(1)
+        per_row = max(time.perf_counter() - t0, 1e-6)
+        return max(1, int(seconds / per_row))
 
 
 def cpu_baseline_sample(host, seconds):
-    """Time the CPU oracle on whole output rows of the step's two GEMMs for about `seconds`."""
-    import numpy as np
-
-    import oracle
-
-    a, b = si.codes(host["A"]), si.codes(host["B"])
-    a8, b8, bias = si.codes(host["A8"]), si.codes(host["B8"]), si.codes(host["bias"])
-    sa, sb = float(host["sa"][0]), float(host["sb"][0])
-
-    def rows_run(r, gemm):
-        rows = np.repeat(np.arange(r, dtype=np.int64), SIZE)
-        cols = np.tile(np.arange(SIZE, dtype=np.int64), r)
-        if gemm == 0:
-            oracle.gemm(a, b, "bf16", "bf16", rows=rows, cols=cols)
-        else:
-            oracle.gemm(a8, b8, "e4m3", "e4m3", bias=bias, sa=sa, sb=sb, rows=rows, cols=cols)
-
+    """Time the CPU oracle on about `seconds` of whole output rows of the step's GEMMs."""
+    o = OracleSample(host)
+    r = o.calibrate(seconds)
     t0 = time.perf_counter()
-    rows_run(1, 0)
-    rows_run(1, 1)
-    per_pair = max(time.perf_counter() - t0, 1e-6)
-    r = max(1, int(seconds / per_pair))
-    t0 = time.perf_counter()
-    rows_run(r, 0)
-    rows_run(r, 1)
+    flop = o.rows(r)
     t = time.perf_counter() - t0
-    flop = 2 * (2.0 * r * SIZE * SIZE)
     cores = len(os.sched_getaffinity(0))
     return {"value": flop / t / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-            "sample": f"{r} full output rows (8192 outputs of K=8192 each) of the bf16 and of the E4M3 GEMM, "
+            "sample": f"{r} full output rows (8192 outputs of K=8192 each) of each of the step's three GEMMs "
+                      f"(bf16, E4M3 with scales+bias, 2:4-sparse bf16 incl. compress of those rows), "
                       f"{t:.1f} s on {cores} host threads (OpenMP)"}
 
 
@@ -224,52 +248,113 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    import numpy as np
-
-    import oracle
-    oracle.build()
     dense = si.llm_case(SIZE, SIZE, SIZE, seed=2)
     f8 = si.fp8_case(SIZE, SIZE, SIZE, b_fmt="e4m3", seed=3)
-    a, b = si.codes(dense["A"]), si.codes(dense["B"])
-    a8, b8, bias = si.codes(f8["A"]), si.codes(f8["B"]), si.codes(f8["bias"])
+    sp = si.sparse_case(SIZE, SIZE, SIZE, seed=4)
+    host = {"A": dense["A"], "B": dense["B"], "A8": f8["A"], "B8": f8["B"], "bias": f8["bias"],
+            "sa": torch.tensor([f8["sa"]]), "sb": torch.tensor([f8["sb"]]),
+            "Asp": sp["A_logical"], "Bsp": sp["B"]}
+    o = OracleSample(host)
     cores = len(os.sched_getaffinity(0))
-
-    def step(r):
-        rows = np.repeat(np.arange(r, dtype=np.int64), SIZE)
-        cols = np.tile(np.arange(SIZE, dtype=np.int64), r)
-        oracle.gemm(a, b, "bf16", "bf16", rows=rows, cols=cols)
-        oracle.gemm(a8, b8, "e4m3", "e4m3", bias=bias, sa=f8["sa"], sb=f8["sb"], rows=rows, cols=cols)
-
-    t0 = time.perf_counter()
-    step(1)
-    per_row = max(time.perf_counter() - t0, 1e-6)
-    budget = 90.0 / max(1, args.steps + args.warmup)
-    r = max(1, int(budget / per_row))
+    r = o.calibrate(90.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
-        step(r)
+        o.rows(r)
     t0 = time.perf_counter()
+    flop = 0.0
     for _ in range(args.steps):
-        step(r)
+        flop += o.rows(r)
     t = time.perf_counter() - t0
-    value = args.steps * 2 * (2.0 * r * SIZE * SIZE) / t / 1e12
+    value = flop / t / 1e12
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16+e4m3",
         "data": "synthetic", "config": config_block(world),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": f"each step: {r} full output rows of the bf16 and of the E4M3 8192^3 GEMM "
+                         "sample": f"each step: {r} full output rows of each of the three 8192^3 GEMMs "
                                    f"(fp64 CPU oracle, {cores} host threads)"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
+def shape_cases():
+    """(name, builder) for every configured workload shape; builders return CPU inputs."""
+    return [
+        ("small bf16 512^3 +C fp32 (alpha=beta=1)", lambda: si.small_case()),
+        ("square fp16 4096^3", lambda: si.square_case(4096, "f16")),
+        ("square bf16 4096^3", lambda: si.square_case(4096, "bf16")),
+        ("llm bf16 8192x28672x8192", lambda: si.llm_case(8192, 28672, 8192)),
+        ("llm bf16 8192x8192x28672", lambda: si.llm_case(8192, 8192, 28672)),
+        ("llm bf16 8192x24576x8192", lambda: si.llm_case(8192, 24576, 8192)),
+        ("skinny bf16 16x28672x8192", lambda: si.llm_case(16, 28672, 8192)),
+        ("fp8 e4m3xe4m3 8192^3 +scales+bias", lambda: si.fp8_case(b_fmt="e4m3")),
+        ("fp8 e4m3xe5m2 8192^3 +scales+bias", lambda: si.fp8_case(b_fmt="e5m2")),
+        ("sparse 2:4 bf16 8192^3", lambda: si.sparse_case()),
+    ]
+
+
+def run_shapes(args, tcm, device, peaks_used):
+    """Median device time of each configured shape, L2 flushed before every timed launch."""
+    p, src = peaks_used
+    bf16_peak = float(p.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    hbm_peak = float(p.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    for name, build in shape_cases():
+        case = build()
+        sparse = "A_logical" in case
+        A = (case["A_logical"] if sparse else case["A"]).to(device)
+        B = case["B"].to(device)
+        M, K = A.shape
+        N = B.shape[0]
+        out_dtype = torch.float32 if case.get("out_fmt") == "f32" else torch.bfloat16
+        D = torch.empty((M, N), dtype=out_dtype, device=device)
+        C = case["C"].to(device) if case.get("C") is not None else None
+        kw = dict(C=C, alpha=case.get("alpha", 1.0), beta=case.get("beta", 0.0))
+        if "sa" in case:
+            kw.update(a_scale=torch.tensor([case["sa"]], device=device), b_scale=torch.tensor([case["sb"]], device=device),
+                      bias=case["bias"].to(device))
+        if sparse:
+            Ac, meta = tcm.tcm_sp_compress(A)
+            launch = lambda: tcm.tcm_gemm_sp(Ac, meta, B, D, C=C, alpha=kw["alpha"], beta=kw["beta"])
+        else:
+            launch = lambda: tcm.tcm_gemm_ex(A, B, D, **kw)
+        for _ in range(3):
+            launch()
+        times = []
+        for _ in range(args.shape_iters):
+            flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            launch()
+            e1.record(stream)
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1))
+        code, site = tcm.tcm_get_device_status()
+        ms = statistics.median(times)
+        flop = 2.0 * M * N * K
+        in_bytes = (A.numel() // (2 if sparse else 1)) * A.element_size() + B.numel() * B.element_size()
+        byts = in_bytes + D.numel() * D.element_size() + (C.numel() * C.element_size() if C is not None else 0)
+        tf = flop / (ms * 1e-3) / 1e12
+        gbs = byts / (ms * 1e-3) / 1e9
+        peak = bf16_peak * (FP8_OVER_BF16 if "fp8" in name else 1.0)
+        line = {"kind": "shape", "workload": name, "M": M, "N": N, "K": K, "ms_median": ms, "ms_min": min(times),
+                "tflops": tf, "frac_of_tensor_peak": tf / peak, "algorithmic_bytes": byts, "gbs": gbs,
+                "frac_of_hbm": gbs / hbm_peak, "bound": "hbm" if M <= 64 else "tensor", "device_status": code,
+                "timing": f"median of {args.shape_iters} launches, L2 flushed (256 MiB write) before each",
+                "peak_source": src}
+        print(json.dumps(line), flush=True)
+        del A, B, D, C, case
+
+
 def config_block(world):
-    return {"workload": "GEMM 8192^3 (M=N=K=8192): bf16 x bf16 -> bf16, and E4M3 x E4M3 with per-tensor "
-                        "scales + bf16 bias -> bf16; A row-major, B K-major, fp32 accumulate",
+    return {"workload": "GEMM 8192^3 (M=N=K=8192): bf16 x bf16 -> bf16; E4M3 x E4M3 with per-tensor "
+                        "scales + bf16 bias -> bf16; 2:4-sparse bf16 A (compress + sparse GEMM) -> bf16; "
+                        "A row-major, B K-major, fp32 accumulate",
             "M": SIZE, "N": SIZE, "K": SIZE,
-            "inputs": "bf16 A ~ N(0,1), B ~ N(0,0.02) (seed 2); E4M3 A, B ~ N(0,1) scaled so amax = 448 (seed 3)",
+            "inputs": "bf16 A ~ N(0,1), B ~ N(0,0.02) (seed 2); E4M3 A, B ~ N(0,1) scaled so amax = 448 (seed 3); "
+                      "sparse: logical A, B ~ N(0,1) bf16 (seed 4)",
             "l2": "no flush: each GEMM's inputs (256 MiB bf16, 128 MiB E4M3) exceed the 129 MB L2",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
@@ -299,6 +384,9 @@ def main():
     tcm.load_library()
     tcm.tcm_clear_device_status()
 
+    if args.shapes:
+        run_shapes(args, tcm, device, peaks())
+        return
     host, pinned, dev = make_inputs(device)
     stream = torch.cuda.Stream(device=device)
 
@@ -307,7 +395,7 @@ def main():
             run_step(tcm, dev, stream)
     stream.synchronize()
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     if pg:
         pg.barrier()
     torch.cuda.synchronize(device)
@@ -324,6 +412,8 @@ def main():
     elapsed_ms = t_start.elapsed_time(t_end)
     bf16_ms = [e[0].elapsed_time(e[1]) for e in ev]
     fp8_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    cmp_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    sp_ms = [e[3].elapsed_time(e[4]) for e in ev]
     code, site = tcm.tcm_get_device_status(stream)
     if code != 0:
         raise SystemExit(f"device status {code} at site {site}")
@@ -331,10 +421,9 @@ def main():
     # end-to-end: pinned host inputs -> device, the step, result -> host, every step
     e2e_ms = None
     h2d = sum(pinned[k].numel() * pinned[k].element_size() for k in pinned)
-    d2h = 2 * SIZE * SIZE * 2
+    d2h = 3 * SIZE * SIZE * 2
     if args.e2e_steps > 0:
-        outD = torch.empty((SIZE, SIZE), dtype=torch.bfloat16).pin_memory()
-        outD8 = torch.empty((SIZE, SIZE), dtype=torch.bfloat16).pin_memory()
+        outs = {k: torch.empty((SIZE, SIZE), dtype=torch.bfloat16).pin_memory() for k in ("D", "D8", "Dsp")}
         if pg:
             pg.barrier()
         torch.cuda.synchronize(device)
@@ -346,8 +435,8 @@ def main():
                 for k in pinned:
                     dev[k].copy_(pinned[k], non_blocking=True)
                 run_step(tcm, dev, stream)
-                outD.copy_(dev["D"], non_blocking=True)
-                outD8.copy_(dev["D8"], non_blocking=True)
+                for k in outs:
+                    outs[k].copy_(dev[k], non_blocking=True)
             e1.record(stream)
         e1.synchronize()
         e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
@@ -362,13 +451,18 @@ def main():
         p, src = peaks()
         bf16_peak = float(p.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
         ms_step = elapsed_ms / args.steps
-        flop_step = KERNELS_PER_STEP * FLOP_PER_GEMM
+        flop_step = GEMMS_PER_STEP * FLOP_PER_GEMM
         value = world * flop_step * args.steps / (elapsed_ms * 1e-3) / 1e12
         t_bf16 = statistics.mean(bf16_ms)
         t_fp8 = statistics.mean(fp8_ms)
         ach_bf16 = FLOP_PER_GEMM / (t_bf16 * 1e-3) / 1e12
         ach_fp8 = FLOP_PER_GEMM / (t_fp8 * 1e-3) / 1e12
         fp8_peak = bf16_peak * FP8_OVER_BF16
+        t_cmp = statistics.mean(cmp_ms)
+        t_sp = statistics.mean(sp_ms)
+        ach_sp = FLOP_PER_GEMM / (t_sp * 1e-3) / 1e12
+        hbm_peak = float(p.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        cmp_gbs = COMPRESS_BYTES / (t_cmp * 1e-3) / 1e9
         traffic = recorded_traffic()
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -377,6 +471,10 @@ def main():
             "parts": {
                 "bf16_dense": {"tflops": ach_bf16, "ms": t_bf16, "frac_of_bf16_peak": ach_bf16 / bf16_peak},
                 "e4m3_scaled_bias": {"tflops": ach_fp8, "ms": t_fp8, "frac_of_fp8_peak": ach_fp8 / fp8_peak},
+                "sp24_compress": {"gbs": cmp_gbs, "ms": t_cmp, "frac_of_hbm": cmp_gbs / hbm_peak,
+                                  "bytes": COMPRESS_BYTES},
+                "sp24_gemm_bf16": {"tflops_logical": ach_sp, "ms": t_sp,
+                                   "frac_of_dense_bf16_peak": ach_sp / bf16_peak},
             },
             "roofline": {"bound": "tensor", "achieved": ach_bf16, "peak": bf16_peak, "unit": "TFLOP/s",
                          "frac": ach_bf16 / bf16_peak, "traffic": traffic,

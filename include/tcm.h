@@ -179,14 +179,18 @@ tcm_status tcm_clear_device_status(void);
 void tcm_set_timeout_ns(uint64_t ns);
 
 /*
- * Tuning / testing knob: force the CTA group (1 = one CTA per 128-row tile,
- * 2 = a CTA pair per 256-row tile) and the tile width (32, 64, 128 or 256
- * columns) of later dense GEMM launches in this process.  0 keeps the
- * automatic choice; combinations the kernels do not provide fall back to it
- * (a CTA pair needs 256-wide tiles).  Results are the same either way, up to
- * the order of the fp32 accumulation.
+ * Tuning / testing knob for later GEMM launches in this process (0 keeps the
+ * automatic choice for that field):
+ *   cta_group  1 = one CTA per 128-row tile, 2 = a CTA pair per 256-row tile
+ *   tile_n     tile width in columns (dense: 32, 64, 128, 256; sparse: 128, 256)
+ *   stages     depth of the shared-memory ring (the kernels provide a few
+ *              depths per tile; others fall back to the default)
+ *   group_m    row blocks per rasterisation group (tiles that run at the same
+ *              time share rows of A and columns of B in L2)
+ * Combinations the kernels do not provide fall back to the automatic choice.
+ * Results are the same either way, up to the order of the fp32 accumulation.
  */
-void tcm_set_config_override(int cta_group, int tile_n);
+void tcm_set_config_override(int cta_group, int tile_n, int stages, int group_m);
 
 /*
  * Test hook for the device-side failure path: with mask bit 1 set, the next

@@ -51,6 +51,8 @@ static int sm_count()
 static std::atomic<unsigned long long> g_timeout_ns{0};
 static std::atomic<int> g_force_cta_group{0};
 static std::atomic<int> g_force_bn{0};
+static std::atomic<int> g_force_stages{0};
+static std::atomic<int> g_force_group_m{0};
 static std::atomic<int> g_fault_once{0};
 
 static unsigned long long timeout_ns()
@@ -139,10 +141,12 @@ int tcm_version(void) { return 100; }
 
 void tcm_set_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns); }
 
-void tcm_set_config_override(int cta_group, int tile_n)
+void tcm_set_config_override(int cta_group, int tile_n, int stages, int group_m)
 {
     g_force_cta_group.store(cta_group);
     g_force_bn.store(tile_n);
+    g_force_stages.store(stages);
+    g_force_group_m.store(group_m);
 }
 
 void tcm_debug_fail_next_launch(int mask) { g_fault_once.store(mask); }
@@ -197,6 +201,7 @@ tcm_status tcm_gemm_ex(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const
     if (force_cg == 1 || force_cg == 2) cfg.cta_group = force_cg;
     if (force_bn == 32 || force_bn == 64 || force_bn == 128 || force_bn == 256) cfg.bn = force_bn;
     if (cfg.cta_group == 2 && (cfg.bn != 256 || swap)) cfg.cta_group = 1;
+    cfg.stages = g_force_stages.load();
 
     // ---- tensor maps (the kernel's "A" operand is the swapped one when swap)
     const int k_elems_stage = kind == 1 ? 128 : 64;
@@ -225,7 +230,7 @@ tcm_status tcm_gemm_ex(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const
     p.tiles_m = static_cast<int>((kM + 128 * cfg.cta_group - 1) / (128 * cfg.cta_group));
     p.tiles_n = static_cast<int>((kN + cfg.bn - 1) / cfg.bn);
     p.num_tiles = p.tiles_m * p.tiles_n;
-    p.group_m = 16;
+    p.group_m = g_force_group_m.load() > 0 ? g_force_group_m.load() : 16;
     p.tile_begin = 0;
     p.tile_end = p.num_tiles;
     p.D = D;
@@ -319,6 +324,8 @@ tcm_status tcm_gemm_sp(int64_t M, int64_t N, int64_t K, tcm_dtype dtype, const v
     const int force_cg = g_force_cta_group.load();
     if (force_cg == 1 || force_cg == 2) cfg.cta_group = force_cg;
     cfg.bn = cfg.cta_group == 2 ? 256 : 128;
+    if (cfg.cta_group == 2 && g_force_bn.load() == 128) cfg.bn = 128;
+    cfg.stages = g_force_stages.load();
 
     CUtensorMap tmA, tmB;
     std::memset(&tmA, 0, sizeof tmA);
@@ -339,7 +346,7 @@ tcm_status tcm_gemm_sp(int64_t M, int64_t N, int64_t K, tcm_dtype dtype, const v
     p.tiles_m = static_cast<int>((M + 128 * cfg.cta_group - 1) / (128 * cfg.cta_group));
     p.tiles_n = static_cast<int>((N + cfg.bn - 1) / cfg.bn);
     p.num_tiles = p.tiles_m * p.tiles_n;
-    p.group_m = 16;
+    p.group_m = g_force_group_m.load() > 0 ? g_force_group_m.load() : 16;
     p.tile_begin = 0;
     p.tile_end = p.num_tiles;
     p.D = D;

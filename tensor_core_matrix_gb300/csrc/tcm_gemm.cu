@@ -281,24 +281,18 @@ static cudaError_t launch_one(const CUtensorMap &a, const CUtensorMap &b, const 
     return cudaLaunchKernelEx(&cfg, kern, a, b, p);
 }
 
-int gemm_stages(const GemmConfig &cfg)
-{
-    if (cfg.cta_group == 2) return 6;
-    switch (cfg.bn) {
-    case 256: return 4;
-    case 128: return 6;
-    case 64: return 8;
-    default: return 10;
-    }
-}
-
 cudaError_t launch_gemm(const GemmConfig &cfg, const CUtensorMap &tmA, const CUtensorMap &tmB,
                         const CUtensorMap * /*tmMeta*/, const GemmParams &p, int grid, cudaStream_t stream)
 {
     if (cfg.cta_group == 2) {
         if (cfg.bn != 256) return cudaErrorInvalidValue;
-        if (cfg.kind == 0) return launch_one<0, 256, 6, 2>(tmA, tmB, p, grid, stream);
-        if (cfg.kind == 1) return launch_one<1, 256, 6, 2>(tmA, tmB, p, grid, stream);
+        const bool deep = cfg.stages == 7;
+        if (cfg.kind == 0)
+            return deep ? launch_one<0, 256, 7, 2>(tmA, tmB, p, grid, stream)
+                        : launch_one<0, 256, 6, 2>(tmA, tmB, p, grid, stream);
+        if (cfg.kind == 1)
+            return deep ? launch_one<1, 256, 7, 2>(tmA, tmB, p, grid, stream)
+                        : launch_one<1, 256, 6, 2>(tmA, tmB, p, grid, stream);
         return cudaErrorInvalidValue;
     }
 #define TCM_DISPATCH(KIND)                                                                                          \

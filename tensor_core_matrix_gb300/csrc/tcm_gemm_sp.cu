@@ -30,6 +30,7 @@ namespace tcm {
 constexpr int SP_THREADS = 320; // warps 0 TMA, 1 MMA, 2-5 epilogue, 6-9 metadata
 constexpr int META_WARPS = 4;
 constexpr uint32_t META_FILL = 0x44444444u; // every group: positions {0, 1}
+constexpr int META_AHEAD = 8;               // metadata items fetched ahead of use
 
 template <int BN_CTA, int STAGES>
 struct SpSmem {
@@ -283,21 +284,35 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
             }
         }
     } else {
-        // metadata warps: TMEM lanes 32*quad .. +31 <- this CTA's rows, 4 columns per stage
+        // metadata warps: TMEM lanes 32*quad .. +31 <- this CTA's rows.  The
+        // (tile, k-block) items are walked in the issuer's order; each item's
+        // words are fetched META_AHEAD items early into a register ring so the
+        // global-memory latency overlaps the stages in between.
         const int quad = warp & 3;
         const int row_in_tile = quad * 32 + lane;
         const uint32_t meta_full_cluster0 = CG == 2 ? mapa_shared(smem_u32(meta_full), 0) : 0u;
         const bool upper = (lane & 8) != 0; // s of lane 16a + 8s + r
+        const int my_tiles = first_tile < p.tile_end ? (p.tile_end - 1 - first_tile) / num_clusters + 1 : 0;
+        const long long items = static_cast<long long>(my_tiles) * p.num_kb;
+        auto row_of = [&](long long i) {
+            const int t = first_tile + static_cast<int>(i / p.num_kb) * num_clusters;
+            int mb, nb;
+            tile_coords(p, t, mb, nb);
+            return mb * (BM * CG) + static_cast<int>(rank) * BM + row_in_tile;
+        };
+        uint32_t ring[META_AHEAD][4];
+#pragma unroll
+        for (int u = 0; u < META_AHEAD; ++u) {
+            if (u < items) load_meta4(p, row_of(u), u % p.num_kb, ring[u]);
+        }
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
-        for (int t = first_tile; ok && t < p.tile_end; t += num_clusters) {
-            int mb, nb;
-            tile_coords(p, t, mb, nb);
-            const int row = mb * (BM * CG) + static_cast<int>(rank) * BM + row_in_tile;
-            for (int kb = 0; kb < p.num_kb; ++kb) {
-                uint32_t own[4];
-                load_meta4(p, row, kb, own); // issued before the wait: global latency overlaps it
+        for (long long base = 0; ok && base < items; base += META_AHEAD) {
+#pragma unroll
+            for (int u = 0; u < META_AHEAD; ++u) {
+                const long long i = base + u;
+                if (!ok || i >= items) break;
                 int okw = 1;
                 if (lane == 0) okw = wait_bar<CG>(empty + stage, phase ^ 1u, w, SITE_META_EMPTY, true);
                 okw = __shfl_sync(0xffffffffu, okw, 0);
@@ -309,9 +324,11 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
                 uint32_t hw[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const uint32_t other = __shfl_xor_sync(0xffffffffu, own[j], 8);
-                    hw[j] = upper ? ((other >> 16) | (own[j] & 0xFFFF0000u)) : ((own[j] & 0xFFFFu) | (other << 16));
+                    const uint32_t other = __shfl_xor_sync(0xffffffffu, ring[u][j], 8);
+                    hw[j] = upper ? ((other >> 16) | (ring[u][j] & 0xFFFF0000u)) : ((ring[u][j] & 0xFFFFu) | (other << 16));
                 }
+                if (i + META_AHEAD < items)
+                    load_meta4(p, row_of(i + META_AHEAD), static_cast<int>((i + META_AHEAD) % p.num_kb), ring[u]);
                 const uint32_t mcol = tmem_base + META_COL + static_cast<uint32_t>(stage) * META_STAGE_COLS +
                                       (static_cast<uint32_t>(quad * 32) << 16);
 #pragma unroll
@@ -369,6 +386,7 @@ cudaError_t launch_gemm_sp(const GemmConfig &cfg, const CUtensorMap &tmA, const 
                            const GemmParams &p, int grid, cudaStream_t stream)
 {
     if (cfg.cta_group == 2 && cfg.bn == 256) return launch_sp_one<256, 4, 2, 1>(tmA, tmB, p, grid, stream);
+    if (cfg.cta_group == 2 && cfg.bn == 128) return launch_sp_one<128, 6, 2, 2>(tmA, tmB, p, grid, stream);
     if (cfg.cta_group == 1 && cfg.bn == 128) return launch_sp_one<128, 4, 1, 2>(tmA, tmB, p, grid, stream);
     return cudaErrorInvalidValue;
 }

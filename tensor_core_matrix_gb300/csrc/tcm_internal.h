@@ -60,12 +60,12 @@ struct GemmConfig {
     int kind;      // 0 = kind::f16, 1 = kind::f8f6f4, 2 = sparse kind::f16
     int bn;        // N tile (columns of the accumulator)
     int cta_group; // 1 = one CTA per 128-row tile, 2 = CTA pair per 256-row tile
+    int stages;    // 0 = the variant's default ring depth
 };
 
 cudaError_t launch_gemm(const GemmConfig &cfg, const CUtensorMap &tmA, const CUtensorMap &tmB,
                         const CUtensorMap *tmMeta, const GemmParams &p, int grid, cudaStream_t stream);
 
-int gemm_stages(const GemmConfig &cfg);
 
 cudaError_t launch_gemm_sp(const GemmConfig &cfg, const CUtensorMap &tmA, const CUtensorMap &tmB,
                            const GemmParams &p, int grid, cudaStream_t stream);

@@ -48,11 +48,10 @@ template <int CG>
 __device__ __noinline__ bool bounded_wait(uint64_t *bar, uint32_t parity, const Waiter &w, int site, bool honour_abort)
 {
     const uint32_t addr = smem_u32(bar);
-    auto try_once = [&]() { return CG == 2 ? mbar_try_wait_cluster(addr, parity) : mbar_try_wait(addr, parity); };
-    if (try_once()) return true;
+    if (mbar_try_wait(addr, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (unsigned long long it = 1; it < kMaxSpin; ++it) {
-        if (try_once()) return true;
+        if (mbar_try_wait(addr, parity)) return true;
         if ((it & 31ull) == 0) {
             if (honour_abort && *w.abort_flag) return false;
             if (globaltimer_ns() - t0 > w.timeout_ns) break;
@@ -196,8 +195,7 @@ __device__ __forceinline__ void epilogue_row32(const GemmParams &p, float scale,
     }
 }
 
-// Wait on a barrier of this CTA; pair kernels use cluster-scope acquire
-// because the arrivals can come from the peer CTA.
+// Wait on a barrier of this CTA (arrivals may come from the peer CTA of a pair).
 template <int CG>
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, const Waiter &w, int site, bool honour_abort)
 {

@@ -8,9 +8,7 @@
 // ties to the lower position.  Nibble = i0 | i1 << 2; eight nibbles per
 // uint32, group g at bits 4*(g%8) of word g/8 of its row.
 //
-// One thread owns one metadata word, i.e. 32 logical elements (64 bytes) of
-// a row: four 16-byte loads in, two 16-byte stores and one word out, so a
-// warp moves 2 KiB of contiguous input per step.  The op is a pure
+// Decompress: one thread per metadata word (32 logical values).  The op is a pure
 // selection on 16-bit codes: magnitudes are compared as the integer value
 // of the code without its sign bit, which orders finite binary16 and
 // bfloat16 values exactly as their absolute values.
@@ -18,66 +16,78 @@
 
 namespace tcm {
 
+// Value at position q (0..3) of a group, by selects (no indexed register array,
+// which would go through local memory).
+__device__ __forceinline__ uint16_t at4(const uint16_t (&v)[4], int q)
+{
+    return q == 0 ? v[0] : (q == 1 ? v[1] : (q == 2 ? v[2] : v[3]));
+}
+
 __device__ __forceinline__ uint32_t pick_group(const uint16_t (&v)[4], uint16_t &k0, uint16_t &k1)
 {
     uint32_t mag[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) mag[q] = v[q] & 0x7FFFu;
+    // first position of the largest magnitude
     int first = 0;
+    uint32_t best = mag[0];
 #pragma unroll
     for (int q = 1; q < 4; ++q)
-        if (mag[q] > mag[first]) first = q;
-    int second = first == 0 ? 1 : 0;
+        if (mag[q] > best) best = mag[q], first = q;
+    // first position of the largest magnitude among the other three
+    int second = -1;
+    uint32_t best2 = 0;
 #pragma unroll
     for (int q = 0; q < 4; ++q)
-        if (q != first && mag[q] > mag[second]) second = q;
+        if (q != first && (second < 0 || mag[q] > best2)) best2 = mag[q], second = q;
     const int i0 = first < second ? first : second;
     const int i1 = first < second ? second : first;
-    k0 = v[i0];
-    k1 = v[i1];
+    k0 = at4(v, i0);
+    k1 = at4(v, i1);
     return static_cast<uint32_t>(i0) | (static_cast<uint32_t>(i1) << 2);
 }
 
+// Compress: thread i owns 8 logical values (one 16-byte load, two groups) of
+// row i / (K/8); consecutive threads read consecutive 16 bytes, so a warp
+// reads 512 contiguous bytes per instruction.  It writes its 4 kept values
+// (8 bytes) and the two nibbles; the 4 lanes that cover one metadata word
+// (32 logical values) OR their bytes together with shuffles and the first of
+// them stores the word.  K % 32 == 0 keeps those 4 lanes in one row and in
+// one aligned quad of the warp.
 __global__ void __launch_bounds__(256) sp_compress16_kernel(int64_t M, int64_t K, const uint16_t *__restrict__ A,
                                                             int64_t lda, uint16_t *__restrict__ Ac,
                                                             uint32_t *__restrict__ meta)
 {
-    const int64_t words_per_row = K / 32;
-    const int64_t total = M * words_per_row;
-    for (int64_t w = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; w < total;
-         w += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t m = w / words_per_row;
-        const int64_t c = w - m * words_per_row;
-        const uint4 *src = reinterpret_cast<const uint4 *>(A + m * lda + c * 32);
-        uint16_t v[32];
+    const int64_t per_row = K / 8;
+    const int64_t total = M * per_row;
+    const int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+    const bool live = i < total;
+    uint32_t byte = 0;
+    int64_t m = 0, c = 0;
+    if (live) {
+        m = i / per_row;
+        c = i - m * per_row;
+        const uint4 x = __ldg(reinterpret_cast<const uint4 *>(A + m * lda + c * 8));
+        const uint32_t u[4] = {x.x, x.y, x.z, x.w};
+        uint16_t out[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const uint4 x = __ldg(src + j);
-            const uint32_t u[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                v[8 * j + 2 * h] = static_cast<uint16_t>(u[h] & 0xFFFFu);
-                v[8 * j + 2 * h + 1] = static_cast<uint16_t>(u[h] >> 16);
-            }
+        for (int g = 0; g < 2; ++g) {
+            const uint16_t grp[4] = {static_cast<uint16_t>(u[2 * g] & 0xFFFFu), static_cast<uint16_t>(u[2 * g] >> 16),
+                                     static_cast<uint16_t>(u[2 * g + 1] & 0xFFFFu),
+                                     static_cast<uint16_t>(u[2 * g + 1] >> 16)};
+            byte |= pick_group(grp, out[2 * g], out[2 * g + 1]) << (4 * g);
         }
-        uint32_t word = 0;
-        uint16_t out[16];
-#pragma unroll
-        for (int g = 0; g < 8; ++g) {
-            const uint16_t grp[4] = {v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]};
-            word |= pick_group(grp, out[2 * g], out[2 * g + 1]) << (4 * g);
-        }
-        uint4 *dst = reinterpret_cast<uint4 *>(Ac + m * (K / 2) + c * 16);
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            uint32_t u[4];
-#pragma unroll
-            for (int h = 0; h < 4; ++h)
-                u[h] = static_cast<uint32_t>(out[8 * j + 2 * h]) | (static_cast<uint32_t>(out[8 * j + 2 * h + 1]) << 16);
-            dst[j] = make_uint4(u[0], u[1], u[2], u[3]);
-        }
-        meta[w] = word;
+        uint2 o;
+        o.x = static_cast<uint32_t>(out[0]) | (static_cast<uint32_t>(out[1]) << 16);
+        o.y = static_cast<uint32_t>(out[2]) | (static_cast<uint32_t>(out[3]) << 16);
+        *reinterpret_cast<uint2 *>(Ac + m * (K / 2) + c * 4) = o;
     }
+    // quad q of the warp = the 4 chunks of one metadata word (chunk c % 4 = lane % 4)
+    const int lane = threadIdx.x & 31;
+    uint32_t word = byte << (8 * (lane & 3));
+    word |= __shfl_xor_sync(0xffffffffu, word, 1);
+    word |= __shfl_xor_sync(0xffffffffu, word, 2);
+    if (live && (lane & 3) == 0) meta[m * (K / 32) + c / 4] = word;
 }
 
 __global__ void __launch_bounds__(256) sp_decompress16_kernel(int64_t M, int64_t K, const uint16_t *__restrict__ Ac,
@@ -138,10 +148,12 @@ cudaError_t launch_sp_compress(int64_t M, int64_t K, int elem_bytes, const void 
                                uint32_t *meta, cudaStream_t stream)
 {
     if (elem_bytes != 2) return cudaErrorInvalidValue;
-    const int64_t work = M * (K / 32);
+    const int64_t work = M * (K / 8); // one thread per 8 logical values
     if (work == 0) return cudaSuccess;
-    sp_compress16_kernel<<<grid_for(work), 256, 0, stream>>>(M, K, static_cast<const uint16_t *>(A), lda,
-                                                              static_cast<uint16_t *>(Ac), meta);
+    const int64_t blocks = (work + 255) / 256;
+    if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    sp_compress16_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        M, K, static_cast<const uint16_t *>(A), lda, static_cast<uint16_t *>(Ac), meta);
     return cudaGetLastError();
 }
 

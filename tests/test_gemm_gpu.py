@@ -94,10 +94,11 @@ def override():
     tcm.tcm_set_config_override(0, 0)
 
 
-@pytest.mark.parametrize("cg,bn", [(1, 256), (1, 128), (1, 64), (1, 32), (2, 256)])
+@pytest.mark.parametrize("cg,bn,stages", [(1, 256, 0), (1, 128, 0), (1, 64, 0), (1, 32, 0), (2, 256, 0),
+                                          (2, 256, 7)])
 @pytest.mark.parametrize("M,N,K", [(256, 256, 64), (512, 768, 320), (300, 520, 136), (1000, 1030, 1024)])
-def test_each_variant_integer_exact(override, cg, bn, M, N, K):
-    override.tcm_set_config_override(cg, bn)
+def test_each_variant_integer_exact(override, cg, bn, stages, M, N, K):
+    override.tcm_set_config_override(cg, bn, stages, 3)
     g = si.generator(M + N + K + cg + bn)
     A = si.integers((M, K), g)
     B = si.integers((N, K), g)
@@ -106,10 +107,10 @@ def test_each_variant_integer_exact(override, cg, bn, M, N, K):
     assert np.array_equal(D.double().numpy(), ref)
 
 
-@pytest.mark.parametrize("cg,bn", [(1, 256), (2, 256), (1, 128)])
+@pytest.mark.parametrize("cg,bn,stages", [(1, 256, 0), (2, 256, 0), (2, 256, 7), (1, 128, 0)])
 @pytest.mark.parametrize("fb", ["e4m3", "e5m2"])
-def test_each_variant_fp8_bound(override, cg, bn, fb):
-    override.tcm_set_config_override(cg, bn)
+def test_each_variant_fp8_bound(override, cg, bn, stages, fb):
+    override.tcm_set_config_override(cg, bn, stages)
     case = si.fp8_case(640, 768, 1024, b_fmt=fb, seed=3)
     D = run_gemm_ex(case["A"], case["B"], torch.bfloat16, sa=case["sa"], sb=case["sb"], bias=case["bias"])
     ref, S = oracle_ref(case["A"], case["B"], sa=case["sa"], sb=case["sb"], bias=case["bias"])

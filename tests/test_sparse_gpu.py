@@ -95,11 +95,11 @@ def oracle_sparse(A_logical, B, fmt, C=None, alpha=1.0, beta=0.0, rows=None, col
                        alpha=alpha, beta=beta, rows=rows, cols=cols)
 
 
-@pytest.mark.parametrize("cg", [0, 1, 2])
+@pytest.mark.parametrize("cg,bn", [(0, 0), (1, 128), (2, 256), (2, 128)])
 @pytest.mark.parametrize("M,N,K", [(128, 128, 32), (256, 224, 128), (300, 520, 160), (512, 672, 1024),
                                    (1000, 448, 2048)])
-def test_sparse_gemm_integer_exact(tcm, cg, M, N, K):
-    tcm.tcm_set_config_override(cg, 0)
+def test_sparse_gemm_integer_exact(tcm, cg, bn, M, N, K):
+    tcm.tcm_set_config_override(cg, bn, 0, 2)
     g = si.generator(M + N + K)
     A = si.integers((M, K), g)
     B = si.integers((N, K), g)
