@@ -187,10 +187,13 @@ void tcm_set_timeout_ns(uint64_t ns);
  *              depths per tile; others fall back to the default)
  *   group_m    row blocks per rasterisation group (tiles that run at the same
  *              time share rows of A and columns of B in L2)
+ *   ksplit     1, 2 or 4 CTAs of a cluster sharing each tile's K range, their
+ *              partial sums added through distributed shared memory (dense
+ *              single-CTA tiles of width 32 or 64, e.g. skinny M)
  * Combinations the kernels do not provide fall back to the automatic choice.
  * Results are the same either way, up to the order of the fp32 accumulation.
  */
-void tcm_set_config_override(int cta_group, int tile_n, int stages, int group_m);
+void tcm_set_config_override(int cta_group, int tile_n, int stages, int group_m, int ksplit);
 
 /*
  * Test hook for the device-side failure path: with mask bit 1 set, the next

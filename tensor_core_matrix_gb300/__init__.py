@@ -68,7 +68,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.tcm_set_timeout_ns.restype = None
     lib.tcm_set_timeout_ns.argtypes = [ctypes.c_uint64]
     lib.tcm_set_config_override.restype = None
-    lib.tcm_set_config_override.argtypes = [i32, i32, i32, i32]
+    lib.tcm_set_config_override.argtypes = [i32, i32, i32, i32, i32]
     lib.tcm_debug_fail_next_launch.restype = None
     lib.tcm_debug_fail_next_launch.argtypes = [i32]
     lib.tcm_status_string.restype = ctypes.c_char_p
@@ -199,9 +199,10 @@ def tcm_set_timeout_ns(ns: int):
     load_library().tcm_set_timeout_ns(int(ns))
 
 
-def tcm_set_config_override(cta_group: int = 0, tile_n: int = 0, stages: int = 0, group_m: int = 0):
+def tcm_set_config_override(cta_group: int = 0, tile_n: int = 0, stages: int = 0, group_m: int = 0,
+                            ksplit: int = 0):
     """Force kernel-variant fields of later GEMMs (see include/tcm.h); zeros restore the automatic choice."""
-    load_library().tcm_set_config_override(int(cta_group), int(tile_n), int(stages), int(group_m))
+    load_library().tcm_set_config_override(int(cta_group), int(tile_n), int(stages), int(group_m), int(ksplit))
 
 
 def tcm_debug_fail_next_launch(mask: int = 1):

@@ -10,7 +10,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/tcm.h"
+#include "tcm.h"
 #include "tcm_internal.h"
 #include "tcm_ptx.cuh"
 
@@ -53,6 +53,7 @@ static std::atomic<int> g_force_cta_group{0};
 static std::atomic<int> g_force_bn{0};
 static std::atomic<int> g_force_stages{0};
 static std::atomic<int> g_force_group_m{0};
+static std::atomic<int> g_force_ksplit{0};
 static std::atomic<int> g_fault_once{0};
 
 static unsigned long long timeout_ns()
@@ -141,12 +142,13 @@ int tcm_version(void) { return 100; }
 
 void tcm_set_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns); }
 
-void tcm_set_config_override(int cta_group, int tile_n, int stages, int group_m)
+void tcm_set_config_override(int cta_group, int tile_n, int stages, int group_m, int ksplit)
 {
     g_force_cta_group.store(cta_group);
     g_force_bn.store(tile_n);
     g_force_stages.store(stages);
     g_force_group_m.store(group_m);
+    g_force_ksplit.store(ksplit);
 }
 
 void tcm_debug_fail_next_launch(int mask) { g_fault_once.store(mask); }
@@ -202,6 +204,26 @@ tcm_status tcm_gemm_ex(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const
     if (force_bn == 32 || force_bn == 64 || force_bn == 128 || force_bn == 256) cfg.bn = force_bn;
     if (cfg.cta_group == 2 && (cfg.bn != 256 || swap)) cfg.cta_group = 1;
     cfg.stages = g_force_stages.load();
+    cfg.ksplit = 1;
+    {
+        // K split across a cluster when single-CTA tiles leave SMs idle: pick the
+        // split (1, 2, 4) whose last round of tiles is fullest, keeping >= 8 K
+        // blocks per CTA; tiles of width 32 and 64 only.
+        const int64_t kbs = (K + (kind == 1 ? 127 : 63)) / (kind == 1 ? 128 : 64);
+        const int64_t tiles = ((kM + 127) / 128) * ((kN + cfg.bn - 1) / cfg.bn);
+        if (cfg.cta_group == 1 && (cfg.bn == 32 || cfg.bn == 64)) {
+            double best = 0.0;
+            for (int ks = 1; ks <= 4; ks *= 2) {
+                if (ks > 1 && kbs / ks < 8) break;
+                const int64_t clusters = sms / ks;
+                const int64_t rounds = (tiles + clusters - 1) / clusters;
+                const double eff = static_cast<double>(tiles) / static_cast<double>(rounds * clusters) / (ks > 1 ? 1.02 : 1.0);
+                if (eff > best + 0.05) best = eff, cfg.ksplit = ks;
+            }
+        }
+        const int fk = g_force_ksplit.load();
+        if (fk == 1 || ((fk == 2 || fk == 4) && cfg.cta_group == 1 && (cfg.bn == 32 || cfg.bn == 64))) cfg.ksplit = fk;
+    }
 
     // ---- tensor maps (the kernel's "A" operand is the swapped one when swap)
     const int k_elems_stage = kind == 1 ? 128 : 64;
@@ -255,8 +277,9 @@ tcm_status tcm_gemm_ex(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const
     if (!p.status) return TCM_ERR_CUDA;
 
     p.fault_inject = g_fault_once.exchange(0);
-    const int64_t clusters = sms / cfg.cta_group;
-    const int grid = static_cast<int>((p.num_tiles < clusters ? p.num_tiles : clusters) * cfg.cta_group);
+    const int64_t per_cluster = static_cast<int64_t>(cfg.cta_group) * cfg.ksplit;
+    const int64_t clusters = sms / per_cluster;
+    const int grid = static_cast<int>((p.num_tiles < clusters ? p.num_tiles : clusters) * per_cluster);
     const cudaError_t e = launch_gemm(cfg, tmA, tmB, nullptr, p, grid, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TCM_OK : TCM_ERR_CUDA;
 }
@@ -319,6 +342,7 @@ tcm_status tcm_gemm_sp(int64_t M, int64_t N, int64_t K, tcm_dtype dtype, const v
 
     GemmConfig cfg{};
     cfg.kind = 2;
+    cfg.ksplit = 1;
     const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
     cfg.cta_group = (M > 128 && N > 128 && pair_tiles >= sms / 2) ? 2 : 1;
     const int force_cg = g_force_cta_group.load();

@@ -12,7 +12,9 @@
 //     128-byte atoms);
 //   * four tcgen05.mma.sp per stage, logical K = 32 each (A +32 bytes, B
 //     +64 bytes per instruction);
-//   * warps 6..9 move the stage's metadata into tensor memory.  The library
+//   * two groups of four warps (6..9, 10..13) move the metadata into tensor
+//     memory, alternating stages so that one group's store-and-signal
+//     latency overlaps the other's.  The library
 //     layout keeps, per row, one 32-bit word per 32 logical K (8 nibbles
 //     i0 | i1 << 2).  The MMA reads, for each 16-row block, lane 16a+8s+r:
 //     bits 0..15 = nibbles 4s..4s+3 of row 16a+r, bits 16..31 = the same
@@ -27,8 +29,9 @@
 
 namespace tcm {
 
-constexpr int SP_THREADS = 320; // warps 0 TMA, 1 MMA, 2-5 epilogue, 6-9 metadata
-constexpr int META_WARPS = 4;
+constexpr int META_GROUPS = 2;  // metadata warpgroups; group g handles the items i with i % 2 == g
+constexpr int SP_THREADS = 32 * (2 + 4 + 4 * META_GROUPS); // warps 0 TMA, 1 MMA, 2-5 epilogue, 6.. metadata
+constexpr int META_WARPS = 4;   // warps per metadata group (one per TMEM lane quadrant)
 constexpr uint32_t META_FILL = 0x44444444u; // every group: positions {0, 1}
 constexpr int META_AHEAD = 8;               // metadata items fetched ahead of use
 
@@ -75,6 +78,17 @@ __device__ __forceinline__ void load_meta4(const GemmParams &p, int row, int kb,
     }
 }
 
+// Row of D (and of A) that metadata item i of this CTA's walk belongs to.
+template <int CG>
+__device__ __forceinline__ int meta_row(const GemmParams &p, long long i, int first_tile, int num_clusters,
+                                        uint32_t rank, int row_in_tile)
+{
+    const int t = first_tile + static_cast<int>(i / p.num_kb) * num_clusters;
+    int mb, nb;
+    tile_coords(p, t, mb, nb);
+    return mb * (BM * CG) + static_cast<int>(rank) * BM + row_in_tile;
+}
+
 // BN: N extent of the (pair) tile; CG: CTA group (see the dense kernel);
 // NACC: accumulators in tensor memory (2 lets the epilogue overlap the next tile).
 template <int BN, int STAGES, int CG, int NACC>
@@ -85,6 +99,7 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
     using L = SpSmem<BN_CTA, STAGES>;
     static_assert(L::ALLOC <= 227 * 1024, "shared memory ring too large");
     static_assert(BN % 32 == 0 && BN_CTA <= 256, "tile width");
+    static_assert(STAGES % META_GROUPS == 0, "each metadata group owns whole stages");
     // accumulators at power-of-two columns, then 16 metadata columns per stage
     constexpr uint32_t ACC_STRIDE = BN <= 128 ? 128u : 256u;
     constexpr uint32_t META_COL = ACC_STRIDE * NACC;
@@ -285,34 +300,32 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
         }
     } else {
         // metadata warps: TMEM lanes 32*quad .. +31 <- this CTA's rows.  The
-        // (tile, k-block) items are walked in the issuer's order; each item's
-        // words are fetched META_AHEAD items early into a register ring so the
-        // global-memory latency overlaps the stages in between.
+        // (tile, k-block) items are walked in the issuer's order; group g takes
+        // items g, g+2, g+4 ... (STAGES is even, so each group owns a fixed set
+        // of stages).  Each item's words are fetched META_AHEAD items of the
+        // group early into a register ring so the global-memory latency
+        // overlaps the stages in between.
         const int quad = warp & 3;
+        const int group = (warp - 2 - EPI_WARPS) / META_WARPS;
         const int row_in_tile = quad * 32 + lane;
         const uint32_t meta_full_cluster0 = CG == 2 ? mapa_shared(smem_u32(meta_full), 0) : 0u;
         const bool upper = (lane & 8) != 0; // s of lane 16a + 8s + r
         const int my_tiles = first_tile < p.tile_end ? (p.tile_end - 1 - first_tile) / num_clusters + 1 : 0;
         const long long items = static_cast<long long>(my_tiles) * p.num_kb;
-        auto row_of = [&](long long i) {
-            const int t = first_tile + static_cast<int>(i / p.num_kb) * num_clusters;
-            int mb, nb;
-            tile_coords(p, t, mb, nb);
-            return mb * (BM * CG) + static_cast<int>(rank) * BM + row_in_tile;
-        };
         uint32_t ring[META_AHEAD][4];
 #pragma unroll
         for (int u = 0; u < META_AHEAD; ++u) {
-            if (u < items) load_meta4(p, row_of(u), u % p.num_kb, ring[u]);
+            const long long i = group + static_cast<long long>(META_GROUPS) * u;
+            if (i < items) load_meta4(p, meta_row<CG>(p, i, first_tile, num_clusters, rank, row_in_tile), static_cast<int>(i % p.num_kb), ring[u]);
         }
-        int stage = 0;
-        uint32_t phase = 0;
         bool ok = true;
-        for (long long base = 0; ok && base < items; base += META_AHEAD) {
+        for (long long base = group; ok && base < items; base += static_cast<long long>(META_GROUPS) * META_AHEAD) {
 #pragma unroll
             for (int u = 0; u < META_AHEAD; ++u) {
-                const long long i = base + u;
+                const long long i = base + static_cast<long long>(META_GROUPS) * u;
                 if (!ok || i >= items) break;
+                const int stage = static_cast<int>(i % STAGES);
+                const uint32_t phase = static_cast<uint32_t>((i / STAGES) & 1);
                 int okw = 1;
                 if (lane == 0) okw = wait_bar<CG>(empty + stage, phase ^ 1u, w, SITE_META_EMPTY, true);
                 okw = __shfl_sync(0xffffffffu, okw, 0);
@@ -327,8 +340,8 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
                     const uint32_t other = __shfl_xor_sync(0xffffffffu, ring[u][j], 8);
                     hw[j] = upper ? ((other >> 16) | (ring[u][j] & 0xFFFF0000u)) : ((ring[u][j] & 0xFFFFu) | (other << 16));
                 }
-                if (i + META_AHEAD < items)
-                    load_meta4(p, row_of(i + META_AHEAD), static_cast<int>((i + META_AHEAD) % p.num_kb), ring[u]);
+                const long long next = i + static_cast<long long>(META_GROUPS) * META_AHEAD;
+                if (next < items) load_meta4(p, meta_row<CG>(p, next, first_tile, num_clusters, rank, row_in_tile), static_cast<int>(next % p.num_kb), ring[u]);
                 const uint32_t mcol = tmem_base + META_COL + static_cast<uint32_t>(stage) * META_STAGE_COLS +
                                       (static_cast<uint32_t>(quad * 32) << 16);
 #pragma unroll
@@ -339,10 +352,6 @@ __global__ void __launch_bounds__(SP_THREADS, 1)
                 if (lane == 0) {
                     if (CG == 2) mbar_arrive_cluster(meta_full_cluster0 + static_cast<uint32_t>(stage) * 8u);
                     else mbar_arrive(meta_full + stage);
-                }
-                if (++stage == STAGES) {
-                    stage = 0;
-                    phase ^= 1u;
                 }
             }
         }

@@ -21,6 +21,8 @@ enum WaitSite : int {
     SITE_DRAIN = 5,
     SITE_MMA_META = 6,   // sparse: issuer waiting for a stage's metadata in TMEM
     SITE_META_EMPTY = 7, // sparse: metadata warps waiting for a free stage
+    SITE_RED_FULL = 8,   // K-split: leader waiting for the other CTAs' partial sums
+    SITE_RED_EMPTY = 9,  // K-split: CTA waiting for the leader to consume its previous partials
 };
 
 // Everything a GEMM kernel needs besides its tensor maps.  "Kernel" rows and
@@ -61,11 +63,17 @@ struct GemmConfig {
     int bn;        // N tile (columns of the accumulator)
     int cta_group; // 1 = one CTA per 128-row tile, 2 = CTA pair per 256-row tile
     int stages;    // 0 = the variant's default ring depth
+    int ksplit;    // CTAs of a cluster that split each tile's K range (1, 2 or 4; needs cta_group 1)
 };
 
 cudaError_t launch_gemm(const GemmConfig &cfg, const CUtensorMap &tmA, const CUtensorMap &tmB,
                         const CUtensorMap *tmMeta, const GemmParams &p, int grid, cudaStream_t stream);
 
+
+cudaError_t launch_gemm_pair(const GemmConfig &cfg, const CUtensorMap &tmA, const CUtensorMap &tmB,
+                             const GemmParams &p, int grid, cudaStream_t stream);
+cudaError_t launch_gemm_ksplit(const GemmConfig &cfg, const CUtensorMap &tmA, const CUtensorMap &tmB,
+                               const GemmParams &p, int grid, cudaStream_t stream);
 
 cudaError_t launch_gemm_sp(const GemmConfig &cfg, const CUtensorMap &tmA, const CUtensorMap &tmB,
                            const GemmParams &p, int grid, cudaStream_t stream);

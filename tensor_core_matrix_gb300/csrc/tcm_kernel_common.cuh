@@ -19,13 +19,14 @@ constexpr int NUM_THREADS = 192;
 constexpr int EPI_WARPS = 4;
 constexpr unsigned long long kMaxSpin = 1ull << 34;
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int RED_BYTES = 0>
 struct Smem {
     static constexpr int B_STAGE = BN * TILE_K_BYTES;
     static constexpr int A_OFF = 0;
     static constexpr int B_OFF = STAGES * A_STAGE_BYTES;
-    static constexpr int BAR_OFF = B_OFF + STAGES * B_STAGE;
-    static constexpr int NUM_BARS = 2 * STAGES + 5; // full, empty, tfull[2], tempty[2], drain
+    static constexpr int RED_OFF = B_OFF + STAGES * B_STAGE; // K-split partial sums (leader CTA)
+    static constexpr int BAR_OFF = RED_OFF + RED_BYTES;
+    static constexpr int NUM_BARS = 2 * STAGES + 7; // full, empty, tfull[2], tempty[2], drain, red_full, red_empty
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
     static constexpr int BYTES = MISC_OFF + 16;
     static constexpr int ALLOC = BYTES + 1024; // slack to align the base to 1024
@@ -44,14 +45,24 @@ __device__ __forceinline__ void record_timeout(const Waiter &w, int site)
 }
 
 // Wait for phase `parity` of `bar`; false if the CTA is aborting or the limit expired.
-template <int CG>
+template <bool ACQ_CLUSTER>
+__device__ __forceinline__ bool poll_bar(uint32_t addr, uint32_t parity)
+{
+    if constexpr (ACQ_CLUSTER) return mbar_try_wait_acq_cluster(addr, parity);
+    else return mbar_try_wait(addr, parity);
+}
+
+// Wait for phase `parity` of `bar`; false if the CTA is aborting or the limit expired.
+// ACQ_CLUSTER: acquire at cluster scope, for barriers whose arrivals publish
+// generic shared-memory data written by another CTA of the cluster.
+template <int CG, bool ACQ_CLUSTER = false>
 __device__ __noinline__ bool bounded_wait(uint64_t *bar, uint32_t parity, const Waiter &w, int site, bool honour_abort)
 {
     const uint32_t addr = smem_u32(bar);
-    if (mbar_try_wait(addr, parity)) return true;
+    if (poll_bar<ACQ_CLUSTER>(addr, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (unsigned long long it = 1; it < kMaxSpin; ++it) {
-        if (mbar_try_wait(addr, parity)) return true;
+        if (poll_bar<ACQ_CLUSTER>(addr, parity)) return true;
         if ((it & 31ull) == 0) {
             if (honour_abort && *w.abort_flag) return false;
             if (globaltimer_ns() - t0 > w.timeout_ns) break;

@@ -47,29 +47,45 @@ __device__ __forceinline__ uint32_t pick_group(const uint16_t (&v)[4], uint16_t 
     return static_cast<uint32_t>(i0) | (static_cast<uint32_t>(i1) << 2);
 }
 
-// Compress: thread i owns 8 logical values (one 16-byte load, two groups) of
-// row i / (K/8); consecutive threads read consecutive 16 bytes, so a warp
-// reads 512 contiguous bytes per instruction.  It writes its 4 kept values
-// (8 bytes) and the two nibbles; the 4 lanes that cover one metadata word
-// (32 logical values) OR their bytes together with shuffles and the first of
-// them stores the word.  K % 32 == 0 keeps those 4 lanes in one row and in
-// one aligned quad of the warp.
+// Compress: a "chunk" is 8 logical values of one row (one 16-byte load, two
+// groups); chunk c of the matrix is row c / (K/8).  Thread t of T handles
+// chunks t, t+T, t+2T, t+3T: its four loads are issued before any is used,
+// and each load instruction of a warp reads 512 contiguous bytes.  Per chunk
+// the thread writes its 4 kept values (8 bytes) and two nibbles; the 4 lanes
+// whose chunks make up one metadata word (32 logical values) OR their bytes
+// together with shuffles and the first of them stores the word.  K % 32 == 0
+// and T % 4 == 0 keep those 4 chunks in one row and in one aligned lane quad.
+constexpr int CMP_CHUNKS = 4;
+
 __global__ void __launch_bounds__(256) sp_compress16_kernel(int64_t M, int64_t K, const uint16_t *__restrict__ A,
                                                             int64_t lda, uint16_t *__restrict__ Ac,
                                                             uint32_t *__restrict__ meta)
 {
     const int64_t per_row = K / 8;
     const int64_t total = M * per_row;
-    const int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
-    const bool live = i < total;
-    uint32_t byte = 0;
-    int64_t m = 0, c = 0;
-    if (live) {
-        m = i / per_row;
-        c = i - m * per_row;
-        const uint4 x = __ldg(reinterpret_cast<const uint4 *>(A + m * lda + c * 8));
-        const uint32_t u[4] = {x.x, x.y, x.z, x.w};
+    const int64_t T = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+    const int lane = threadIdx.x & 31;
+    uint4 x[CMP_CHUNKS];
+#pragma unroll
+    for (int j = 0; j < CMP_CHUNKS; ++j) {
+        const int64_t c = t + j * T;
+        if (c < total) {
+            const int64_t m = c / per_row;
+            x[j] = __ldg(reinterpret_cast<const uint4 *>(A + m * lda + (c - m * per_row) * 8));
+        } else {
+            x[j] = make_uint4(0, 0, 0, 0);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < CMP_CHUNKS; ++j) {
+        const int64_t c = t + j * T;
+        const bool live = c < total;
+        const int64_t m = c / per_row;
+        const int64_t cc = c - m * per_row;
+        const uint32_t u[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
         uint16_t out[4];
+        uint32_t byte = 0;
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
             const uint16_t grp[4] = {static_cast<uint16_t>(u[2 * g] & 0xFFFFu), static_cast<uint16_t>(u[2 * g] >> 16),
@@ -77,17 +93,17 @@ __global__ void __launch_bounds__(256) sp_compress16_kernel(int64_t M, int64_t K
                                      static_cast<uint16_t>(u[2 * g + 1] >> 16)};
             byte |= pick_group(grp, out[2 * g], out[2 * g + 1]) << (4 * g);
         }
-        uint2 o;
-        o.x = static_cast<uint32_t>(out[0]) | (static_cast<uint32_t>(out[1]) << 16);
-        o.y = static_cast<uint32_t>(out[2]) | (static_cast<uint32_t>(out[3]) << 16);
-        *reinterpret_cast<uint2 *>(Ac + m * (K / 2) + c * 4) = o;
+        if (live) {
+            uint2 o;
+            o.x = static_cast<uint32_t>(out[0]) | (static_cast<uint32_t>(out[1]) << 16);
+            o.y = static_cast<uint32_t>(out[2]) | (static_cast<uint32_t>(out[3]) << 16);
+            *reinterpret_cast<uint2 *>(Ac + m * (K / 2) + cc * 4) = o;
+        }
+        uint32_t word = live ? byte << (8 * (lane & 3)) : 0u;
+        word |= __shfl_xor_sync(0xffffffffu, word, 1);
+        word |= __shfl_xor_sync(0xffffffffu, word, 2);
+        if (live && (lane & 3) == 0) meta[m * (K / 32) + cc / 4] = word;
     }
-    // quad q of the warp = the 4 chunks of one metadata word (chunk c % 4 = lane % 4)
-    const int lane = threadIdx.x & 31;
-    uint32_t word = byte << (8 * (lane & 3));
-    word |= __shfl_xor_sync(0xffffffffu, word, 1);
-    word |= __shfl_xor_sync(0xffffffffu, word, 2);
-    if (live && (lane & 3) == 0) meta[m * (K / 32) + c / 4] = word;
 }
 
 __global__ void __launch_bounds__(256) sp_decompress16_kernel(int64_t M, int64_t K, const uint16_t *__restrict__ Ac,
@@ -148,9 +164,9 @@ cudaError_t launch_sp_compress(int64_t M, int64_t K, int elem_bytes, const void 
                                uint32_t *meta, cudaStream_t stream)
 {
     if (elem_bytes != 2) return cudaErrorInvalidValue;
-    const int64_t work = M * (K / 8); // one thread per 8 logical values
+    const int64_t work = M * (K / 8); // chunks of 8 logical values
     if (work == 0) return cudaSuccess;
-    const int64_t blocks = (work + 255) / 256;
+    const int64_t blocks = (work + 256 * CMP_CHUNKS - 1) / (256 * CMP_CHUNKS);
     if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
     sp_compress16_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
         M, K, static_cast<const uint16_t *>(A), lda, static_cast<uint16_t *>(Ac), meta);

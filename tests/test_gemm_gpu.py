@@ -91,7 +91,7 @@ def test_rank1_closed_form():
 def override():
     import tensor_core_matrix_gb300 as tcm
     yield tcm
-    tcm.tcm_set_config_override(0, 0)
+    tcm.tcm_set_config_override(0, 0, 0, 0, 0)
 
 
 @pytest.mark.parametrize("cg,bn,stages", [(1, 256, 0), (1, 128, 0), (1, 64, 0), (1, 32, 0), (2, 256, 0),
@@ -114,6 +114,32 @@ def test_each_variant_fp8_bound(override, cg, bn, stages, fb):
     case = si.fp8_case(640, 768, 1024, b_fmt=fb, seed=3)
     D = run_gemm_ex(case["A"], case["B"], torch.bfloat16, sa=case["sa"], sb=case["sb"], bias=case["bias"])
     ref, S = oracle_ref(case["A"], case["B"], sa=case["sa"], sb=case["sb"], bias=case["bias"])
+    assert ratio(D, ref, S, scale=case["sa"] * case["sb"]) <= 1.0
+
+
+@pytest.mark.parametrize("ks", [2, 4])
+@pytest.mark.parametrize("M,N,K", [(16, 1024, 2048), (64, 384, 1000), (1, 256, 512), (16, 512, 64), (40, 300, 4096)])
+def test_k_split_cluster_integer_exact(override, ks, M, N, K):
+    """Skinny M (operands swapped) with each tile's K split over a cluster and reduced through DSMEM;
+    K = 64 leaves some CTAs of a 4-way split with no K blocks."""
+    override.tcm_set_config_override(0, 0, 0, 0, ks)
+    g = si.generator(M * 3 + N + K + ks)
+    A = si.integers((M, K), g)
+    B = si.integers((N, K), g)
+    D = run_gemm_ex(A, B, torch.float32)
+    ref, _ = oracle_ref(A, B)
+    assert np.array_equal(D.double().numpy(), ref)
+
+
+@pytest.mark.parametrize("ks", [2, 4])
+def test_k_split_cluster_fp8_with_epilogue(override, ks):
+    override.tcm_set_config_override(0, 0, 0, 0, ks)
+    case = si.fp8_case(16, 2048, 4096, b_fmt="e5m2", seed=5)
+    g = si.generator(9)
+    C = si.normal((16, 2048), g)
+    D = run_gemm_ex(case["A"], case["B"], torch.bfloat16, C=C, beta=0.5, sa=case["sa"], sb=case["sb"],
+                    bias=case["bias"])
+    ref, S = oracle_ref(case["A"], case["B"], C=C, beta=0.5, sa=case["sa"], sb=case["sb"], bias=case["bias"])
     assert ratio(D, ref, S, scale=case["sa"] * case["sb"]) <= 1.0
 
 

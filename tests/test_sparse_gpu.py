@@ -30,7 +30,7 @@ def _build():
 def tcm():
     import tensor_core_matrix_gb300 as t
     yield t
-    t.tcm_set_config_override(0, 0)
+    t.tcm_set_config_override(0, 0, 0, 0, 0)
 
 
 def gpu_compress(tcm, A):
