@@ -54,6 +54,7 @@ static std::atomic<int> g_force_bn{0};
 static std::atomic<int> g_force_stages{0};
 static std::atomic<int> g_force_group_m{0};
 static std::atomic<int> g_force_ksplit{0};
+
 static std::atomic<int> g_fault_once{0};
 
 static unsigned long long timeout_ns()
@@ -224,6 +225,9 @@ tcm_status tcm_gemm_ex(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const
         const int fk = g_force_ksplit.load();
         if (fk == 1 || ((fk == 2 || fk == 4) && cfg.cta_group == 1 && (cfg.bn == 32 || cfg.bn == 64))) cfg.ksplit = fk;
     }
+    // two 128-byte K atoms per stage for 32-wide single-CTA tiles (the skinny,
+    // HBM-bound shapes): longer contiguous reads of each weight row
+    cfg.katoms = (cfg.cta_group == 1 && cfg.bn == 32 && cfg.ksplit <= 2) ? 2 : 1;
 
     // ---- tensor maps (the kernel's "A" operand is the swapped one when swap)
     const int k_elems_stage = kind == 1 ? 128 : 64;
@@ -248,7 +252,7 @@ tcm_status tcm_gemm_ex(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const
     p.kM = static_cast<int>(kM);
     p.kN = static_cast<int>(kN);
     p.K = static_cast<int>(K);
-    p.num_kb = static_cast<int>((K + k_elems_stage - 1) / k_elems_stage);
+    p.num_kb = static_cast<int>((K + k_elems_stage * cfg.katoms - 1) / (k_elems_stage * cfg.katoms));
     p.tiles_m = static_cast<int>((kM + 128 * cfg.cta_group - 1) / (128 * cfg.cta_group));
     p.tiles_n = static_cast<int>((kN + cfg.bn - 1) / cfg.bn);
     p.num_tiles = p.tiles_m * p.tiles_n;
@@ -343,6 +347,7 @@ tcm_status tcm_gemm_sp(int64_t M, int64_t N, int64_t K, tcm_dtype dtype, const v
     GemmConfig cfg{};
     cfg.kind = 2;
     cfg.ksplit = 1;
+    cfg.katoms = 1;
     const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
     cfg.cta_group = (M > 128 && N > 128 && pair_tiles >= sms / 2) ? 2 : 1;
     const int force_cg = g_force_cta_group.load();

@@ -14,7 +14,9 @@ cudaError_t launch_gemm(const GemmConfig &cfg, const CUtensorMap &tmA, const CUt
     case 256: return launch_one<KIND, 256, 4, 1>(tmA, tmB, p, grid, stream);                                        \
     case 128: return launch_one<KIND, 128, 6, 1>(tmA, tmB, p, grid, stream);                                        \
     case 64: return launch_one<KIND, 64, 8, 1>(tmA, tmB, p, grid, stream);                                          \
-    case 32: return launch_one<KIND, 32, 10, 1>(tmA, tmB, p, grid, stream);                                         \
+    case 32:                                                                                                        \
+        return cfg.katoms == 2 ? launch_one<KIND, 32, 5, 1, 1, 2>(tmA, tmB, p, grid, stream)                        \
+                               : launch_one<KIND, 32, 10, 1>(tmA, tmB, p, grid, stream);                            \
     default: return cudaErrorInvalidValue;                                                                          \
     }
     if (cfg.kind == 0) { TCM_DISPATCH(0) }

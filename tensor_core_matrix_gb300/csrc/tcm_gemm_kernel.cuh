@@ -56,20 +56,23 @@ __device__ __forceinline__ uint32_t red_offset(int slot, int row, int c, int j)
 // and CTA 0 adds them in rank order (a fixed order, so results do not depend
 // on timing) before the epilogue.  This keeps every SM streaming when a
 // problem has fewer tiles than the GPU has SMs (skinny M after the swap).
-template <int KIND, int BN, int STAGES, int CG, int KS>
+// KATOMS: 128-byte K atoms per stage; more than one gives each weight row
+// a longer contiguous run per stage (skinny, HBM-bound shapes).
+template <int KIND, int BN, int STAGES, int CG, int KS, int KATOMS = 1>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GemmParams p)
 {
     constexpr int RED_SLOT = BM * BN * 4; // one CTA's fp32 partial tile
-    using L = Smem<BN / CG, STAGES, (KS - 1) * RED_SLOT>;
+    using L = Smem<BN / CG, STAGES, (KS - 1) * RED_SLOT, KATOMS>;
     static_assert(CG == 1 || CG == 2, "CTA group of 1 or 2");
     static_assert(KS == 1 || (CG == 1 && (KS == 2 || KS == 4)), "K split of 2 or 4 CTAs, single-CTA tiles only");
+    static_assert(KATOMS == 1 || CG == 1, "multi-atom stages for single-CTA tiles only");
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN must be a multiple of 32 in [32, 256]");
     static_assert(L::ALLOC <= 227 * 1024, "shared memory ring too large");
     constexpr uint32_t TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
     constexpr int KB_ELEMS = KIND == 1 ? 128 : 64; // K elements per stage (128 bytes)
     constexpr int BN_CTA = BN / CG;                  // rows of B this CTA loads
-    constexpr uint32_t STAGE_TX = CG * (A_STAGE_BYTES + L::B_STAGE);
+    constexpr uint32_t STAGE_TX = CG * (L::A_STAGE + L::B_STAGE);
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -156,7 +159,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         break;
                     }
                     if (!(p.fault_inject & FAULT_SKIP_FIRST_LOAD) || issued != 0) {
-                        const uint32_t sa = sbase + L::A_OFF + stage * A_STAGE_BYTES;
+                        const uint32_t sa = sbase + L::A_OFF + stage * L::A_STAGE;
                         const uint32_t sb = sbase + L::B_OFF + stage * L::B_STAGE;
                         if (CG == 2) {
                             if (leader) mbar_arrive_expect_tx(full + stage, STAGE_TX);
@@ -165,8 +168,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             tma_load_2d_pair(sb, &tmB, fb, kb * KB_ELEMS, b_row);
                         } else {
                             mbar_arrive_expect_tx(full + stage, STAGE_TX);
-                            tma_load_2d(sa, &tmA, full + stage, kb * KB_ELEMS, a_row);
-                            tma_load_2d(sb, &tmB, full + stage, kb * KB_ELEMS, b_row);
+#pragma unroll
+                            for (int a = 0; a < KATOMS; ++a)
+                                tma_load_2d(sa + a * A_STAGE_BYTES, &tmA, full + stage, (kb * KATOMS + a) * KB_ELEMS, a_row);
+#pragma unroll
+                            for (int a = 0; a < KATOMS; ++a)
+                                tma_load_2d(sb + a * BN_CTA * TILE_K_BYTES, &tmB, full + stage,
+                                            (kb * KATOMS + a) * KB_ELEMS, b_row);
                         }
                     }
                     ++issued;
@@ -207,18 +215,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t ad = sdesc_kmajor_sw128(sbase + L::A_OFF + stage * A_STAGE_BYTES);
-                    const uint64_t bd = sdesc_kmajor_sw128(sbase + L::B_OFF + stage * L::B_STAGE);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        // +32 bytes of K per instruction = +2 in the descriptor's address field
-                        const uint32_t accum = (kb > kb0 || k > 0) ? 1u : 0u;
-                        if (CG == 2) {
-                            if (KIND == 1) mma_f8_pair(d_tmem, ad + 2 * k, bd + 2 * k, p.idesc, accum);
-                            else mma_f16_pair(d_tmem, ad + 2 * k, bd + 2 * k, p.idesc, accum);
-                        } else {
-                            if (KIND == 1) mma_f8(d_tmem, ad + 2 * k, bd + 2 * k, p.idesc, accum);
-                            else mma_f16(d_tmem, ad + 2 * k, bd + 2 * k, p.idesc, accum);
+                    for (int a = 0; a < KATOMS; ++a) {
+                        const uint64_t ad =
+                            sdesc_kmajor_sw128(sbase + L::A_OFF + stage * L::A_STAGE + a * A_STAGE_BYTES);
+                        const uint64_t bd =
+                            sdesc_kmajor_sw128(sbase + L::B_OFF + stage * L::B_STAGE + a * BN_CTA * TILE_K_BYTES);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            // +32 bytes of K per instruction = +2 in the descriptor's address field
+                            const uint32_t accum = (kb > kb0 || a > 0 || k > 0) ? 1u : 0u;
+                            if (CG == 2) {
+                                if (KIND == 1) mma_f8_pair(d_tmem, ad + 2 * k, bd + 2 * k, p.idesc, accum);
+                                else mma_f16_pair(d_tmem, ad + 2 * k, bd + 2 * k, p.idesc, accum);
+                            } else {
+                                if (KIND == 1) mma_f8(d_tmem, ad + 2 * k, bd + 2 * k, p.idesc, accum);
+                                else mma_f16(d_tmem, ad + 2 * k, bd + 2 * k, p.idesc, accum);
+                            }
                         }
                     }
                     if (CG == 2) mma_commit_pair(empty + stage, 0x3);
@@ -341,12 +354,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 }
 
-template <int KIND, int BN, int STAGES, int CG, int KS = 1>
+template <int KIND, int BN, int STAGES, int CG, int KS = 1, int KATOMS = 1>
 inline cudaError_t launch_one(const CUtensorMap &a, const CUtensorMap &b, const GemmParams &p, int grid,
                               cudaStream_t stream)
 {
-    using L = Smem<BN / CG, STAGES, (KS - 1) * BM * BN * 4>;
-    auto kern = gemm_kernel<KIND, BN, STAGES, CG, KS>;
+    using L = Smem<BN / CG, STAGES, (KS - 1) * BM * BN * 4, KATOMS>;
+    auto kern = gemm_kernel<KIND, BN, STAGES, CG, KS, KATOMS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};

@@ -10,6 +10,8 @@ cudaError_t launch_gemm_ksplit(const GemmConfig &cfg, const CUtensorMap &tmA, co
 {
     if (cfg.cta_group != 1) return cudaErrorInvalidValue;
 #define TCM_KSPLIT(KIND)                                                                                            \
+    if (cfg.bn == 32 && cfg.ksplit == 2 && cfg.katoms == 2)                                                         \
+        return launch_one<KIND, 32, 5, 1, 2, 2>(tmA, tmB, p, grid, stream);                                          \
     if (cfg.bn == 32 && cfg.ksplit == 2) return launch_one<KIND, 32, 10, 1, 2>(tmA, tmB, p, grid, stream);          \
     if (cfg.bn == 32 && cfg.ksplit == 4) return launch_one<KIND, 32, 8, 1, 4>(tmA, tmB, p, grid, stream);           \
     if (cfg.bn == 64 && cfg.ksplit == 2) return launch_one<KIND, 64, 8, 1, 2>(tmA, tmB, p, grid, stream);           \

@@ -64,6 +64,7 @@ struct GemmConfig {
     int cta_group; // 1 = one CTA per 128-row tile, 2 = CTA pair per 256-row tile
     int stages;    // 0 = the variant's default ring depth
     int ksplit;    // CTAs of a cluster that split each tile's K range (1, 2 or 4; needs cta_group 1)
+    int katoms;    // 128-byte K atoms per stage (1, or 2 for 32-wide single-CTA tiles)
 };
 
 cudaError_t launch_gemm(const GemmConfig &cfg, const CUtensorMap &tmA, const CUtensorMap &tmB,

@@ -19,11 +19,13 @@ constexpr int NUM_THREADS = 192;
 constexpr int EPI_WARPS = 4;
 constexpr unsigned long long kMaxSpin = 1ull << 34;
 
-template <int BN, int STAGES, int RED_BYTES = 0>
+// KATOMS: 128-byte K atoms per stage (each atom is a separate SW128 tile).
+template <int BN, int STAGES, int RED_BYTES = 0, int KATOMS = 1>
 struct Smem {
-    static constexpr int B_STAGE = BN * TILE_K_BYTES;
+    static constexpr int A_STAGE = KATOMS * A_STAGE_BYTES;
+    static constexpr int B_STAGE = KATOMS * BN * TILE_K_BYTES;
     static constexpr int A_OFF = 0;
-    static constexpr int B_OFF = STAGES * A_STAGE_BYTES;
+    static constexpr int B_OFF = STAGES * A_STAGE;
     static constexpr int RED_OFF = B_OFF + STAGES * B_STAGE; // K-split partial sums (leader CTA)
     static constexpr int BAR_OFF = RED_OFF + RED_BYTES;
     static constexpr int NUM_BARS = 2 * STAGES + 7; // full, empty, tfull[2], tempty[2], drain, red_full, red_empty

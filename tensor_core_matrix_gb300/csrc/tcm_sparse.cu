@@ -16,93 +16,69 @@
 
 namespace tcm {
 
-// Value at position q (0..3) of a group, by selects (no indexed register array,
-// which would go through local memory).
-__device__ __forceinline__ uint16_t at4(const uint16_t (&v)[4], int q)
+// Kept positions and values of one group of four 16-bit codes (v0 | v1 << 16,
+// v2 | v3 << 16).  Each position q gets the key (|code| << 2) | (3 - q):
+// keys are distinct, and a larger key means a larger magnitude or, for equal
+// magnitudes, a lower position -- so the two largest keys are exactly the two
+// kept positions with ties going to the lower one.  The top two of four keys
+// take seven integer min / max operations; no branches, no indexed arrays.
+__device__ __forceinline__ uint32_t pick_group(uint32_t lo, uint32_t hi, uint32_t &kept)
 {
-    return q == 0 ? v[0] : (q == 1 ? v[1] : (q == 2 ? v[2] : v[3]));
+    const uint32_t k0 = ((lo & 0x7FFFu) << 2) | 3u;
+    const uint32_t k1 = (((lo >> 16) & 0x7FFFu) << 2) | 2u;
+    const uint32_t k2 = ((hi & 0x7FFFu) << 2) | 1u;
+    const uint32_t k3 = (((hi >> 16) & 0x7FFFu) << 2) | 0u;
+    const uint32_t a = max(k0, k1), b = min(k0, k1), c = max(k2, k3), d = min(k2, k3);
+    const uint32_t top = max(a, c);
+    const uint32_t second = max(min(a, c), max(b, d));
+    const uint32_t qa = 3u - (top & 3u), qb = 3u - (second & 3u);
+    const uint32_t i0 = min(qa, qb), i1 = max(qa, qb);
+    const uint64_t grp = static_cast<uint64_t>(lo) | (static_cast<uint64_t>(hi) << 32);
+    const uint32_t v0 = static_cast<uint32_t>(grp >> (16u * i0)) & 0xFFFFu;
+    const uint32_t v1 = static_cast<uint32_t>(grp >> (16u * i1)) & 0xFFFFu;
+    kept = v0 | (v1 << 16);
+    return i0 | (i1 << 2);
 }
 
-__device__ __forceinline__ uint32_t pick_group(const uint16_t (&v)[4], uint16_t &k0, uint16_t &k1)
-{
-    uint32_t mag[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) mag[q] = v[q] & 0x7FFFu;
-    // first position of the largest magnitude
-    int first = 0;
-    uint32_t best = mag[0];
-#pragma unroll
-    for (int q = 1; q < 4; ++q)
-        if (mag[q] > best) best = mag[q], first = q;
-    // first position of the largest magnitude among the other three
-    int second = -1;
-    uint32_t best2 = 0;
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-        if (q != first && (second < 0 || mag[q] > best2)) best2 = mag[q], second = q;
-    const int i0 = first < second ? first : second;
-    const int i1 = first < second ? second : first;
-    k0 = at4(v, i0);
-    k1 = at4(v, i1);
-    return static_cast<uint32_t>(i0) | (static_cast<uint32_t>(i1) << 2);
-}
-
-// Compress: a "chunk" is 8 logical values of one row (one 16-byte load, two
-// groups); chunk c of the matrix is row c / (K/8).  Thread t of T handles
-// chunks t, t+T, t+2T, t+3T: its four loads are issued before any is used,
-// and each load instruction of a warp reads 512 contiguous bytes.  Per chunk
-// the thread writes its 4 kept values (8 bytes) and two nibbles; the 4 lanes
-// whose chunks make up one metadata word (32 logical values) OR their bytes
-// together with shuffles and the first of them stores the word.  K % 32 == 0
-// and T % 4 == 0 keep those 4 chunks in one row and in one aligned lane quad.
+// Compress: a "chunk" is 8 logical values of a row (one 16-byte load, two
+// groups).  Block (x, y) handles chunks [x*1024, x*1024 + 1024) of rows y,
+// y + gridDim.y, ...; thread t takes chunks t, t+256, t+512, t+768 of that
+// range, issuing the four loads before using any, and each warp load reads
+// 512 contiguous bytes.  Per chunk it writes its 4 kept values (8 bytes) and
+// two nibbles; the 4 lanes whose chunks form one metadata word (32 logical
+// values) OR their bytes with shuffles and the first stores the word.  K % 32
+// == 0 keeps those 4 chunks in one row and in one aligned lane quad.
 constexpr int CMP_CHUNKS = 4;
+constexpr int CMP_SEG = 256 * CMP_CHUNKS; // chunks per block and row
 
 __global__ void __launch_bounds__(256) sp_compress16_kernel(int64_t M, int64_t K, const uint16_t *__restrict__ A,
                                                             int64_t lda, uint16_t *__restrict__ Ac,
                                                             uint32_t *__restrict__ meta)
 {
-    const int64_t per_row = K / 8;
-    const int64_t total = M * per_row;
-    const int64_t T = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    const int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+    const int per_row = static_cast<int>(K / 8);
     const int lane = threadIdx.x & 31;
-    uint4 x[CMP_CHUNKS];
+    const int c_first = static_cast<int>(blockIdx.x) * CMP_SEG + static_cast<int>(threadIdx.x);
+    for (int64_t m = blockIdx.y; m < M; m += gridDim.y) {
+        const uint16_t *arow = A + m * lda;
+        uint2 *crow = reinterpret_cast<uint2 *>(Ac + m * (K / 2));
+        uint32_t *mrow = meta + m * (K / 32);
+        uint4 x[CMP_CHUNKS];
 #pragma unroll
-    for (int j = 0; j < CMP_CHUNKS; ++j) {
-        const int64_t c = t + j * T;
-        if (c < total) {
-            const int64_t m = c / per_row;
-            x[j] = __ldg(reinterpret_cast<const uint4 *>(A + m * lda + (c - m * per_row) * 8));
-        } else {
-            x[j] = make_uint4(0, 0, 0, 0);
+        for (int j = 0; j < CMP_CHUNKS; ++j) {
+            const int c = c_first + 256 * j;
+            x[j] = c < per_row ? __ldg(reinterpret_cast<const uint4 *>(arow) + c) : make_uint4(0, 0, 0, 0);
         }
-    }
 #pragma unroll
-    for (int j = 0; j < CMP_CHUNKS; ++j) {
-        const int64_t c = t + j * T;
-        const bool live = c < total;
-        const int64_t m = c / per_row;
-        const int64_t cc = c - m * per_row;
-        const uint32_t u[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
-        uint16_t out[4];
-        uint32_t byte = 0;
-#pragma unroll
-        for (int g = 0; g < 2; ++g) {
-            const uint16_t grp[4] = {static_cast<uint16_t>(u[2 * g] & 0xFFFFu), static_cast<uint16_t>(u[2 * g] >> 16),
-                                     static_cast<uint16_t>(u[2 * g + 1] & 0xFFFFu),
-                                     static_cast<uint16_t>(u[2 * g + 1] >> 16)};
-            byte |= pick_group(grp, out[2 * g], out[2 * g + 1]) << (4 * g);
+        for (int j = 0; j < CMP_CHUNKS; ++j) {
+            const int c = c_first + 256 * j;
+            uint32_t k0, k1;
+            const uint32_t byte = pick_group(x[j].x, x[j].y, k0) | (pick_group(x[j].z, x[j].w, k1) << 4);
+            if (c < per_row) crow[c] = make_uint2(k0, k1);
+            uint32_t word = byte << (8 * (lane & 3));
+            word |= __shfl_xor_sync(0xffffffffu, word, 1);
+            word |= __shfl_xor_sync(0xffffffffu, word, 2);
+            if (c < per_row && (lane & 3) == 0) mrow[c >> 2] = word;
         }
-        if (live) {
-            uint2 o;
-            o.x = static_cast<uint32_t>(out[0]) | (static_cast<uint32_t>(out[1]) << 16);
-            o.y = static_cast<uint32_t>(out[2]) | (static_cast<uint32_t>(out[3]) << 16);
-            *reinterpret_cast<uint2 *>(Ac + m * (K / 2) + cc * 4) = o;
-        }
-        uint32_t word = live ? byte << (8 * (lane & 3)) : 0u;
-        word |= __shfl_xor_sync(0xffffffffu, word, 1);
-        word |= __shfl_xor_sync(0xffffffffu, word, 2);
-        if (live && (lane & 3) == 0) meta[m * (K / 32) + cc / 4] = word;
     }
 }
 
@@ -164,12 +140,11 @@ cudaError_t launch_sp_compress(int64_t M, int64_t K, int elem_bytes, const void 
                                uint32_t *meta, cudaStream_t stream)
 {
     if (elem_bytes != 2) return cudaErrorInvalidValue;
-    const int64_t work = M * (K / 8); // chunks of 8 logical values
-    if (work == 0) return cudaSuccess;
-    const int64_t blocks = (work + 256 * CMP_CHUNKS - 1) / (256 * CMP_CHUNKS);
-    if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
-    sp_compress16_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        M, K, static_cast<const uint16_t *>(A), lda, static_cast<uint16_t *>(Ac), meta);
+    if (M == 0 || K == 0) return cudaSuccess;
+    const int64_t segs = (K / 8 + CMP_SEG - 1) / CMP_SEG;
+    const dim3 grid(static_cast<unsigned>(segs), static_cast<unsigned>(M < 65535 ? M : 65535), 1);
+    sp_compress16_kernel<<<grid, 256, 0, stream>>>(M, K, static_cast<const uint16_t *>(A), lda,
+                                                   static_cast<uint16_t *>(Ac), meta);
     return cudaGetLastError();
 }
 
