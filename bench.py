@@ -42,7 +42,8 @@ METRIC = "GEMM TFLOP/s (2MNK/t) at 8192^3 bf16 and FP8; % of GB300 dense tensor 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_OVER_BF16 = 4.5 / 2.25  # nominal dense ratio
 L2_BYTES = 129 * 10 ** 6
-KERNEL_SOURCES = ["tensor_core_matrix_gb300/csrc/tcm_gemm.cu", "tensor_core_matrix_gb300/csrc/tcm_ptx.cuh"]
+KERNEL_SOURCES = ["tensor_core_matrix_gb300/csrc/tcm_gemm_kernel.cuh", "tensor_core_matrix_gb300/csrc/tcm_kernel_common.cuh",
+                  "tensor_core_matrix_gb300/csrc/tcm_ptx.cuh", "tensor_core_matrix_gb300/csrc/tcm_gemm_pair.cu"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_kernel_bf16_8192cubed.md")
 
 
@@ -58,6 +59,7 @@ def parse_args():
     ap.add_argument("--shapes", action="store_true",
                     help="instead of the step, time every configured workload shape (one JSON line each)")
     ap.add_argument("--shape-iters", type=int, default=20)
+    ap.add_argument("--only", default="", help="with --shapes: only workloads whose name contains this text")
     return ap.parse_args()
 
 
@@ -157,6 +159,26 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
                 "reasons": reasons, "samples": len(rows), "samples_under_load": len(loaded),
                 "power_w_max": max(r[2] for r in rows)}
+
+
+def gpu_local_cpus(device_index):
+    """CPUs the kernel lists as local to the GPU (sysfs), or None if unknown."""
+    try:
+        props = torch.cuda.get_device_properties(device_index)
+        bdf = f"{props.pci_domain_id:04x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
+        text = open(f"/sys/bus/pci/devices/{bdf}/local_cpulist").read().strip()
+        cpus = set()
+        for part in text.split(","):
+            lo, _, hi = part.partition("-")
+            cpus.update(range(int(lo), int(hi or lo) + 1))
+        cpus &= os.sched_getaffinity(0)
+        return cpus or None
+    except (AttributeError, OSError, ValueError):
+        return None
+
+
+def local_rank_index(device):
+    return device.index if device.index is not None else torch.cuda.current_device()
 
 
 def make_inputs(device):
@@ -303,6 +325,8 @@ def run_shapes(args, tcm, device, peaks_used):
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
     for name, build in shape_cases():
+        if args.only and args.only not in name:
+            continue
         case = build()
         sparse = "A_logical" in case
         A = (case["A_logical"] if sparse else case["A"]).to(device)
@@ -392,7 +416,14 @@ def main():
     if args.shapes:
         run_shapes(args, tcm, device, peaks())
         return
+    # allocate (first-touch) the pinned host buffers from CPUs local to the GPU,
+    # so host<->device copies do not cross the CPU-to-CPU link
+    saved_affinity = os.sched_getaffinity(0)
+    local = gpu_local_cpus(local_rank_index(device))
+    if local:
+        os.sched_setaffinity(0, local)
     host, pinned, dev = make_inputs(device)
+    os.sched_setaffinity(0, saved_affinity)
     stream = torch.cuda.Stream(device=device)
 
     with torch.cuda.stream(stream):
@@ -504,7 +535,7 @@ def main():
             },
             "roofline": {"bound": "tensor", "achieved": ach_bf16, "peak": bf16_peak, "unit": "TFLOP/s",
                          "frac": ach_bf16 / bf16_peak, "traffic": traffic,
-                         "kernel": "gemm_kernel<kind::f16, BN=256> bf16 8192^3",
+                         "kernel": "gemm_kernel<kind::f16, 256x256 CTA-pair tile, 6 stages> bf16 8192^3",
                          "peak_source": f"{src} bf16_tflops_sustained (kernel timed inside a multi-second "
                                         f"back-to-back loop)",
                          "algorithmic_flop_per_launch": FLOP_PER_GEMM},
@@ -515,7 +546,9 @@ def main():
             line["e2e"] = {"value": world * flop_step / (e2e_max * 1e-3) / 1e12, "unit": "TFLOP/s",
                            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                            "note": f"{args.e2e_steps} steps; every step copies all inputs in from pinned host "
-                                   f"memory and all three D out; copies overlap the GEMMs of neighbouring steps"}
+                                   f"memory and all three D out; copies overlap the GEMMs of neighbouring steps; "
+                                   f"pinned buffers allocated from "
+                                   f"{'GPU-local CPUs ' + str(len(local)) if local else 'the default CPU set'}"}
         if not args.no_cpu_baseline and world == 1:
             line["cpu_baseline"] = cpu_baseline_sample(host, args.cpu_seconds)
         print(json.dumps(line), flush=True)
