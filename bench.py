@@ -184,6 +184,19 @@ def gpu_local_cpus(device_index):
         return None
 
 
+def slowest_rank(pg, values, device):
+    """Element-wise maximum of `values` over all ranks (the slowest rank's times decide)."""
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if pg is not None:
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def whole_job_rate(world, units_per_rank, seconds):
+    """Throughput of the whole job: the units all ranks processed over the slowest rank's time."""
+    return world * units_per_rank / seconds
+
+
 def local_rank_index(device):
     return device.index if device.index is not None else torch.cuda.current_device()
 
@@ -505,18 +518,14 @@ def main():
         e1.synchronize()
         e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
 
-    # slowest rank decides
-    times = torch.tensor([elapsed_ms, e2e_ms or 0.0], dtype=torch.float64, device=device)
-    if pg:
-        pg.all_reduce(times, op=pg.ReduceOp.MAX)
-    elapsed_ms, e2e_max = float(times[0]), float(times[1])
+    elapsed_ms, e2e_max = slowest_rank(pg, [elapsed_ms, e2e_ms or 0.0], device)
 
     if rank == 0:
         p, src = peaks()
         bf16_peak = float(p.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
         ms_step = elapsed_ms / args.steps
         flop_step = GEMMS_PER_STEP * FLOP_PER_GEMM
-        value = world * flop_step * args.steps / (elapsed_ms * 1e-3) / 1e12
+        value = whole_job_rate(world, flop_step * args.steps, elapsed_ms * 1e-3) / 1e12
         t_bf16 = statistics.mean(bf16_ms)
         t_fp8 = statistics.mean(fp8_ms)
         ach_bf16 = FLOP_PER_GEMM / (t_bf16 * 1e-3) / 1e12
@@ -550,7 +559,7 @@ def main():
             "clocks": clocks.summary(),
         }
         if e2e_ms:
-            line["e2e"] = {"value": world * flop_step / (e2e_max * 1e-3) / 1e12, "unit": "TFLOP/s",
+            line["e2e"] = {"value": whole_job_rate(world, flop_step, e2e_max * 1e-3) / 1e12, "unit": "TFLOP/s",
                            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                            "note": f"{args.e2e_steps} steps; every step copies all inputs in from pinned host "
                                    f"memory and all three D out; copies overlap the GEMMs of neighbouring steps; "
