@@ -18,6 +18,9 @@ Sources of the definitions (page titles and sections):
   (scale / bias / cast): "NVIDIA MMA", section "输入/累加/输出".
 * 2:4 sparse A with ordered position metadata: "NVIDIA MMA", sections
   "稠密乘法与 2:4 结构化稀疏乘法" and "Ampere：FP16/BF16 与整数 MMA 基线".
+* Block-scaled MMA (per-K-block scales applied before accumulation) and the
+  MXFP8 block size of 32 with E8M0 scales: "NVIDIA MMA", sections
+  "SM100：tcgen05.mma" and "MXFP4 与 NVFP4".
 """
 from __future__ import annotations
 
@@ -35,8 +38,8 @@ _lock = threading.Lock()
 _lib = None
 
 # The oracle's own format codes (mirrors the enum in oracle.c only).
-FMT = {"bf16": 0, "f16": 1, "f32": 2, "e4m3": 3, "e5m2": 4}
-ELEM_BYTES = {"bf16": 2, "f16": 2, "f32": 4, "e4m3": 1, "e5m2": 1}
+FMT = {"bf16": 0, "f16": 1, "f32": 2, "e4m3": 3, "e5m2": 4, "e8m0": 5}
+ELEM_BYTES = {"bf16": 2, "f16": 2, "f32": 4, "e4m3": 1, "e5m2": 1, "e8m0": 1}
 CODE_DTYPE = {1: np.uint8, 2: np.uint16, 4: np.uint32}
 # significand precision p (bits incl. the implicit one) and the smallest
 # positive subnormal of each output format; an RNE cast to the format is
@@ -79,6 +82,9 @@ def _load():
     lib.orc_gemm.restype = i32
     lib.orc_gemm.argtypes = [i64, i64, i64, i32, vp, i64, i32, vp, i64, i32, vp, i64,
                              i32, vp, dbl, dbl, dbl, dbl, i64, vp, vp, vp, vp]
+    lib.orc_gemm_mx.restype = i32
+    lib.orc_gemm_mx.argtypes = [i64, i64, i64, i64, i32, vp, i64, vp, i64, i32, vp, i64, vp, i64,
+                                i32, vp, i64, i32, vp, dbl, dbl, i64, vp, vp, vp, vp]
     lib.orc_sp_compress.restype = i32
     lib.orc_sp_compress.argtypes = [i64, i64, i32, vp, i64, vp, vp]
     lib.orc_sp_decompress.restype = i32
@@ -146,6 +152,44 @@ def gemm(A, B, a_fmt, b_fmt, *, C=None, c_fmt="f32", bias=None, bias_fmt="bf16",
                           nsamp, _ptr(r), _ptr(c), _ptr(ref), _ptr(S))
     if rc != 0:
         raise ValueError("orc_gemm rejected its arguments")
+    return ref, S
+
+
+def gemm_mx(A, SA, B, SB, a_fmt, b_fmt, *, block=32, C=None, c_fmt="f32", bias=None, bias_fmt="bf16",
+            alpha=1.0, beta=0.0, rows=None, cols=None):
+    """fp64 block-scaled reference (MX): sum_g 2^(SA[m,g]-127) 2^(SB[n,g]-127) sum_{k in g} a[m,k] b[n,k].
+
+    ``A`` M x K and ``B`` N x K element codes, ``SA`` M x K/block and ``SB``
+    N x K/block E8M0 scale codes (uint8); other arguments as :func:`gemm`.
+    Returns ``(ref, S)``.
+    """
+    A = _codes(A, a_fmt)
+    B = _codes(B, b_fmt)
+    SA = np.ascontiguousarray(SA, dtype=np.uint8)
+    SB = np.ascontiguousarray(SB, dtype=np.uint8)
+    M, lda = A.shape
+    N, ldb = B.shape
+    K = lda
+    if SA.shape != (M, K // block) or SB.shape != (N, K // block):
+        raise ValueError("scale arrays must be M x K/block and N x K/block")
+    Cc = None if C is None else _codes(C, c_fmt)
+    ldc = 0 if Cc is None else Cc.shape[1]
+    bc = None if bias is None else _codes(bias, bias_fmt)
+    if rows is None:
+        nsamp, r, c = -1, None, None
+        ref = np.empty((M, N), dtype=np.float64)
+    else:
+        r = np.ascontiguousarray(rows, dtype=np.int64)
+        c = np.ascontiguousarray(cols, dtype=np.int64)
+        nsamp = r.size
+        ref = np.empty(r.shape, dtype=np.float64)
+    S = np.empty_like(ref)
+    rc = _load().orc_gemm_mx(M, N, K, block, FMT[a_fmt], _ptr(A), lda, _ptr(SA), SA.shape[1],
+                             FMT[b_fmt], _ptr(B), ldb, _ptr(SB), SB.shape[1], FMT[c_fmt], _ptr(Cc), ldc,
+                             FMT[bias_fmt], _ptr(bc), float(alpha), float(beta), nsamp, _ptr(r), _ptr(c),
+                             _ptr(ref), _ptr(S))
+    if rc != 0:
+        raise ValueError("orc_gemm_mx rejected its arguments")
     return ref, S
 
 

@@ -39,8 +39,8 @@
 #include <stdlib.h>
 #include <string.h>
 
-/* The oracle's own element-format codes. */
-enum { ORC_BF16 = 0, ORC_F16 = 1, ORC_F32 = 2, ORC_E4M3 = 3, ORC_E5M2 = 4 };
+/* The oracle's own element-format codes (E8M0: the UE8M0 block-scale format). */
+enum { ORC_BF16 = 0, ORC_F16 = 1, ORC_F32 = 2, ORC_E4M3 = 3, ORC_E5M2 = 4, ORC_E8M0 = 5 };
 
 /* Width in bytes of one stored element of each format (0 = unknown). */
 int orc_elem_bytes(int fmt)
@@ -48,7 +48,7 @@ int orc_elem_bytes(int fmt)
     switch (fmt) {
     case ORC_BF16: case ORC_F16: return 2;
     case ORC_F32: return 4;
-    case ORC_E4M3: case ORC_E5M2: return 1;
+    case ORC_E4M3: case ORC_E5M2: case ORC_E8M0: return 1;
     default: return 0;
     }
 }
@@ -62,6 +62,7 @@ int orc_elem_bytes(int fmt)
  *              s.1111.111 is NaN, so e=15 with m<7 is an ordinary normal
  *              number (largest 1.75 * 2^8 = 448).
  *   E5M2 (OCP): s | e(5, bias 15) | m(2); e=31 is inf (m=0) or NaN.
+ *   E8M0 (OCP MX scale): e(8), value 2^(e - 127); e = 255 is NaN.
  * A zero exponent field means a subnormal: m * 2^(1 - bias - mbits).
  */
 double orc_decode(uint32_t code, int fmt)
@@ -78,6 +79,9 @@ double orc_decode(uint32_t code, int fmt)
         memcpy(&f, &u, sizeof f);
         return (double)f;
     }
+    case ORC_E8M0:
+        /* unsigned 8-bit exponent, no sign, no mantissa: 2^(e - 127); e = 255 is NaN */
+        return (code & 0xFFu) == 0xFFu ? NAN : ldexp(1.0, (int)(code & 0xFFu) - 127);
     default: return NAN;
     }
     sbit = ebits + mbits;
@@ -272,4 +276,64 @@ int orc_sp_decompress(int64_t M, int64_t K, int fmt, const void *Ac,
         }
     }
     return 0;
+}
+
+/*
+ * Block-scaled GEMM ("NVIDIA MMA", section "SM100：tcgen05.mma", the
+ * block-scaled form): D = C + sum_g (A_{q,g} S_{A,g}) (B_{q,g} S_{B,g}), the
+ * scales applied to each K block's partial sum before it enters the total.
+ * Blocks are `blk` consecutive K elements; sa[m*lds_a + g] and sb[n*lds_b + g]
+ * are the E8M0 scales of block g of row m of A and of row n of B.
+ *     acc = sum_g 2^(sa - 127) 2^(sb - 127) sum_{k in g} a[m,k] b[n,k]
+ *     S   = sum_g 2^(sa - 127) 2^(sb - 127) sum_{k in g} |a[m,k] b[n,k]|
+ *     ref = alpha * acc + beta * c[m,n] + bias[n]
+ * All in fp64 (block sums of at most 32 products of <= 4-bit significands
+ * are exact; the power-of-two scales are exact).  nsamp / rows / cols as in
+ * orc_gemm.  Returns 0 or -1.
+ */
+int orc_gemm_mx(int64_t M, int64_t N, int64_t K, int64_t blk,
+                int a_fmt, const void *A, int64_t lda, const uint8_t *sa, int64_t lds_a,
+                int b_fmt, const void *B, int64_t ldb, const uint8_t *sb, int64_t lds_b,
+                int c_fmt, const void *C, int64_t ldc, int bias_fmt, const void *bias,
+                double alpha, double beta,
+                int64_t nsamp, const int64_t *rows, const int64_t *cols,
+                double *ref, double *S)
+{
+    if (M < 0 || N < 0 || K < 0 || blk <= 0 || K % blk != 0) return -1;
+    if (!orc_elem_bytes(a_fmt) || !orc_elem_bytes(b_fmt)) return -1;
+    if (C && !orc_elem_bytes(c_fmt)) return -1;
+    if (bias && !orc_elem_bytes(bias_fmt)) return -1;
+    double *ta = decode_table(a_fmt);
+    double *tb = decode_table(b_fmt);
+    int64_t total = nsamp < 0 ? M * N : nsamp;
+    int bad = 0;
+
+#pragma omp parallel for schedule(dynamic, 16) reduction(| : bad)
+    for (int64_t s = 0; s < total; ++s) {
+        int64_t m = nsamp < 0 ? s / N : rows[s];
+        int64_t n = nsamp < 0 ? s % N : cols[s];
+        if (m < 0 || m >= M || n < 0 || n >= N) {
+            bad = 1;
+            continue;
+        }
+        double acc = 0.0, sabs = 0.0;
+        for (int64_t g = 0; g < K / blk; ++g) {
+            double part = 0.0, pabs = 0.0;
+            for (int64_t k = g * blk; k < (g + 1) * blk; ++k) {
+                double p = decoded(A, a_fmt, ta, m * lda + k) * decoded(B, b_fmt, tb, n * ldb + k);
+                part += p;
+                pabs += fabs(p);
+            }
+            double scale = orc_decode(sa[m * lds_a + g], ORC_E8M0) * orc_decode(sb[n * lds_b + g], ORC_E8M0);
+            acc += scale * part;
+            sabs += scale * pabs;
+        }
+        double c = C ? orc_decode(load_code(C, c_fmt, m * ldc + n), c_fmt) : 0.0;
+        double bv = bias ? orc_decode(load_code(bias, bias_fmt, n), bias_fmt) : 0.0;
+        ref[s] = alpha * acc + beta * c + bv;
+        S[s] = sabs;
+    }
+    free(ta);
+    free(tb);
+    return bad ? -1 : 0;
 }

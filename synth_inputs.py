@@ -14,6 +14,8 @@ Workloads (shapes, value distributions, seeds):
 * ``fp8``         8192^3 E4M3 (x E4M3 or E5M2), N(0,1) scaled so amax lands
                   on the format's largest finite value, bias bf16 ~ N(0,1), seed 3
 * ``sparse``      logical A ~ N(0,1) bf16 (pruned by the method), B ~ N(0,1), seed 4
+* ``mx``          MXFP8: N(0,1) in blocks of 32 along K with E8M0 scales (OCP MX
+                  conversion), E4M3 elements, seed 5
 """
 from __future__ import annotations
 
@@ -64,6 +66,34 @@ def fp8_per_tensor(x: torch.Tensor, fmt: str):
     s_quant = FP8_MAX[fmt] / amax if amax > 0 else 1.0
     q = (x * s_quant).clamp(-FP8_MAX[fmt], FP8_MAX[fmt]).to(TORCH_DTYPE[fmt])
     return q, float(torch.tensor(1.0 / s_quant, dtype=torch.float32))
+
+
+FP8_EMAX = {"e4m3": 8, "e5m2": 15}  # exponent of the largest finite value
+
+
+def mx_quantize(x: torch.Tensor, fmt: str, block: int = 32):
+    """Store fp32 ``x`` (rows x K) as MX blocks: per ``block`` consecutive K
+    elements one E8M0 scale 2^e with e = floor(log2(amax)) - emax(fmt) (the OCP
+    MX conversion; an all-zero block gets e = -127), elements stored in ``fmt``
+    with torch's round-to-nearest-even cast of x / 2^e, clamped to the format's
+    finite range.  Returns ``(q, scale_codes)``: q in ``fmt``, scale codes uint8
+    (rows x K/block, code = e + 127)."""
+    rows, K = x.shape
+    xb = x.reshape(rows, K // block, block).to(torch.float32)
+    amax = xb.abs().amax(dim=2)
+    e = torch.floor(torch.log2(torch.where(amax > 0, amax, torch.ones_like(amax)))) - FP8_EMAX[fmt]
+    e = torch.where(amax > 0, e, torch.full_like(e, -127.0)).clamp(-127, 127)
+    q = (xb / torch.exp2(e)[..., None]).clamp(-FP8_MAX[fmt], FP8_MAX[fmt]).reshape(rows, K)
+    return q.to(TORCH_DTYPE[fmt]), (e + 127).to(torch.uint8)
+
+
+def mx_case(M=8192, N=8192, K=8192, a_fmt="e4m3", b_fmt="e4m3", seed=5):
+    g = generator(seed)
+    xa = torch.randn((M, K), generator=g, dtype=torch.float32)
+    xb = torch.randn((N, K), generator=g, dtype=torch.float32)
+    A, SA = mx_quantize(xa, a_fmt)
+    B, SB = mx_quantize(xb, b_fmt)
+    return dict(A=A, SA=SA, B=B, SB=SB, a_fmt=a_fmt, b_fmt=b_fmt, out_fmt="bf16")
 
 
 def small_case(M=512, N=512, K=512, seed=0):

@@ -332,3 +332,89 @@ def test_sparse_decompress_rejects_unordered_metadata():
     meta = np.array([[0x33333333]], dtype=np.uint32)  # i0 = i1 = 3: not ascending
     with pytest.raises(ValueError):
         oracle.sp_decompress(Ac, meta, "bf16")
+
+
+# ---------------------------------------------------------------- block-scaled (MX)
+
+def test_decode_e8m0_exhaustive_closed_form():
+    import math
+    c = np.arange(256, dtype=np.uint8)
+    got = oracle.decode(c, "e8m0")
+    for e in range(255):
+        assert got[e] == math.ldexp(1.0, e - 127)
+    assert np.isnan(got[255])
+    if hasattr(torch, "float8_e8m0fnu"):
+        theirs = torch.from_numpy(c.copy()).view(torch.float8_e8m0fnu).to(torch.float64).numpy()
+        assert _same(got, theirs)
+
+
+def _mx_inputs(M, N, K, seed, fa="e4m3", fb="e4m3"):
+    g = si.generator(seed)
+    A, SA = si.mx_quantize(torch.randn((M, K), generator=g), fa)
+    B, SB = si.mx_quantize(torch.randn((N, K), generator=g), fb)
+    return si.codes(A), SA.numpy(), si.codes(B), SB.numpy()
+
+
+def test_mx_ones_closed_form():
+    """a = b = 1 everywhere, scales 2^u and 2^v per block: D = sum_g 32 * 2^(u_mg + v_ng)."""
+    M, N, K = 6, 5, 128
+    g = np.random.default_rng(4)
+    u = g.integers(-6, 6, (M, K // 32))
+    v = g.integers(-6, 6, (N, K // 32))
+    ones_a = si.codes(torch.ones((M, K), dtype=torch.float8_e4m3fn))
+    ones_b = si.codes(torch.ones((N, K), dtype=torch.float8_e4m3fn))
+    ref, S = oracle.gemm_mx(ones_a, (u + 127).astype(np.uint8), ones_b, (v + 127).astype(np.uint8),
+                            "e4m3", "e4m3")
+    expect = (32.0 * 2.0 ** (u[:, None, :] + v[None, :, :])).sum(axis=2)
+    assert np.array_equal(ref, expect) and np.array_equal(S, expect)
+
+
+@pytest.mark.parametrize("fa,fb", [("e4m3", "e4m3"), ("e4m3", "e5m2"), ("e5m2", "e5m2")])
+def test_mx_matches_numpy_expansion(fa, fb):
+    """Expanding every block scale onto its 32 elements and multiplying (numpy fp64)."""
+    M, N, K = 48, 40, 256
+    A, SA, B, SB = _mx_inputs(M, N, K, 17, fa, fb)
+    ref, S = oracle.gemm_mx(A, SA, B, SB, fa, fb)
+    ea = oracle.decode(A, fa) * np.repeat(oracle.decode(SA, "e8m0"), 32, axis=1)
+    eb = oracle.decode(B, fb) * np.repeat(oracle.decode(SB, "e8m0"), 32, axis=1)
+    assert np.all(np.abs(ref - ea @ eb.T) <= 1e-12 * S)
+    assert np.allclose(S, np.abs(ea) @ np.abs(eb).T, rtol=1e-12, atol=0)
+
+
+def test_mx_scales_enter_per_block_exact():
+    """Tiny case against exact rationals: each block's sum is scaled before it is added."""
+    M, N, K = 3, 2, 96
+    A, SA, B, SB = _mx_inputs(M, N, K, 23)
+    SA[0, 1] = 127 + 5  # make the per-block scales differ strongly
+    SB[1, 2] = 127 - 7
+    ref, _ = oracle.gemm_mx(A, SA, B, SB, "e4m3", "e4m3", alpha=0.5, bias=si.codes(torch.tensor([1.0, -2.0],
+                                                                                                  dtype=torch.bfloat16)))
+    a = oracle.decode(A, "e4m3")
+    b = oracle.decode(B, "e4m3")
+    for m in range(M):
+        for n in range(N):
+            total = Fraction(0)
+            for gi in range(K // 32):
+                part = sum(Fraction(a[m, k]) * Fraction(b[n, k]) for k in range(32 * gi, 32 * gi + 32))
+                total += part * Fraction(2) ** (int(SA[m, gi]) - 127) * Fraction(2) ** (int(SB[n, gi]) - 127)
+            want = Fraction(1, 2) * total + [Fraction(1), Fraction(-2)][n]
+            assert Fraction(ref[m, n]) == want
+
+
+def test_mx_unit_scales_equal_plain_gemm():
+    M, N, K = 20, 24, 160
+    A, _, B, _ = _mx_inputs(M, N, K, 29)
+    ones_a = np.full((M, K // 32), 127, dtype=np.uint8)
+    ones_b = np.full((N, K // 32), 127, dtype=np.uint8)
+    r1, s1 = oracle.gemm_mx(A, ones_a, B, ones_b, "e4m3", "e4m3")
+    r2, s2 = oracle.gemm(A, B, "e4m3", "e4m3")
+    assert np.array_equal(r1, r2) and np.array_equal(s1, s2)
+
+
+def test_mx_sampled_equals_full():
+    M, N, K = 30, 20, 64
+    A, SA, B, SB = _mx_inputs(M, N, K, 31)
+    full, Sf = oracle.gemm_mx(A, SA, B, SB, "e4m3", "e4m3")
+    r = np.array([0, 5, 29, 7]); c = np.array([0, 19, 3, 3])
+    samp, Ss = oracle.gemm_mx(A, SA, B, SB, "e4m3", "e4m3", rows=r, cols=c)
+    assert np.array_equal(samp, full[r, c]) and np.array_equal(Ss, Sf[r, c])
