@@ -157,6 +157,28 @@ tcm_status tcm_gemm_sp(int64_t M, int64_t N, int64_t K, tcm_dtype dtype,
                        tcm_dtype out_dtype, tcm_stream_t stream);
 
 /*
+ * tcm_gemm_mx -- block-scaled FP8 GEMM (MXFP8):
+ *   D = alpha * sum_g (A_g * 2^(sa_g - 127)) . (B_g * 2^(sb_g - 127)) + beta * C + bias
+ *
+ * "NVIDIA MMA", section "SM100：tcgen05.mma" (block-scaled form: each K block's
+ * partial sum is scaled by the A and B block scales before it is accumulated)
+ * and section "MXFP4 与 NVFP4" (MX formats: one UE8M0 scale per 32 elements).
+ *  a_dtype, b_dtype  TCM_E4M3 or TCM_E5M2 (any pair).
+ *  A                 M x K row-major (pitch K), B N x K (pitch K): the elements.
+ *  a_scales          M x K/32 uint8 row-major (pitch K/32): E8M0 scale codes
+ *                    (value 2^(code - 127); 255 is NaN) of the 32-element blocks
+ *                    of each row of A; b_scales likewise N x K/32 for B.
+ *  K                 a multiple of 32.
+ *  C, D, bias        as in tcm_gemm_ex with packed pitches (C, D: N; bias: N).
+ * All pointers 16-byte aligned; N * sizeof(out) a multiple of 16.
+ */
+tcm_status tcm_gemm_mx(int64_t M, int64_t N, int64_t K,
+                       tcm_dtype a_dtype, const void *A, const uint8_t *a_scales,
+                       tcm_dtype b_dtype, const void *B, const uint8_t *b_scales,
+                       const void *C, void *D, float alpha, float beta, const void *bias,
+                       tcm_dtype out_dtype, tcm_stream_t stream);
+
+/*
  * tcm_get_device_status -- synchronise `stream`, then report the first
  * device-side failure recorded since the last tcm_clear_device_status():
  * *code = TCM_OK or TCM_ERR_TIMEOUT, *site = which pipeline wait gave up

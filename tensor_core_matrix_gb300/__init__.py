@@ -26,7 +26,7 @@ STATUS_NAMES = {0: "TCM_OK", 1: "TCM_ERR_INVALID_ARG", 2: "TCM_ERR_UNSUPPORTED",
 DTYPE_CODE = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2,
               torch.float8_e4m3fn: 3, torch.float8_e5m2: 4}
 # Symbols the C ABI (include/tcm.h) exports.
-EXPORTS = ("tcm_gemm", "tcm_gemm_ex", "tcm_sp_compress", "tcm_sp_decompress", "tcm_gemm_sp",
+EXPORTS = ("tcm_gemm", "tcm_gemm_ex", "tcm_sp_compress", "tcm_sp_decompress", "tcm_gemm_sp", "tcm_gemm_mx",
            "tcm_get_device_status", "tcm_clear_device_status", "tcm_set_timeout_ns",
            "tcm_status_string", "tcm_version", "tcm_set_config_override", "tcm_debug_fail_next_launch")
 
@@ -61,6 +61,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.tcm_sp_decompress.argtypes = [i64, i64, i32, vp, vp, vp, i64, vp]
     lib.tcm_gemm_sp.restype = i32
     lib.tcm_gemm_sp.argtypes = [i64, i64, i64, i32, vp, vp, vp, vp, vp, f32, f32, i32, vp]
+    lib.tcm_gemm_mx.restype = i32
+    lib.tcm_gemm_mx.argtypes = [i64, i64, i64, i32, vp, vp, i32, vp, vp, vp, vp, f32, f32, vp, i32, vp]
     lib.tcm_get_device_status.restype = i32
     lib.tcm_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
     lib.tcm_clear_device_status.restype = i32
@@ -179,6 +181,23 @@ def tcm_gemm_sp(A_comp, meta, B, D, *, C=None, alpha=1.0, beta=0.0, stream=None)
     st = lib.tcm_gemm_sp(M, N, K, _code(A_comp, "A_comp"), _ptr(A_comp), _ptr(meta), _ptr(B), _ptr(C),
                          _ptr(D), float(alpha), float(beta), _code(D, "D"), _stream(stream))
     _check(st, "tcm_gemm_sp")
+    return D
+
+
+def tcm_gemm_mx(A, a_scales, B, b_scales, D, *, C=None, alpha=1.0, beta=0.0, bias=None, stream=None):
+    """Block-scaled FP8 GEMM: A (M x K) and B (N x K) in E4M3/E5M2, a_scales (M x K/32)
+    and b_scales (N x K/32) uint8 E8M0 codes; D (M x N); all contiguous CUDA tensors."""
+    lib = load_library()
+    M, K = A.shape
+    N = B.shape[0]
+    for t, n in ((A, "A"), (B, "B"), (a_scales, "a_scales"), (b_scales, "b_scales"), (D, "D")):
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    if tuple(a_scales.shape) != (M, K // 32) or tuple(b_scales.shape) != (N, K // 32):
+        raise ValueError("scales must be M x K/32 and N x K/32")
+    st = lib.tcm_gemm_mx(M, N, K, _code(A, "A"), _ptr(A), _ptr(a_scales), _code(B, "B"), _ptr(B), _ptr(b_scales),
+                         _ptr(C), _ptr(D), float(alpha), float(beta), _ptr(bias), _code(D, "D"), _stream(stream))
+    _check(st, "tcm_gemm_mx")
     return D
 
 

@@ -403,6 +403,81 @@ tcm_status tcm_gemm_sp(int64_t M, int64_t N, int64_t K, tcm_dtype dtype, const v
     return e == cudaSuccess ? TCM_OK : TCM_ERR_CUDA;
 }
 
+tcm_status tcm_gemm_mx(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const void *A, const uint8_t *a_scales,
+                       tcm_dtype b_dtype, const void *B, const uint8_t *b_scales, const void *C, void *D,
+                       float alpha, float beta, const void *bias, tcm_dtype out_dtype, tcm_stream_t stream)
+{
+    const bool a8 = a_dtype == TCM_E4M3 || a_dtype == TCM_E5M2;
+    const bool b8 = b_dtype == TCM_E4M3 || b_dtype == TCM_E5M2;
+    if (!a8 || !b8) return TCM_ERR_UNSUPPORTED;
+    if (out_dtype != TCM_BF16 && out_dtype != TCM_F16 && out_dtype != TCM_F32) return TCM_ERR_UNSUPPORTED;
+    if (M < 1 || N < 1 || K < 0 || K % 32 != 0) return TCM_ERR_INVALID_ARG;
+    if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2) return TCM_ERR_UNSUPPORTED;
+    if (!D || (K > 0 && (!A || !B || !a_scales || !b_scales)) || (beta != 0.f && !C)) return TCM_ERR_INVALID_ARG;
+    const int eo = elem_bytes(out_dtype);
+    if ((A && !aligned16(A)) || (B && !aligned16(B)) || (a_scales && !aligned16(a_scales)) ||
+        (b_scales && !aligned16(b_scales)) || !aligned16(D) || (C && !aligned16(C)) || (bias && !aligned16(bias)))
+        return TCM_ERR_MISALIGNED;
+    if ((N * eo) % 16) return TCM_ERR_MISALIGNED;
+    const int64_t sms = sm_count();
+    if (sms <= 0) return TCM_ERR_CUDA;
+
+    GemmConfig cfg{};
+    cfg.kind = 3;
+    cfg.cta_group = 1;
+    cfg.ksplit = 1;
+    cfg.katoms = 1;
+    cfg.bn = N > 128 ? 256 : 128;
+    if (g_force_bn.load() == 128 || g_force_bn.load() == 256) cfg.bn = g_force_bn.load();
+
+    CUtensorMap tmA, tmB;
+    std::memset(&tmA, 0, sizeof tmA);
+    std::memset(&tmB, 0, sizeof tmB);
+    if (K > 0) {
+        if (!encode_kmajor(&tmA, A, 1, static_cast<uint64_t>(K), static_cast<uint64_t>(M), static_cast<uint64_t>(K), 128))
+            return TCM_ERR_CUDA;
+        if (!encode_kmajor(&tmB, B, 1, static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(K),
+                           static_cast<uint32_t>(cfg.bn)))
+            return TCM_ERR_CUDA;
+    }
+    GemmParams p{};
+    p.kM = static_cast<int>(M);
+    p.kN = static_cast<int>(N);
+    p.K = static_cast<int>(K);
+    p.num_kb = static_cast<int>((K + 127) / 128);
+    p.tiles_m = static_cast<int>((M + 127) / 128);
+    p.tiles_n = static_cast<int>((N + cfg.bn - 1) / cfg.bn);
+    p.num_tiles = p.tiles_m * p.tiles_n;
+    p.group_m = g_force_group_m.load() > 0 ? g_force_group_m.load() : 16;
+    p.tile_begin = 0;
+    p.tile_end = p.num_tiles;
+    p.D = D;
+    p.ldd = N;
+    p.C = beta != 0.f ? C : nullptr;
+    p.ldc = N;
+    p.bias = bias;
+    p.a_scale = p.b_scale = nullptr;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.out_fmt = static_cast<int>(out_dtype);
+    p.swap_ab = 0;
+    // block-scaled instruction descriptor: [7,10) A format, [10,13) B format (E4M3 = 0,
+    // E5M2 = 1), [17,23) N >> 3, [23] scale type (1 = UE8M0), [24,29) M >> 4; the
+    // per-MMA scale-factor ids ([4,6) B, [29,31) A) are added by the kernel
+    p.idesc = ((a_dtype == TCM_E5M2 ? 1u : 0u) << 7) | ((b_dtype == TCM_E5M2 ? 1u : 0u) << 10) |
+              ((static_cast<uint32_t>(cfg.bn) >> 3) << 17) | (1u << 23) | ((128u >> 4) << 24);
+    p.timeout_ns = timeout_ns();
+    p.status = device_status_ptr();
+    if (!p.status) return TCM_ERR_CUDA;
+    p.fault_inject = 0;
+    p.sfa = a_scales;
+    p.sfb = b_scales;
+    p.sf_ld = K / 32;
+    const int grid = static_cast<int>(p.num_tiles < sms ? p.num_tiles : sms);
+    const cudaError_t e = launch_gemm_mx(cfg, tmA, tmB, p, grid, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TCM_OK : TCM_ERR_CUDA;
+}
+
 tcm_status tcm_get_device_status(tcm_stream_t stream, int32_t *code, int32_t *site)
 {
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return TCM_ERR_CUDA;

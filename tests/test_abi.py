@@ -87,3 +87,10 @@ def test_sparse_rejects_bad_arguments(lib, M, K, dtype, lda, status):
 def test_library_is_built_for_sm_103a_only():
     src = open(os.path.join(ROOT, "tensor_core_matrix_gb300", "build.py")).read()
     assert "arch=compute_103a,code=sm_103a" in src
+
+
+@pytest.mark.parametrize("a,b,K,status", [(E4M3, BF16, 64, 2), (BF16, BF16, 64, 2), (E4M3, E5M2, 48, 1),
+                                          (E4M3, E4M3, -32, 1)])
+def test_gemm_mx_rejects_bad_arguments(lib, a, b, K, status):
+    assert lib.tcm_gemm_mx(64, 64, K, a, ALIGNED, ALIGNED, b, ALIGNED, ALIGNED, None, ALIGNED, 1.0, 0.0, None,
+                           BF16, None) == status

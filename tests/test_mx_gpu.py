@@ -1,0 +1,91 @@
+"""GPU parity of the block-scaled (MXFP8) GEMM against the oracle's block-scaled reference."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth_inputs as si
+from parity import dev, ratio, sample_indices
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _build():
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    import tensor_core_matrix_gb300 as tcm
+    tcm.tcm_clear_device_status()
+
+
+@pytest.fixture
+def tcm():
+    import tensor_core_matrix_gb300 as t
+    yield t
+    t.tcm_set_config_override(0, 0, 0, 0, 0)
+
+
+def run_mx(tcm, A, SA, B, SB, out=torch.bfloat16, C=None, beta=0.0, alpha=1.0, bias=None):
+    d = dev()
+    M, N = A.shape[0], B.shape[0]
+    D = torch.full((M, N), float("nan"), dtype=out, device=d)
+    tcm.tcm_gemm_mx(A.to(d), SA.to(d), B.to(d), SB.to(d), D, C=None if C is None else C.to(d), alpha=alpha,
+                    beta=beta, bias=None if bias is None else bias.to(d))
+    code, site = tcm.tcm_get_device_status()
+    assert code == 0, (code, site)
+    return D.cpu()
+
+
+def oracle_mx(A, SA, B, SB, fa, fb, **kw):
+    return oracle.gemm_mx(si.codes(A), SA.numpy(), si.codes(B), SB.numpy(), fa, fb, **kw)
+
+
+@pytest.mark.parametrize("bn", [0, 128, 256])
+@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (256, 512, 1024), (300, 520, 416), (1000, 136, 96)])
+def test_mx_integer_exact(tcm, bn, M, N, K):
+    tcm.tcm_set_config_override(0, bn)
+    g = si.generator(M + N + K)
+    A = si.integers((M, K), g, dtype="e4m3")
+    B = si.integers((N, K), g, dtype="e4m3")
+    SA = torch.randint(126, 129, (M, K // 32), generator=g).to(torch.uint8)
+    SB = torch.randint(126, 129, (N, K // 32), generator=g).to(torch.uint8)
+    D = run_mx(tcm, A, SA, B, SB, out=torch.float32)
+    ref, _ = oracle_mx(A, SA, B, SB, "e4m3", "e4m3")
+    assert np.array_equal(D.double().numpy(), ref)
+
+
+@pytest.mark.parametrize("fa,fb", [("e4m3", "e4m3"), ("e4m3", "e5m2"), ("e5m2", "e4m3")])
+@pytest.mark.parametrize("bn", [128, 256])
+def test_mx_normal_data_bound(tcm, fa, fb, bn):
+    tcm.tcm_set_config_override(0, bn)
+    c = si.mx_case(640, 768, 1024, a_fmt=fa, b_fmt=fb, seed=7)
+    g = si.generator(8)
+    C = si.normal((640, 768), g)
+    bias = si.normal((768,), g)
+    D = run_mx(tcm, c["A"], c["SA"], c["B"], c["SB"], C=C, beta=0.5, alpha=2.0, bias=bias)
+    ref, S = oracle_mx(c["A"], c["SA"], c["B"], c["SB"], fa, fb, C=si.codes(C), c_fmt="bf16", beta=0.5,
+                       alpha=2.0, bias=si.codes(bias))
+    assert ratio(D, ref, S, scale=2.0) <= 1.0
+
+
+def test_mx_wide_scale_range_bound(tcm):
+    """Block scales spread over many binades (2^-20 .. 2^20) still meet the bound."""
+    M, N, K = 256, 256, 512
+    g = si.generator(9)
+    A = si.normal((M, K), g, dtype="e4m3")
+    B = si.normal((N, K), g, dtype="e4m3")
+    SA = torch.randint(107, 148, (M, K // 32), generator=g).to(torch.uint8)
+    SB = torch.randint(107, 148, (N, K // 32), generator=g).to(torch.uint8)
+    D = run_mx(tcm, A, SA, B, SB, out=torch.float32)
+    ref, S = oracle_mx(A, SA, B, SB, "e4m3", "e4m3")
+    assert ratio(D, ref, S) <= 1.0
+
+
+def test_mx_8192_sampled(tcm):
+    c = si.mx_case()
+    D = run_mx(tcm, c["A"], c["SA"], c["B"], c["SB"])
+    rows, cols = sample_indices(8192, 8192)
+    ref, S = oracle_mx(c["A"], c["SA"], c["B"], c["SB"], "e4m3", "e4m3", rows=rows, cols=cols)
+    assert ratio(D, ref, S, rows=rows, cols=cols) <= 1.0
+    assert not torch.isnan(D).any()
