@@ -334,6 +334,7 @@ def shape_cases():
         ("fp8 e4m3xe4m3 8192^3 +scales+bias", lambda: si.fp8_case(b_fmt="e4m3")),
         ("fp8 e4m3xe5m2 8192^3 +scales+bias", lambda: si.fp8_case(b_fmt="e5m2")),
         ("sparse 2:4 bf16 8192^3", lambda: si.sparse_case()),
+        ("mxfp8 e4m3 8192^3 (E8M0 scales per 32)", lambda: si.mx_case()),
     ]
 
 
@@ -363,6 +364,9 @@ def run_shapes(args, tcm, device, peaks_used):
         if sparse:
             Ac, meta = tcm.tcm_sp_compress(A)
             launch = lambda: tcm.tcm_gemm_sp(Ac, meta, B, D, C=C, alpha=kw["alpha"], beta=kw["beta"])
+        elif "SA" in case:
+            SA, SB = case["SA"].to(device), case["SB"].to(device)
+            launch = lambda: tcm.tcm_gemm_mx(A, SA, B, SB, D)
         else:
             launch = lambda: tcm.tcm_gemm_ex(A, B, D, **kw)
         for _ in range(3):
@@ -386,7 +390,7 @@ def run_shapes(args, tcm, device, peaks_used):
         byts = in_bytes + D.numel() * D.element_size() + (C.numel() * C.element_size() if C is not None else 0)
         tf = flop / (ms * 1e-3) / 1e12
         gbs = byts / (ms * 1e-3) / 1e9
-        peak = bf16_peak * (FP8_OVER_BF16 if "fp8" in name else 1.0)
+        peak = bf16_peak * (FP8_OVER_BF16 if ("fp8" in name or "mx" in name) else 1.0)
         line = {"kind": "shape", "workload": name, "M": M, "N": N, "K": K, "ms_median": ms, "ms_min": min(times),
                 "tflops": tf, "frac_of_tensor_peak": tf / peak, "algorithmic_bytes": byts, "gbs": gbs,
                 "frac_of_hbm": gbs / hbm_peak, "bound": "hbm" if M <= 64 else "tensor", "device_status": code,
