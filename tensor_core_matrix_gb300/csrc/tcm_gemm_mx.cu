@@ -11,7 +11,8 @@
 // Pipeline as the dense kernel (TMA ring of 128-byte K stages = 128 FP8
 // values, four MMAs of K = 32 per stage, one thread issuing, TMEM
 // accumulators, tcgen05.ld epilogue), plus two groups of four warps that put
-// each stage's scales into tensor memory, alternating stages.
+// each stage's scales into tensor memory (each group owns half of the
+// stages of the ring).
 //
 // Scale layout in tensor memory (established on the GPU by a decoding probe,
 // every (row, MMA) traced to its source; 0 mismatches): the scale of operand
@@ -28,7 +29,6 @@ namespace tcm {
 
 constexpr int MX_GROUPS = 2;
 constexpr int MX_THREADS = 32 * (2 + 4 + 4 * MX_GROUPS); // TMA, MMA, 4 epilogue, 2 x 4 scale warps
-constexpr int MX_AHEAD = 4;                               // stages of scales fetched ahead, per group
 constexpr uint32_t MX_SCALE_ONE = 0x7F7F7F7Fu;           // four E8M0 codes 127 = 1.0
 
 template <int BN, int STAGES>
@@ -56,18 +56,26 @@ __device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t
         : "memory");
 }
 
-// The four scale codes of row `row` (of `rows` rows) for logical K [128 kb, 128 kb + 128).
-__device__ __forceinline__ uint32_t load_scales4(const uint8_t *scales, long long ld, int row, int rows, int kb)
+// The sixteen scale codes of row `row` (of `rows` rows) for K blocks
+// [kb0, kb0 + 4) of 128 values each, as four words (word j = K block kb0 + j,
+// byte i of it = the i-th 32-element block).  Missing rows and blocks read 1.0.
+__device__ __forceinline__ uint4 load_scales16(const uint8_t *scales, long long ld, int row, int rows, int kb0)
 {
-    if (row >= rows) return MX_SCALE_ONE;
-    const long long first = static_cast<long long>(kb) * 4;
+    uint4 v = make_uint4(MX_SCALE_ONE, MX_SCALE_ONE, MX_SCALE_ONE, MX_SCALE_ONE);
+    if (row >= rows) return v;
+    const long long first = static_cast<long long>(kb0) * 4;
     const uint8_t *src = scales + static_cast<long long>(row) * ld + first;
-    if (first + 4 <= ld && (reinterpret_cast<uintptr_t>(src) & 3u) == 0) return __ldg(reinterpret_cast<const uint32_t *>(src));
-    uint32_t w = MX_SCALE_ONE;
+    if (first + 16 <= ld && (reinterpret_cast<uintptr_t>(src) & 15u) == 0) return __ldg(reinterpret_cast<const uint4 *>(src));
+    uint32_t w[4] = {MX_SCALE_ONE, MX_SCALE_ONE, MX_SCALE_ONE, MX_SCALE_ONE};
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-        if (first + j < ld) w = (w & ~(0xFFu << (8 * j))) | (static_cast<uint32_t>(__ldg(src + j)) << (8 * j));
-    return w;
+    for (int b = 0; b < 16; ++b)
+        if (first + b < ld) w[b / 4] = (w[b / 4] & ~(0xFFu << (8 * (b % 4)))) | (static_cast<uint32_t>(__ldg(src + b)) << (8 * (b % 4)));
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4 &v, int j)
+{
+    return j == 0 ? v.x : (j == 1 ? v.y : (j == 2 ? v.z : v.w));
 }
 
 template <int BN, int STAGES, int NACC>
@@ -237,67 +245,64 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
             }
         }
     } else {
-        // scale warps: group g takes stages i with i % 2 == g; each warp writes the
-        // stage's scales into its own lane quadrant (every quadrant reads its copy)
+        // Scale warps.  Group g owns stages [g*S/2, (g+1)*S/2) of the S-stage ring
+        // and handles, in order, every (tile, K block) item that lands in one of
+        // its stages -- so it never skips a use of its stages and its parity
+        // waits are never two phases ahead.  Per row it loads 16 bytes at a time:
+        // the scales of K blocks 4q .. 4q+3 (one load per row for up to four
+        // items), issued before the wait for the item's free stage so the
+        // latency overlaps that wait.  Per item it writes word (kb % 4) of each
+        // row into the stage's scale columns of its own lane quadrant (every
+        // quadrant reads its own copy).
         const int quad = warp & 3;
         const int group = (warp - 2 - EPI_WARPS) / 4;
+        constexpr int OWN = STAGES / MX_GROUPS;
+        const int s_lo = group * OWN;
         const uint32_t lanebase = static_cast<uint32_t>(quad * 32) << 16;
         const int my_tiles = first_tile < p.tile_end ? (p.tile_end - 1 - first_tile) / step + 1 : 0;
         const long long items = static_cast<long long>(my_tiles) * p.num_kb;
-        uint32_t ring_a[MX_AHEAD][4], ring_b[MX_AHEAD][SFB_COLS];
-#pragma unroll
-        for (int u = 0; u < MX_AHEAD; ++u) {
-            const long long i = group + static_cast<long long>(MX_GROUPS) * u;
-            if (i < items) {
+        long long cached = -1;
+        uint4 sa[4], sb[SFB_COLS];
+        bool ok = true;
+        for (long long i = 0; ok && i < items; ++i) {
+            const int stage = static_cast<int>(i % STAGES);
+            if (stage < s_lo || stage >= s_lo + OWN) continue;
+            const int tl = static_cast<int>(i / p.num_kb);
+            const int kb = static_cast<int>(i % p.num_kb);
+            const long long key = static_cast<long long>(tl) * p.num_kb + (kb & ~3);
+            if (key != cached) {
                 int mb, nb;
-                tile_coords(p, first_tile + static_cast<int>(i / p.num_kb) * step, mb, nb);
-                const int kb = static_cast<int>(i % p.num_kb);
+                tile_coords(p, first_tile + tl * step, mb, nb);
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    ring_a[u][c] = load_scales4(p.sfa, p.sf_ld, mb * BM + 32 * c + lane, p.kM, kb);
+                for (int c = 0; c < 4; ++c) sa[c] = load_scales16(p.sfa, p.sf_ld, mb * BM + 32 * c + lane, p.kM, kb & ~3);
 #pragma unroll
                 for (int c = 0; c < SFB_COLS; ++c)
-                    ring_b[u][c] = load_scales4(p.sfb, p.sf_ld, nb * BN + 32 * c + lane, p.kN, kb);
+                    sb[c] = load_scales16(p.sfb, p.sf_ld, nb * BN + 32 * c + lane, p.kN, kb & ~3);
+                cached = key;
             }
-        }
-        bool ok = true;
-        for (long long base = group; ok && base < items; base += static_cast<long long>(MX_GROUPS) * MX_AHEAD) {
-#pragma unroll
-            for (int u = 0; u < MX_AHEAD; ++u) {
-                const long long i = base + static_cast<long long>(MX_GROUPS) * u;
-                if (!ok || i >= items) break;
-                const int stage = static_cast<int>(i % STAGES);
-                const uint32_t phase = static_cast<uint32_t>((i / STAGES) & 1);
-                int okw = 1;
-                if (lane == 0) okw = wait_bar<1>(empty + stage, phase ^ 1u, w, SITE_META_EMPTY, true);
-                okw = __shfl_sync(0xffffffffu, okw, 0);
-                if (!okw) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t col = tmem_base + SF_COL + static_cast<uint32_t>(stage) * SF_STAGE_COLS + lanebase;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_st_32x32b_x1(col + c, ring_a[u][c]);
-#pragma unroll
-                for (int c = 0; c < SFB_COLS; ++c) tmem_st_32x32b_x1(col + 8 + c, ring_b[u][c]);
-                const long long next = i + static_cast<long long>(MX_GROUPS) * MX_AHEAD;
-                if (next < items) {
-                    int mb, nb;
-                    tile_coords(p, first_tile + static_cast<int>(next / p.num_kb) * step, mb, nb);
-                    const int kb = static_cast<int>(next % p.num_kb);
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        ring_a[u][c] = load_scales4(p.sfa, p.sf_ld, mb * BM + 32 * c + lane, p.kM, kb);
-#pragma unroll
-                    for (int c = 0; c < SFB_COLS; ++c)
-                        ring_b[u][c] = load_scales4(p.sfb, p.sf_ld, nb * BN + 32 * c + lane, p.kN, kb);
-                }
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(sf_full + stage);
+            const uint32_t phase = static_cast<uint32_t>((i / STAGES) & 1);
+            int okw = 1;
+            if (lane == 0) okw = wait_bar<1>(empty + stage, phase ^ 1u, w, SITE_META_EMPTY, true);
+            okw = __shfl_sync(0xffffffffu, okw, 0);
+            if (!okw) {
+                ok = false;
+                break;
             }
+            tc_fence_after();
+            const int j = kb & 3;
+            uint32_t wa[4], wb[SFB_COLS];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) wa[c] = word_of(sa[c], j);
+#pragma unroll
+            for (int c = 0; c < SFB_COLS; ++c) wb[c] = word_of(sb[c], j);
+            const uint32_t col = tmem_base + SF_COL + static_cast<uint32_t>(stage) * SF_STAGE_COLS + lanebase;
+            tmem_st_32x32b_x4(col, wa);
+            if constexpr (SFB_COLS == 8) tmem_st_32x32b_x8(col + 8, wb);
+            else tmem_st_32x32b_x4(col + 8, wb);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sf_full + stage);
         }
     }
 
