@@ -429,6 +429,10 @@ tcm_status tcm_gemm_mx(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const
     cfg.katoms = 1;
     cfg.bn = N > 128 ? 256 : 128;
     if (g_force_bn.load() == 128 || g_force_bn.load() == 256) cfg.bn = g_force_bn.load();
+    // CTA pairs (256 x 256 tiles) when they still give every pair work
+    if (cfg.bn == 256 && M > 128 && ((M + 255) / 256) * ((N + 255) / 256) >= sms / 2) cfg.cta_group = 2;
+    if (g_force_cta_group.load() == 1 || g_force_cta_group.load() == 2) cfg.cta_group = g_force_cta_group.load();
+    if (cfg.bn != 256) cfg.cta_group = 1;
 
     CUtensorMap tmA, tmB;
     std::memset(&tmA, 0, sizeof tmA);
@@ -437,7 +441,7 @@ tcm_status tcm_gemm_mx(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const
         if (!encode_kmajor(&tmA, A, 1, static_cast<uint64_t>(K), static_cast<uint64_t>(M), static_cast<uint64_t>(K), 128))
             return TCM_ERR_CUDA;
         if (!encode_kmajor(&tmB, B, 1, static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(K),
-                           static_cast<uint32_t>(cfg.bn)))
+                           static_cast<uint32_t>(cfg.bn / cfg.cta_group)))
             return TCM_ERR_CUDA;
     }
     GemmParams p{};
@@ -445,7 +449,7 @@ tcm_status tcm_gemm_mx(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const
     p.kN = static_cast<int>(N);
     p.K = static_cast<int>(K);
     p.num_kb = static_cast<int>((K + 127) / 128);
-    p.tiles_m = static_cast<int>((M + 127) / 128);
+    p.tiles_m = static_cast<int>((M + 128 * cfg.cta_group - 1) / (128 * cfg.cta_group));
     p.tiles_n = static_cast<int>((N + cfg.bn - 1) / cfg.bn);
     p.num_tiles = p.tiles_m * p.tiles_n;
     p.group_m = g_force_group_m.load() > 0 ? g_force_group_m.load() : 16;
@@ -465,7 +469,8 @@ tcm_status tcm_gemm_mx(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const
     // E5M2 = 1), [17,23) N >> 3, [23] scale type (1 = UE8M0), [24,29) M >> 4; the
     // per-MMA scale-factor ids ([4,6) B, [29,31) A) are added by the kernel
     p.idesc = ((a_dtype == TCM_E5M2 ? 1u : 0u) << 7) | ((b_dtype == TCM_E5M2 ? 1u : 0u) << 10) |
-              ((static_cast<uint32_t>(cfg.bn) >> 3) << 17) | (1u << 23) | ((128u >> 4) << 24);
+              ((static_cast<uint32_t>(cfg.bn) >> 3) << 17) | (1u << 23) |
+              (((128u * static_cast<uint32_t>(cfg.cta_group)) >> 4) << 24);
     p.timeout_ns = timeout_ns();
     p.status = device_status_ptr();
     if (!p.status) return TCM_ERR_CUDA;
@@ -473,7 +478,8 @@ tcm_status tcm_gemm_mx(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const
     p.sfa = a_scales;
     p.sfb = b_scales;
     p.sf_ld = K / 32;
-    const int grid = static_cast<int>(p.num_tiles < sms ? p.num_tiles : sms);
+    const int64_t clusters = sms / cfg.cta_group;
+    const int grid = static_cast<int>((p.num_tiles < clusters ? p.num_tiles : clusters) * cfg.cta_group);
     const cudaError_t e = launch_gemm_mx(cfg, tmA, tmB, p, grid, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TCM_OK : TCM_ERR_CUDA;
 }

@@ -41,10 +41,14 @@ def oracle_mx(A, SA, B, SB, fa, fb, **kw):
     return oracle.gemm_mx(si.codes(A), SA.numpy(), si.codes(B), SB.numpy(), fa, fb, **kw)
 
 
-@pytest.mark.parametrize("bn", [0, 128, 256])
+# (cta_group, tile_n): 0 = the library's choice; (2, 256) = the CTA-pair 256 x 256 tile
+VARIANTS = [(0, 0), (1, 128), (1, 256), (2, 256)]
+
+
+@pytest.mark.parametrize("cg,bn", VARIANTS)
 @pytest.mark.parametrize("M,N,K", [(128, 128, 128), (256, 512, 1024), (300, 520, 416), (1000, 136, 96)])
-def test_mx_integer_exact(tcm, bn, M, N, K):
-    tcm.tcm_set_config_override(0, bn)
+def test_mx_integer_exact(tcm, cg, bn, M, N, K):
+    tcm.tcm_set_config_override(cg, bn)
     g = si.generator(M + N + K)
     A = si.integers((M, K), g, dtype="e4m3")
     B = si.integers((N, K), g, dtype="e4m3")
@@ -56,9 +60,9 @@ def test_mx_integer_exact(tcm, bn, M, N, K):
 
 
 @pytest.mark.parametrize("fa,fb", [("e4m3", "e4m3"), ("e4m3", "e5m2"), ("e5m2", "e4m3")])
-@pytest.mark.parametrize("bn", [128, 256])
-def test_mx_normal_data_bound(tcm, fa, fb, bn):
-    tcm.tcm_set_config_override(0, bn)
+@pytest.mark.parametrize("cg,bn", VARIANTS[1:])
+def test_mx_normal_data_bound(tcm, fa, fb, cg, bn):
+    tcm.tcm_set_config_override(cg, bn)
     c = si.mx_case(640, 768, 1024, a_fmt=fa, b_fmt=fb, seed=7)
     g = si.generator(8)
     C = si.normal((640, 768), g)
@@ -82,7 +86,9 @@ def test_mx_wide_scale_range_bound(tcm):
     assert ratio(D, ref, S) <= 1.0
 
 
-def test_mx_8192_sampled(tcm):
+@pytest.mark.parametrize("cg", [0, 1])
+def test_mx_8192_sampled(tcm, cg):
+    tcm.tcm_set_config_override(cg, 0)
     c = si.mx_case()
     D = run_mx(tcm, c["A"], c["SA"], c["B"], c["SB"])
     rows, cols = sample_indices(8192, 8192)
