@@ -365,7 +365,9 @@ def run_shapes(args, tcm, device, peaks_used):
             Ac, meta = tcm.tcm_sp_compress(A)
             launch = lambda: tcm.tcm_gemm_sp(Ac, meta, B, D, C=C, alpha=kw["alpha"], beta=kw["beta"])
         elif "SA" in case:
-            SA, SB = case["SA"].to(device), case["SB"].to(device)
+            # scales packed once into the blocked layout (as a quantiser would emit them)
+            SA = tcm.tcm_mx_pack_scales(case["SA"].to(device), K)
+            SB = tcm.tcm_mx_pack_scales(case["SB"].to(device), K)
             launch = lambda: tcm.tcm_gemm_mx(A, SA, B, SB, D)
         else:
             launch = lambda: tcm.tcm_gemm_ex(A, B, D, **kw)

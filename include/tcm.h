@@ -162,12 +162,14 @@ tcm_status tcm_gemm_sp(int64_t M, int64_t N, int64_t K, tcm_dtype dtype,
  *
  * "NVIDIA MMA", section "SM100：tcgen05.mma" (block-scaled form: each K block's
  * partial sum is scaled by the A and B block scales before it is accumulated)
- * and section "MXFP4 与 NVFP4" (MX formats: one UE8M0 scale per 32 elements).
+ * and section "MXFP4 与 NVFP4" (MX formats: one UE8M0 scale per 32 elements;
+ * kernels follow a scale layout contract, which is the blocked layout below).
  *  a_dtype, b_dtype  TCM_E4M3 or TCM_E5M2 (any pair).
  *  A                 M x K row-major (pitch K), B N x K (pitch K): the elements.
- *  a_scales          M x K/32 uint8 row-major (pitch K/32): E8M0 scale codes
- *                    (value 2^(code - 127); 255 is NaN) of the 32-element blocks
- *                    of each row of A; b_scales likewise N x K/32 for B.
+ *  a_scales          E8M0 scale codes (value 2^(code - 127); 255 is NaN) of the
+ *                    32-element blocks of the rows of A, in the BLOCKED layout
+ *                    written by tcm_mx_pack_scales (tcm_mx_scales_bytes(M, K)
+ *                    bytes); b_scales likewise for the N rows of B.
  *  K                 a multiple of 32.
  *  C, D, bias        as in tcm_gemm_ex with packed pitches (C, D: N; bias: N).
  * All pointers 16-byte aligned; N * sizeof(out) a multiple of 16.
@@ -177,6 +179,31 @@ tcm_status tcm_gemm_mx(int64_t M, int64_t N, int64_t K,
                        tcm_dtype b_dtype, const void *B, const uint8_t *b_scales,
                        const void *C, void *D, float alpha, float beta, const void *bias,
                        tcm_dtype out_dtype, tcm_stream_t stream);
+
+/*
+ * Blocked scale layout of tcm_gemm_mx.  For `rows` rows of K elements
+ * (K % 32 == 0) the codes of row r, 32-block j (row-major code index
+ * r * K/32 + j) live in 512-byte atoms, one per 128 rows x 4 blocks:
+ *   atom (t, k) = (r / 128, j / 4) at byte (t * KT + k) * 512, KT = ceil(K / 128),
+ *   byte inside the atom: (r % 32) * 16 + ((r / 32) % 4) * 4 + j % 4.
+ * Positions of rows >= rows or blocks >= K/32 hold code 127 (1.0).  This is
+ * the tensor-memory scale layout of the block-scaled tcgen05.mma, one atom per
+ * 32 x 128-bit tcgen05.cp.
+ *
+ * tcm_mx_scales_bytes -- size of the blocked array: ceil(rows/128) *
+ * ceil(K/128) * 512; -1 if rows < 0, K < 0 or K % 32 != 0.  Host only.
+ */
+int64_t tcm_mx_scales_bytes(int64_t rows, int64_t K);
+
+/*
+ * tcm_mx_pack_scales -- write the blocked layout from row-major codes.
+ *  scales  device, rows x K/32 uint8 row-major (pitch K/32), caller-owned.
+ *  packed  device, tcm_mx_scales_bytes(rows, K) bytes, 16-byte aligned, caller-owned.
+ * Bit-exact (a permutation plus the 127 padding).  rows == 0 or K == 0 launches
+ * nothing.  Asynchronous on `stream`.
+ */
+tcm_status tcm_mx_pack_scales(int64_t rows, int64_t K, const uint8_t *scales, uint8_t *packed,
+                              tcm_stream_t stream);
 
 /*
  * tcm_get_device_status -- synchronise `stream`, then report the first

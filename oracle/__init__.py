@@ -21,6 +21,9 @@ Sources of the definitions (page titles and sections):
 * Block-scaled MMA (per-K-block scales applied before accumulation) and the
   MXFP8 block size of 32 with E8M0 scales: "NVIDIA MMA", sections
   "SM100：tcgen05.mma" and "MXFP4 与 NVFP4".
+* Blocked scale layout (:func:`mx_pack_scales`): the pages require a scale
+  layout contract without stating one ("MXFP4 与 NVFP4"); the layout checked
+  here is the library's documented one, a pure index permutation.
 """
 from __future__ import annotations
 
@@ -191,6 +194,24 @@ def gemm_mx(A, SA, B, SB, a_fmt, b_fmt, *, block=32, C=None, c_fmt="f32", bias=N
     if rc != 0:
         raise ValueError("orc_gemm_mx rejected its arguments")
     return ref, S
+
+
+def mx_pack_scales(SC, K):
+    """Blocked layout of row-major E8M0 codes ``SC`` (rows x K/32 uint8).
+
+    Code (r, j) goes to byte ``(r//128 * KT + j//4) * 512 + (r%32)*16 + ((r//32)%4)*4 + j%4``
+    with ``KT = ceil(K/128)``; every other byte of the ``ceil(rows/128) * KT * 512``
+    bytes holds 127.  Written as a plain loop over the source codes."""
+    SC = np.ascontiguousarray(SC, dtype=np.uint8)
+    rows, nblk = SC.shape
+    assert K % 32 == 0 and nblk == K // 32
+    kt = (K + 127) // 128
+    out = np.full(((rows + 127) // 128) * kt * 512, 127, dtype=np.uint8)
+    for r in range(rows):
+        for j in range(nblk):
+            atom = (r // 128) * kt + j // 4
+            out[atom * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + j % 4] = SC[r, j]
+    return out
 
 
 def sp_compress(A, fmt):

@@ -27,6 +27,7 @@ DTYPE_CODE = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2,
               torch.float8_e4m3fn: 3, torch.float8_e5m2: 4}
 # Symbols the C ABI (include/tcm.h) exports.
 EXPORTS = ("tcm_gemm", "tcm_gemm_ex", "tcm_sp_compress", "tcm_sp_decompress", "tcm_gemm_sp", "tcm_gemm_mx",
+           "tcm_mx_scales_bytes", "tcm_mx_pack_scales",
            "tcm_get_device_status", "tcm_clear_device_status", "tcm_set_timeout_ns",
            "tcm_status_string", "tcm_version", "tcm_set_config_override", "tcm_debug_fail_next_launch")
 
@@ -63,6 +64,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.tcm_gemm_sp.argtypes = [i64, i64, i64, i32, vp, vp, vp, vp, vp, f32, f32, i32, vp]
     lib.tcm_gemm_mx.restype = i32
     lib.tcm_gemm_mx.argtypes = [i64, i64, i64, i32, vp, vp, i32, vp, vp, vp, vp, f32, f32, vp, i32, vp]
+    lib.tcm_mx_scales_bytes.restype = i64
+    lib.tcm_mx_scales_bytes.argtypes = [i64, i64]
+    lib.tcm_mx_pack_scales.restype = i32
+    lib.tcm_mx_pack_scales.argtypes = [i64, i64, vp, vp, vp]
     lib.tcm_get_device_status.restype = i32
     lib.tcm_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
     lib.tcm_clear_device_status.restype = i32
@@ -184,17 +189,37 @@ def tcm_gemm_sp(A_comp, meta, B, D, *, C=None, alpha=1.0, beta=0.0, stream=None)
     return D
 
 
+def tcm_mx_scales_bytes(rows: int, K: int) -> int:
+    """Bytes of the blocked scale array of `rows` rows of K elements (-1 if K % 32 != 0)."""
+    return int(load_library().tcm_mx_scales_bytes(int(rows), int(K)))
+
+
+def tcm_mx_pack_scales(scales, K: int, packed=None, stream=None):
+    """Blocked layout of row-major E8M0 codes `scales` (rows x K/32 uint8, CUDA);
+    allocates `packed` (uint8, tcm_mx_scales_bytes(rows, K) bytes) if not given."""
+    import torch
+    lib = load_library()
+    rows = scales.shape[0]
+    if tuple(scales.shape) != (rows, K // 32) or not scales.is_contiguous():
+        raise ValueError("scales must be a contiguous rows x K/32 tensor")
+    if packed is None:
+        packed = torch.empty(max(tcm_mx_scales_bytes(rows, K), 0), dtype=torch.uint8, device=scales.device)
+    _check(lib.tcm_mx_pack_scales(rows, K, _ptr(scales), _ptr(packed), _stream(stream)), "tcm_mx_pack_scales")
+    return packed
+
+
 def tcm_gemm_mx(A, a_scales, B, b_scales, D, *, C=None, alpha=1.0, beta=0.0, bias=None, stream=None):
-    """Block-scaled FP8 GEMM: A (M x K) and B (N x K) in E4M3/E5M2, a_scales (M x K/32)
-    and b_scales (N x K/32) uint8 E8M0 codes; D (M x N); all contiguous CUDA tensors."""
+    """Block-scaled FP8 GEMM: A (M x K) and B (N x K) in E4M3/E5M2; a_scales and
+    b_scales the blocked E8M0 arrays of tcm_mx_pack_scales; D (M x N); all
+    contiguous CUDA tensors."""
     lib = load_library()
     M, K = A.shape
     N = B.shape[0]
     for t, n in ((A, "A"), (B, "B"), (a_scales, "a_scales"), (b_scales, "b_scales"), (D, "D")):
         if not t.is_contiguous():
             raise ValueError(f"{n} must be contiguous")
-    if tuple(a_scales.shape) != (M, K // 32) or tuple(b_scales.shape) != (N, K // 32):
-        raise ValueError("scales must be M x K/32 and N x K/32")
+    if a_scales.numel() < tcm_mx_scales_bytes(M, K) or b_scales.numel() < tcm_mx_scales_bytes(N, K):
+        raise ValueError("scales must be blocked arrays of tcm_mx_scales_bytes(rows, K) bytes")
     st = lib.tcm_gemm_mx(M, N, K, _code(A, "A"), _ptr(A), _ptr(a_scales), _code(B, "B"), _ptr(B), _ptr(b_scales),
                          _ptr(C), _ptr(D), float(alpha), float(beta), _ptr(bias), _code(D, "D"), _stream(stream))
     _check(st, "tcm_gemm_mx")

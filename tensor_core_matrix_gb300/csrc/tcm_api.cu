@@ -108,6 +108,22 @@ static bool encode_kmajor(CUtensorMap *map, const void *base, int elem_bytes, ui
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Blocked E8M0 scales (see tcm_gemm_mx.cu) as a 2-D byte tensor of
+// ceil(rows / 128) * ceil(K / 128) * 32 rows of 16 bytes, boxes of one 512-byte atom.
+static bool encode_sf_atoms(CUtensorMap *map, const void *base, uint64_t rows, uint64_t K)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const uint64_t atoms = ((rows + 127) / 128) * ((K + 127) / 128);
+    const cuuint64_t dims[2] = {16, atoms * 32};
+    const cuuint64_t strides[1] = {16};
+    const cuuint32_t box[2] = {16, 32};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 static int elem_bytes(tcm_dtype t)
 {
     switch (t) {
@@ -413,6 +429,9 @@ tcm_status tcm_gemm_mx(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const
     if (out_dtype != TCM_BF16 && out_dtype != TCM_F16 && out_dtype != TCM_F32) return TCM_ERR_UNSUPPORTED;
     if (M < 1 || N < 1 || K < 0 || K % 32 != 0) return TCM_ERR_INVALID_ARG;
     if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2) return TCM_ERR_UNSUPPORTED;
+    // scale-atom rows (32 per atom) are addressed with 32-bit coordinates
+    if (((M + 255) / 128) * ((K + 127) / 128) * 32 > INT32_MAX || ((N + 255) / 128) * ((K + 127) / 128) * 32 > INT32_MAX)
+        return TCM_ERR_UNSUPPORTED;
     if (!D || (K > 0 && (!A || !B || !a_scales || !b_scales)) || (beta != 0.f && !C)) return TCM_ERR_INVALID_ARG;
     const int eo = elem_bytes(out_dtype);
     if ((A && !aligned16(A)) || (B && !aligned16(B)) || (a_scales && !aligned16(a_scales)) ||
@@ -434,14 +453,14 @@ tcm_status tcm_gemm_mx(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const
     if (g_force_cta_group.load() == 1 || g_force_cta_group.load() == 2) cfg.cta_group = g_force_cta_group.load();
     if (cfg.bn != 256) cfg.cta_group = 1;
 
-    CUtensorMap tmA, tmB;
-    std::memset(&tmA, 0, sizeof tmA);
-    std::memset(&tmB, 0, sizeof tmB);
+    MxMaps maps;
+    std::memset(&maps, 0, sizeof maps);
     if (K > 0) {
-        if (!encode_kmajor(&tmA, A, 1, static_cast<uint64_t>(K), static_cast<uint64_t>(M), static_cast<uint64_t>(K), 128))
-            return TCM_ERR_CUDA;
-        if (!encode_kmajor(&tmB, B, 1, static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(K),
-                           static_cast<uint32_t>(cfg.bn / cfg.cta_group)))
+        const uint64_t uK = static_cast<uint64_t>(K);
+        if (!encode_kmajor(&maps.a, A, 1, uK, static_cast<uint64_t>(M), uK, 128) ||
+            !encode_kmajor(&maps.b, B, 1, uK, static_cast<uint64_t>(N), uK, static_cast<uint32_t>(cfg.bn / cfg.cta_group)) ||
+            !encode_sf_atoms(&maps.sa, a_scales, static_cast<uint64_t>(M), uK) ||
+            !encode_sf_atoms(&maps.sb, b_scales, static_cast<uint64_t>(N), uK))
             return TCM_ERR_CUDA;
     }
     GemmParams p{};
@@ -475,13 +494,28 @@ tcm_status tcm_gemm_mx(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const
     p.status = device_status_ptr();
     if (!p.status) return TCM_ERR_CUDA;
     p.fault_inject = 0;
-    p.sfa = a_scales;
-    p.sfb = b_scales;
-    p.sf_ld = K / 32;
     const int64_t clusters = sms / cfg.cta_group;
     const int grid = static_cast<int>((p.num_tiles < clusters ? p.num_tiles : clusters) * cfg.cta_group);
-    const cudaError_t e = launch_gemm_mx(cfg, tmA, tmB, p, grid, reinterpret_cast<cudaStream_t>(stream));
+    const cudaError_t e = launch_gemm_mx(cfg, maps, p, grid, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TCM_OK : TCM_ERR_CUDA;
+}
+
+int64_t tcm_mx_scales_bytes(int64_t rows, int64_t K)
+{
+    if (rows < 0 || K < 0 || K % 32 != 0) return -1;
+    return ((rows + 127) / 128) * ((K + 127) / 128) * 512;
+}
+
+tcm_status tcm_mx_pack_scales(int64_t rows, int64_t K, const uint8_t *scales, uint8_t *packed, tcm_stream_t stream)
+{
+    if (rows < 0 || K < 0 || K % 32 != 0) return TCM_ERR_INVALID_ARG;
+    if (rows > INT32_MAX / 2 || K > INT32_MAX / 2) return TCM_ERR_UNSUPPORTED;
+    if (rows == 0 || K == 0) return TCM_OK;
+    if (!scales || !packed) return TCM_ERR_INVALID_ARG;
+    if (!aligned16(packed)) return TCM_ERR_MISALIGNED;
+    return launch_mx_pack_scales(scales, rows, K, packed, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? TCM_OK
+               : TCM_ERR_CUDA;
 }
 
 tcm_status tcm_get_device_status(tcm_stream_t stream, int32_t *code, int32_t *site)

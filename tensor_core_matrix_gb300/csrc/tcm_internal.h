@@ -50,9 +50,6 @@ struct GemmParams {
     int fault_inject;         // test hook (FaultBits); 0 in normal launches
     const uint32_t *meta;     // sparse: 2:4 metadata, kM x meta_ld words (library layout)
     long long meta_ld;        // sparse: words per metadata row (K / 32)
-    const uint8_t *sfa;       // block-scaled: E8M0 scales of A, kM x sf_ld bytes
-    const uint8_t *sfb;       // block-scaled: E8M0 scales of B, kN x sf_ld bytes
-    long long sf_ld;          // block-scaled: scales per row (K / 32)
 };
 
 // Test hook bits: make a pipeline wait run out without touching memory.
@@ -79,8 +76,15 @@ cudaError_t launch_gemm_pair(const GemmConfig &cfg, const CUtensorMap &tmA, cons
 cudaError_t launch_gemm_ksplit(const GemmConfig &cfg, const CUtensorMap &tmA, const CUtensorMap &tmB,
                                const GemmParams &p, int grid, cudaStream_t stream);
 
-cudaError_t launch_gemm_mx(const GemmConfig &cfg, const CUtensorMap &tmA, const CUtensorMap &tmB,
-                           const GemmParams &p, int grid, cudaStream_t stream);
+// Tensor maps of a block-scaled GEMM: the FP8 operands (as for the dense
+// kernel) and the blocked scale arrays viewed as (atoms x 32) rows of 16 bytes.
+struct MxMaps {
+    CUtensorMap a, b, sa, sb;
+};
+
+cudaError_t launch_gemm_mx(const GemmConfig &cfg, const MxMaps &maps, const GemmParams &p, int grid,
+                           cudaStream_t stream);
+cudaError_t launch_mx_pack_scales(const uint8_t *src, int64_t rows, int64_t K, uint8_t *dst, cudaStream_t stream);
 
 cudaError_t launch_gemm_sp(const GemmConfig &cfg, const CUtensorMap &tmA, const CUtensorMap &tmB,
                            const GemmParams &p, int grid, cudaStream_t stream);

@@ -27,10 +27,14 @@ def tcm():
 
 
 def run_mx(tcm, A, SA, B, SB, out=torch.bfloat16, C=None, beta=0.0, alpha=1.0, bias=None):
+    """Row-major scales are packed on the device by the library, then the GEMM runs."""
     d = dev()
-    M, N = A.shape[0], B.shape[0]
+    M, K = A.shape
+    N = B.shape[0]
     D = torch.full((M, N), float("nan"), dtype=out, device=d)
-    tcm.tcm_gemm_mx(A.to(d), SA.to(d), B.to(d), SB.to(d), D, C=None if C is None else C.to(d), alpha=alpha,
+    pa = tcm.tcm_mx_pack_scales(SA.to(d), K)
+    pb = tcm.tcm_mx_pack_scales(SB.to(d), K)
+    tcm.tcm_gemm_mx(A.to(d), pa, B.to(d), pb, D, C=None if C is None else C.to(d), alpha=alpha,
                     beta=beta, bias=None if bias is None else bias.to(d))
     code, site = tcm.tcm_get_device_status()
     assert code == 0, (code, site)
@@ -39,6 +43,14 @@ def run_mx(tcm, A, SA, B, SB, out=torch.bfloat16, C=None, beta=0.0, alpha=1.0, b
 
 def oracle_mx(A, SA, B, SB, fa, fb, **kw):
     return oracle.gemm_mx(si.codes(A), SA.numpy(), si.codes(B), SB.numpy(), fa, fb, **kw)
+
+
+@pytest.mark.parametrize("rows,K", [(1, 32), (127, 96), (128, 128), (130, 160), (300, 1024), (8192, 8192)])
+def test_mx_pack_scales_bit_exact(tcm, rows, K):
+    g = si.generator(rows + K)
+    SC = torch.randint(0, 255, (rows, K // 32), generator=g).to(torch.uint8)
+    got = tcm.tcm_mx_pack_scales(SC.to(dev()), K).cpu().numpy()
+    assert np.array_equal(got, oracle.mx_pack_scales(SC.numpy(), K))
 
 
 # (cta_group, tile_n): 0 = the library's choice; (2, 256) = the CTA-pair 256 x 256 tile

@@ -418,3 +418,43 @@ def test_mx_sampled_equals_full():
     r = np.array([0, 5, 29, 7]); c = np.array([0, 19, 3, 3])
     samp, Ss = oracle.gemm_mx(A, SA, B, SB, "e4m3", "e4m3", rows=r, cols=c)
     assert np.array_equal(samp, full[r, c]) and np.array_equal(Ss, Sf[r, c])
+
+
+# ---- blocked scale layout (a pure permutation defined by the library header)
+
+def _pack_source(rows, K):
+    nblk = K // 32
+    r = np.arange(rows)[:, None]
+    j = np.arange(nblk)[None, :]
+    return ((r * 7 + j * 3) % 254).astype(np.uint8)  # never 127 at most positions, never 255
+
+
+def test_mx_pack_hand_worked_positions():
+    """rows = 130, K = 160: 2 row tiles x 2 K stages of 512-byte atoms; positions worked by hand."""
+    SC = _pack_source(130, 160)
+    out = oracle.mx_pack_scales(SC, 160)
+    assert out.shape == (2048,)
+    cases = {  # (row, block) -> byte offset
+        (0, 0): 0, (1, 0): 16, (32, 0): 4, (33, 3): 23, (127, 2): 510,
+        (0, 4): 512, (31, 4): 1008, (96, 4): 524, (128, 0): 1024, (129, 4): 1552,
+    }
+    for (r, j), pos in cases.items():
+        assert out[pos] == SC[r, j], (r, j, pos)
+    for pos in (513, 515, 1056, 2047, 1024 + 64):  # block 5+ of stage 1, rows 130+
+        assert out[pos] == 127, pos
+
+
+@pytest.mark.parametrize("rows,K", [(1, 32), (127, 96), (128, 128), (130, 160), (300, 1024)])
+def test_mx_pack_is_a_permutation_with_unit_padding(rows, K):
+    SC = _pack_source(rows, K)
+    out = oracle.mx_pack_scales(SC, K)
+    kt = (K + 127) // 128
+    assert out.size == ((rows + 127) // 128) * kt * 512
+    # a block-by-block view (tile, quarter, lane, stage, block) read back in row-major order
+    rt = (rows + 127) // 128
+    atoms = out.reshape(rt, kt, 32, 4, 4)  # (tile, stage, lane, quarter, block-in-stage)
+    back = atoms.transpose(0, 3, 2, 1, 4).reshape(rt * 128, kt * 4)
+    assert np.array_equal(back[:rows, :K // 32], SC)
+    pad = np.ones_like(back, dtype=bool)
+    pad[:rows, :K // 32] = False
+    assert np.all(back[pad] == 127)
