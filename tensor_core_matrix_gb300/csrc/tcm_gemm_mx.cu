@@ -34,9 +34,16 @@
 // four MMAs of K = 32 per stage, one thread issuing, TMEM accumulators), with
 // the stage's scale atoms loaded by the same TMA producer onto the same
 // barrier, and the issuing thread copying them to tensor memory (tcgen05.cp,
-// ordered before the MMAs that read them) -- no other warp touches the scales.
-// The scale columns of a stage are rewritten only after the stage's barrier
-// has completed again, i.e. after the MMAs that read them have finished.
+// ordered before the MMAs that read them), one atom after each MMA of the
+// previous stage -- no other warp touches the scales.  The scale columns of a
+// stage are rewritten only after the stage's barrier has completed again,
+// i.e. after the MMAs that read them have finished.
+//
+// One accumulator of 256 columns fills half of tensor memory and the scale
+// columns take part of the rest, so a 256-wide tile has a single accumulator
+// buffer; for 16-bit outputs without C the epilogue converts while it drains
+// tensor memory and frees it before its global stores, shortening the gap
+// before the next tile's MMAs.
 #include "tcm_kernel_common.cuh"
 
 namespace tcm {
@@ -59,6 +66,17 @@ struct MxSmem {
     static constexpr int BYTES = MISC_OFF + 16;
     static constexpr int ALLOC = BYTES + 1024;
 };
+
+// Two values rounded to nearest-even in the 16-bit output format, packed low/high.
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, int fmt)
+{
+    if (fmt == OUT_BF16) {
+        const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t *>(&b);
+    }
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
 
 // Shared-memory descriptor of a 32-row x 16-byte block without swizzle:
 // core matrices of 8 rows x 16 bytes, 128 bytes apart.
@@ -239,9 +257,26 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
         }
     } else if (warp == 1) {
         if (lane == 0 && leader) {
+            // Item i = (tile, K block) in ring stage i % STAGES.  The scale copies
+            // of item i + 1 are issued between the four MMAs of item i (after its
+            // data has landed): measured much faster than copying a stage's three
+            // atoms back to back in front of its own MMAs.
+            const int my_tiles = first_tile < p.tile_end ? (p.tile_end - 1 - first_tile) / step + 1 : 0;
+            const long long items = static_cast<long long>(my_tiles) * p.num_kb;
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
+            if (items > 0) {
+                ok = wait_bar<CG>(full, 0, w, SITE_MMA_FULL, true);
+                if (ok) {
+                    tc_fence_after();
+                    const uint32_t sf0 = tmem_base + SF_COL;
+#pragma unroll
+                    for (int a = 0; a <= SFB_ATOMS; ++a)
+                        tmem_cp_sf<CG>(sf0 + (a == 0 ? 0u : 4u + 4u * a), sdesc_sf_atom(sbase + L::SF_OFF + SF_ATOM * a));
+                }
+            }
+            long long item = 0;
             int local = 0;
             for (int t = first_tile; ok && t < p.tile_end; t += step, ++local) {
                 const int acc = local % NACC;
@@ -249,32 +284,35 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
                 if (!wait_bar<CG>(tempty + acc, acc_phase ^ 1u, w, SITE_MMA_ACC_EMPTY, true)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * ACC_STRIDE;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (!wait_bar<CG>(full + stage, phase, w, SITE_MMA_FULL, true)) {
-                        ok = false;
-                        break;
+                for (int kb = 0; kb < p.num_kb; ++kb, ++item) {
+                    const int next_stage = stage + 1 == STAGES ? 0 : stage + 1;
+                    const uint32_t next_phase = stage + 1 == STAGES ? phase ^ 1u : phase;
+                    const bool has_next = item + 1 < items;
+                    if (has_next) {
+                        if (!wait_bar<CG>(full + next_stage, next_phase, w, SITE_MMA_FULL, true)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
                     }
-                    tc_fence_after();
                     const uint64_t ad = sdesc_kmajor_sw128(sbase + L::A_OFF + stage * A_STAGE_BYTES);
                     const uint64_t bd = sdesc_kmajor_sw128(sbase + L::B_OFF + stage * L::B_STAGE);
-                    const uint32_t ss = sbase + L::SF_OFF + stage * L::SF_STAGE;
                     const uint32_t sf = tmem_base + SF_COL + static_cast<uint32_t>(stage) * SF_STAGE_COLS;
-                    tmem_cp_sf<CG>(sf, sdesc_sf_atom(ss));
-#pragma unroll
-                    for (int i = 0; i < SFB_ATOMS; ++i)
-                        tmem_cp_sf<CG>(sf + 8 + 4 * i, sdesc_sf_atom(ss + SF_ATOM * (1 + i)));
+                    const uint32_t nss = sbase + L::SF_OFF + next_stage * L::SF_STAGE;
+                    const uint32_t nsf = tmem_base + SF_COL + static_cast<uint32_t>(next_stage) * SF_STAGE_COLS;
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         // scale-factor ids: byte k of the stage's scale words (A bits [29,31), B bits [4,6))
                         const uint32_t idesc = p.idesc | (static_cast<uint32_t>(k) << 29) | (static_cast<uint32_t>(k) << 4);
                         mma_mx<CG>(d_tmem, ad + 2 * k, bd + 2 * k, idesc, sf, sf + 8, (kb > 0 || k > 0) ? 1u : 0u);
+                        // after MMA k: atom k of the next stage (0 = A, 1.. = B), at most one per MMA
+                        if (has_next && k <= SFB_ATOMS)
+                            tmem_cp_sf<CG>(nsf + (k == 0 ? 0u : 4u + 4u * k), sdesc_sf_atom(nss + SF_ATOM * k));
                     }
                     if (CG == 2) mma_commit_pair(empty + stage, 0x3);
                     else mma_commit(empty + stage);
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+                    stage = next_stage;
+                    phase = next_phase;
                 }
                 if (!ok) break;
                 if (CG == 2) mma_commit_pair(tfull + acc, 0x3);
@@ -304,6 +342,47 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
             tile_coords(p, t, mb, nb);
             const int row = mb * (BM * CG) + static_cast<int>(rank) * BM + row_in_tile;
             const uint32_t tbase = tmem_base + static_cast<uint32_t>(acc) * ACC_STRIDE + (static_cast<uint32_t>(quad * 32) << 16);
+            const int col0 = nb * BN + c_lo;
+            if (p.out_fmt != OUT_F32 && p.beta == 0.f && col0 + EPI_COLS <= p.kN) {
+                // out = alpha * acc (+ bias), rounded once -- the same operations as
+                // epilogue_row32 with beta = 0 -- packed two per register
+                uint32_t packed[EPI_COLS / 2];
+#pragma unroll
+                for (int c = 0; c < EPI_COLS; c += 32) {
+                    uint32_t r[32];
+                    if (p.num_kb > 0) {
+                        tmem_ld_32x32b_x32(tbase + c_lo + c, r);
+                        tmem_ld_wait();
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) r[j] = 0u;
+                    }
+                    float v[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = p.alpha * __uint_as_float(r[j]);
+                    if (p.bias) {
+                        float b[32];
+                        ld32(p.bias, col0 + c, p.out_fmt, b);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] += b[j];
+                    }
+#pragma unroll
+                    for (int h = 0; h < 16; ++h) packed[c / 2 + h] = pack2(v[2 * h], v[2 * h + 1], p.out_fmt);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if (CG == 2) mbar_arrive_cluster(tempty_cluster0 + static_cast<uint32_t>(acc) * 8u);
+                    else mbar_arrive(tempty + acc);
+                }
+                if (row < p.kM) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.D) + static_cast<long long>(row) * p.ldd + col0);
+#pragma unroll
+                    for (int q = 0; q < EPI_COLS / 8; ++q)
+                        dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+                }
+                continue;
+            }
 #pragma unroll 1
             for (int c = c_lo; c < c_lo + EPI_COLS; c += 32) {
                 uint32_t r[32];

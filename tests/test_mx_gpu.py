@@ -85,6 +85,20 @@ def test_mx_normal_data_bound(tcm, fa, fb, cg, bn):
     assert ratio(D, ref, S, scale=2.0) <= 1.0
 
 
+@pytest.mark.parametrize("cg,bn", VARIANTS)
+@pytest.mark.parametrize("out,fmt", [(torch.bfloat16, "bf16"), (torch.float16, "f16")])
+def test_mx_bias_without_c_bound(tcm, cg, bn, out, fmt):
+    """16-bit output, beta = 0, bias: full-width tiles take the drain-and-convert epilogue,
+    the ragged last tile (N = 520) the general one."""
+    tcm.tcm_set_config_override(cg, bn)
+    c = si.mx_case(300, 520, 416, seed=11)
+    bias = si.normal((520,), si.generator(12), dtype=fmt)
+    D = run_mx(tcm, c["A"], c["SA"], c["B"], c["SB"], out=out, alpha=0.75, bias=bias)
+    ref, S = oracle_mx(c["A"], c["SA"], c["B"], c["SB"], "e4m3", "e4m3", alpha=0.75, bias=si.codes(bias),
+                       bias_fmt=fmt)
+    assert ratio(D, ref, S, scale=0.75) <= 1.0
+
+
 def test_mx_wide_scale_range_bound(tcm):
     """Block scales spread over many binades (2^-20 .. 2^20) still meet the bound."""
     M, N, K = 256, 256, 512
