@@ -34,8 +34,8 @@
 // four MMAs of K = 32 per stage, one thread issuing, TMEM accumulators), with
 // the stage's scale atoms loaded by the same TMA producer onto the same
 // barrier, and the issuing thread copying them to tensor memory (tcgen05.cp,
-// ordered before the MMAs that read them), one atom after each MMA of the
-// previous stage -- no other warp touches the scales.  The scale columns of a
+// ordered before the MMAs that read them), normally one atom after each MMA
+// of the previous stage -- no other warp touches the scales.  The scale columns of a
 // stage are rewritten only after the stage's barrier has completed again,
 // i.e. after the MMAs that read them have finished.
 //
@@ -257,10 +257,12 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
         }
     } else if (warp == 1) {
         if (lane == 0 && leader) {
-            // Item i = (tile, K block) in ring stage i % STAGES.  The scale copies
-            // of item i + 1 are issued between the four MMAs of item i (after its
-            // data has landed): measured much faster than copying a stage's three
-            // atoms back to back in front of its own MMAs.
+            // Item i = (tile, K block) in ring stage i % STAGES.  If the data of
+            // item i + 1 has already landed (a non-blocking test), its scale copies
+            // are issued between the four MMAs of item i; otherwise they go in
+            // front of item i + 1's own MMAs once its data arrives.  Measured:
+            // three copies back to back in front of the MMAs, or a blocking wait
+            // for the next stage, cost 16-35%.
             const int my_tiles = first_tile < p.tile_end ? (p.tile_end - 1 - first_tile) / step + 1 : 0;
             const long long items = static_cast<long long>(my_tiles) * p.num_kb;
             int stage = 0;
@@ -278,6 +280,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
             }
             long long item = 0;
             int local = 0;
+            bool fetched = true; // stage 0: data seen and scales copied above
             for (int t = first_tile; ok && t < p.tile_end; t += step, ++local) {
                 const int acc = local % NACC;
                 const uint32_t acc_phase = (local / NACC) & 1;
@@ -287,14 +290,22 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
                 for (int kb = 0; kb < p.num_kb; ++kb, ++item) {
                     const int next_stage = stage + 1 == STAGES ? 0 : stage + 1;
                     const uint32_t next_phase = stage + 1 == STAGES ? phase ^ 1u : phase;
-                    const bool has_next = item + 1 < items;
-                    if (has_next) {
-                        if (!wait_bar<CG>(full + next_stage, next_phase, w, SITE_MMA_FULL, true)) {
+                    if (!fetched) { // data not seen yet: wait for it, copy this stage's scales up front
+                        if (!wait_bar<CG>(full + stage, phase, w, SITE_MMA_FULL, true)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
+                        const uint32_t ss = sbase + L::SF_OFF + stage * L::SF_STAGE;
+                        const uint32_t s0 = tmem_base + SF_COL + static_cast<uint32_t>(stage) * SF_STAGE_COLS;
+#pragma unroll
+                        for (int a = 0; a <= SFB_ATOMS; ++a)
+                            tmem_cp_sf<CG>(s0 + (a == 0 ? 0u : 4u + 4u * a), sdesc_sf_atom(ss + SF_ATOM * a));
                     }
+                    // next stage already landed: interleave its copies with this stage's MMAs
+                    const bool has_next = item + 1 < items && mbar_try_wait(smem_u32(full + next_stage), next_phase);
+                    if (has_next) tc_fence_after();
+                    fetched = has_next;
                     const uint64_t ad = sdesc_kmajor_sw128(sbase + L::A_OFF + stage * A_STAGE_BYTES);
                     const uint64_t bd = sdesc_kmajor_sw128(sbase + L::B_OFF + stage * L::B_STAGE);
                     const uint32_t sf = tmem_base + SF_COL + static_cast<uint32_t>(stage) * SF_STAGE_COLS;
