@@ -47,8 +47,11 @@ CODE_DTYPE = {1: np.uint8, 2: np.uint16, 4: np.uint32}
 # significand precision p (bits incl. the implicit one) and the smallest
 # positive subnormal of each output format; an RNE cast to the format is
 # within 2^-p relative (half an ulp) of its argument, plus the subnormal step.
-PRECISION = {"bf16": 8, "f16": 11, "f32": 24}
-MIN_SUBNORMAL = {"bf16": 2.0 ** -133, "f16": 2.0 ** -24, "f32": 2.0 ** -149}
+PRECISION = {"bf16": 8, "f16": 11, "f32": 24, "e4m3": 4, "e5m2": 3}
+MIN_SUBNORMAL = {"bf16": 2.0 ** -133, "f16": 2.0 ** -24, "f32": 2.0 ** -149, "e4m3": 2.0 ** -9, "e5m2": 2.0 ** -16}
+ACT = {None: 0, "none": 0, "relu": 1, "gelu": 2}
+# max |d/dx x Phi(x)| = 1.1289 (at x = +-sqrt 2): how far GELU can stretch an input error
+GELU_LIPSCHITZ = 1.13
 # Accumulation allowance relative to sum_k |a*b|, the tolerance the GEMM is
 # held to for fp32 accumulation of any K.
 ACC_REL = 1e-5
@@ -89,6 +92,10 @@ def _load():
     lib.orc_gemm_mx.argtypes = [i64, i64, i64, i64, i32, vp, i64, vp, i64, i32, vp, i64, vp, i64,
                                 i32, vp, i64, i32, vp, dbl, dbl, i64, vp, vp, vp, vp]
     lib.orc_sp_compress.restype = i32
+    lib.orc_activate.restype = i32
+    lib.orc_activate.argtypes = [i64, vp, i32, vp]
+    lib.orc_fp8_target.restype = i32
+    lib.orc_fp8_target.argtypes = [i64, vp, ctypes.c_double, i32, vp]
     lib.orc_sp_compress.argtypes = [i64, i64, i32, vp, i64, vp, vp]
     lib.orc_sp_decompress.restype = i32
     lib.orc_sp_decompress.argtypes = [i64, i64, i32, vp, vp, vp, i64]
@@ -235,6 +242,39 @@ def sp_decompress(Ac, meta, fmt):
     if _load().orc_sp_decompress(M, K, FMT[fmt], _ptr(Ac), _ptr(meta), _ptr(A), K) != 0:
         raise ValueError("orc_sp_decompress rejected its arguments")
     return A
+
+
+def activate(x, act):
+    """act(x) in fp64 (``oracle.c``: RELU, GELU = x Phi(x)); x any float array."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    y = np.empty_like(x)
+    if _load().orc_activate(x.size, _ptr(x), ACT[act], _ptr(y)) != 0:
+        raise ValueError(f"unknown activation {act!r}")
+    return y
+
+
+def fused_reference(ref, S, act, out_fmt, scale=1.0, d_scale=1.0):
+    """Expected outputs of the fused epilogue and their bounds.
+
+    ``ref``/``S`` come from :func:`gemm` (alpha, scales, C and bias applied).
+    Returns ``(target, bound, y, bound_y)``: ``y = act(ref)`` with the bound
+    ``bound_y`` on |y_gpu - y| (accumulation allowance and the fp32 epilogue
+    arithmetic, stretched by the activation's Lipschitz constant, plus the
+    device GELU's own evaluation error), and the stored value's target -- y,
+    or y / d_scale saturated for FP8 outputs -- with the bound on the decoded
+    output (bound_y carried through d_scale, plus one RNE cast of the format)."""
+    ref = np.asarray(ref, dtype=np.float64)
+    y = activate(ref, act)
+    lip = GELU_LIPSCHITZ if ACT[act] == 2 else 1.0
+    e_pre = ACC_REL * abs(scale) * np.asarray(S) + 2.0 ** -23 * np.abs(ref)
+    e_y = lip * e_pre + (2.0 ** -20 * np.abs(ref) if ACT[act] == 2 else 0.0)
+    if out_fmt in ("e4m3", "e5m2"):
+        target = np.empty_like(y)
+        _load().orc_fp8_target(y.size, _ptr(np.ascontiguousarray(y)), float(d_scale), FMT[out_fmt], _ptr(target))
+        e_t = e_y / abs(d_scale) + 2.0 ** -23 * np.abs(target)
+    else:
+        target, e_t = y, e_y
+    return target, e_t + 2.0 ** -PRECISION[out_fmt] * np.abs(target) + MIN_SUBNORMAL[out_fmt], y, e_y
 
 
 def bound(ref, S, out_fmt, scale=1.0):

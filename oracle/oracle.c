@@ -337,3 +337,43 @@ int orc_gemm_mx(int64_t M, int64_t N, int64_t K, int64_t blk,
     free(tb);
     return bad ? -1 : 0;
 }
+
+/*
+ * Fused epilogue tail, "NVIDIA MMA" page, section "输入/累加/输出": after the K
+ * reduction the epilogue scales, adds the bias, applies an activation and
+ * casts; an FP8 output feeds the next layer.  Readings where the page is
+ * silent: the activation acts on ref = alpha*sA*sB*acc + beta*C + bias;
+ *   RELU(x) = x if x > 0 else 0 (a NaN gives 0),
+ *   GELU(x) = x * Phi(x) = 0.5 * x * (1 + erf(x / sqrt 2)), Phi the standard
+ *             normal distribution function;
+ * an FP8 output holds y / d_scale rounded to nearest even and saturated to
+ * the format's largest finite value (E4M3 448 = 1.75 * 2^8, E5M2 57344 =
+ * 1.75 * 2^15); amax = max |y| over the outputs.
+ */
+enum { ORC_ACT_NONE = 0, ORC_ACT_RELU = 1, ORC_ACT_GELU = 2 };
+
+int orc_activate(int64_t n, const double *x, int act, double *y)
+{
+    if (act < ORC_ACT_NONE || act > ORC_ACT_GELU) return -1;
+    for (int64_t i = 0; i < n; ++i) {
+        const double v = x[i];
+        if (act == ORC_ACT_RELU) y[i] = v > 0.0 ? v : 0.0;
+        else if (act == ORC_ACT_GELU) y[i] = 0.5 * v * (1.0 + erf(v / sqrt(2.0)));
+        else y[i] = v;
+    }
+    return 0;
+}
+
+/* The unrounded value an FP8 output element targets: y / d_scale, saturated. */
+int orc_fp8_target(int64_t n, const double *y, double d_scale, int fmt, double *out)
+{
+    double top;
+    if (fmt == ORC_E4M3) top = ldexp(1.75, 8);
+    else if (fmt == ORC_E5M2) top = ldexp(1.75, 15);
+    else return -1;
+    for (int64_t i = 0; i < n; ++i) {
+        const double t = y[i] / d_scale;
+        out[i] = t > top ? top : (t < -top ? -top : t); /* a NaN passes through */
+    }
+    return 0;
+}

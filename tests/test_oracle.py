@@ -458,3 +458,65 @@ def test_mx_pack_is_a_permutation_with_unit_padding(rows, K):
     pad = np.ones_like(back, dtype=bool)
     pad[:rows, :K // 32] = False
     assert np.all(back[pad] == 127)
+
+
+# ---- fused epilogue tail: activation, FP8 target, bound
+
+def _phi_simpson(x, n=20000):
+    """Standard normal distribution function by Simpson's rule on the density (independent of erf)."""
+    import math
+    if x == 0:
+        return 0.5
+    h = x / n
+    s = 1.0 + math.exp(-0.5 * x * x)
+    for i in range(1, n):
+        t = i * h
+        s += (4 if i % 2 else 2) * math.exp(-0.5 * t * t)
+    return 0.5 + s * h / 3.0 / math.sqrt(2.0 * math.pi)
+
+
+def test_gelu_is_x_times_normal_cdf():
+    xs = np.array([-4.0, -1.5, -0.25, 0.3, 1.0, 2.5])
+    got = oracle.activate(xs, "gelu")
+    for x, g in zip(xs, got):
+        assert abs(g - x * _phi_simpson(float(x))) <= 1e-12 * max(1.0, abs(x))
+    # Phi(1) from the standard normal table
+    assert abs(oracle.activate(np.array([1.0]), "gelu")[0] - 0.8413447460685429) < 1e-15
+
+
+def test_gelu_odd_part_identity_and_limits():
+    g = np.random.default_rng(3)
+    x = g.normal(0, 3, 1000)
+    assert np.allclose(oracle.activate(x, "gelu") - oracle.activate(-x, "gelu"), x, rtol=0, atol=1e-12)
+    assert oracle.activate(np.array([0.0]), "gelu")[0] == 0.0
+    big = oracle.activate(np.array([12.0, -12.0]), "gelu")
+    assert big[0] == 12.0 and abs(big[1]) < 1e-30
+
+
+def test_relu_definition():
+    x = np.array([-2.0, -0.0, 0.0, 1e-300, 3.5, np.nan, -np.inf, np.inf])
+    y = oracle.activate(x, "relu")
+    assert list(y[:5]) == [0.0, 0.0, 0.0, 1e-300, 3.5]
+    assert y[5] == 0.0 and y[6] == 0.0 and y[7] == np.inf
+    assert np.array_equal(oracle.activate(x[:5], "none"), x[:5])
+
+
+def test_fp8_target_divides_and_saturates():
+    y = np.array([100.0, 896.0, 897.0, -1e9, 0.5, np.nan])
+    t, *_ = oracle.fused_reference(y, np.zeros_like(y), None, "e4m3", d_scale=2.0)
+    assert list(t[:5]) == [50.0, 448.0, 448.0, -448.0, 0.25] and np.isnan(t[5])
+    t, *_ = oracle.fused_reference(np.array([1e6, -57344.0 * 4]), np.zeros(2), None, "e5m2", d_scale=4.0)
+    assert list(t) == [57344.0, -57344.0]
+
+
+def test_fused_bound_without_activation_covers_the_plain_bound():
+    g = np.random.default_rng(5)
+    ref = g.normal(0, 10, 200)
+    S = np.abs(g.normal(0, 100, 200))
+    for fmt in ("bf16", "f16", "f32"):
+        t, b, y, ey = oracle.fused_reference(ref, S, None, fmt, scale=0.5)
+        assert np.array_equal(t, ref) and np.array_equal(y, ref)
+        assert np.all(b >= oracle.bound(ref, S, fmt, 0.5))
+    _, b_relu, _, e_relu = oracle.fused_reference(ref, S, "relu", "bf16")
+    _, b_gelu, _, e_gelu = oracle.fused_reference(ref, S, "gelu", "bf16")
+    assert np.all(e_gelu >= e_relu)
