@@ -61,6 +61,13 @@ typedef enum {
     TCM_E5M2 = 4
 } tcm_dtype;
 
+/* Activation of the fused epilogue (tcm_gemm_fused). */
+typedef enum {
+    TCM_ACT_NONE = 0,
+    TCM_ACT_RELU = 1, /* max(y, 0); NaN -> 0 */
+    TCM_ACT_GELU = 2  /* y * Phi(y) = 0.5 y (1 + erf(y / sqrt 2)), with the device erff */
+} tcm_activation;
+
 /*
  * tcm_gemm -- D = alpha * (A . B) + beta * C
  *
@@ -110,6 +117,38 @@ tcm_status tcm_gemm_ex(int64_t M, int64_t N, int64_t K,
                        tcm_dtype out_dtype, float alpha, float beta,
                        const float *a_scale, const float *b_scale, const void *bias,
                        tcm_stream_t stream);
+
+/*
+ * tcm_gemm_fused -- tcm_gemm_ex with the rest of the epilogue chain:
+ *   y   = act(alpha * sA * sB * (A . B) + beta * C + bias)
+ *   D   = y / d_scale, cast to out_dtype (FP8: round to nearest even, saturating to
+ *         the largest finite value; 16/32-bit: RNE, d_scale not used)
+ *   amax = max over all M x N outputs of |y| (before the division and the cast)
+ *
+ * "NVIDIA MMA", section "输入/累加/输出": the epilogue does scale / bias /
+ * activation / cast, and FP8 outputs feed the next layer, whose per-tensor
+ * scale comes from the amax of this one (delayed scaling).
+ *  a_dtype .. bias   as tcm_gemm_ex, except: out_dtype may also be TCM_E4M3 or
+ *                    TCM_E5M2, and then beta must be 0 (TCM_ERR_UNSUPPORTED
+ *                    otherwise: there is no FP8 C) and bias is bf16[N].
+ *                    ldd * sizeof(out) must be a multiple of 16.
+ *  act               TCM_ACT_NONE, TCM_ACT_RELU or TCM_ACT_GELU; else
+ *                    TCM_ERR_INVALID_ARG.
+ *  d_scale           DEVICE pointer to one fp32 (dequantisation factor of D:
+ *                    real value = stored value * d_scale), or NULL for 1.0.
+ *                    Read only for FP8 outputs.
+ *  amax              DEVICE pointer to one fp32, 4-byte aligned, or NULL.  The
+ *                    call sets it to 0 on `stream` before the GEMM, then to the
+ *                    maximum |y| (NaN if any y is NaN).
+ */
+tcm_status tcm_gemm_fused(int64_t M, int64_t N, int64_t K,
+                          tcm_dtype a_dtype, const void *A, int64_t lda,
+                          tcm_dtype b_dtype, const void *B, int64_t ldb,
+                          const void *C, int64_t ldc, void *D, int64_t ldd,
+                          tcm_dtype out_dtype, float alpha, float beta,
+                          const float *a_scale, const float *b_scale, const void *bias,
+                          tcm_activation act, const float *d_scale, float *amax,
+                          tcm_stream_t stream);
 
 /*
  * tcm_sp_compress -- prune a logical M x K matrix to 2:4 along K and compress it.

@@ -25,8 +25,10 @@ STATUS_NAMES = {0: "TCM_OK", 1: "TCM_ERR_INVALID_ARG", 2: "TCM_ERR_UNSUPPORTED",
                 3: "TCM_ERR_MISALIGNED", 4: "TCM_ERR_CUDA", 5: "TCM_ERR_TIMEOUT"}
 DTYPE_CODE = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2,
               torch.float8_e4m3fn: 3, torch.float8_e5m2: 4}
+# tcm_activation codes of the fused epilogue
+ACT_CODE = {None: 0, "none": 0, "relu": 1, "gelu": 2}
 # Symbols the C ABI (include/tcm.h) exports.
-EXPORTS = ("tcm_gemm", "tcm_gemm_ex", "tcm_sp_compress", "tcm_sp_decompress", "tcm_gemm_sp", "tcm_gemm_mx",
+EXPORTS = ("tcm_gemm", "tcm_gemm_ex", "tcm_gemm_fused", "tcm_sp_compress", "tcm_sp_decompress", "tcm_gemm_sp", "tcm_gemm_mx",
            "tcm_mx_scales_bytes", "tcm_mx_pack_scales",
            "tcm_get_device_status", "tcm_clear_device_status", "tcm_set_timeout_ns",
            "tcm_status_string", "tcm_version", "tcm_set_config_override", "tcm_debug_fail_next_launch")
@@ -56,6 +58,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.tcm_gemm_ex.restype = i32
     lib.tcm_gemm_ex.argtypes = [i64, i64, i64, i32, vp, i64, i32, vp, i64, vp, i64, vp, i64,
                                 i32, f32, f32, vp, vp, vp, vp]
+    lib.tcm_gemm_fused.restype = i32
+    lib.tcm_gemm_fused.argtypes = [i64, i64, i64, i32, vp, i64, i32, vp, i64, vp, i64, vp, i64,
+                                   i32, f32, f32, vp, vp, vp, i32, vp, vp, vp]
     lib.tcm_sp_compress.restype = i32
     lib.tcm_sp_compress.argtypes = [i64, i64, i32, vp, i64, vp, vp, vp]
     lib.tcm_sp_decompress.restype = i32
@@ -131,6 +136,29 @@ def tcm_gemm_ex(A, B, D, *, C=None, alpha=1.0, beta=0.0, a_scale=None, b_scale=N
                          _ptr(D), _row_pitch(D, "D"), _code(D, "D"), float(alpha), float(beta),
                          _ptr(a_scale), _ptr(b_scale), _ptr(bias), _stream(stream))
     _check(st, "tcm_gemm_ex")
+    return D
+
+
+def tcm_gemm_fused(A, B, D, *, C=None, alpha=1.0, beta=0.0, a_scale=None, b_scale=None, bias=None,
+                   act=None, d_scale=None, amax=None, stream=None):
+    """y = act(alpha * a_scale * b_scale * (A @ B_stored.T) + beta * C + bias); D = y / d_scale in D's
+    dtype (FP8 outputs saturate); amax (one-element fp32 CUDA tensor or None) receives max |y|.
+
+    act: None/"none", "relu" or "gelu"; d_scale: one-element fp32 CUDA tensor or None (FP8 D only).
+    """
+    lib = load_library()
+    M, K = A.shape
+    N = B.shape[0]
+    if B.shape[1] != K or tuple(D.shape) != (M, N):
+        raise ValueError("shape mismatch")
+    if act not in ACT_CODE:
+        raise ValueError(f"unknown activation {act!r}")
+    st = lib.tcm_gemm_fused(M, N, K, _code(A, "A"), _ptr(A), _row_pitch(A, "A"), _code(B, "B"), _ptr(B),
+                            _row_pitch(B, "B"), _ptr(C), _row_pitch(C, "C") if C is not None else 0,
+                            _ptr(D), _row_pitch(D, "D"), _code(D, "D"), float(alpha), float(beta),
+                            _ptr(a_scale), _ptr(b_scale), _ptr(bias), ACT_CODE[act], _ptr(d_scale), _ptr(amax),
+                            _stream(stream))
+    _check(st, "tcm_gemm_fused")
     return D
 
 

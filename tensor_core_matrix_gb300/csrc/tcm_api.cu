@@ -170,10 +170,14 @@ void tcm_set_config_override(int cta_group, int tile_n, int stages, int group_m,
 
 void tcm_debug_fail_next_launch(int mask) { g_fault_once.store(mask); }
 
-tcm_status tcm_gemm_ex(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const void *A, int64_t lda,
-                       tcm_dtype b_dtype, const void *B, int64_t ldb, const void *C, int64_t ldc, void *D,
-                       int64_t ldd, tcm_dtype out_dtype, float alpha, float beta, const float *a_scale,
-                       const float *b_scale, const void *bias, tcm_stream_t stream)
+// Dense GEMM with the full epilogue: y = act(alpha * sa * sb * acc + beta * C + bias),
+// D = y / d_scale cast to out_dtype (FP8 outputs: saturating), amax = max |y|.
+// tcm_gemm_ex is the act = none, 16/32-bit-output case.
+static tcm_status gemm_impl(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const void *A, int64_t lda,
+                            tcm_dtype b_dtype, const void *B, int64_t ldb, const void *C, int64_t ldc, void *D,
+                            int64_t ldd, tcm_dtype out_dtype, float alpha, float beta, const float *a_scale,
+                            const float *b_scale, const void *bias, int act, const float *d_scale, float *amax,
+                            bool fused, tcm_stream_t stream)
 {
     // ---- argument checks (nothing is launched on failure)
     const bool a16 = a_dtype == TCM_BF16 || a_dtype == TCM_F16;
@@ -183,7 +187,13 @@ tcm_status tcm_gemm_ex(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const
     if (a16 && b_dtype == a_dtype) kind = 0;
     else if (a8 && b8) kind = 1;
     else return TCM_ERR_UNSUPPORTED;
-    if (out_dtype != TCM_BF16 && out_dtype != TCM_F16 && out_dtype != TCM_F32) return TCM_ERR_UNSUPPORTED;
+    const bool out8 = out_dtype == TCM_E4M3 || out_dtype == TCM_E5M2;
+    if (out_dtype != TCM_BF16 && out_dtype != TCM_F16 && out_dtype != TCM_F32 && !(fused && out8))
+        return TCM_ERR_UNSUPPORTED;
+    if (act < TCM_ACT_NONE || act > TCM_ACT_GELU) return TCM_ERR_INVALID_ARG;
+    if (out8 && beta != 0.f) return TCM_ERR_UNSUPPORTED; // no FP8 C
+    if ((amax && (reinterpret_cast<uintptr_t>(amax) & 3u)) || (d_scale && (reinterpret_cast<uintptr_t>(d_scale) & 3u)))
+        return TCM_ERR_MISALIGNED;
     if (M < 1 || N < 1 || K < 0) return TCM_ERR_INVALID_ARG;
     if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2) return TCM_ERR_UNSUPPORTED;
     if (!D) return TCM_ERR_INVALID_ARG;
@@ -285,6 +295,10 @@ tcm_status tcm_gemm_ex(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const
     p.alpha = alpha;
     p.beta = beta;
     p.out_fmt = static_cast<int>(out_dtype);
+    p.bias_fmt = out8 ? OUT_BF16 : p.out_fmt;
+    p.act = act;
+    p.d_scale = out8 ? d_scale : nullptr;
+    p.amax = amax;
     p.swap_ab = swap ? 1 : 0;
     const uint32_t fa = static_cast<uint32_t>(swap ? b_dtype : a_dtype);
     const uint32_t fb = static_cast<uint32_t>(swap ? a_dtype : b_dtype);
@@ -300,8 +314,29 @@ tcm_status tcm_gemm_ex(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const
     const int64_t per_cluster = static_cast<int64_t>(cfg.cta_group) * cfg.ksplit;
     const int64_t clusters = sms / per_cluster;
     const int grid = static_cast<int>((p.num_tiles < clusters ? p.num_tiles : clusters) * per_cluster);
+    if (amax && cudaMemsetAsync(amax, 0, sizeof(float), reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return TCM_ERR_CUDA;
     const cudaError_t e = launch_gemm(cfg, tmA, tmB, nullptr, p, grid, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TCM_OK : TCM_ERR_CUDA;
+}
+
+tcm_status tcm_gemm_ex(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const void *A, int64_t lda,
+                       tcm_dtype b_dtype, const void *B, int64_t ldb, const void *C, int64_t ldc, void *D,
+                       int64_t ldd, tcm_dtype out_dtype, float alpha, float beta, const float *a_scale,
+                       const float *b_scale, const void *bias, tcm_stream_t stream)
+{
+    return gemm_impl(M, N, K, a_dtype, A, lda, b_dtype, B, ldb, C, ldc, D, ldd, out_dtype, alpha, beta, a_scale,
+                     b_scale, bias, TCM_ACT_NONE, nullptr, nullptr, false, stream);
+}
+
+tcm_status tcm_gemm_fused(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const void *A, int64_t lda,
+                          tcm_dtype b_dtype, const void *B, int64_t ldb, const void *C, int64_t ldc, void *D,
+                          int64_t ldd, tcm_dtype out_dtype, float alpha, float beta, const float *a_scale,
+                          const float *b_scale, const void *bias, tcm_activation act, const float *d_scale,
+                          float *amax, tcm_stream_t stream)
+{
+    return gemm_impl(M, N, K, a_dtype, A, lda, b_dtype, B, ldb, C, ldc, D, ldd, out_dtype, alpha, beta, a_scale,
+                     b_scale, bias, static_cast<int>(act), d_scale, amax, true, stream);
 }
 
 tcm_status tcm_gemm(int64_t M, int64_t N, int64_t K, tcm_dtype in_dtype, const void *A, const void *B,
@@ -403,6 +438,7 @@ tcm_status tcm_gemm_sp(int64_t M, int64_t N, int64_t K, tcm_dtype dtype, const v
     p.alpha = alpha;
     p.beta = beta;
     p.out_fmt = static_cast<int>(out_dtype);
+    p.bias_fmt = p.out_fmt;
     p.swap_ab = 0;
     const uint32_t code = dtype == TCM_BF16 ? 1u : 0u;
     p.idesc = make_idesc(code, code, 128u * static_cast<uint32_t>(cfg.cta_group), static_cast<uint32_t>(cfg.bn)) |
@@ -483,6 +519,7 @@ tcm_status tcm_gemm_mx(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const
     p.alpha = alpha;
     p.beta = beta;
     p.out_fmt = static_cast<int>(out_dtype);
+    p.bias_fmt = p.out_fmt;
     p.swap_ab = 0;
     // block-scaled instruction descriptor: [7,10) A format, [10,13) B format (E4M3 = 0,
     // E5M2 = 1), [17,23) N >> 3, [23] scale type (1 = UE8M0), [24,29) M >> 4; the

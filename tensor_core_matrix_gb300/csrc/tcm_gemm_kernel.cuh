@@ -265,6 +265,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
 
         int local = 0;
+        float amax_local = 0.f; // max |y| of this lane's outputs (when p.amax is set)
         for (int t = first_tile; t < p.tile_end; t += num_clusters, ++local) {
             const int acc = local & 1;
             const uint32_t acc_phase = (local >> 1) & 1;
@@ -326,7 +327,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                     for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(sum[j]);
                 }
-                epilogue_row32(p, scale, row, nb * BN + c, r);
+                const float m = epilogue_row32(p, scale, row, nb * BN + c, r);
+                if (p.amax) amax_local = amax_combine(amax_local, m);
             }
             if constexpr (KS > 1) {
                 __syncwarp();
@@ -341,6 +343,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
         }
+        if (p.amax) amax_flush(p.amax, amax_local);
     }
 
     __syncwarp();

@@ -9,7 +9,10 @@
 namespace tcm {
 
 // Output / C / bias element formats; values equal the public tcm_dtype codes.
-enum OutFmt : int { OUT_BF16 = 0, OUT_F16 = 1, OUT_F32 = 2 };
+enum OutFmt : int { OUT_BF16 = 0, OUT_F16 = 1, OUT_F32 = 2, OUT_E4M3 = 3, OUT_E5M2 = 4 };
+
+// Epilogue activations; values equal the public tcm_activation codes.
+enum Act : int { ACT_NONE = 0, ACT_RELU = 1, ACT_GELU = 2 };
 
 // Device-status codes and the wait sites that can record a timeout.
 enum DevCode : int { DEV_OK = 0, DEV_TIMEOUT = 5 };
@@ -43,6 +46,10 @@ struct GemmParams {
     const float *b_scale;
     float alpha, beta;
     int out_fmt;
+    int bias_fmt;             // bias element format (bf16 when the output is FP8)
+    int act;                  // Act applied after the bias
+    const float *d_scale;     // FP8 output: dequantisation factor of D (D = y / d_scale); null = 1
+    float *amax;              // if set: max |y| over the launch, max-combined as fp32 bits
     int swap_ab;
     uint32_t idesc;
     unsigned long long timeout_ns;

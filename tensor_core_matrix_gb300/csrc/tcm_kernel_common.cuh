@@ -1,11 +1,13 @@
 // tcm_kernel_common.cuh -- pieces shared by the dense and the 2:4-sparse
 // tcgen05 GEMM kernels: shared-memory ring layout, bounded mbarrier waits
 // that record a device status instead of hanging, the grouped tile order,
-// and the epilogue (alpha*sA*sB*acc + beta*C + bias, RNE cast, stores).
+// and the epilogue (alpha*sA*sB*acc + beta*C + bias, activation, amax,
+// RNE cast -- saturating for FP8 outputs -- and stores).
 #pragma once
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "tcm_internal.h"
 #include "tcm_ptx.cuh"
@@ -92,11 +94,46 @@ __device__ __forceinline__ float ld_elem(const void *base, long long i, int fmt)
     return static_cast<const float *>(base)[i];
 }
 
+__device__ __forceinline__ __nv_fp8_interpretation_t fp8_kind(int fmt)
+{
+    return fmt == OUT_E4M3 ? __NV_E4M3 : __NV_E5M2;
+}
+
+// Two values, round to nearest even with saturation to the largest finite FP8 value.
+__device__ __forceinline__ uint32_t fp8x2(float lo, float hi, int fmt)
+{
+    return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, fp8_kind(fmt)));
+}
+
 __device__ __forceinline__ void st_elem(void *base, long long i, int fmt, float v)
 {
     if (fmt == OUT_BF16) static_cast<__nv_bfloat16 *>(base)[i] = __float2bfloat16_rn(v);
     else if (fmt == OUT_F16) static_cast<__half *>(base)[i] = __float2half_rn(v);
-    else static_cast<float *>(base)[i] = v;
+    else if (fmt == OUT_F32) static_cast<float *>(base)[i] = v;
+    else static_cast<uint8_t *>(base)[i] = __nv_cvt_float_to_fp8(v, __NV_SATFINITE, fp8_kind(fmt));
+}
+
+__device__ __forceinline__ float activate(float v, int act)
+{
+    if (act == ACT_RELU) return v > 0.f ? v : 0.f;
+    if (act == ACT_GELU) return 0.5f * v * (1.f + erff(v * 0.70710678118654752f));
+    return v;
+}
+
+// max(m, |x|) that keeps a NaN once seen (fmaxf would drop it).
+__device__ __forceinline__ float amax_combine(float m, float x)
+{
+    const float a = fabsf(x);
+    return (a > m || a != a) ? a : m;
+}
+
+// Warp-wide amax of the per-lane maxima, max-combined into *amax as fp32 bits
+// (non-negative floats order like their bit patterns; a NaN is above +inf).
+__device__ __forceinline__ void amax_flush(float *amax, float m)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = amax_combine(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((threadIdx.x & 31) == 0) atomicMax(reinterpret_cast<unsigned int *>(amax), __float_as_uint(m));
 }
 
 // 32 consecutive elements starting at a 16-byte-aligned address.
@@ -131,7 +168,14 @@ __device__ __forceinline__ void ld32(const void *base, long long i, int fmt, flo
 
 __device__ __forceinline__ void st32(void *base, long long i, int fmt, const float (&v)[32])
 {
-    if (fmt == OUT_F32) {
+    if (fmt == OUT_E4M3 || fmt == OUT_E5M2) {
+        uint4 *q = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(base) + i);
+        uint32_t w[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) w[j] = fp8x2(v[4 * j], v[4 * j + 1], fmt) | (fp8x2(v[4 * j + 2], v[4 * j + 3], fmt) << 16);
+        q[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        q[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    } else if (fmt == OUT_F32) {
         float4 *q = reinterpret_cast<float4 *>(static_cast<float *>(base) + i);
 #pragma unroll
         for (int j = 0; j < 8; ++j) q[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
@@ -155,11 +199,15 @@ __device__ __forceinline__ void st32(void *base, long long i, int fmt, const flo
     }
 }
 
-// Epilogue of 32 accumulator columns of one kernel row: out = scale*acc + beta*C + bias.
-__device__ __forceinline__ void epilogue_row32(const GemmParams &p, float scale, int row, int col0,
-                                               const uint32_t (&r)[32])
+// Epilogue of 32 accumulator columns of one kernel row:
+//   y = act(scale*acc + beta*C + bias), stored as y / d_scale in the output format.
+// Returns max |y| over the stored elements when p.amax is set (else 0).
+__device__ __forceinline__ float epilogue_row32(const GemmParams &p, float scale, int row, int col0,
+                                                const uint32_t (&r)[32])
 {
-    if (row >= p.kM) return;
+    float m = 0.f;
+    if (row >= p.kM) return m;
+    const float inv_d = p.d_scale ? __frcp_rn(*p.d_scale) : 1.f;
     float v[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] = scale * __uint_as_float(r[j]);
@@ -174,9 +222,21 @@ __device__ __forceinline__ void epilogue_row32(const GemmParams &p, float scale,
             }
             if (p.bias) {
                 float b[32];
-                ld32(p.bias, col0, p.out_fmt, b);
+                ld32(p.bias, col0, p.bias_fmt, b);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] += b[j];
+            }
+            if (p.act != ACT_NONE) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = activate(v[j], p.act);
+            }
+            if (p.amax) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) m = amax_combine(m, v[j]);
+            }
+            if (p.d_scale) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] *= inv_d;
             }
             st32(p.D, doff, p.out_fmt, v);
         } else {
@@ -187,25 +247,30 @@ __device__ __forceinline__ void epilogue_row32(const GemmParams &p, float scale,
                     float x = v[j];
                     if (p.beta != 0.f)
                         x = fmaf(p.beta, ld_elem(p.C, static_cast<long long>(row) * p.ldc + col, p.out_fmt), x);
-                    if (p.bias) x += ld_elem(p.bias, col, p.out_fmt);
-                    st_elem(p.D, doff + j, p.out_fmt, x);
+                    if (p.bias) x += ld_elem(p.bias, col, p.bias_fmt);
+                    x = activate(x, p.act);
+                    if (p.amax) m = amax_combine(m, x);
+                    st_elem(p.D, doff + j, p.out_fmt, p.d_scale ? x * inv_d : x);
                 }
             }
         }
     } else {
         // kernel row = column n of D, kernel column = row m of D
-        const float b = p.bias ? ld_elem(p.bias, row, p.out_fmt) : 0.f;
+        const float b = p.bias ? ld_elem(p.bias, row, p.bias_fmt) : 0.f;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-            const int m = col0 + j;
-            if (m < p.kN) {
+            const int mm = col0 + j;
+            if (mm < p.kN) {
                 float x = v[j];
-                if (p.beta != 0.f) x = fmaf(p.beta, ld_elem(p.C, static_cast<long long>(m) * p.ldc + row, p.out_fmt), x);
+                if (p.beta != 0.f) x = fmaf(p.beta, ld_elem(p.C, static_cast<long long>(mm) * p.ldc + row, p.out_fmt), x);
                 x += b;
-                st_elem(p.D, static_cast<long long>(m) * p.ldd + row, p.out_fmt, x);
+                x = activate(x, p.act);
+                if (p.amax) m = amax_combine(m, x);
+                st_elem(p.D, static_cast<long long>(mm) * p.ldd + row, p.out_fmt, p.d_scale ? x * inv_d : x);
             }
         }
     }
+    return m;
 }
 
 // Wait on a barrier of this CTA (arrivals may come from the peer CTA of a pair).

@@ -94,3 +94,29 @@ def test_library_is_built_for_sm_103a_only():
 def test_gemm_mx_rejects_bad_arguments(lib, a, b, K, status):
     assert lib.tcm_gemm_mx(64, 64, K, a, ALIGNED, ALIGNED, b, ALIGNED, ALIGNED, None, ALIGNED, 1.0, 0.0, None,
                            BF16, None) == status
+
+
+def fused(lib, **kw):
+    a = dict(M=64, N=64, K=64, a_dtype=BF16, A=ALIGNED, lda=64, b_dtype=BF16, B=ALIGNED, ldb=64,
+             C=None, ldc=0, D=ALIGNED, ldd=64, out_dtype=BF16, alpha=1.0, beta=0.0,
+             a_scale=None, b_scale=None, bias=None, act=0, d_scale=None, amax=None, stream=None)
+    a.update(kw)
+    return lib.tcm_gemm_fused(a["M"], a["N"], a["K"], a["a_dtype"], a["A"], a["lda"], a["b_dtype"], a["B"],
+                              a["ldb"], a["C"], a["ldc"], a["D"], a["ldd"], a["out_dtype"], a["alpha"],
+                              a["beta"], a["a_scale"], a["b_scale"], a["bias"], a["act"], a["d_scale"],
+                              a["amax"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(act=3), 1), (dict(act=-1), 1), (dict(M=0), 1),
+    (dict(out_dtype=E4M3, beta=1.0, C=ALIGNED, ldc=64), 2),   # no FP8 C
+    (dict(out_dtype=E4M3, ldd=72), 3),                        # 72 bytes: not a multiple of 16
+    (dict(amax=ALIGNED + 2), 3), (dict(d_scale=ALIGNED + 1), 3),
+    (dict(a_dtype=E4M3, b_dtype=BF16), 2),
+])
+def test_gemm_fused_rejects_bad_arguments(lib, kw, status):
+    assert fused(lib, **kw) == status
+
+
+def test_gemm_ex_still_rejects_fp8_output(lib):
+    assert gemm_ex(lib, out_dtype=E5M2) == 2
