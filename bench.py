@@ -335,6 +335,8 @@ def shape_cases():
         ("fp8 e4m3xe5m2 8192^3 +scales+bias", lambda: si.fp8_case(b_fmt="e5m2")),
         ("sparse 2:4 bf16 8192^3", lambda: si.sparse_case()),
         ("mxfp8 e4m3 8192^3 (E8M0 scales per 32)", lambda: si.mx_case()),
+        ("fused fp8 e4m3 8192^3 +scales+bias -> GELU -> e4m3 out (d_scale 2) + amax",
+         lambda: dict(si.fp8_case(b_fmt="e4m3"), fused="gelu")),
     ]
 
 
@@ -355,6 +357,8 @@ def run_shapes(args, tcm, device, peaks_used):
         M, K = A.shape
         N = B.shape[0]
         out_dtype = torch.float32 if case.get("out_fmt") == "f32" else torch.bfloat16
+        if case.get("fused"):
+            out_dtype = torch.float8_e4m3fn
         D = torch.empty((M, N), dtype=out_dtype, device=device)
         C = case["C"].to(device) if case.get("C") is not None else None
         kw = dict(C=C, alpha=case.get("alpha", 1.0), beta=case.get("beta", 0.0))
@@ -369,6 +373,10 @@ def run_shapes(args, tcm, device, peaks_used):
             SA = tcm.tcm_mx_pack_scales(case["SA"].to(device), K)
             SB = tcm.tcm_mx_pack_scales(case["SB"].to(device), K)
             launch = lambda: tcm.tcm_gemm_mx(A, SA, B, SB, D)
+        elif case.get("fused"):
+            d_scale = torch.tensor([2.0], device=device)
+            amax = torch.zeros(1, device=device)
+            launch = lambda: tcm.tcm_gemm_fused(A, B, D, act=case["fused"], d_scale=d_scale, amax=amax, **kw)
         else:
             launch = lambda: tcm.tcm_gemm_ex(A, B, D, **kw)
         for _ in range(3):
@@ -392,7 +400,7 @@ def run_shapes(args, tcm, device, peaks_used):
         byts = in_bytes + D.numel() * D.element_size() + (C.numel() * C.element_size() if C is not None else 0)
         tf = flop / (ms * 1e-3) / 1e12
         gbs = byts / (ms * 1e-3) / 1e9
-        peak = bf16_peak * (FP8_OVER_BF16 if ("fp8" in name or "mx" in name) else 1.0)
+        peak = bf16_peak * (FP8_OVER_BF16 if ("fp8" in name or "mx" in name) else 1.0)  # "fused" is FP8 too
         line = {"kind": "shape", "workload": name, "M": M, "N": N, "K": K, "ms_median": ms, "ms_min": min(times),
                 "tflops": tf, "frac_of_tensor_peak": tf / peak, "algorithmic_bytes": byts, "gbs": gbs,
                 "frac_of_hbm": gbs / hbm_peak, "bound": "hbm" if M <= 64 else "tensor", "device_status": code,
