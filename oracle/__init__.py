@@ -41,8 +41,10 @@ _lock = threading.Lock()
 _lib = None
 
 # The oracle's own format codes (mirrors the enum in oracle.c only).
-FMT = {"bf16": 0, "f16": 1, "f32": 2, "e4m3": 3, "e5m2": 4, "e8m0": 5}
-ELEM_BYTES = {"bf16": 2, "f16": 2, "f32": 4, "e4m3": 1, "e5m2": 1, "e8m0": 1}
+FMT = {"bf16": 0, "f16": 1, "f32": 2, "e4m3": 3, "e5m2": 4, "e8m0": 5, "e2m1": 6}
+# bytes of one stored unit; an E2M1 byte holds two elements (element 2i in the low nibble)
+ELEM_BYTES = {"bf16": 2, "f16": 2, "f32": 4, "e4m3": 1, "e5m2": 1, "e8m0": 1, "e2m1": 1}
+PER_UNIT = {"e2m1": 2}
 CODE_DTYPE = {1: np.uint8, 2: np.uint16, 4: np.uint32}
 # significand precision p (bits incl. the implicit one) and the smallest
 # positive subnormal of each output format; an RNE cast to the format is
@@ -118,8 +120,9 @@ def _ptr(a):
 def decode(codes: np.ndarray, fmt: str) -> np.ndarray:
     """Exact real values (float64) of an array of stored codes of ``fmt``."""
     c = _codes(codes, fmt)
-    out = np.empty(c.shape, dtype=np.float64)
-    if _load().orc_decode_array(_ptr(c), FMT[fmt], c.size, _ptr(out)) != 0:
+    per = PER_UNIT.get(fmt, 1)
+    out = np.empty(c.shape[:-1] + (c.shape[-1] * per,) if c.ndim else (per,), dtype=np.float64)
+    if _load().orc_decode_array(_ptr(c), FMT[fmt], c.size * per, _ptr(out)) != 0:
         raise ValueError("bad format")
     return out
 
@@ -138,6 +141,8 @@ def gemm(A, B, a_fmt, b_fmt, *, C=None, c_fmt="f32", bias=None, bias_fmt="bf16",
     B = _codes(B, b_fmt)
     M, lda = A.shape
     N, ldb = B.shape
+    lda *= PER_UNIT.get(a_fmt, 1)  # leading dimensions in elements
+    ldb *= PER_UNIT.get(b_fmt, 1)
     K = lda if K is None else K
     if K > lda or K > ldb:
         raise ValueError("K exceeds a leading dimension")

@@ -39,8 +39,9 @@
 #include <stdlib.h>
 #include <string.h>
 
-/* The oracle's own element-format codes (E8M0: the UE8M0 block-scale format). */
-enum { ORC_BF16 = 0, ORC_F16 = 1, ORC_F32 = 2, ORC_E4M3 = 3, ORC_E5M2 = 4, ORC_E8M0 = 5 };
+/* The oracle's own element-format codes (E8M0: the UE8M0 block-scale format;
+ * E2M1: 4-bit, stored two per byte, element 2i in the low nibble). */
+enum { ORC_BF16 = 0, ORC_F16 = 1, ORC_F32 = 2, ORC_E4M3 = 3, ORC_E5M2 = 4, ORC_E8M0 = 5, ORC_E2M1 = 6 };
 
 /* Width in bytes of one stored element of each format (0 = unknown). */
 int orc_elem_bytes(int fmt)
@@ -49,6 +50,7 @@ int orc_elem_bytes(int fmt)
     case ORC_BF16: case ORC_F16: return 2;
     case ORC_F32: return 4;
     case ORC_E4M3: case ORC_E5M2: case ORC_E8M0: return 1;
+    case ORC_E2M1: return 1; /* a byte holds two elements: see load_code */
     default: return 0;
     }
 }
@@ -63,6 +65,8 @@ int orc_elem_bytes(int fmt)
  *              number (largest 1.75 * 2^8 = 448).
  *   E5M2 (OCP): s | e(5, bias 15) | m(2); e=31 is inf (m=0) or NaN.
  *   E8M0 (OCP MX scale): e(8), value 2^(e - 127); e = 255 is NaN.
+ *   E2M1 (OCP FP4): s | e(2, bias 1) | m(1); no infinities or NaN
+ *              (magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6).
  * A zero exponent field means a subnormal: m * 2^(1 - bias - mbits).
  */
 double orc_decode(uint32_t code, int fmt)
@@ -73,6 +77,7 @@ double orc_decode(uint32_t code, int fmt)
     case ORC_F16: ebits = 5; mbits = 10; bias = 15; break;
     case ORC_E4M3: ebits = 4; mbits = 3; bias = 7; break;
     case ORC_E5M2: ebits = 5; mbits = 2; bias = 15; break;
+    case ORC_E2M1: ebits = 2; mbits = 1; bias = 1; code &= 0xFu; break;
     case ORC_F32: {
         float f;
         uint32_t u = code;
@@ -91,6 +96,8 @@ double orc_decode(uint32_t code, int fmt)
     uint32_t emax = (1u << ebits) - 1u;
     if (fmt == ORC_E4M3) {
         if (e == emax && m == (1u << mbits) - 1u) return NAN;
+    } else if (fmt == ORC_E2M1) {
+        /* every code is a number */
     } else if (e == emax) {
         return m == 0 ? sign * INFINITY : NAN;
     }
@@ -101,6 +108,10 @@ double orc_decode(uint32_t code, int fmt)
 /* Fetch code number idx of a buffer of format fmt. */
 static uint32_t load_code(const void *buf, int fmt, int64_t idx)
 {
+    if (fmt == ORC_E2M1) {
+        const uint8_t b = ((const uint8_t *)buf)[idx >> 1];
+        return (idx & 1) ? (uint32_t)(b >> 4) : (uint32_t)(b & 0xFu);
+    }
     switch (orc_elem_bytes(fmt)) {
     case 1: return ((const uint8_t *)buf)[idx];
     case 2: return ((const uint16_t *)buf)[idx];
@@ -122,7 +133,7 @@ static double *decode_table(int fmt)
 {
     int bytes = orc_elem_bytes(fmt);
     if (bytes != 1 && bytes != 2) return NULL;
-    size_t n = (size_t)1 << (8 * bytes);
+    size_t n = fmt == ORC_E2M1 ? 16 : (size_t)1 << (8 * bytes);
     double *t = (double *)malloc(n * sizeof(double));
     if (!t) return NULL;
     for (size_t c = 0; c < n; ++c) t[c] = orc_decode((uint32_t)c, fmt);

@@ -16,6 +16,12 @@ Workloads (shapes, value distributions, seeds):
 * ``sparse``      logical A ~ N(0,1) bf16 (pruned by the method), B ~ N(0,1), seed 4
 * ``mx``          MXFP8: N(0,1) in blocks of 32 along K with E8M0 scales (OCP MX
                   conversion), E4M3 elements, seed 5
+* ``w4a8``        8192^3 A E4M3 activations x B E2M1 weights (FP4, two per byte),
+                  N(0,1) each scaled per tensor so amax lands on the format max
+                  (448, 6), seed 6
+
+torch has no cast to FP4 E2M1, so :func:`fp4_e2m1` rounds to the E2M1 grid
+itself: nearest value, ties to the even code, saturating at +-6 (OCP FP4).
 """
 from __future__ import annotations
 
@@ -53,6 +59,35 @@ def integers(shape, g, lo=-8, hi=8, dtype="bf16"):
     """Integer-valued inputs in [lo, hi]; exactly representable in every format here."""
     x = torch.randint(lo, hi + 1, shape, generator=g, dtype=torch.int32).to(torch.float32)
     return x.to(TORCH_DTYPE[dtype])
+
+
+FP4_GRID = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)  # E2M1 magnitudes of codes 0..7
+
+
+def fp4_e2m1(x: torch.Tensor) -> torch.Tensor:
+    """E2M1 codes (uint8, one per element) of fp32 ``x``: nearest grid value, ties to
+    the even code, |x| > 6 saturating to 6; the sign is bit 3."""
+    x = x.to(torch.float32)
+    grid = torch.tensor(FP4_GRID, dtype=torch.float32)
+    a = x.abs().clamp(max=6.0)
+    d = (a[..., None] - grid).abs()
+    best = d == d.min(dim=-1, keepdim=True).values
+    idx = torch.arange(8)
+    score = best.to(torch.int64) * (2 - (idx & 1))  # of two nearest codes the even one wins
+    code = score.argmax(dim=-1).to(torch.uint8)
+    return code | ((x < 0).to(torch.uint8) << 3)
+
+
+def pack_fp4(codes: torch.Tensor) -> torch.Tensor:
+    """Two E2M1 codes per byte along the last dimension: element 2i in the low nibble."""
+    return (codes[..., 0::2] | (codes[..., 1::2] << 4)).contiguous()
+
+
+def fp4_per_tensor(x: torch.Tensor):
+    """Packed E2M1 of fp32 ``x`` scaled so its amax lands on 6; returns (packed, dequant scale)."""
+    amax = float(x.abs().max())
+    s_quant = 6.0 / amax if amax > 0 else 1.0
+    return pack_fp4(fp4_e2m1(x * s_quant)), float(torch.tensor(1.0 / s_quant, dtype=torch.float32))
 
 
 def fp8_per_tensor(x: torch.Tensor, fmt: str):
@@ -94,6 +129,16 @@ def mx_case(M=8192, N=8192, K=8192, a_fmt="e4m3", b_fmt="e4m3", seed=5):
     A, SA = mx_quantize(xa, a_fmt)
     B, SB = mx_quantize(xb, b_fmt)
     return dict(A=A, SA=SA, B=B, SB=SB, a_fmt=a_fmt, b_fmt=b_fmt, out_fmt="bf16")
+
+
+def w4a8_case(M=8192, N=8192, K=8192, a_fmt="e4m3", seed=6):
+    """FP8 activations A (M x K) times FP4 E2M1 weights B (N x K, packed: N x K/2 bytes)."""
+    g = generator(seed)
+    xa = torch.randn((M, K), generator=g, dtype=torch.float32)
+    xb = torch.randn((N, K), generator=g, dtype=torch.float32)
+    A, sa = fp8_per_tensor(xa, a_fmt)
+    B, sb = fp4_per_tensor(xb)
+    return dict(A=A, B=B, sa=sa, sb=sb, a_fmt=a_fmt, b_fmt="e2m1", out_fmt="bf16")
 
 
 def small_case(M=512, N=512, K=512, seed=0):

@@ -520,3 +520,39 @@ def test_fused_bound_without_activation_covers_the_plain_bound():
     _, b_relu, _, e_relu = oracle.fused_reference(ref, S, "relu", "bf16")
     _, b_gelu, _, e_gelu = oracle.fused_reference(ref, S, "gelu", "bf16")
     assert np.all(e_gelu >= e_relu)
+
+
+# ---- FP4 E2M1 (OCP): decode, packing order, GEMM with packed operands
+
+def test_e2m1_decode_all_codes():
+    """The 16 E2M1 codes from the format definition: s | e(2, bias 1) | m(1), no inf/NaN."""
+    table = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    codes = np.array([(2 * i + 1) << 4 | (2 * i) for i in range(8)], dtype=np.uint8)  # codes 0..15 in order
+    got = oracle.decode(codes, "e2m1")
+    assert list(got[:8]) == table
+    assert list(-got[8:]) == table and np.signbit(got[8])
+
+
+def test_e2m1_packing_puts_element_2i_in_the_low_nibble():
+    got = oracle.decode(np.array([[0x21, 0x7F]], dtype=np.uint8), "e2m1")
+    assert got.tolist() == [[0.5, 1.0, -6.0, 6.0]]
+
+
+def test_gemm_with_e2m1_operand_matches_numpy():
+    g = np.random.default_rng(11)
+    M, N, K = 20, 24, 96
+    A = si.codes(si.fp8_per_tensor(torch.from_numpy(g.normal(size=(M, K)).astype(np.float32)), "e4m3")[0])
+    B = g.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    ref, S = oracle.gemm(A, B, "e4m3", "e2m1", sa=0.5, sb=2.0)
+    da, db = oracle.decode(A, "e4m3"), oracle.decode(B, "e2m1")
+    assert db.shape == (N, K)
+    assert np.all(np.abs(ref - da @ db.T) <= 1e-12 * np.maximum(S, 1e-300))
+    # swapped roles: E2M1 A
+    ref2, _ = oracle.gemm(B, A, "e2m1", "e4m3")
+    assert np.allclose(ref2, db @ da.T, rtol=1e-12, atol=0)
+
+
+def test_fp4_input_rounding_ties_to_even_and_saturates():
+    x = torch.tensor([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, -5.0, 7.0, -0.3, 0.26, 100.0])
+    vals = oracle.decode(si.pack_fp4(si.fp4_e2m1(x)).numpy(), "e2m1")
+    assert vals.tolist() == [0.0, 1.0, 1.0, 2.0, 2.0, 4.0, 4.0, -4.0, 6.0, -0.5, 0.5, 6.0]
