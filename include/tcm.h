@@ -58,7 +58,8 @@ typedef enum {
     TCM_F16 = 1,
     TCM_F32 = 2,
     TCM_E4M3 = 3,
-    TCM_E5M2 = 4
+    TCM_E5M2 = 4,
+    TCM_E2M1 = 5 /* OCP FP4: s | e(2, bias 1) | m(1), packed two per byte, element 2i in the low nibble */
 } tcm_dtype;
 
 /* Activation of the fused epilogue (tcm_gemm_fused). */
@@ -98,11 +99,16 @@ tcm_status tcm_gemm(int64_t M, int64_t N, int64_t K, tcm_dtype in_dtype,
  * (FP8 A x FP8 B -> FP32 accumulator -> scale / bias / cast -> output),
  * read as: scale, then + beta*C, then + bias[n], then one RNE cast.
  *
- *  a_dtype, b_dtype  (bf16,bf16), (f16,f16), or any pair of {e4m3, e5m2}
- *                    (section "Blackwell ... SM100" table: kind::f8f6f4
- *                    lets A and B differ).  Other pairs: TCM_ERR_UNSUPPORTED.
+ *  a_dtype, b_dtype  (bf16,bf16), (f16,f16), or any pair of {e4m3, e5m2, e2m1}
+ *                    (section "SM100：tcgen05.mma" table: kind::f8f6f4 lets A
+ *                    and B differ, e.g. FP4 x FP8; section "量化配置如何映射到 MMA":
+ *                    W4A8 on Blackwell is bare FP4 x bare FP8).  Other pairs:
+ *                    TCM_ERR_UNSUPPORTED.  An E2M1 operand needs K % 128 == 0
+ *                    (else TCM_ERR_UNSUPPORTED), its pitch a multiple of 64
+ *                    elements and its base 32-byte aligned (else
+ *                    TCM_ERR_MISALIGNED).
  *  lda, ldb          row pitches in ELEMENTS of A (M x K) and of B (N x K);
- *                    lda, ldb >= K.
+ *                    lda, ldb >= K (an E2M1 row of lda elements is lda/2 bytes).
  *  ldc, ldd          row pitches in elements of C and D; >= N.
  *  a_scale, b_scale  DEVICE pointers to one fp32 each (per-tensor
  *                    dequantisation factors: real value = stored value *

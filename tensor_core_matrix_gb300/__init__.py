@@ -119,20 +119,38 @@ def _code(t, name):
         raise ValueError(f"{name}: unsupported dtype {t.dtype}") from None
 
 
-def tcm_gemm_ex(A, B, D, *, C=None, alpha=1.0, beta=0.0, a_scale=None, b_scale=None, bias=None, stream=None):
+TCM_E2M1 = 5
+
+
+def _operand(t, fmt, name):
+    """(dtype code, element columns, pitch in elements) of a GEMM operand; fmt="e2m1"
+    marks a uint8 tensor of packed FP4 (two elements per byte)."""
+    if fmt == "e2m1":
+        if t.dtype != torch.uint8:
+            raise ValueError(f"{name}: packed E2M1 operands are uint8 tensors")
+        return TCM_E2M1, 2 * t.shape[1], 2 * _row_pitch(t, name)
+    if fmt is not None:
+        raise ValueError(f"{name}: unknown format {fmt!r}")
+    return _code(t, name), t.shape[1], _row_pitch(t, name)
+
+
+def tcm_gemm_ex(A, B, D, *, C=None, alpha=1.0, beta=0.0, a_scale=None, b_scale=None, bias=None, stream=None,
+                a_fmt=None, b_fmt=None):
     """D = alpha * a_scale * b_scale * (A @ B_stored.T) + beta * C + bias.
 
     A: M x K (row-major, pitch = A.stride(0)); B: N x K (K-major storage of
     the K x N operand); C, D: M x N; bias: N; a_scale, b_scale: one-element
-    fp32 CUDA tensors or None.
+    fp32 CUDA tensors or None.  a_fmt / b_fmt = "e2m1": that operand is a
+    uint8 tensor of packed FP4 (M x K/2 or N x K/2 bytes).
     """
     lib = load_library()
-    M, K = A.shape
-    N = B.shape[0]
-    if B.shape[1] != K or tuple(D.shape) != (M, N):
+    ca, K, lda = _operand(A, a_fmt, "A")
+    cb, Kb, ldb = _operand(B, b_fmt, "B")
+    M, N = A.shape[0], B.shape[0]
+    if Kb != K or tuple(D.shape) != (M, N):
         raise ValueError("shape mismatch")
-    st = lib.tcm_gemm_ex(M, N, K, _code(A, "A"), _ptr(A), _row_pitch(A, "A"), _code(B, "B"), _ptr(B),
-                         _row_pitch(B, "B"), _ptr(C), _row_pitch(C, "C") if C is not None else 0,
+    st = lib.tcm_gemm_ex(M, N, K, ca, _ptr(A), lda, cb, _ptr(B),
+                         ldb, _ptr(C), _row_pitch(C, "C") if C is not None else 0,
                          _ptr(D), _row_pitch(D, "D"), _code(D, "D"), float(alpha), float(beta),
                          _ptr(a_scale), _ptr(b_scale), _ptr(bias), _stream(stream))
     _check(st, "tcm_gemm_ex")
@@ -140,21 +158,22 @@ def tcm_gemm_ex(A, B, D, *, C=None, alpha=1.0, beta=0.0, a_scale=None, b_scale=N
 
 
 def tcm_gemm_fused(A, B, D, *, C=None, alpha=1.0, beta=0.0, a_scale=None, b_scale=None, bias=None,
-                   act=None, d_scale=None, amax=None, stream=None):
+                   act=None, d_scale=None, amax=None, stream=None, a_fmt=None, b_fmt=None):
     """y = act(alpha * a_scale * b_scale * (A @ B_stored.T) + beta * C + bias); D = y / d_scale in D's
     dtype (FP8 outputs saturate); amax (one-element fp32 CUDA tensor or None) receives max |y|.
 
     act: None/"none", "relu" or "gelu"; d_scale: one-element fp32 CUDA tensor or None (FP8 D only).
     """
     lib = load_library()
-    M, K = A.shape
-    N = B.shape[0]
-    if B.shape[1] != K or tuple(D.shape) != (M, N):
+    ca, K, lda = _operand(A, a_fmt, "A")
+    cb, Kb, ldb = _operand(B, b_fmt, "B")
+    M, N = A.shape[0], B.shape[0]
+    if Kb != K or tuple(D.shape) != (M, N):
         raise ValueError("shape mismatch")
     if act not in ACT_CODE:
         raise ValueError(f"unknown activation {act!r}")
-    st = lib.tcm_gemm_fused(M, N, K, _code(A, "A"), _ptr(A), _row_pitch(A, "A"), _code(B, "B"), _ptr(B),
-                            _row_pitch(B, "B"), _ptr(C), _row_pitch(C, "C") if C is not None else 0,
+    st = lib.tcm_gemm_fused(M, N, K, ca, _ptr(A), lda, cb, _ptr(B),
+                            ldb, _ptr(C), _row_pitch(C, "C") if C is not None else 0,
                             _ptr(D), _row_pitch(D, "D"), _code(D, "D"), float(alpha), float(beta),
                             _ptr(a_scale), _ptr(b_scale), _ptr(bias), ACT_CODE[act], _ptr(d_scale), _ptr(amax),
                             _stream(stream))

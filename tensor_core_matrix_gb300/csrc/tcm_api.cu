@@ -93,15 +93,21 @@ static EncodeTiledFn encode_fn()
 // Tensor map of a K-major operand: `rows` rows of `inner` elements, pitch `ld`
 // elements; tiles of box_rows x 128 bytes with 128-byte swizzling; reads
 // outside the matrix return zeros.
+// elem_bytes 0 = FP4 E2M1 packed two per byte: loaded with 16U4_ALIGN16B, which
+// places each 16 packed values (8 bytes) at the start of a 16-byte shared-memory
+// slot -- a 128-element K stage is then 128 bytes per row, the FP8 stage layout
+// (the padded 8-bit container that kind::f8f6f4 reads for FP4).
 static bool encode_kmajor(CUtensorMap *map, const void *base, int elem_bytes, uint64_t inner, uint64_t rows,
                           uint64_t ld, uint32_t box_rows)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
-    const CUtensorMapDataType dt = elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+    const CUtensorMapDataType dt = elem_bytes == 0   ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B
+                                   : elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                                     : CU_TENSOR_MAP_DATA_TYPE_UINT16;
     const cuuint64_t dims[2] = {inner, rows};
-    const cuuint64_t strides[1] = {ld * static_cast<uint64_t>(elem_bytes)};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / elem_bytes), box_rows};
+    const cuuint64_t strides[1] = {elem_bytes == 0 ? ld / 2 : ld * static_cast<uint64_t>(elem_bytes)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(elem_bytes == 0 ? 128 : 128 / elem_bytes), box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return fn(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -130,11 +136,14 @@ static int elem_bytes(tcm_dtype t)
     case TCM_BF16: case TCM_F16: return 2;
     case TCM_F32: return 4;
     case TCM_E4M3: case TCM_E5M2: return 1;
-    default: return 0;
+    default: return 0; // TCM_E2M1: half a byte, handled where pitches are checked
     }
 }
 
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// kind::f8f6f4 instruction-descriptor format of an 8/4-bit operand
+static uint32_t f8code(uint32_t f) { return f == TCM_E5M2 ? 1u : (f == TCM_E2M1 ? 5u : 0u); }
 
 } // namespace tcm
 
@@ -181,12 +190,13 @@ static tcm_status gemm_impl(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, 
 {
     // ---- argument checks (nothing is launched on failure)
     const bool a16 = a_dtype == TCM_BF16 || a_dtype == TCM_F16;
-    const bool a8 = a_dtype == TCM_E4M3 || a_dtype == TCM_E5M2;
-    const bool b8 = b_dtype == TCM_E4M3 || b_dtype == TCM_E5M2;
+    const bool a8 = a_dtype == TCM_E4M3 || a_dtype == TCM_E5M2 || a_dtype == TCM_E2M1;
+    const bool b8 = b_dtype == TCM_E4M3 || b_dtype == TCM_E5M2 || b_dtype == TCM_E2M1;
     int kind;
     if (a16 && b_dtype == a_dtype) kind = 0;
     else if (a8 && b8) kind = 1;
     else return TCM_ERR_UNSUPPORTED;
+    const bool a4 = a_dtype == TCM_E2M1, b4 = b_dtype == TCM_E2M1;
     const bool out8 = out_dtype == TCM_E4M3 || out_dtype == TCM_E5M2;
     if (out_dtype != TCM_BF16 && out_dtype != TCM_F16 && out_dtype != TCM_F32 && !(fused && out8))
         return TCM_ERR_UNSUPPORTED;
@@ -204,7 +214,14 @@ static tcm_status gemm_impl(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, 
     if ((A && !aligned16(A)) || (B && !aligned16(B)) || !aligned16(D) || (C && !aligned16(C)) ||
         (bias && !aligned16(bias)))
         return TCM_ERR_MISALIGNED;
-    if ((lda * ea) % 16 || (ldb * eb) % 16 || (ldd * eo) % 16 || (C && (ldc * eo) % 16)) return TCM_ERR_MISALIGNED;
+    if ((!a4 && (lda * ea) % 16) || (!b4 && (ldb * eb) % 16) || (ldd * eo) % 16 || (C && (ldc * eo) % 16))
+        return TCM_ERR_MISALIGNED;
+    // packed FP4 operands (16U4_ALIGN16B tensor maps): K a multiple of 128, rows of a
+    // multiple of 32 bytes (64 elements) starting on 32-byte boundaries
+    if ((a4 || b4) && K % 128 != 0) return TCM_ERR_UNSUPPORTED;
+    if ((a4 && (lda % 64 || (reinterpret_cast<uintptr_t>(A) & 31u))) ||
+        (b4 && (ldb % 64 || (reinterpret_cast<uintptr_t>(B) & 31u))))
+        return TCM_ERR_MISALIGNED;
 
     // ---- configuration: swap A and B for skinny M so the weight fills the 128-row MMA
     const bool swap = M <= 64 && N >= 128;
@@ -302,14 +319,22 @@ static tcm_status gemm_impl(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, 
     p.swap_ab = swap ? 1 : 0;
     const uint32_t fa = static_cast<uint32_t>(swap ? b_dtype : a_dtype);
     const uint32_t fb = static_cast<uint32_t>(swap ? a_dtype : b_dtype);
-    // kind::f16: 0 = f16, 1 = bf16; kind::f8f6f4: 0 = E4M3, 1 = E5M2
-    const uint32_t codeA = kind == 0 ? (fa == TCM_BF16 ? 1u : 0u) : (fa == TCM_E5M2 ? 1u : 0u);
-    const uint32_t codeB = kind == 0 ? (fb == TCM_BF16 ? 1u : 0u) : (fb == TCM_E5M2 ? 1u : 0u);
+    // kind::f16: 0 = f16, 1 = bf16; kind::f8f6f4: 0 = E4M3, 1 = E5M2, 5 = E2M1
+    const uint32_t codeA = kind == 0 ? (fa == TCM_BF16 ? 1u : 0u) : f8code(fa);
+    const uint32_t codeB = kind == 0 ? (fb == TCM_BF16 ? 1u : 0u) : f8code(fb);
     p.idesc = make_idesc(codeA, codeB, 128u * static_cast<uint32_t>(cfg.cta_group), static_cast<uint32_t>(cfg.bn));
     p.timeout_ns = timeout_ns();
     p.status = device_status_ptr();
     if (!p.status) return TCM_ERR_CUDA;
 
+    // a packed FP4 (E2M1) tile row counts 64 bytes on the barrier, not the 128 it occupies
+    // in shared memory (16U4_ALIGN16B leaves an 8-byte gap after every 8 bytes)
+    if (kind == 1 && (a4 || b4)) {
+        const bool kA4 = swap ? b4 : a4, kB4 = swap ? a4 : b4;
+        const uint32_t row_a = kA4 ? 64u : 128u, row_b = kB4 ? 64u : 128u;
+        p.stage_tx = static_cast<uint32_t>(cfg.cta_group) * static_cast<uint32_t>(cfg.katoms) *
+                     (row_a * 128u + row_b * static_cast<uint32_t>(cfg.bn / cfg.cta_group));
+    }
     p.fault_inject = g_fault_once.exchange(0);
     const int64_t per_cluster = static_cast<int64_t>(cfg.cta_group) * cfg.ksplit;
     const int64_t clusters = sms / per_cluster;

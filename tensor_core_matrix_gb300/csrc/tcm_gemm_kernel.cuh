@@ -73,6 +73,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     constexpr int KB_ELEMS = KIND == 1 ? 128 : 64; // K elements per stage (128 bytes)
     constexpr int BN_CTA = BN / CG;                  // rows of B this CTA loads
     constexpr uint32_t STAGE_TX = CG * (L::A_STAGE + L::B_STAGE);
+    // packed FP4 operands land as 128 bytes per row but count 64 (the packed bytes)
+    const uint32_t stage_tx = p.stage_tx ? p.stage_tx : STAGE_TX;
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -162,12 +164,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const uint32_t sa = sbase + L::A_OFF + stage * L::A_STAGE;
                         const uint32_t sb = sbase + L::B_OFF + stage * L::B_STAGE;
                         if (CG == 2) {
-                            if (leader) mbar_arrive_expect_tx(full + stage, STAGE_TX);
+                            if (leader) mbar_arrive_expect_tx(full + stage, stage_tx);
                             const uint32_t fb = full_cluster0 + static_cast<uint32_t>(stage) * 8u;
                             tma_load_2d_pair(sa, &tmA, fb, kb * KB_ELEMS, a_row);
                             tma_load_2d_pair(sb, &tmB, fb, kb * KB_ELEMS, b_row);
                         } else {
-                            mbar_arrive_expect_tx(full + stage, STAGE_TX);
+                            mbar_arrive_expect_tx(full + stage, stage_tx);
 #pragma unroll
                             for (int a = 0; a < KATOMS; ++a)
                                 tma_load_2d(sa + a * A_STAGE_BYTES, &tmA, full + stage, (kb * KATOMS + a) * KB_ELEMS, a_row);

@@ -51,6 +51,7 @@ struct GemmParams {
     const float *d_scale;     // FP8 output: dequantisation factor of D (D = y / d_scale); null = 1
     float *amax;              // if set: max |y| over the launch, max-combined as fp32 bits
     int swap_ab;
+    uint32_t stage_tx;        // bytes a stage's TMA loads complete (all CTAs of a pair); 0 = from the tile sizes
     uint32_t idesc;
     unsigned long long timeout_ns;
     int *status;              // device status word pair {code, site}

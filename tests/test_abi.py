@@ -120,3 +120,16 @@ def test_gemm_fused_rejects_bad_arguments(lib, kw, status):
 
 def test_gemm_ex_still_rejects_fp8_output(lib):
     assert gemm_ex(lib, out_dtype=E5M2) == 2
+
+
+E2M1 = 5
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(a_dtype=E2M1, b_dtype=E4M3, K=64, lda=64, ldb=64), 2),                # K not a multiple of 128
+    (dict(a_dtype=E2M1, b_dtype=E4M3, K=128, lda=160, ldb=128), 3),             # 80-byte FP4 rows
+    (dict(a_dtype=E4M3, b_dtype=E2M1, K=128, lda=128, ldb=128, B=ALIGNED + 16), 3),  # FP4 base not 32-aligned
+    (dict(a_dtype=E2M1, b_dtype=BF16, K=128, lda=128, ldb=128), 2),
+])
+def test_gemm_ex_fp4_argument_rules(lib, kw, status):
+    assert gemm_ex(lib, **kw) == status
