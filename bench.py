@@ -335,6 +335,7 @@ def shape_cases():
         ("fp8 e4m3xe5m2 8192^3 +scales+bias", lambda: si.fp8_case(b_fmt="e5m2")),
         ("sparse 2:4 bf16 8192^3", lambda: si.sparse_case()),
         ("mxfp8 e4m3 8192^3 (E8M0 scales per 32)", lambda: si.mx_case()),
+        ("w4a8 fp8 e4m3 x fp4 e2m1 8192^3 +scales", lambda: si.w4a8_case()),
         ("fused fp8 e4m3 8192^3 +scales+bias -> GELU -> e4m3 out (d_scale 2) + amax",
          lambda: dict(si.fp8_case(b_fmt="e4m3"), fused="gelu")),
     ]
@@ -363,8 +364,11 @@ def run_shapes(args, tcm, device, peaks_used):
         C = case["C"].to(device) if case.get("C") is not None else None
         kw = dict(C=C, alpha=case.get("alpha", 1.0), beta=case.get("beta", 0.0))
         if "sa" in case:
-            kw.update(a_scale=torch.tensor([case["sa"]], device=device), b_scale=torch.tensor([case["sb"]], device=device),
-                      bias=case["bias"].to(device))
+            kw.update(a_scale=torch.tensor([case["sa"]], device=device), b_scale=torch.tensor([case["sb"]], device=device))
+            if case.get("bias") is not None:
+                kw.update(bias=case["bias"].to(device))
+        if case.get("b_fmt") == "e2m1":
+            kw.update(b_fmt="e2m1")  # B holds N x K/2 bytes of packed FP4
         if sparse:
             Ac, meta = tcm.tcm_sp_compress(A)
             launch = lambda: tcm.tcm_gemm_sp(Ac, meta, B, D, C=C, alpha=kw["alpha"], beta=kw["beta"])
@@ -400,7 +404,7 @@ def run_shapes(args, tcm, device, peaks_used):
         byts = in_bytes + D.numel() * D.element_size() + (C.numel() * C.element_size() if C is not None else 0)
         tf = flop / (ms * 1e-3) / 1e12
         gbs = byts / (ms * 1e-3) / 1e9
-        peak = bf16_peak * (FP8_OVER_BF16 if ("fp8" in name or "mx" in name) else 1.0)  # "fused" is FP8 too
+        peak = bf16_peak * (FP8_OVER_BF16 if ("fp8" in name or "mx" in name) else 1.0)  # fused, w4a8: FP8 rate
         line = {"kind": "shape", "workload": name, "M": M, "N": N, "K": K, "ms_median": ms, "ms_min": min(times),
                 "tflops": tf, "frac_of_tensor_peak": tf / peak, "algorithmic_bytes": byts, "gbs": gbs,
                 "frac_of_hbm": gbs / hbm_peak, "bound": "hbm" if M <= 64 else "tensor", "device_status": code,
