@@ -41,9 +41,9 @@ _lock = threading.Lock()
 _lib = None
 
 # The oracle's own format codes (mirrors the enum in oracle.c only).
-FMT = {"bf16": 0, "f16": 1, "f32": 2, "e4m3": 3, "e5m2": 4, "e8m0": 5, "e2m1": 6}
+FMT = {"bf16": 0, "f16": 1, "f32": 2, "e4m3": 3, "e5m2": 4, "e8m0": 5, "e2m1": 6, "ue4m3": 7}
 # bytes of one stored unit; an E2M1 byte holds two elements (element 2i in the low nibble)
-ELEM_BYTES = {"bf16": 2, "f16": 2, "f32": 4, "e4m3": 1, "e5m2": 1, "e8m0": 1, "e2m1": 1}
+ELEM_BYTES = {"bf16": 2, "f16": 2, "f32": 4, "e4m3": 1, "e5m2": 1, "e8m0": 1, "e2m1": 1, "ue4m3": 1}
 PER_UNIT = {"e2m1": 2}
 CODE_DTYPE = {1: np.uint8, 2: np.uint16, 4: np.uint32}
 # significand precision p (bits incl. the implicit one) and the smallest
@@ -91,7 +91,7 @@ def _load():
     lib.orc_gemm.argtypes = [i64, i64, i64, i32, vp, i64, i32, vp, i64, i32, vp, i64,
                              i32, vp, dbl, dbl, dbl, dbl, i64, vp, vp, vp, vp]
     lib.orc_gemm_mx.restype = i32
-    lib.orc_gemm_mx.argtypes = [i64, i64, i64, i64, i32, vp, i64, vp, i64, i32, vp, i64, vp, i64,
+    lib.orc_gemm_mx.argtypes = [i64, i64, i64, i64, i32, i32, vp, i64, vp, i64, i32, vp, i64, vp, i64,
                                 i32, vp, i64, i32, vp, dbl, dbl, i64, vp, vp, vp, vp]
     lib.orc_sp_compress.restype = i32
     lib.orc_activate.restype = i32
@@ -170,13 +170,14 @@ def gemm(A, B, a_fmt, b_fmt, *, C=None, c_fmt="f32", bias=None, bias_fmt="bf16",
     return ref, S
 
 
-def gemm_mx(A, SA, B, SB, a_fmt, b_fmt, *, block=32, C=None, c_fmt="f32", bias=None, bias_fmt="bf16",
-            alpha=1.0, beta=0.0, rows=None, cols=None):
-    """fp64 block-scaled reference (MX): sum_g 2^(SA[m,g]-127) 2^(SB[n,g]-127) sum_{k in g} a[m,k] b[n,k].
+def gemm_mx(A, SA, B, SB, a_fmt, b_fmt, *, block=32, sf_fmt="e8m0", C=None, c_fmt="f32", bias=None,
+            bias_fmt="bf16", alpha=1.0, beta=0.0, rows=None, cols=None):
+    """fp64 block-scaled reference: alpha * sum_g sa[m,g] sb[n,g] sum_{k in g} a[m,k] b[n,k] + beta C + bias.
 
-    ``A`` M x K and ``B`` N x K element codes, ``SA`` M x K/block and ``SB``
-    N x K/block E8M0 scale codes (uint8); other arguments as :func:`gemm`.
-    Returns ``(ref, S)``.
+    ``A`` M x K and ``B`` N x K element codes (packed for E2M1), ``SA`` M x K/block
+    and ``SB`` N x K/block scale codes (uint8) of ``sf_fmt``: "e8m0" (MX, block 32:
+    2^(code-127)) or "ue4m3" (NVFP4, block 16); other arguments as :func:`gemm`.
+    Returns ``(ref, S)`` with S = sum_g sa sb sum_k |a b|.
     """
     A = _codes(A, a_fmt)
     B = _codes(B, b_fmt)
@@ -184,6 +185,8 @@ def gemm_mx(A, SA, B, SB, a_fmt, b_fmt, *, block=32, C=None, c_fmt="f32", bias=N
     SB = np.ascontiguousarray(SB, dtype=np.uint8)
     M, lda = A.shape
     N, ldb = B.shape
+    lda *= PER_UNIT.get(a_fmt, 1)
+    ldb *= PER_UNIT.get(b_fmt, 1)
     K = lda
     if SA.shape != (M, K // block) or SB.shape != (N, K // block):
         raise ValueError("scale arrays must be M x K/block and N x K/block")
@@ -199,7 +202,7 @@ def gemm_mx(A, SA, B, SB, a_fmt, b_fmt, *, block=32, C=None, c_fmt="f32", bias=N
         nsamp = r.size
         ref = np.empty(r.shape, dtype=np.float64)
     S = np.empty_like(ref)
-    rc = _load().orc_gemm_mx(M, N, K, block, FMT[a_fmt], _ptr(A), lda, _ptr(SA), SA.shape[1],
+    rc = _load().orc_gemm_mx(M, N, K, block, FMT[sf_fmt], FMT[a_fmt], _ptr(A), lda, _ptr(SA), SA.shape[1],
                              FMT[b_fmt], _ptr(B), ldb, _ptr(SB), SB.shape[1], FMT[c_fmt], _ptr(Cc), ldc,
                              FMT[bias_fmt], _ptr(bc), float(alpha), float(beta), nsamp, _ptr(r), _ptr(c),
                              _ptr(ref), _ptr(S))

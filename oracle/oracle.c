@@ -41,7 +41,8 @@
 
 /* The oracle's own element-format codes (E8M0: the UE8M0 block-scale format;
  * E2M1: 4-bit, stored two per byte, element 2i in the low nibble). */
-enum { ORC_BF16 = 0, ORC_F16 = 1, ORC_F32 = 2, ORC_E4M3 = 3, ORC_E5M2 = 4, ORC_E8M0 = 5, ORC_E2M1 = 6 };
+enum { ORC_BF16 = 0, ORC_F16 = 1, ORC_F32 = 2, ORC_E4M3 = 3, ORC_E5M2 = 4, ORC_E8M0 = 5, ORC_E2M1 = 6,
+       ORC_UE4M3 = 7 };
 
 /* Width in bytes of one stored element of each format (0 = unknown). */
 int orc_elem_bytes(int fmt)
@@ -49,7 +50,7 @@ int orc_elem_bytes(int fmt)
     switch (fmt) {
     case ORC_BF16: case ORC_F16: return 2;
     case ORC_F32: return 4;
-    case ORC_E4M3: case ORC_E5M2: case ORC_E8M0: return 1;
+    case ORC_E4M3: case ORC_E5M2: case ORC_E8M0: case ORC_UE4M3: return 1;
     case ORC_E2M1: return 1; /* a byte holds two elements: see load_code */
     default: return 0;
     }
@@ -67,6 +68,8 @@ int orc_elem_bytes(int fmt)
  *   E8M0 (OCP MX scale): e(8), value 2^(e - 127); e = 255 is NaN.
  *   E2M1 (OCP FP4): s | e(2, bias 1) | m(1); no infinities or NaN
  *              (magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6).
+ *   UE4M3 (NVFP4 block scale): E4M3 without a sign bit: e(4, bias 7) | m(3),
+ *              0x7F NaN, largest 448; bit 7 unused (read as 0).
  * A zero exponent field means a subnormal: m * 2^(1 - bias - mbits).
  */
 double orc_decode(uint32_t code, int fmt)
@@ -76,6 +79,7 @@ double orc_decode(uint32_t code, int fmt)
     case ORC_BF16: ebits = 8; mbits = 7; bias = 127; break;
     case ORC_F16: ebits = 5; mbits = 10; bias = 15; break;
     case ORC_E4M3: ebits = 4; mbits = 3; bias = 7; break;
+    case ORC_UE4M3: ebits = 4; mbits = 3; bias = 7; code &= 0x7Fu; break;
     case ORC_E5M2: ebits = 5; mbits = 2; bias = 15; break;
     case ORC_E2M1: ebits = 2; mbits = 1; bias = 1; code &= 0xFu; break;
     case ORC_F32: {
@@ -94,7 +98,7 @@ double orc_decode(uint32_t code, int fmt)
     uint32_t e = (code >> mbits) & ((1u << ebits) - 1u);
     double sign = ((code >> sbit) & 1u) ? -1.0 : 1.0;
     uint32_t emax = (1u << ebits) - 1u;
-    if (fmt == ORC_E4M3) {
+    if (fmt == ORC_E4M3 || fmt == ORC_UE4M3) {
         if (e == emax && m == (1u << mbits) - 1u) return NAN;
     } else if (fmt == ORC_E2M1) {
         /* every code is a number */
@@ -302,7 +306,7 @@ int orc_sp_decompress(int64_t M, int64_t K, int fmt, const void *Ac,
  * are exact; the power-of-two scales are exact).  nsamp / rows / cols as in
  * orc_gemm.  Returns 0 or -1.
  */
-int orc_gemm_mx(int64_t M, int64_t N, int64_t K, int64_t blk,
+int orc_gemm_mx(int64_t M, int64_t N, int64_t K, int64_t blk, int sf_fmt,
                 int a_fmt, const void *A, int64_t lda, const uint8_t *sa, int64_t lds_a,
                 int b_fmt, const void *B, int64_t ldb, const uint8_t *sb, int64_t lds_b,
                 int c_fmt, const void *C, int64_t ldc, int bias_fmt, const void *bias,
@@ -311,6 +315,7 @@ int orc_gemm_mx(int64_t M, int64_t N, int64_t K, int64_t blk,
                 double *ref, double *S)
 {
     if (M < 0 || N < 0 || K < 0 || blk <= 0 || K % blk != 0) return -1;
+    if (sf_fmt != ORC_E8M0 && sf_fmt != ORC_UE4M3) return -1;
     if (!orc_elem_bytes(a_fmt) || !orc_elem_bytes(b_fmt)) return -1;
     if (C && !orc_elem_bytes(c_fmt)) return -1;
     if (bias && !orc_elem_bytes(bias_fmt)) return -1;
@@ -335,7 +340,7 @@ int orc_gemm_mx(int64_t M, int64_t N, int64_t K, int64_t blk,
                 part += p;
                 pabs += fabs(p);
             }
-            double scale = orc_decode(sa[m * lds_a + g], ORC_E8M0) * orc_decode(sb[n * lds_b + g], ORC_E8M0);
+            double scale = orc_decode(sa[m * lds_a + g], sf_fmt) * orc_decode(sb[n * lds_b + g], sf_fmt);
             acc += scale * part;
             sabs += scale * pabs;
         }

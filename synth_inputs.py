@@ -16,6 +16,9 @@ Workloads (shapes, value distributions, seeds):
 * ``sparse``      logical A ~ N(0,1) bf16 (pruned by the method), B ~ N(0,1), seed 4
 * ``mx``          MXFP8: N(0,1) in blocks of 32 along K with E8M0 scales (OCP MX
                   conversion), E4M3 elements, seed 5
+* ``nvfp4``       8192^3 NVFP4 x NVFP4: N(0,1), per-tensor fp32 scale, UE4M3 scales per
+                  16 along K, E2M1 elements (packed), seed 7; alpha = product of the
+                  two per-tensor scales
 * ``w4a8``        8192^3 A E4M3 activations x B E2M1 weights (FP4, two per byte),
                   N(0,1) each scaled per tensor so amax lands on the format max
                   (448, 6), seed 6
@@ -129,6 +132,32 @@ def mx_case(M=8192, N=8192, K=8192, a_fmt="e4m3", b_fmt="e4m3", seed=5):
     A, SA = mx_quantize(xa, a_fmt)
     B, SB = mx_quantize(xb, b_fmt)
     return dict(A=A, SA=SA, B=B, SB=SB, a_fmt=a_fmt, b_fmt=b_fmt, out_fmt="bf16")
+
+
+def nvfp4_quantize(x: torch.Tensor, block: int = 16):
+    """NVFP4 storage of fp32 ``x`` (rows x K): a per-tensor fp32 scale g = amax / (448 * 6),
+    per ``block`` K elements a UE4M3 scale s = RNE_e4m3(block_amax / 6 / g) (torch's cast of
+    a non-negative value; its code is the UE4M3 code), and E2M1 elements RNE(x / (s g)).
+    Real value ~= element * s * g.  Returns (packed E2M1, scale codes uint8 rows x K/block, g)."""
+    rows, K = x.shape
+    x = x.to(torch.float32)
+    amax = float(x.abs().max())
+    g = float(torch.tensor(amax / (448.0 * 6.0) if amax > 0 else 1.0, dtype=torch.float32))
+    xb = x.reshape(rows, K // block, block)
+    s = (xb.abs().amax(dim=2) / 6.0 / g).clamp(max=448.0).to(torch.float8_e4m3fn)
+    s_val = s.to(torch.float32)
+    denom = torch.where(s_val > 0, s_val * g, torch.ones_like(s_val))
+    q = fp4_e2m1((xb / denom[..., None]).reshape(rows, K))
+    return pack_fp4(q), s.view(torch.uint8), g
+
+
+def nvfp4_case(M=8192, N=8192, K=8192, seed=7):
+    g = generator(seed)
+    xa = torch.randn((M, K), generator=g, dtype=torch.float32)
+    xb = torch.randn((N, K), generator=g, dtype=torch.float32)
+    A, SA, ga = nvfp4_quantize(xa)
+    B, SB, gb = nvfp4_quantize(xb)
+    return dict(A=A, SA=SA, B=B, SB=SB, alpha=float(torch.tensor(ga * gb, dtype=torch.float32)), out_fmt="bf16")
 
 
 def w4a8_case(M=8192, N=8192, K=8192, a_fmt="e4m3", seed=6):

@@ -556,3 +556,36 @@ def test_fp4_input_rounding_ties_to_even_and_saturates():
     x = torch.tensor([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, -5.0, 7.0, -0.3, 0.26, 100.0])
     vals = oracle.decode(si.pack_fp4(si.fp4_e2m1(x)).numpy(), "e2m1")
     assert vals.tolist() == [0.0, 1.0, 1.0, 2.0, 2.0, 4.0, 4.0, -4.0, 6.0, -0.5, 0.5, 6.0]
+
+
+# ---- NVFP4: UE4M3 block scales per 16 over E2M1 elements
+
+def test_ue4m3_decode():
+    c = np.arange(128, dtype=np.uint8)
+    got = oracle.decode(c, "ue4m3")
+    theirs = torch.from_numpy(c.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert _same(got, theirs)
+    assert got[0x38] == 1.0 and got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9 and np.isnan(got[0x7F])
+
+
+def test_nvfp4_ones_closed_form():
+    """a = b = 1 (E2M1 code 2) everywhere, block scales 2^u, 2^v per 16: D = sum_g 16 * 2^(u + v)."""
+    M, N, K = 5, 6, 128
+    g = np.random.default_rng(9)
+    u = g.integers(-5, 6, (M, K // 16))
+    v = g.integers(-5, 6, (N, K // 16))
+    ones_a = np.full((M, K // 2), 0x22, dtype=np.uint8)
+    ones_b = np.full((N, K // 2), 0x22, dtype=np.uint8)
+    ref, S = oracle.gemm_mx(ones_a, ((u + 7) << 3).astype(np.uint8), ones_b, ((v + 7) << 3).astype(np.uint8),
+                            "e2m1", "e2m1", block=16, sf_fmt="ue4m3")
+    expect = (16.0 * 2.0 ** (u[:, None, :] + v[None, :, :])).sum(axis=2)
+    assert np.array_equal(ref, expect) and np.array_equal(S, expect)
+
+
+def test_nvfp4_matches_numpy_expansion():
+    c = si.nvfp4_case(40, 24, 192, seed=3)
+    ref, S = oracle.gemm_mx(c["A"].numpy(), c["SA"].numpy(), c["B"].numpy(), c["SB"].numpy(), "e2m1", "e2m1",
+                            block=16, sf_fmt="ue4m3", alpha=c["alpha"])
+    ea = oracle.decode(c["A"].numpy(), "e2m1") * np.repeat(oracle.decode(c["SA"].numpy(), "ue4m3"), 16, axis=1)
+    eb = oracle.decode(c["B"].numpy(), "e2m1") * np.repeat(oracle.decode(c["SB"].numpy(), "ue4m3"), 16, axis=1)
+    assert np.all(np.abs(ref - c["alpha"] * (ea @ eb.T)) <= 1e-12 * c["alpha"] * np.maximum(S, 1e-300))
