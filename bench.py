@@ -40,6 +40,7 @@ SIZE = 8192
 FLOP_PER_GEMM = 2.0 * SIZE ** 3
 METRIC = "GEMM TFLOP/s (2MNK/t) at 8192^3 bf16 and FP8; % of GB300 dense tensor peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense FP4 / bf16 tensor rates (GB300)
 FP8_OVER_BF16 = 4.5 / 2.25  # nominal dense ratio
 L2_BYTES = 129 * 10 ** 6
 KERNEL_SOURCES = ["tensor_core_matrix_gb300/csrc/tcm_gemm_kernel.cuh", "tensor_core_matrix_gb300/csrc/tcm_kernel_common.cuh",
@@ -335,6 +336,7 @@ def shape_cases():
         ("fp8 e4m3xe5m2 8192^3 +scales+bias", lambda: si.fp8_case(b_fmt="e5m2")),
         ("sparse 2:4 bf16 8192^3", lambda: si.sparse_case()),
         ("mxfp8 e4m3 8192^3 (E8M0 scales per 32)", lambda: si.mx_case()),
+        ("nvfp4 e2m1 8192^3 (UE4M3 scales per 16, per-tensor scales in alpha)", lambda: dict(si.nvfp4_case(), nv=True)),
         ("w4a8 fp8 e4m3 x fp4 e2m1 8192^3 +scales", lambda: si.w4a8_case()),
         ("fused fp8 e4m3 8192^3 +scales+bias -> GELU -> e4m3 out (d_scale 2) + amax",
          lambda: dict(si.fp8_case(b_fmt="e4m3"), fused="gelu")),
@@ -372,6 +374,11 @@ def run_shapes(args, tcm, device, peaks_used):
         if sparse:
             Ac, meta = tcm.tcm_sp_compress(A)
             launch = lambda: tcm.tcm_gemm_sp(Ac, meta, B, D, C=C, alpha=kw["alpha"], beta=kw["beta"])
+        elif case.get("nv"):
+            SA = tcm.tcm_nvfp4_pack_scales(case["SA"].to(device), 2 * K)
+            SB = tcm.tcm_nvfp4_pack_scales(case["SB"].to(device), 2 * K)
+            K = 2 * K  # A holds K/2 bytes per row
+            launch = lambda: tcm.tcm_gemm_nvfp4(A, SA, B, SB, D, alpha=case["alpha"])
         elif "SA" in case:
             # scales packed once into the blocked layout (as a quantiser would emit them)
             SA = tcm.tcm_mx_pack_scales(case["SA"].to(device), K)
@@ -404,7 +411,8 @@ def run_shapes(args, tcm, device, peaks_used):
         byts = in_bytes + D.numel() * D.element_size() + (C.numel() * C.element_size() if C is not None else 0)
         tf = flop / (ms * 1e-3) / 1e12
         gbs = byts / (ms * 1e-3) / 1e9
-        peak = bf16_peak * (FP8_OVER_BF16 if ("fp8" in name or "mx" in name) else 1.0)  # fused, w4a8: FP8 rate
+        peak = bf16_peak * (FP4_OVER_BF16 if "nvfp4" in name else
+                            FP8_OVER_BF16 if ("fp8" in name or "mx" in name) else 1.0)  # fused, w4a8: FP8 rate
         line = {"kind": "shape", "workload": name, "M": M, "N": N, "K": K, "ms_median": ms, "ms_min": min(times),
                 "tflops": tf, "frac_of_tensor_peak": tf / peak, "algorithmic_bytes": byts, "gbs": gbs,
                 "frac_of_hbm": gbs / hbm_peak, "bound": "hbm" if M <= 64 else "tensor", "device_status": code,

@@ -251,6 +251,49 @@ tcm_status tcm_mx_pack_scales(int64_t rows, int64_t K, const uint8_t *scales, ui
                               tcm_stream_t stream);
 
 /*
+ * tcm_gemm_nvfp4 -- block-scaled FP4 GEMM (NVFP4):
+ *   D = alpha * sum_g (A_g * sa_g) . (B_g * sb_g) + beta * C + bias
+ * with A (M x K) and B (N x K) in FP4 E2M1 and one UE4M3 scale per 16
+ * consecutive K elements of every row; alpha carries the product of the two
+ * per-tensor fp32 scales of the NVFP4 format.
+ *
+ * "NVIDIA MMA", section "SM100：tcgen05.mma" (kind::mxf4nvf4: MXFP4 or NVFP4,
+ * each K block's partial sum scaled before accumulation) and section
+ * "MXFP4 与 NVFP4" (NVFP4: E2M1 elements, UE4M3 scale per 16 elements);
+ * section "量化配置如何映射到 MMA": W4A4 NVFP4 x NVFP4 -> FP32.
+ *  A, B              packed E2M1, two per byte (element 2i in the low nibble),
+ *                    rows of K/2 bytes; K a multiple of 256 (else
+ *                    TCM_ERR_INVALID_ARG).
+ *  a_scales, b_scales  UE4M3 codes (E4M3 without sign; 0x7F is NaN) in the
+ *                    blocked layout of tcm_nvfp4_pack_scales
+ *                    (tcm_nvfp4_scales_bytes(rows, K) bytes).
+ *  C, D, bias, alpha, beta, out_dtype  as tcm_gemm_mx.
+ */
+tcm_status tcm_gemm_nvfp4(int64_t M, int64_t N, int64_t K,
+                          const void *A, const uint8_t *a_scales,
+                          const void *B, const uint8_t *b_scales,
+                          const void *C, void *D, float alpha, float beta, const void *bias,
+                          tcm_dtype out_dtype, tcm_stream_t stream);
+
+/*
+ * NVFP4 scales use the same 512-byte atoms as tcm_gemm_mx with 16-element
+ * blocks: the code of row r, block j (row-major index r * K/16 + j) is at
+ * atom (r / 128, j / 4) = byte offset (t * KT + k) * 512 with KT = ceil(K / 64),
+ * byte (r % 32) * 16 + ((r / 32) % 4) * 4 + j % 4 inside it; padding holds
+ * 0x38 (1.0).  One atom is the tensor-memory scale operand of one K = 64
+ * block-scaled MMA (scale_vec::4X; probed on the GPU).
+ *
+ * tcm_nvfp4_scales_bytes -- ceil(rows/128) * ceil(K/64) * 512; -1 if rows < 0,
+ * K < 0 or K % 16 != 0.  Host only.
+ * tcm_nvfp4_pack_scales -- blocked layout from row-major codes (rows x K/16,
+ * device, caller-owned) into `packed` (device, 16-byte aligned, caller-owned);
+ * bit-exact; asynchronous on `stream`.
+ */
+int64_t tcm_nvfp4_scales_bytes(int64_t rows, int64_t K);
+tcm_status tcm_nvfp4_pack_scales(int64_t rows, int64_t K, const uint8_t *scales, uint8_t *packed,
+                                 tcm_stream_t stream);
+
+/*
  * tcm_get_device_status -- synchronise `stream`, then report the first
  * device-side failure recorded since the last tcm_clear_device_status():
  * *code = TCM_OK or TCM_ERR_TIMEOUT, *site = which pipeline wait gave up

@@ -29,7 +29,8 @@ DTYPE_CODE = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2,
 ACT_CODE = {None: 0, "none": 0, "relu": 1, "gelu": 2}
 # Symbols the C ABI (include/tcm.h) exports.
 EXPORTS = ("tcm_gemm", "tcm_gemm_ex", "tcm_gemm_fused", "tcm_sp_compress", "tcm_sp_decompress", "tcm_gemm_sp", "tcm_gemm_mx",
-           "tcm_mx_scales_bytes", "tcm_mx_pack_scales",
+           "tcm_mx_scales_bytes", "tcm_mx_pack_scales", "tcm_gemm_nvfp4", "tcm_nvfp4_scales_bytes",
+           "tcm_nvfp4_pack_scales",
            "tcm_get_device_status", "tcm_clear_device_status", "tcm_set_timeout_ns",
            "tcm_status_string", "tcm_version", "tcm_set_config_override", "tcm_debug_fail_next_launch")
 
@@ -73,6 +74,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.tcm_mx_scales_bytes.argtypes = [i64, i64]
     lib.tcm_mx_pack_scales.restype = i32
     lib.tcm_mx_pack_scales.argtypes = [i64, i64, vp, vp, vp]
+    lib.tcm_gemm_nvfp4.restype = i32
+    lib.tcm_gemm_nvfp4.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp, vp, f32, f32, vp, i32, vp]
+    lib.tcm_nvfp4_scales_bytes.restype = i64
+    lib.tcm_nvfp4_scales_bytes.argtypes = [i64, i64]
+    lib.tcm_nvfp4_pack_scales.restype = i32
+    lib.tcm_nvfp4_pack_scales.argtypes = [i64, i64, vp, vp, vp]
     lib.tcm_get_device_status.restype = i32
     lib.tcm_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
     lib.tcm_clear_device_status.restype = i32
@@ -270,6 +277,42 @@ def tcm_gemm_mx(A, a_scales, B, b_scales, D, *, C=None, alpha=1.0, beta=0.0, bia
     st = lib.tcm_gemm_mx(M, N, K, _code(A, "A"), _ptr(A), _ptr(a_scales), _code(B, "B"), _ptr(B), _ptr(b_scales),
                          _ptr(C), _ptr(D), float(alpha), float(beta), _ptr(bias), _code(D, "D"), _stream(stream))
     _check(st, "tcm_gemm_mx")
+    return D
+
+
+def tcm_nvfp4_scales_bytes(rows: int, K: int) -> int:
+    """Bytes of the blocked NVFP4 scale array of `rows` rows of K elements (-1 if K % 16 != 0)."""
+    return int(load_library().tcm_nvfp4_scales_bytes(int(rows), int(K)))
+
+
+def tcm_nvfp4_pack_scales(scales, K: int, packed=None, stream=None):
+    """Blocked layout of row-major UE4M3 codes `scales` (rows x K/16 uint8, CUDA)."""
+    import torch
+    lib = load_library()
+    rows = scales.shape[0]
+    if tuple(scales.shape) != (rows, K // 16) or not scales.is_contiguous():
+        raise ValueError("scales must be a contiguous rows x K/16 tensor")
+    if packed is None:
+        packed = torch.empty(max(tcm_nvfp4_scales_bytes(rows, K), 0), dtype=torch.uint8, device=scales.device)
+    _check(lib.tcm_nvfp4_pack_scales(rows, K, _ptr(scales), _ptr(packed), _stream(stream)), "tcm_nvfp4_pack_scales")
+    return packed
+
+
+def tcm_gemm_nvfp4(A, a_scales, B, b_scales, D, *, C=None, alpha=1.0, beta=0.0, bias=None, stream=None):
+    """NVFP4 GEMM: A (M x K/2 bytes) and B (N x K/2 bytes) packed E2M1, a_scales / b_scales the
+    blocked UE4M3 arrays of tcm_nvfp4_pack_scales, D (M x N); alpha = product of the per-tensor scales."""
+    lib = load_library()
+    M, N, K = A.shape[0], B.shape[0], 2 * A.shape[1]
+    for t, n in ((A, "A"), (B, "B"), (a_scales, "a_scales"), (b_scales, "b_scales"), (D, "D")):
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    if A.dtype != torch.uint8 or B.dtype != torch.uint8 or 2 * B.shape[1] != K or tuple(D.shape) != (M, N):
+        raise ValueError("A, B must be packed uint8 rows of K/2 bytes; D M x N")
+    if a_scales.numel() < tcm_nvfp4_scales_bytes(M, K) or b_scales.numel() < tcm_nvfp4_scales_bytes(N, K):
+        raise ValueError("scales must be blocked arrays of tcm_nvfp4_scales_bytes(rows, K) bytes")
+    st = lib.tcm_gemm_nvfp4(M, N, K, _ptr(A), _ptr(a_scales), _ptr(B), _ptr(b_scales), _ptr(C), _ptr(D),
+                            float(alpha), float(beta), _ptr(bias), _code(D, "D"), _stream(stream))
+    _check(st, "tcm_gemm_nvfp4")
     return D
 
 

@@ -116,14 +116,17 @@ static bool encode_kmajor(CUtensorMap *map, const void *base, int elem_bytes, ui
 
 // Blocked E8M0 scales (see tcm_gemm_mx.cu) as a 2-D byte tensor of
 // ceil(rows / 128) * ceil(K / 128) * 32 rows of 16 bytes, boxes of one 512-byte atom.
-static bool encode_sf_atoms(CUtensorMap *map, const void *base, uint64_t rows, uint64_t K)
+// k_per_atom: K values covered by one atom (MX 128 = 4 blocks of 32, NVFP4 64 = 4 of 16);
+// box_atoms: atoms per TMA box (the atoms of one 128-row tile in one K stage).
+static bool encode_sf_atoms(CUtensorMap *map, const void *base, uint64_t rows, uint64_t K, uint64_t k_per_atom,
+                            uint32_t box_atoms)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
-    const uint64_t atoms = ((rows + 127) / 128) * ((K + 127) / 128);
+    const uint64_t atoms = ((rows + 127) / 128) * ((K + k_per_atom - 1) / k_per_atom);
     const cuuint64_t dims[2] = {16, atoms * 32};
     const cuuint64_t strides[1] = {16};
-    const cuuint32_t box[2] = {16, 32};
+    const cuuint32_t box[2] = {16, 32u * box_atoms};
     const cuuint32_t estr[2] = {1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
@@ -480,18 +483,26 @@ tcm_status tcm_gemm_sp(int64_t M, int64_t N, int64_t K, tcm_dtype dtype, const v
     return e == cudaSuccess ? TCM_OK : TCM_ERR_CUDA;
 }
 
-tcm_status tcm_gemm_mx(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const void *A, const uint8_t *a_scales,
-                       tcm_dtype b_dtype, const void *B, const uint8_t *b_scales, const void *C, void *D,
-                       float alpha, float beta, const void *bias, tcm_dtype out_dtype, tcm_stream_t stream)
+// Block-scaled GEMM (nv = false: MXFP8, E8M0 per 32, kind::mxf8f6f4; nv = true: NVFP4,
+// packed E2M1 with UE4M3 per 16, kind::mxf4nvf4.scale_vec::4X).
+static tcm_status block_scaled_impl(bool nv, int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const void *A,
+                                    const uint8_t *a_scales, tcm_dtype b_dtype, const void *B, const uint8_t *b_scales,
+                                    const void *C, void *D, float alpha, float beta, const void *bias,
+                                    tcm_dtype out_dtype, tcm_stream_t stream)
 {
-    const bool a8 = a_dtype == TCM_E4M3 || a_dtype == TCM_E5M2;
-    const bool b8 = b_dtype == TCM_E4M3 || b_dtype == TCM_E5M2;
-    if (!a8 || !b8) return TCM_ERR_UNSUPPORTED;
+    if (!nv) {
+        const bool a8 = a_dtype == TCM_E4M3 || a_dtype == TCM_E5M2;
+        const bool b8 = b_dtype == TCM_E4M3 || b_dtype == TCM_E5M2;
+        if (!a8 || !b8) return TCM_ERR_UNSUPPORTED;
+    }
     if (out_dtype != TCM_BF16 && out_dtype != TCM_F16 && out_dtype != TCM_F32) return TCM_ERR_UNSUPPORTED;
-    if (M < 1 || N < 1 || K < 0 || K % 32 != 0) return TCM_ERR_INVALID_ARG;
+    const int64_t k_stage = nv ? 256 : 128;     // K values per 128-byte stage
+    const int64_t k_atom = nv ? 64 : 128;       // K values per scale atom
+    if (M < 1 || N < 1 || K < 0 || K % (nv ? 256 : 32) != 0) return TCM_ERR_INVALID_ARG;
     if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2) return TCM_ERR_UNSUPPORTED;
     // scale-atom rows (32 per atom) are addressed with 32-bit coordinates
-    if (((M + 255) / 128) * ((K + 127) / 128) * 32 > INT32_MAX || ((N + 255) / 128) * ((K + 127) / 128) * 32 > INT32_MAX)
+    if (((M + 255) / 128) * ((K + k_atom - 1) / k_atom) * 32 > INT32_MAX ||
+        ((N + 255) / 128) * ((K + k_atom - 1) / k_atom) * 32 > INT32_MAX)
         return TCM_ERR_UNSUPPORTED;
     if (!D || (K > 0 && (!A || !B || !a_scales || !b_scales)) || (beta != 0.f && !C)) return TCM_ERR_INVALID_ARG;
     const int eo = elem_bytes(out_dtype);
@@ -503,7 +514,7 @@ tcm_status tcm_gemm_mx(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const
     if (sms <= 0) return TCM_ERR_CUDA;
 
     GemmConfig cfg{};
-    cfg.kind = 3;
+    cfg.kind = nv ? 4 : 3;
     cfg.cta_group = 1;
     cfg.ksplit = 1;
     cfg.katoms = 1;
@@ -518,17 +529,20 @@ tcm_status tcm_gemm_mx(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const
     std::memset(&maps, 0, sizeof maps);
     if (K > 0) {
         const uint64_t uK = static_cast<uint64_t>(K);
-        if (!encode_kmajor(&maps.a, A, 1, uK, static_cast<uint64_t>(M), uK, 128) ||
-            !encode_kmajor(&maps.b, B, 1, uK, static_cast<uint64_t>(N), uK, static_cast<uint32_t>(cfg.bn / cfg.cta_group)) ||
-            !encode_sf_atoms(&maps.sa, a_scales, static_cast<uint64_t>(M), uK) ||
-            !encode_sf_atoms(&maps.sb, b_scales, static_cast<uint64_t>(N), uK))
+        const uint64_t row_bytes = nv ? uK / 2 : uK; // packed E2M1: two values per byte
+        const uint32_t box_atoms = static_cast<uint32_t>(k_stage / k_atom);
+        if (!encode_kmajor(&maps.a, A, 1, row_bytes, static_cast<uint64_t>(M), row_bytes, 128) ||
+            !encode_kmajor(&maps.b, B, 1, row_bytes, static_cast<uint64_t>(N), row_bytes,
+                           static_cast<uint32_t>(cfg.bn / cfg.cta_group)) ||
+            !encode_sf_atoms(&maps.sa, a_scales, static_cast<uint64_t>(M), uK, static_cast<uint64_t>(k_atom), box_atoms) ||
+            !encode_sf_atoms(&maps.sb, b_scales, static_cast<uint64_t>(N), uK, static_cast<uint64_t>(k_atom), box_atoms))
             return TCM_ERR_CUDA;
     }
     GemmParams p{};
     p.kM = static_cast<int>(M);
     p.kN = static_cast<int>(N);
     p.K = static_cast<int>(K);
-    p.num_kb = static_cast<int>((K + 127) / 128);
+    p.num_kb = static_cast<int>((K + k_stage - 1) / k_stage);
     p.tiles_m = static_cast<int>((M + 128 * cfg.cta_group - 1) / (128 * cfg.cta_group));
     p.tiles_n = static_cast<int>((N + cfg.bn - 1) / cfg.bn);
     p.num_tiles = p.tiles_m * p.tiles_n;
@@ -546,12 +560,14 @@ tcm_status tcm_gemm_mx(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const
     p.out_fmt = static_cast<int>(out_dtype);
     p.bias_fmt = p.out_fmt;
     p.swap_ab = 0;
-    // block-scaled instruction descriptor: [7,10) A format, [10,13) B format (E4M3 = 0,
-    // E5M2 = 1), [17,23) N >> 3, [23] scale type (1 = UE8M0), [24,29) M >> 4; the
-    // per-MMA scale-factor ids ([4,6) B, [29,31) A) are added by the kernel
-    p.idesc = ((a_dtype == TCM_E5M2 ? 1u : 0u) << 7) | ((b_dtype == TCM_E5M2 ? 1u : 0u) << 10) |
-              ((static_cast<uint32_t>(cfg.bn) >> 3) << 17) | (1u << 23) |
-              (((128u * static_cast<uint32_t>(cfg.cta_group)) >> 4) << 24);
+    // block-scaled instruction descriptor: [7,10) A format, [10,13) B format, [17,23) N >> 3,
+    // [23] scale type, [24,29) M >> 4.  kind::mxf8f6f4: E4M3 = 0, E5M2 = 1, scale UE8M0 (1);
+    // the per-MMA scale-factor ids ([4,6) B, [29,31) A) are added by the kernel.
+    // kind::mxf4nvf4: E2M1 = 1, scale UE4M3 (0), ids 0 (probed on the GPU).
+    const uint32_t dims = ((static_cast<uint32_t>(cfg.bn) >> 3) << 17) |
+                          (((128u * static_cast<uint32_t>(cfg.cta_group)) >> 4) << 24);
+    p.idesc = nv ? ((1u << 7) | (1u << 10) | dims)
+                 : (((a_dtype == TCM_E5M2 ? 1u : 0u) << 7) | ((b_dtype == TCM_E5M2 ? 1u : 0u) << 10) | (1u << 23) | dims);
     p.timeout_ns = timeout_ns();
     p.status = device_status_ptr();
     if (!p.status) return TCM_ERR_CUDA;
@@ -560,6 +576,22 @@ tcm_status tcm_gemm_mx(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const
     const int grid = static_cast<int>((p.num_tiles < clusters ? p.num_tiles : clusters) * cfg.cta_group);
     const cudaError_t e = launch_gemm_mx(cfg, maps, p, grid, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TCM_OK : TCM_ERR_CUDA;
+}
+
+tcm_status tcm_gemm_mx(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const void *A, const uint8_t *a_scales,
+                       tcm_dtype b_dtype, const void *B, const uint8_t *b_scales, const void *C, void *D,
+                       float alpha, float beta, const void *bias, tcm_dtype out_dtype, tcm_stream_t stream)
+{
+    return block_scaled_impl(false, M, N, K, a_dtype, A, a_scales, b_dtype, B, b_scales, C, D, alpha, beta, bias,
+                             out_dtype, stream);
+}
+
+tcm_status tcm_gemm_nvfp4(int64_t M, int64_t N, int64_t K, const void *A, const uint8_t *a_scales, const void *B,
+                          const uint8_t *b_scales, const void *C, void *D, float alpha, float beta, const void *bias,
+                          tcm_dtype out_dtype, tcm_stream_t stream)
+{
+    return block_scaled_impl(true, M, N, K, TCM_E2M1, A, a_scales, TCM_E2M1, B, b_scales, C, D, alpha, beta, bias,
+                             out_dtype, stream);
 }
 
 int64_t tcm_mx_scales_bytes(int64_t rows, int64_t K)
@@ -575,7 +607,28 @@ tcm_status tcm_mx_pack_scales(int64_t rows, int64_t K, const uint8_t *scales, ui
     if (rows == 0 || K == 0) return TCM_OK;
     if (!scales || !packed) return TCM_ERR_INVALID_ARG;
     if (!aligned16(packed)) return TCM_ERR_MISALIGNED;
-    return launch_mx_pack_scales(scales, rows, K, packed, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+    return launch_mx_pack_scales(scales, rows, K / 32, 127u, packed, reinterpret_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? TCM_OK
+               : TCM_ERR_CUDA;
+}
+
+int64_t tcm_nvfp4_scales_bytes(int64_t rows, int64_t K)
+{
+    if (rows < 0 || K < 0 || K % 16 != 0) return -1;
+    return ((rows + 127) / 128) * ((K + 63) / 64) * 512;
+}
+
+tcm_status tcm_nvfp4_pack_scales(int64_t rows, int64_t K, const uint8_t *scales, uint8_t *packed, tcm_stream_t stream)
+{
+    if (rows < 0 || K < 0 || K % 16 != 0) return TCM_ERR_INVALID_ARG;
+    if (rows > INT32_MAX / 2 || K > INT32_MAX / 2) return TCM_ERR_UNSUPPORTED;
+    if (rows == 0 || K == 0) return TCM_OK;
+    if (!scales || !packed) return TCM_ERR_INVALID_ARG;
+    if (!aligned16(packed)) return TCM_ERR_MISALIGNED;
+    // padding code 0x38 = UE4M3 1.0
+    return launch_mx_pack_scales(scales, rows, K / 16, 0x38u, packed, reinterpret_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
                ? TCM_OK
                : TCM_ERR_CUDA;
 }

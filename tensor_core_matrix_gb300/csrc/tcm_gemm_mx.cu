@@ -51,12 +51,11 @@ namespace tcm {
 constexpr int MX_EPI_WARPS = 8;                    // two per TMEM lane quadrant, half the columns each
 constexpr int MX_THREADS = 32 * (2 + MX_EPI_WARPS); // TMA, MMA, epilogue
 constexpr int SF_ATOM = 512;                       // scales of 128 rows x one 128-value K stage
-constexpr uint32_t SF_STAGE_COLS = 16;             // per stage: A at +0..3, B at +8..8+BN/32-1
 
-template <int BN_CTA, int BN, int STAGES>
+template <int BN_CTA, int BN, int STAGES, int APT>
 struct MxSmem {
     static constexpr int B_STAGE = BN_CTA * TILE_K_BYTES;
-    static constexpr int SF_STAGE = SF_ATOM * (1 + BN / 128); // A atom, then BN/128 B atoms
+    static constexpr int SF_STAGE = SF_ATOM * APT * (1 + BN / 128); // A atoms, then APT per B row tile
     static constexpr int A_OFF = 0;
     static constexpr int B_OFF = STAGES * A_STAGE_BYTES;
     static constexpr int SF_OFF = B_OFF + STAGES * B_STAGE;
@@ -123,10 +122,54 @@ __device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t
             : "memory");
 }
 
+template <int CG>
+__device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
+{
+    if constexpr (CG == 2)
+        asm volatile(
+            "{\n"
+            ".reg .pred p;\n"
+            "setp.ne.b32 p, %6, 0;\n"
+            "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n"
+            "}\n" ::"r"(d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+            : "memory");
+    else
+        asm volatile(
+            "{\n"
+            ".reg .pred p;\n"
+            "setp.ne.b32 p, %6, 0;\n"
+            "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n"
+            "}\n" ::"r"(d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+            : "memory");
+}
+
+// Scale formats of the block-scaled kernel.  MX: MXFP8 (kind::mxf8f6f4, K = 32 per
+// MMA, one E8M0 atom per 128 rows per stage shared by the stage's four MMAs
+// through scale-factor ids 0..3).  NV: NVFP4 (kind::mxf4nvf4.scale_vec::4X, packed
+// E2M1, K = 64 per MMA, one UE4M3 atom per 128 rows per MMA, scale-factor id 0).
+template <bool NV, int SFB_ATOMS>
+struct SfLayout {
+    static constexpr int APT = NV ? 4 : 1;             // atoms per 128-row tile per stage
+    static constexpr int NCP = APT * (1 + SFB_ATOMS);  // copies per stage
+    static constexpr uint32_t COLS = NV ? 16u + 16u * SFB_ATOMS : 16u; // TMEM columns per stage
+    // TMEM column (within the stage) of copy e: e = tile * APT + kk, tile 0 = A, 1.. = B row tiles
+    __device__ static constexpr uint32_t col(int e)
+    {
+        return NV ? (e < APT ? 4u * e : 16u + 4u * SFB_ATOMS * static_cast<uint32_t>((e - APT) % APT) +
+                                              4u * static_cast<uint32_t>((e - APT) / APT))
+                  : (e == 0 ? 0u : 4u + 4u * e);
+    }
+    __device__ static constexpr uint32_t sfa(int k) { return NV ? 4u * k : 0u; }
+    __device__ static constexpr uint32_t sfb(int k) { return NV ? 16u + 4u * SFB_ATOMS * k : 8u; }
+};
+
 // BN: N extent of the (pair) tile; CG: 1 = one CTA per 128 x BN tile, 2 = a CTA
 // pair per 256 x BN tile (each CTA loads 128 rows of A and BN/2 rows of B, its
 // own A scale atom and all BN/128 B scale atoms).
-template <int BN, int STAGES, int NACC, int CG>
+template <int BN, int STAGES, int NACC, int CG, bool NV>
 __global__ void __launch_bounds__(MX_THREADS, 1)
     gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
@@ -134,11 +177,14 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
 {
     constexpr int BN_CTA = BN / CG;
     constexpr int SFB_ATOMS = BN / 128;
-    using L = MxSmem<BN_CTA, BN, STAGES>;
+    using SF = SfLayout<NV, SFB_ATOMS>;
+    constexpr int APT = SF::APT;
+    using L = MxSmem<BN_CTA, BN, STAGES, APT>;
     static_assert(L::ALLOC <= 227 * 1024, "shared memory ring too large");
     static_assert(BN == 128 || BN == 256, "tile width");
     constexpr uint32_t ACC_STRIDE = BN;            // BN is a power of two here
-    constexpr uint32_t SF_COL = ACC_STRIDE * NACC; // then SF_STAGE_COLS scale columns per stage
+    constexpr uint32_t SF_COL = ACC_STRIDE * NACC; // then SF::COLS scale columns per stage
+    constexpr uint32_t SF_STAGE_COLS = SF::COLS;
     static_assert(SF_COL + SF_STAGE_COLS * STAGES <= 512, "tensor memory budget");
     constexpr uint32_t TMEM_COLS = 512;
     constexpr uint32_t STAGE_TX = CG * (A_STAGE_BYTES + L::B_STAGE + L::SF_STAGE);
@@ -202,7 +248,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
     if (warp == 0) {
         if (lane == 0) {
             const uint32_t full_cluster0 = CG == 2 ? mapa_shared(smem_u32(full), 0) : 0u;
-            const int kt = p.num_kb; // scale atoms per row tile
+            const int kt = p.num_kb * APT; // scale atoms per 128-row tile along K
             int stage = 0;
             uint32_t phase = 0;
             long long issued = 0;
@@ -221,7 +267,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
                     const uint32_t sa = sbase + L::A_OFF + stage * A_STAGE_BYTES;
                     const uint32_t sb = sbase + L::B_OFF + stage * L::B_STAGE;
                     const uint32_t ss = sbase + L::SF_OFF + stage * L::SF_STAGE;
-                    const int ya = (a_tile * kt + kb) * 32;
+                    const int ya = (a_tile * kt + kb * APT) * 32;
                     if (CG == 2) {
                         if (leader) mbar_arrive_expect_tx(full + stage, STAGE_TX);
                         const uint32_t fb = full_cluster0 + static_cast<uint32_t>(stage) * 8u;
@@ -230,7 +276,8 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
                         tma_load_2d_pair(ss, &tmSA, fb, 0, ya);
 #pragma unroll
                         for (int i = 0; i < SFB_ATOMS; ++i)
-                            tma_load_2d_pair(ss + SF_ATOM * (1 + i), &tmSB, fb, 0, ((nb * SFB_ATOMS + i) * kt + kb) * 32);
+                            tma_load_2d_pair(ss + SF_ATOM * APT * (1 + i), &tmSB, fb, 0,
+                                             ((nb * SFB_ATOMS + i) * kt + kb * APT) * 32);
                     } else {
                         mbar_arrive_expect_tx(full + stage, STAGE_TX);
                         tma_load_2d(sa, &tmA, full + stage, kb * 128, a_row);
@@ -238,7 +285,8 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
                         tma_load_2d(ss, &tmSA, full + stage, 0, ya);
 #pragma unroll
                         for (int i = 0; i < SFB_ATOMS; ++i)
-                            tma_load_2d(ss + SF_ATOM * (1 + i), &tmSB, full + stage, 0, ((nb * SFB_ATOMS + i) * kt + kb) * 32);
+                            tma_load_2d(ss + SF_ATOM * APT * (1 + i), &tmSB, full + stage, 0,
+                                        ((nb * SFB_ATOMS + i) * kt + kb * APT) * 32);
                     }
                     ++issued;
                     if (++stage == STAGES) {
@@ -274,8 +322,8 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
                     tc_fence_after();
                     const uint32_t sf0 = tmem_base + SF_COL;
 #pragma unroll
-                    for (int a = 0; a <= SFB_ATOMS; ++a)
-                        tmem_cp_sf<CG>(sf0 + (a == 0 ? 0u : 4u + 4u * a), sdesc_sf_atom(sbase + L::SF_OFF + SF_ATOM * a));
+                    for (int e = 0; e < SF::NCP; ++e)
+                        tmem_cp_sf<CG>(sf0 + SF::col(e), sdesc_sf_atom(sbase + L::SF_OFF + SF_ATOM * e));
                 }
             }
             long long item = 0;
@@ -299,8 +347,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
                         const uint32_t ss = sbase + L::SF_OFF + stage * L::SF_STAGE;
                         const uint32_t s0 = tmem_base + SF_COL + static_cast<uint32_t>(stage) * SF_STAGE_COLS;
 #pragma unroll
-                        for (int a = 0; a <= SFB_ATOMS; ++a)
-                            tmem_cp_sf<CG>(s0 + (a == 0 ? 0u : 4u + 4u * a), sdesc_sf_atom(ss + SF_ATOM * a));
+                        for (int e = 0; e < SF::NCP; ++e) tmem_cp_sf<CG>(s0 + SF::col(e), sdesc_sf_atom(ss + SF_ATOM * e));
                     }
                     // next stage already landed: interleave its copies with this stage's MMAs
                     const bool has_next = item + 1 < items && mbar_try_wait(smem_u32(full + next_stage), next_phase);
@@ -313,12 +360,20 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
                     const uint32_t nsf = tmem_base + SF_COL + static_cast<uint32_t>(next_stage) * SF_STAGE_COLS;
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        // scale-factor ids: byte k of the stage's scale words (A bits [29,31), B bits [4,6))
-                        const uint32_t idesc = p.idesc | (static_cast<uint32_t>(k) << 29) | (static_cast<uint32_t>(k) << 4);
-                        mma_mx<CG>(d_tmem, ad + 2 * k, bd + 2 * k, idesc, sf, sf + 8, (kb > 0 || k > 0) ? 1u : 0u);
-                        // after MMA k: atom k of the next stage (0 = A, 1.. = B), at most one per MMA
-                        if (has_next && k <= SFB_ATOMS)
-                            tmem_cp_sf<CG>(nsf + (k == 0 ? 0u : 4u + 4u * k), sdesc_sf_atom(nss + SF_ATOM * k));
+                        const uint32_t accum = (kb > 0 || k > 0) ? 1u : 0u;
+                        if constexpr (NV) {
+                            mma_nvf4<CG>(d_tmem, ad + 2 * k, bd + 2 * k, p.idesc, sf + SF::sfa(k), sf + SF::sfb(k), accum);
+                        } else {
+                            // scale-factor ids: byte k of the stage's scale words (A bits [29,31), B bits [4,6))
+                            const uint32_t idesc = p.idesc | (static_cast<uint32_t>(k) << 29) | (static_cast<uint32_t>(k) << 4);
+                            mma_mx<CG>(d_tmem, ad + 2 * k, bd + 2 * k, idesc, sf + SF::sfa(k), sf + SF::sfb(k), accum);
+                        }
+                        // after MMA k: the next stage's copies [k*NCP/4, (k+1)*NCP/4), rounded up
+                        if (has_next) {
+#pragma unroll
+                            for (int e = (k * SF::NCP + 3) / 4; e < ((k + 1) * SF::NCP + 3) / 4; ++e)
+                                tmem_cp_sf<CG>(nsf + SF::col(e), sdesc_sf_atom(nss + SF_ATOM * e));
+                        }
                     }
                     if (CG == 2) mma_commit_pair(empty + stage, 0x3);
                     else mma_commit(empty + stage);
@@ -428,11 +483,11 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
     }
 }
 
-template <int BN, int STAGES, int NACC, int CG>
+template <int BN, int STAGES, int NACC, int CG, bool NV>
 static cudaError_t launch_mx_one(const MxMaps &m, const GemmParams &p, int grid, cudaStream_t stream)
 {
-    using L = MxSmem<BN / CG, BN, STAGES>;
-    auto kern = gemm_mx_kernel<BN, STAGES, NACC, CG>;
+    using L = MxSmem<BN / CG, BN, STAGES, NV ? 4 : 1>;
+    auto kern = gemm_mx_kernel<BN, STAGES, NACC, CG, NV>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -453,20 +508,27 @@ static cudaError_t launch_mx_one(const MxMaps &m, const GemmParams &p, int grid,
 cudaError_t launch_gemm_mx(const GemmConfig &cfg, const MxMaps &maps, const GemmParams &p, int grid,
                            cudaStream_t stream)
 {
-    if (cfg.cta_group == 2) return cfg.bn == 256 ? launch_mx_one<256, 6, 1, 2>(maps, p, grid, stream)
+    if (cfg.kind == 4) { // NVFP4
+        if (cfg.cta_group == 2) return cfg.bn == 256 ? launch_mx_one<256, 5, 1, 2, true>(maps, p, grid, stream)
+                                                     : cudaErrorInvalidValue;
+        if (cfg.bn == 256) return launch_mx_one<256, 4, 1, 1, true>(maps, p, grid, stream);
+        if (cfg.bn == 128) return launch_mx_one<128, 6, 2, 1, true>(maps, p, grid, stream);
+        return cudaErrorInvalidValue;
+    }
+    if (cfg.cta_group == 2) return cfg.bn == 256 ? launch_mx_one<256, 6, 1, 2, false>(maps, p, grid, stream)
                                                  : cudaErrorInvalidValue;
-    if (cfg.bn == 256) return launch_mx_one<256, 4, 1, 1>(maps, p, grid, stream);
-    if (cfg.bn == 128) return launch_mx_one<128, 6, 2, 1>(maps, p, grid, stream);
+    if (cfg.bn == 256) return launch_mx_one<256, 4, 1, 1, false>(maps, p, grid, stream);
+    if (cfg.bn == 128) return launch_mx_one<128, 6, 2, 1, false>(maps, p, grid, stream);
     return cudaErrorInvalidValue;
 }
 
 // ---------------------------------------------------------------- scale packing
 
 // One thread per 16-byte row of an atom: row l of atom (t, k) holds, for the
-// four rows r = 128 t + 32 q + l (q = 0..3), the four codes of 32-blocks
-// 4k .. 4k+3.  Rows past `rows` and blocks past `nblk` read code 127 (= 1.0).
+// four rows r = 128 t + 32 q + l (q = 0..3), the four codes of blocks 4k .. 4k+3.
+// Rows past `rows` and blocks past `nblk` read `pad` (the format's 1.0).
 __global__ void __launch_bounds__(256) mx_pack_scales_kernel(const uint8_t *__restrict__ src, int64_t rows,
-                                                             int64_t nblk, int64_t kt, int64_t total,
+                                                             int64_t nblk, int64_t kt, int64_t total, uint32_t pad,
                                                              uint4 *__restrict__ dst)
 {
     const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -483,7 +545,7 @@ __global__ void __launch_bounds__(256) mx_pack_scales_kernel(const uint8_t *__re
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int64_t b = 4 * k + j;
-            const uint32_t code = (r < rows && b < nblk) ? static_cast<uint32_t>(__ldg(src + r * nblk + b)) : 127u;
+            const uint32_t code = (r < rows && b < nblk) ? static_cast<uint32_t>(__ldg(src + r * nblk + b)) : pad;
             v |= code << (8 * j);
         }
         wv[q] = v;
@@ -491,14 +553,14 @@ __global__ void __launch_bounds__(256) mx_pack_scales_kernel(const uint8_t *__re
     dst[i] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
 }
 
-cudaError_t launch_mx_pack_scales(const uint8_t *src, int64_t rows, int64_t K, uint8_t *dst, cudaStream_t stream)
+cudaError_t launch_mx_pack_scales(const uint8_t *src, int64_t rows, int64_t nblk, uint32_t pad, uint8_t *dst,
+                                  cudaStream_t stream)
 {
-    const int64_t nblk = K / 32;
-    const int64_t kt = (K + 127) / 128;
+    const int64_t kt = (nblk + 3) / 4;
     const int64_t total = ((rows + 127) / 128) * kt * 32;
     if (total == 0) return cudaSuccess;
     const int64_t blocks = (total + 255) / 256;
-    mx_pack_scales_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(src, rows, nblk, kt, total,
+    mx_pack_scales_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(src, rows, nblk, kt, total, pad,
                                                                              reinterpret_cast<uint4 *>(dst));
     return cudaGetLastError();
 }

@@ -92,7 +92,9 @@ struct MxMaps {
 
 cudaError_t launch_gemm_mx(const GemmConfig &cfg, const MxMaps &maps, const GemmParams &p, int grid,
                            cudaStream_t stream);
-cudaError_t launch_mx_pack_scales(const uint8_t *src, int64_t rows, int64_t K, uint8_t *dst, cudaStream_t stream);
+// rows x nblk row-major scale codes -> blocked atoms (pad = the format's code of 1.0)
+cudaError_t launch_mx_pack_scales(const uint8_t *src, int64_t rows, int64_t nblk, uint32_t pad, uint8_t *dst,
+                                  cudaStream_t stream);
 
 cudaError_t launch_gemm_sp(const GemmConfig &cfg, const CUtensorMap &tmA, const CUtensorMap &tmB,
                            const GemmParams &p, int grid, cudaStream_t stream);

@@ -133,3 +133,16 @@ E2M1 = 5
 ])
 def test_gemm_ex_fp4_argument_rules(lib, kw, status):
     assert gemm_ex(lib, **kw) == status
+
+
+@pytest.mark.parametrize("K,out,D,status", [(128, BF16, ALIGNED, 1), (256, E4M3, ALIGNED, 2),
+                                            (256, BF16, ALIGNED + 8, 3), (-256, BF16, ALIGNED, 1)])
+def test_gemm_nvfp4_rejects_bad_arguments(lib, K, out, D, status):
+    assert lib.tcm_gemm_nvfp4(64, 64, K, ALIGNED, ALIGNED, ALIGNED, ALIGNED, None, D, 1.0, 0.0, None, out,
+                              None) == status
+
+
+def test_nvfp4_scales_bytes(lib):
+    assert lib.tcm_nvfp4_scales_bytes(130, 256) == 2 * 4 * 512
+    assert lib.tcm_nvfp4_scales_bytes(1, 64) == 512
+    assert lib.tcm_nvfp4_scales_bytes(1, 24) == -1
