@@ -108,6 +108,19 @@ def recorded_traffic():
         return None
 
 
+def smi_gpu_id(dev_index):
+    """nvidia-smi's name for CUDA device `dev_index`: its UUID (nvidia-smi numbers the
+    machine's GPUs itself and ignores CUDA_VISIBLE_DEVICES, so an index may name another GPU)."""
+    try:
+        u = str(torch.cuda.get_device_properties(dev_index).uuid)
+        if u:
+            return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        pass
+    vis = [v for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
+    return vis[dev_index].strip() if dev_index < len(vis) else str(dev_index)
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle samples taken while the timed region runs."""
 
@@ -123,9 +136,10 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.out = open(self.path, "w")
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+            self.err = open(self.path + ".err", "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", smi_gpu_id(self.index), f"--query-gpu={self.QUERY}",
                                           "--format=csv,noheader,nounits", "-lms", "100"],
-                                         stdout=self.out, stderr=subprocess.DEVNULL)
+                                         stdout=self.out, stderr=self.err)
         except (OSError, FileNotFoundError):
             self.proc = None
             return self
@@ -145,6 +159,7 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
             self.out.close()
+            self.err.close()
 
     def summary(self):
         if self.proc is None:
@@ -159,8 +174,14 @@ class ClockSampler:
             except ValueError:
                 continue
         os.unlink(self.path)
+        err = ""
+        if os.path.exists(self.path + ".err"):
+            err = open(self.path + ".err").read().strip().splitlines()[:1]
+            err = err[0][:200] if err else ""
+            os.unlink(self.path + ".err")
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples" + (f": {err}" if err else "")],
+                    "samples": 0}
         loaded = [r for r in rows if r[2] > 300.0] or rows
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[3]) if v.lower() == "active"})
