@@ -6,8 +6,9 @@ input at M = N = K = 8192:
   * E4M3 x E4M3 with per-tensor fp32 dequantisation scales and a bf16 bias
     -> bf16 D
   * 2:4 structured-sparse bf16 A: compress of the logical A (keep the two
-    largest of every four along K, ordered metadata) plus the sparse GEMM,
-    counted at its logical 2*M*N*K
+    largest of every four along K, ordered metadata), a copy of the metadata
+    into the sparse MMA's tensor-memory order, and the sparse GEMM, counted
+    at its logical 2*M*N*K
 value = sum of 2*M*N*K over the step's three GEMMs / step time (TFLOP/s).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tcm|reference]
@@ -240,6 +241,7 @@ def make_inputs(device):
         dev[k] = torch.empty((SIZE, SIZE), dtype=torch.bfloat16, device=device)
     dev["Ac"] = torch.empty((SIZE, SIZE // 2), dtype=torch.bfloat16, device=device)
     dev["meta"] = torch.empty((SIZE, SIZE // 32), dtype=torch.int32, device=device)
+    dev["meta_tc"] = torch.empty(META_TC_BYTES, dtype=torch.uint8, device=device)
     return host, pinned, dev
 
 
@@ -255,14 +257,18 @@ def run_step(tcm, dev, stream, events=None):
                     stream=stream)
     mark(2)
     tcm.tcm_sp_compress(dev["Asp"], dev["Ac"], dev["meta"], stream=stream)
+    tcm.tcm_sp_meta_pack(dev["meta"], SIZE, dev["meta_tc"], stream=stream)
     mark(3)
-    tcm.tcm_gemm_sp(dev["Ac"], dev["meta"], dev["Bsp"], dev["Dsp"], stream=stream)
+    tcm.tcm_gemm_sp_tc(dev["Ac"], dev["meta_tc"], dev["Bsp"], dev["Dsp"], stream=stream)
     mark(4)
 
 
-KERNELS_PER_STEP = 4
+KERNELS_PER_STEP = 5
+# hardware-ordered metadata: ceil(M/128) * ceil(K/128) * 8192 bytes
+META_TC_BYTES = (SIZE // 128) * (SIZE // 128) * 8192
 GEMMS_PER_STEP = 3
-COMPRESS_BYTES = SIZE * SIZE * 2 + SIZE * (SIZE // 2) * 2 + SIZE * (SIZE // 32) * 4
+# compress (read A, write A_comp + canonical metadata) and metadata pack (read it, write meta_tc)
+COMPRESS_BYTES = SIZE * SIZE * 2 + SIZE * (SIZE // 2) * 2 + 2 * SIZE * (SIZE // 32) * 4 + META_TC_BYTES
 
 
 class OracleSample:
@@ -394,7 +400,8 @@ def run_shapes(args, tcm, device, peaks_used):
             kw.update(b_fmt="e2m1")  # B holds N x K/2 bytes of packed FP4
         if sparse:
             Ac, meta = tcm.tcm_sp_compress(A)
-            launch = lambda: tcm.tcm_gemm_sp(Ac, meta, B, D, C=C, alpha=kw["alpha"], beta=kw["beta"])
+            meta_tc = tcm.tcm_sp_meta_pack(meta, K)
+            launch = lambda: tcm.tcm_gemm_sp_tc(Ac, meta_tc, B, D, C=C, alpha=kw["alpha"], beta=kw["beta"])
         elif case.get("nv"):
             SA = tcm.tcm_nvfp4_pack_scales(case["SA"].to(device), 2 * K)
             SB = tcm.tcm_nvfp4_pack_scales(case["SB"].to(device), 2 * K)
@@ -446,7 +453,7 @@ def run_shapes(args, tcm, device, peaks_used):
 
 def config_block(world):
     return {"workload": "GEMM 8192^3 (M=N=K=8192): bf16 x bf16 -> bf16; E4M3 x E4M3 with per-tensor "
-                        "scales + bf16 bias -> bf16; 2:4-sparse bf16 A (compress + sparse GEMM) -> bf16; "
+                        "scales + bf16 bias -> bf16; 2:4-sparse bf16 A (compress + metadata pack + sparse GEMM) -> bf16; "
                         "A row-major, B K-major, fp32 accumulate",
             "M": SIZE, "N": SIZE, "K": SIZE,
             "inputs": "bf16 A ~ N(0,1), B ~ N(0,0.02) (seed 2); E4M3 A, B ~ N(0,1) scaled so amax = 448 (seed 3); "
@@ -591,8 +598,8 @@ def main():
             "parts": {
                 "bf16_dense": {"tflops": ach_bf16, "ms": t_bf16, "frac_of_bf16_peak": ach_bf16 / bf16_peak},
                 "e4m3_scaled_bias": {"tflops": ach_fp8, "ms": t_fp8, "frac_of_fp8_peak": ach_fp8 / fp8_peak},
-                "sp24_compress": {"gbs": cmp_gbs, "ms": t_cmp, "frac_of_hbm": cmp_gbs / hbm_peak,
-                                  "bytes": COMPRESS_BYTES},
+                "sp24_compress_and_meta_pack": {"gbs": cmp_gbs, "ms": t_cmp, "frac_of_hbm": cmp_gbs / hbm_peak,
+                                                "bytes": COMPRESS_BYTES},
                 "sp24_gemm_bf16": {"tflops_logical": ach_sp, "ms": t_sp,
                                    "frac_of_dense_bf16_peak": ach_sp / bf16_peak},
             },

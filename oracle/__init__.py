@@ -228,6 +228,34 @@ def mx_pack_scales(SC, K, block=32, pad=127):
             out[atom * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + j % 4] = SC[r, j]
     return out
 
+def sp_meta_pack(meta, K):
+    """Hardware-ordered 2:4 metadata (the layout of ``tcm_sp_meta_pack`` in include/tcm.h) of
+    canonical words ``meta`` (M x K/32 uint32), as bytes.  Plain loops over the definition:
+    block (t, kb, k), lane L = 16a + 8s + r gets bits 16s..16s+15 of row 128t+16a+r's word
+    q = 4kb+k in its low half and those of row 128t+16a+8+r in its high half."""
+    meta = np.ascontiguousarray(meta).view(np.uint32)
+    M, qn = meta.shape
+    assert K % 32 == 0 and qn == K // 32
+    kbs = (K + 127) // 128
+    tiles = (M + 127) // 128
+    out = np.zeros(tiles * kbs * 4 * 128 * 4, dtype=np.uint32)  # 16-byte rows as 4 words
+    fill = 0x44444444
+
+    def word(row, q):
+        return int(meta[row, q]) if row < M and q < qn else fill
+
+    for t in range(tiles):
+        for kb in range(kbs):
+            for k in range(4):
+                q = 4 * kb + k
+                for L in range(128):
+                    a, s, r = L // 16, (L // 8) % 2, L % 8
+                    lo = (word(128 * t + 16 * a + r, q) >> (16 * s)) & 0xFFFF
+                    hi = (word(128 * t + 16 * a + 8 + r, q) >> (16 * s)) & 0xFFFF
+                    out[(((t * kbs + kb) * 4 + k) * 128 + L) * 4] = lo | (hi << 16)
+    return out.view(np.uint8)
+
+
 def sp_compress(A, fmt):
     """2:4 prune+compress of logical A (M x K codes) -> (Ac M x K/2, meta M x K/32 uint32)."""
     A = _codes(A, fmt)

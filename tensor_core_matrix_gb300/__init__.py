@@ -28,7 +28,8 @@ DTYPE_CODE = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2,
 # tcm_activation codes of the fused epilogue
 ACT_CODE = {None: 0, "none": 0, "relu": 1, "gelu": 2}
 # Symbols the C ABI (include/tcm.h) exports.
-EXPORTS = ("tcm_gemm", "tcm_gemm_ex", "tcm_gemm_fused", "tcm_sp_compress", "tcm_sp_decompress", "tcm_gemm_sp", "tcm_gemm_mx",
+EXPORTS = ("tcm_gemm", "tcm_gemm_ex", "tcm_gemm_fused", "tcm_sp_compress", "tcm_sp_meta_tc_bytes",
+           "tcm_sp_meta_pack", "tcm_gemm_sp_tc", "tcm_sp_decompress", "tcm_gemm_sp", "tcm_gemm_mx",
            "tcm_mx_scales_bytes", "tcm_mx_pack_scales", "tcm_gemm_nvfp4", "tcm_nvfp4_scales_bytes",
            "tcm_nvfp4_pack_scales",
            "tcm_get_device_status", "tcm_clear_device_status", "tcm_set_timeout_ns",
@@ -74,6 +75,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.tcm_mx_scales_bytes.argtypes = [i64, i64]
     lib.tcm_mx_pack_scales.restype = i32
     lib.tcm_mx_pack_scales.argtypes = [i64, i64, vp, vp, vp]
+    lib.tcm_sp_meta_tc_bytes.restype = i64
+    lib.tcm_sp_meta_tc_bytes.argtypes = [i64, i64]
+    lib.tcm_sp_meta_pack.restype = i32
+    lib.tcm_sp_meta_pack.argtypes = [i64, i64, vp, vp, vp]
+    lib.tcm_gemm_sp_tc.restype = i32
+    lib.tcm_gemm_sp_tc.argtypes = [i64, i64, i64, i32, vp, vp, vp, vp, vp, f32, f32, i32, vp]
     lib.tcm_gemm_nvfp4.restype = i32
     lib.tcm_gemm_nvfp4.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp, vp, f32, f32, vp, i32, vp]
     lib.tcm_nvfp4_scales_bytes.restype = i64
@@ -277,6 +284,39 @@ def tcm_gemm_mx(A, a_scales, B, b_scales, D, *, C=None, alpha=1.0, beta=0.0, bia
     st = lib.tcm_gemm_mx(M, N, K, _code(A, "A"), _ptr(A), _ptr(a_scales), _code(B, "B"), _ptr(B), _ptr(b_scales),
                          _ptr(C), _ptr(D), float(alpha), float(beta), _ptr(bias), _code(D, "D"), _stream(stream))
     _check(st, "tcm_gemm_mx")
+    return D
+
+
+def tcm_sp_meta_tc_bytes(M: int, K: int) -> int:
+    """Bytes of the hardware-ordered 2:4 metadata of an M x K (logical) matrix."""
+    return int(load_library().tcm_sp_meta_tc_bytes(int(M), int(K)))
+
+
+def tcm_sp_meta_pack(meta, K: int, meta_tc=None, stream=None):
+    """Hardware-ordered copy of canonical metadata `meta` (M x K/32 int32/uint32, CUDA)."""
+    lib = load_library()
+    M = meta.shape[0]
+    if tuple(meta.shape) != (M, K // 32) or not meta.is_contiguous():
+        raise ValueError("meta must be a contiguous M x K/32 tensor")
+    if meta_tc is None:
+        meta_tc = torch.empty(max(tcm_sp_meta_tc_bytes(M, K), 0), dtype=torch.uint8, device=meta.device)
+    _check(lib.tcm_sp_meta_pack(M, K, _ptr(meta), _ptr(meta_tc), _stream(stream)), "tcm_sp_meta_pack")
+    return meta_tc
+
+
+def tcm_gemm_sp_tc(A_comp, meta_tc, B, D, *, C=None, alpha=1.0, beta=0.0, stream=None):
+    """tcm_gemm_sp with hardware-ordered metadata (tcm_sp_meta_pack); A_comp M x K/2, B N x K."""
+    lib = load_library()
+    M, K = A_comp.shape[0], B.shape[1]
+    N = B.shape[0]
+    for t, n in ((A_comp, "A_comp"), (meta_tc, "meta_tc"), (B, "B"), (D, "D")):
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    if A_comp.shape[1] * 2 != K or tuple(D.shape) != (M, N) or meta_tc.numel() < tcm_sp_meta_tc_bytes(M, K):
+        raise ValueError("shape mismatch")
+    st = lib.tcm_gemm_sp_tc(M, N, K, _code(A_comp, "A_comp"), _ptr(A_comp), _ptr(meta_tc), _ptr(B), _ptr(C), _ptr(D),
+                            float(alpha), float(beta), _code(D, "D"), _stream(stream))
+    _check(st, "tcm_gemm_sp_tc")
     return D
 
 

@@ -406,6 +406,109 @@ tcm_status tcm_sp_decompress(int64_t M, int64_t K, tcm_dtype dtype, const void *
                : TCM_ERR_CUDA;
 }
 
+int64_t tcm_sp_meta_tc_bytes(int64_t M, int64_t K)
+{
+    if (M < 0 || K < 0 || K % 32 != 0) return -1;
+    return ((M + 127) / 128) * ((K + 127) / 128) * 4 * 2048;
+}
+
+tcm_status tcm_sp_meta_pack(int64_t M, int64_t K, const uint32_t *meta, void *meta_tc, tcm_stream_t stream)
+{
+    if (M < 0 || K < 0 || K % 32 != 0) return TCM_ERR_INVALID_ARG;
+    if (M > INT32_MAX / 2 || K > INT32_MAX / 2) return TCM_ERR_UNSUPPORTED;
+    if (M == 0 || K == 0) return TCM_OK;
+    if (!meta || !meta_tc) return TCM_ERR_INVALID_ARG;
+    if (!aligned16(meta_tc) || (reinterpret_cast<uintptr_t>(meta) & 3u)) return TCM_ERR_MISALIGNED;
+    return launch_sp_meta_pack(meta, M, K, static_cast<uint8_t *>(meta_tc), reinterpret_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? TCM_OK
+               : TCM_ERR_CUDA;
+}
+
+tcm_status tcm_gemm_sp_tc(int64_t M, int64_t N, int64_t K, tcm_dtype dtype, const void *A_comp, const void *meta_tc,
+                          const void *B, const void *C, void *D, float alpha, float beta, tcm_dtype out_dtype,
+                          tcm_stream_t stream)
+{
+    if (dtype != TCM_BF16 && dtype != TCM_F16) return TCM_ERR_UNSUPPORTED;
+    if (out_dtype != TCM_BF16 && out_dtype != TCM_F16 && out_dtype != TCM_F32) return TCM_ERR_UNSUPPORTED;
+    if (M < 1 || N < 1 || K < 0 || K % 32 != 0) return TCM_ERR_INVALID_ARG;
+    if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2) return TCM_ERR_UNSUPPORTED;
+    // metadata rows (128 per 2 KB block) are addressed with 32-bit coordinates
+    if (((M + 255) / 128) * ((K + 127) / 128) * 4 * 128 > INT32_MAX) return TCM_ERR_UNSUPPORTED;
+    if (!D || (K > 0 && (!A_comp || !meta_tc || !B)) || (beta != 0.f && !C)) return TCM_ERR_INVALID_ARG;
+    const int eo = elem_bytes(out_dtype);
+    if ((A_comp && !aligned16(A_comp)) || (B && !aligned16(B)) || (meta_tc && !aligned16(meta_tc)) || !aligned16(D) ||
+        (C && !aligned16(C)))
+        return TCM_ERR_MISALIGNED;
+    if ((N * eo) % 16) return TCM_ERR_MISALIGNED;
+    const int64_t sms = sm_count();
+    if (sms <= 0) return TCM_ERR_CUDA;
+
+    GemmConfig cfg{};
+    cfg.kind = 5;
+    cfg.ksplit = 1;
+    cfg.katoms = 1;
+    const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
+    cfg.cta_group = (M > 128 && N > 128 && pair_tiles >= sms / 2) ? 2 : 1;
+    const int force_cg = g_force_cta_group.load();
+    if (force_cg == 1 || force_cg == 2) cfg.cta_group = force_cg;
+    cfg.bn = cfg.cta_group == 2 ? 256 : 128;
+    if (cfg.cta_group == 2 && g_force_bn.load() == 128) cfg.bn = 128;
+
+    MxMaps maps;
+    std::memset(&maps, 0, sizeof maps);
+    if (K > 0) {
+        const uint64_t meta_rows = static_cast<uint64_t>((M + 127) / 128) * static_cast<uint64_t>((K + 127) / 128) * 512u;
+        EncodeTiledFn fn = encode_fn();
+        const cuuint64_t dims[2] = {16, meta_rows};
+        const cuuint64_t strides[1] = {16};
+        const cuuint32_t box[2] = {16, 256}; // two MMA blocks
+        const cuuint32_t estr[2] = {1, 1};
+        if (!fn || !encode_kmajor(&maps.a, A_comp, 2, static_cast<uint64_t>(K / 2), static_cast<uint64_t>(M),
+                                  static_cast<uint64_t>(K / 2), 128) ||
+            !encode_kmajor(&maps.b, B, 2, static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(K),
+                           static_cast<uint32_t>(cfg.bn / cfg.cta_group)) ||
+            fn(&maps.sa, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(meta_tc), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return TCM_ERR_CUDA;
+        maps.sb = maps.sa;
+    }
+    GemmParams p{};
+    p.kM = static_cast<int>(M);
+    p.kN = static_cast<int>(N);
+    p.K = static_cast<int>(K);
+    p.num_kb = static_cast<int>((K + 127) / 128);
+    p.tiles_m = static_cast<int>((M + 128 * cfg.cta_group - 1) / (128 * cfg.cta_group));
+    p.tiles_n = static_cast<int>((N + cfg.bn - 1) / cfg.bn);
+    p.num_tiles = p.tiles_m * p.tiles_n;
+    p.group_m = g_force_group_m.load() > 0 ? g_force_group_m.load() : 16;
+    p.tile_begin = 0;
+    p.tile_end = p.num_tiles;
+    p.D = D;
+    p.ldd = N;
+    p.C = beta != 0.f ? C : nullptr;
+    p.ldc = N;
+    p.bias = nullptr;
+    p.a_scale = p.b_scale = nullptr;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.out_fmt = static_cast<int>(out_dtype);
+    p.bias_fmt = p.out_fmt;
+    p.swap_ab = 0;
+    const uint32_t code = dtype == TCM_BF16 ? 1u : 0u;
+    p.idesc = make_idesc(code, code, 128u * static_cast<uint32_t>(cfg.cta_group), static_cast<uint32_t>(cfg.bn)) |
+              (1u << 2); // sparsity enabled
+    p.timeout_ns = timeout_ns();
+    p.status = device_status_ptr();
+    if (!p.status) return TCM_ERR_CUDA;
+    p.fault_inject = 0;
+    const int64_t clusters = sms / cfg.cta_group;
+    const int grid = static_cast<int>((p.num_tiles < clusters ? p.num_tiles : clusters) * cfg.cta_group);
+    const cudaError_t e = launch_gemm_mx(cfg, maps, p, grid, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TCM_OK : TCM_ERR_CUDA;
+}
+
 tcm_status tcm_gemm_sp(int64_t M, int64_t N, int64_t K, tcm_dtype dtype, const void *A_comp, const uint32_t *meta,
                        const void *B, const void *C, void *D, float alpha, float beta, tcm_dtype out_dtype,
                        tcm_stream_t stream)

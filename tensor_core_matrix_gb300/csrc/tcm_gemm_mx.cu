@@ -52,10 +52,17 @@ constexpr int MX_EPI_WARPS = 8;                    // two per TMEM lane quadrant
 constexpr int MX_THREADS = 32 * (2 + MX_EPI_WARPS); // TMA, MMA, epilogue
 constexpr int SF_ATOM = 512;                       // scales of 128 rows x one 128-value K stage
 
-template <int BN_CTA, int BN, int STAGES, int APT>
+// Formats of the kernel: MX (MXFP8), NV (NVFP4), SP (2:4-sparse bf16/fp16 A,
+// metadata in the hardware order -- the "side" data of a stage is then the
+// sparse metadata instead of block scales).
+enum SideFmt : int { FMT_MX = 0, FMT_NV = 1, FMT_SP = 2 };
+constexpr int SP_META_STAGE = 4 * 2048; // four 128-lane x 16-byte blocks, one per MMA
+
+template <int BN_CTA, int BN, int STAGES, int FMT>
 struct MxSmem {
-    static constexpr int B_STAGE = BN_CTA * TILE_K_BYTES;
-    static constexpr int SF_STAGE = SF_ATOM * APT * (1 + BN / 128); // A atoms, then APT per B row tile
+    static constexpr int B_STAGE = BN_CTA * TILE_K_BYTES * (FMT == FMT_SP ? 2 : 1); // SP: 128 logical K = 2 atoms
+    static constexpr int SF_STAGE = FMT == FMT_SP ? SP_META_STAGE
+                                                  : SF_ATOM * (FMT == FMT_NV ? 4 : 1) * (1 + BN / 128);
     static constexpr int A_OFF = 0;
     static constexpr int B_OFF = STAGES * A_STAGE_BYTES;
     static constexpr int SF_OFF = B_OFF + STAGES * B_STAGE;
@@ -150,26 +157,90 @@ __device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64
 // MMA, one E8M0 atom per 128 rows per stage shared by the stage's four MMAs
 // through scale-factor ids 0..3).  NV: NVFP4 (kind::mxf4nvf4.scale_vec::4X, packed
 // E2M1, K = 64 per MMA, one UE4M3 atom per 128 rows per MMA, scale-factor id 0).
-template <bool NV, int SFB_ATOMS>
+// SP: two tcgen05.cp.128x256b per stage, each moving the blocks of two MMAs
+// (lane l <- 16 bytes of block k at l*16 and 16 of block k+1, LBO 2048) to 8
+// columns, so MMA k finds its word at column 4k, a multiple of 4 as the
+// sparse MMA's metadata address requires.
+template <int FMT, int SFB_ATOMS>
 struct SfLayout {
+    static constexpr bool NV = FMT == FMT_NV;
     static constexpr int APT = NV ? 4 : 1;             // atoms per 128-row tile per stage
-    static constexpr int NCP = APT * (1 + SFB_ATOMS);  // copies per stage
-    static constexpr uint32_t COLS = NV ? 16u + 16u * SFB_ATOMS : 16u; // TMEM columns per stage
+    static constexpr int NCP = FMT == FMT_SP ? 2 : APT * (1 + SFB_ATOMS);  // copies per stage
+    static constexpr uint32_t COLS = NV ? 16u + 16u * SFB_ATOMS : 16u;      // TMEM columns per stage
     // TMEM column (within the stage) of copy e: e = tile * APT + kk, tile 0 = A, 1.. = B row tiles
     __device__ static constexpr uint32_t col(int e)
     {
-        return NV ? (e < APT ? 4u * e : 16u + 4u * SFB_ATOMS * static_cast<uint32_t>((e - APT) % APT) +
-                                              4u * static_cast<uint32_t>((e - APT) / APT))
-                  : (e == 0 ? 0u : 4u + 4u * e);
+        return FMT == FMT_SP ? 8u * e
+               : NV ? (e < APT ? 4u * e : 16u + 4u * SFB_ATOMS * static_cast<uint32_t>((e - APT) % APT) +
+                                             4u * static_cast<uint32_t>((e - APT) / APT))
+                    : (e == 0 ? 0u : 4u + 4u * e);
     }
+    // byte offset of copy e's source within the stage's side data
+    __device__ static constexpr uint32_t src(int e) { return FMT == FMT_SP ? 4096u * e : static_cast<uint32_t>(SF_ATOM) * e; }
     __device__ static constexpr uint32_t sfa(int k) { return NV ? 4u * k : 0u; }
     __device__ static constexpr uint32_t sfb(int k) { return NV ? 16u + 4u * SFB_ATOMS * k : 8u; }
 };
 
+// Shared-memory descriptor of two 128-row x 16-byte blocks 2048 bytes apart, no
+// swizzle: the source of one tcgen05.cp.128x256b (lane l <- row l of both).
+__device__ __forceinline__ uint64_t sdesc_meta_pair(uint32_t smem_addr)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(2048 >> 4) << 16;
+    d |= static_cast<uint64_t>(128 >> 4) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    return d;
+}
+
+template <int FMT, int CG>
+__device__ __forceinline__ void tmem_cp_side(uint32_t taddr, uint32_t smem_addr)
+{
+    if constexpr (FMT == FMT_SP) {
+        const uint64_t d = sdesc_meta_pair(smem_addr);
+        if constexpr (CG == 2) asm volatile("tcgen05.cp.cta_group::2.128x256b [%0], %1;" ::"r"(taddr), "l"(d) : "memory");
+        else asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(d) : "memory");
+    } else {
+        tmem_cp_sf<CG>(taddr, sdesc_sf_atom(smem_addr));
+    }
+}
+
+template <int CG>
+__device__ __forceinline__ void mma_sp16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t meta_tmem,
+                                         uint32_t idesc, uint32_t accumulate)
+{
+    if constexpr (CG == 2)
+        asm volatile(
+            "{\n"
+            ".reg .pred p;\n"
+            "setp.ne.b32 p, %5, 0;\n"
+            "tcgen05.mma.sp.cta_group::2.kind::f16 [%0], %1, %2, [%3], %4, p;\n"
+            "}\n" ::"r"(d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(meta_tmem), "r"(idesc), "r"(accumulate)
+            : "memory");
+    else
+        asm volatile(
+            "{\n"
+            ".reg .pred p;\n"
+            "setp.ne.b32 p, %5, 0;\n"
+            "tcgen05.mma.sp.cta_group::1.kind::f16 [%0], %1, %2, [%3], %4, p;\n"
+            "}\n" ::"r"(d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(meta_tmem), "r"(idesc), "r"(accumulate)
+            : "memory");
+}
+
+// One TMA tile load onto this stage's barrier (pair: the even CTA's barrier, cluster address fb).
+template <int CG>
+__device__ __forceinline__ void tma_ld(uint32_t dst, const CUtensorMap *map, uint64_t *bar, uint32_t fb, int x, int y)
+{
+    if constexpr (CG == 2) tma_load_2d_pair(dst, map, fb, x, y);
+    else tma_load_2d(dst, map, bar, x, y);
+}
+
 // BN: N extent of the (pair) tile; CG: 1 = one CTA per 128 x BN tile, 2 = a CTA
 // pair per 256 x BN tile (each CTA loads 128 rows of A and BN/2 rows of B, its
 // own A scale atom and all BN/128 B scale atoms).
-template <int BN, int STAGES, int NACC, int CG, bool NV>
+template <int BN, int STAGES, int NACC, int CG, int FMT>
 __global__ void __launch_bounds__(MX_THREADS, 1)
     gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
@@ -177,9 +248,9 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
 {
     constexpr int BN_CTA = BN / CG;
     constexpr int SFB_ATOMS = BN / 128;
-    using SF = SfLayout<NV, SFB_ATOMS>;
+    using SF = SfLayout<FMT, SFB_ATOMS>;
     constexpr int APT = SF::APT;
-    using L = MxSmem<BN_CTA, BN, STAGES, APT>;
+    using L = MxSmem<BN_CTA, BN, STAGES, FMT>;
     static_assert(L::ALLOC <= 227 * 1024, "shared memory ring too large");
     static_assert(BN == 128 || BN == 256, "tile width");
     constexpr uint32_t ACC_STRIDE = BN;            // BN is a power of two here
@@ -267,26 +338,26 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
                     const uint32_t sa = sbase + L::A_OFF + stage * A_STAGE_BYTES;
                     const uint32_t sb = sbase + L::B_OFF + stage * L::B_STAGE;
                     const uint32_t ss = sbase + L::SF_OFF + stage * L::SF_STAGE;
-                    const int ya = (a_tile * kt + kb * APT) * 32;
-                    if (CG == 2) {
-                        if (leader) mbar_arrive_expect_tx(full + stage, STAGE_TX);
-                        const uint32_t fb = full_cluster0 + static_cast<uint32_t>(stage) * 8u;
-                        tma_load_2d_pair(sa, &tmA, fb, kb * 128, a_row);
-                        tma_load_2d_pair(sb, &tmB, fb, kb * 128, b_row);
-                        tma_load_2d_pair(ss, &tmSA, fb, 0, ya);
-#pragma unroll
-                        for (int i = 0; i < SFB_ATOMS; ++i)
-                            tma_load_2d_pair(ss + SF_ATOM * APT * (1 + i), &tmSB, fb, 0,
-                                             ((nb * SFB_ATOMS + i) * kt + kb * APT) * 32);
+                    if (leader || CG == 1) mbar_arrive_expect_tx(full + stage, STAGE_TX);
+                    const uint32_t fb = CG == 2 ? full_cluster0 + static_cast<uint32_t>(stage) * 8u : 0u;
+                    if constexpr (FMT == FMT_SP) {
+                        // compressed A: 64 kept values (128 bytes) of the stage's 128 logical K;
+                        // B: two 64-value atoms; metadata: the tile's four 2 KB blocks of this stage
+                        const int ym = (a_tile * p.num_kb + kb) * 4 * 128;
+                        tma_ld<CG>(sa, &tmA, full + stage, fb, kb * 64, a_row);
+                        tma_ld<CG>(sb, &tmB, full + stage, fb, kb * 128, b_row);
+                        tma_ld<CG>(sb + BN_CTA * TILE_K_BYTES, &tmB, full + stage, fb, kb * 128 + 64, b_row);
+                        tma_ld<CG>(ss, &tmSA, full + stage, fb, 0, ym);
+                        tma_ld<CG>(ss + 4096, &tmSA, full + stage, fb, 0, ym + 256);
                     } else {
-                        mbar_arrive_expect_tx(full + stage, STAGE_TX);
-                        tma_load_2d(sa, &tmA, full + stage, kb * 128, a_row);
-                        tma_load_2d(sb, &tmB, full + stage, kb * 128, b_row);
-                        tma_load_2d(ss, &tmSA, full + stage, 0, ya);
+                        const int ya = (a_tile * kt + kb * APT) * 32;
+                        tma_ld<CG>(sa, &tmA, full + stage, fb, kb * 128, a_row);
+                        tma_ld<CG>(sb, &tmB, full + stage, fb, kb * 128, b_row);
+                        tma_ld<CG>(ss, &tmSA, full + stage, fb, 0, ya);
 #pragma unroll
                         for (int i = 0; i < SFB_ATOMS; ++i)
-                            tma_load_2d(ss + SF_ATOM * APT * (1 + i), &tmSB, full + stage, 0,
-                                        ((nb * SFB_ATOMS + i) * kt + kb * APT) * 32);
+                            tma_ld<CG>(ss + SF_ATOM * APT * (1 + i), &tmSB, full + stage, fb, 0,
+                                       ((nb * SFB_ATOMS + i) * kt + kb * APT) * 32);
                     }
                     ++issued;
                     if (++stage == STAGES) {
@@ -323,7 +394,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
                     const uint32_t sf0 = tmem_base + SF_COL;
 #pragma unroll
                     for (int e = 0; e < SF::NCP; ++e)
-                        tmem_cp_sf<CG>(sf0 + SF::col(e), sdesc_sf_atom(sbase + L::SF_OFF + SF_ATOM * e));
+                        tmem_cp_side<FMT, CG>(sf0 + SF::col(e), sbase + L::SF_OFF + SF::src(e));
                 }
             }
             long long item = 0;
@@ -347,7 +418,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
                         const uint32_t ss = sbase + L::SF_OFF + stage * L::SF_STAGE;
                         const uint32_t s0 = tmem_base + SF_COL + static_cast<uint32_t>(stage) * SF_STAGE_COLS;
 #pragma unroll
-                        for (int e = 0; e < SF::NCP; ++e) tmem_cp_sf<CG>(s0 + SF::col(e), sdesc_sf_atom(ss + SF_ATOM * e));
+                        for (int e = 0; e < SF::NCP; ++e) tmem_cp_side<FMT, CG>(s0 + SF::col(e), ss + SF::src(e));
                     }
                     // next stage already landed: interleave its copies with this stage's MMAs
                     const bool has_next = item + 1 < items && mbar_try_wait(smem_u32(full + next_stage), next_phase);
@@ -355,13 +426,18 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
                     fetched = has_next;
                     const uint64_t ad = sdesc_kmajor_sw128(sbase + L::A_OFF + stage * A_STAGE_BYTES);
                     const uint64_t bd = sdesc_kmajor_sw128(sbase + L::B_OFF + stage * L::B_STAGE);
+                    const uint64_t bd1 = sdesc_kmajor_sw128(sbase + L::B_OFF + stage * L::B_STAGE + BN_CTA * TILE_K_BYTES);
                     const uint32_t sf = tmem_base + SF_COL + static_cast<uint32_t>(stage) * SF_STAGE_COLS;
                     const uint32_t nss = sbase + L::SF_OFF + next_stage * L::SF_STAGE;
                     const uint32_t nsf = tmem_base + SF_COL + static_cast<uint32_t>(next_stage) * SF_STAGE_COLS;
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const uint32_t accum = (kb > 0 || k > 0) ? 1u : 0u;
-                        if constexpr (NV) {
+                        if constexpr (FMT == FMT_SP) {
+                            // logical K 32 per MMA: A +32 bytes (16 kept values), B +64 bytes within its
+                            // atom (atom k / 2); metadata word of MMA k at column 4k
+                            mma_sp16<CG>(d_tmem, ad + 2 * k, (k < 2 ? bd : bd1) + 4 * (k & 1), sf + 4u * k, p.idesc, accum);
+                        } else if constexpr (FMT == FMT_NV) {
                             mma_nvf4<CG>(d_tmem, ad + 2 * k, bd + 2 * k, p.idesc, sf + SF::sfa(k), sf + SF::sfb(k), accum);
                         } else {
                             // scale-factor ids: byte k of the stage's scale words (A bits [29,31), B bits [4,6))
@@ -372,7 +448,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
                         if (has_next) {
 #pragma unroll
                             for (int e = (k * SF::NCP + 3) / 4; e < ((k + 1) * SF::NCP + 3) / 4; ++e)
-                                tmem_cp_sf<CG>(nsf + SF::col(e), sdesc_sf_atom(nss + SF_ATOM * e));
+                                tmem_cp_side<FMT, CG>(nsf + SF::col(e), nss + SF::src(e));
                         }
                     }
                     if (CG == 2) mma_commit_pair(empty + stage, 0x3);
@@ -483,11 +559,11 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
     }
 }
 
-template <int BN, int STAGES, int NACC, int CG, bool NV>
+template <int BN, int STAGES, int NACC, int CG, int FMT>
 static cudaError_t launch_mx_one(const MxMaps &m, const GemmParams &p, int grid, cudaStream_t stream)
 {
-    using L = MxSmem<BN / CG, BN, STAGES, NV ? 4 : 1>;
-    auto kern = gemm_mx_kernel<BN, STAGES, NACC, CG, NV>;
+    using L = MxSmem<BN / CG, BN, STAGES, FMT>;
+    auto kern = gemm_mx_kernel<BN, STAGES, NACC, CG, FMT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -508,17 +584,26 @@ static cudaError_t launch_mx_one(const MxMaps &m, const GemmParams &p, int grid,
 cudaError_t launch_gemm_mx(const GemmConfig &cfg, const MxMaps &maps, const GemmParams &p, int grid,
                            cudaStream_t stream)
 {
-    if (cfg.kind == 4) { // NVFP4
-        if (cfg.cta_group == 2) return cfg.bn == 256 ? launch_mx_one<256, 5, 1, 2, true>(maps, p, grid, stream)
-                                                     : cudaErrorInvalidValue;
-        if (cfg.bn == 256) return launch_mx_one<256, 4, 1, 1, true>(maps, p, grid, stream);
-        if (cfg.bn == 128) return launch_mx_one<128, 6, 2, 1, true>(maps, p, grid, stream);
+    if (cfg.kind == 5) { // 2:4-sparse A with hardware-ordered metadata
+        if (cfg.cta_group == 2) {
+            if (cfg.bn == 256) return launch_mx_one<256, 4, 1, 2, FMT_SP>(maps, p, grid, stream);
+            if (cfg.bn == 128) return launch_mx_one<128, 5, 2, 2, FMT_SP>(maps, p, grid, stream);
+            return cudaErrorInvalidValue;
+        }
+        if (cfg.bn == 128) return launch_mx_one<128, 4, 2, 1, FMT_SP>(maps, p, grid, stream);
         return cudaErrorInvalidValue;
     }
-    if (cfg.cta_group == 2) return cfg.bn == 256 ? launch_mx_one<256, 6, 1, 2, false>(maps, p, grid, stream)
+    if (cfg.kind == 4) { // NVFP4
+        if (cfg.cta_group == 2) return cfg.bn == 256 ? launch_mx_one<256, 5, 1, 2, FMT_NV>(maps, p, grid, stream)
+                                                     : cudaErrorInvalidValue;
+        if (cfg.bn == 256) return launch_mx_one<256, 4, 1, 1, FMT_NV>(maps, p, grid, stream);
+        if (cfg.bn == 128) return launch_mx_one<128, 6, 2, 1, FMT_NV>(maps, p, grid, stream);
+        return cudaErrorInvalidValue;
+    }
+    if (cfg.cta_group == 2) return cfg.bn == 256 ? launch_mx_one<256, 6, 1, 2, FMT_MX>(maps, p, grid, stream)
                                                  : cudaErrorInvalidValue;
-    if (cfg.bn == 256) return launch_mx_one<256, 4, 1, 1, false>(maps, p, grid, stream);
-    if (cfg.bn == 128) return launch_mx_one<128, 6, 2, 1, false>(maps, p, grid, stream);
+    if (cfg.bn == 256) return launch_mx_one<256, 4, 1, 1, FMT_MX>(maps, p, grid, stream);
+    if (cfg.bn == 128) return launch_mx_one<128, 6, 2, 1, FMT_MX>(maps, p, grid, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -92,6 +92,8 @@ struct MxMaps {
 
 cudaError_t launch_gemm_mx(const GemmConfig &cfg, const MxMaps &maps, const GemmParams &p, int grid,
                            cudaStream_t stream);
+// canonical 2:4 metadata (M x K/32 words) -> the sparse MMA's tensor-memory order, 2 KB per MMA block
+cudaError_t launch_sp_meta_pack(const uint32_t *meta, int64_t M, int64_t K, uint8_t *out, cudaStream_t stream);
 // rows x nblk row-major scale codes -> blocked atoms (pad = the format's code of 1.0)
 cudaError_t launch_mx_pack_scales(const uint8_t *src, int64_t rows, int64_t nblk, uint32_t pad, uint8_t *dst,
                                   cudaStream_t stream);

@@ -146,3 +146,12 @@ def test_nvfp4_scales_bytes(lib):
     assert lib.tcm_nvfp4_scales_bytes(130, 256) == 2 * 4 * 512
     assert lib.tcm_nvfp4_scales_bytes(1, 64) == 512
     assert lib.tcm_nvfp4_scales_bytes(1, 24) == -1
+
+
+def test_sp_meta_tc_bytes_and_rejections(lib):
+    assert lib.tcm_sp_meta_tc_bytes(130, 160) == 2 * 2 * 8192
+    assert lib.tcm_sp_meta_tc_bytes(1, 48) == -1
+    assert lib.tcm_sp_meta_pack(64, 48, ALIGNED, ALIGNED, None) == 1
+    assert lib.tcm_sp_meta_pack(64, 64, ALIGNED, ALIGNED + 4, None) == 3
+    assert lib.tcm_gemm_sp_tc(64, 64, 48, BF16, ALIGNED, ALIGNED, ALIGNED, None, ALIGNED, 1.0, 0.0, BF16, None) == 1
+    assert lib.tcm_gemm_sp_tc(64, 64, 64, E4M3, ALIGNED, ALIGNED, ALIGNED, None, ALIGNED, 1.0, 0.0, BF16, None) == 2

@@ -76,11 +76,18 @@ def test_compress_with_pitch(tcm):
     assert np.array_equal(si.codes(Ac.cpu()), rAc) and np.array_equal(meta_codes(meta.cpu()), rmeta)
 
 
-def run_sparse(tcm, A_logical, B, out_dtype, C=None, alpha=1.0, beta=0.0):
+def run_sparse(tcm, A_logical, B, out_dtype, C=None, alpha=1.0, beta=0.0, tc=False):
+    """Compress on the GPU, then tcm_gemm_sp (canonical metadata) or, with tc, tcm_sp_meta_pack +
+    tcm_gemm_sp_tc (hardware-ordered metadata copied into tensor memory by tcgen05.cp)."""
     d = dev()
     Ac, meta = tcm.tcm_sp_compress(A_logical.to(d))
     D = torch.full((A_logical.shape[0], B.shape[0]), float("nan"), dtype=out_dtype, device=d)
-    tcm.tcm_gemm_sp(Ac, meta, B.to(d), D, C=None if C is None else C.to(d), alpha=alpha, beta=beta)
+    Cd = None if C is None else C.to(d)
+    if tc:
+        meta_tc = tcm.tcm_sp_meta_pack(meta, A_logical.shape[1])
+        tcm.tcm_gemm_sp_tc(Ac, meta_tc, B.to(d), D, C=Cd, alpha=alpha, beta=beta)
+    else:
+        tcm.tcm_gemm_sp(Ac, meta, B.to(d), D, C=Cd, alpha=alpha, beta=beta)
     code, site = tcm.tcm_get_device_status()
     assert code == 0, (code, site)
     return D.cpu(), Ac.cpu(), meta.cpu()
@@ -95,27 +102,29 @@ def oracle_sparse(A_logical, B, fmt, C=None, alpha=1.0, beta=0.0, rows=None, col
                        alpha=alpha, beta=beta, rows=rows, cols=cols)
 
 
+@pytest.mark.parametrize("tc", [False, True])
 @pytest.mark.parametrize("cg,bn", [(0, 0), (1, 128), (2, 256), (2, 128)])
 @pytest.mark.parametrize("M,N,K", [(128, 128, 32), (256, 224, 128), (300, 520, 160), (512, 672, 1024),
                                    (1000, 448, 2048)])
-def test_sparse_gemm_integer_exact(tcm, cg, bn, M, N, K):
+def test_sparse_gemm_integer_exact(tcm, cg, bn, M, N, K, tc):
     tcm.tcm_set_config_override(cg, bn, 0, 2)
     g = si.generator(M + N + K)
     A = si.integers((M, K), g)
     B = si.integers((N, K), g)
-    D, _, _ = run_sparse(tcm, A, B, torch.float32)
+    D, _, _ = run_sparse(tcm, A, B, torch.float32, tc=tc)
     ref, _ = oracle_sparse(A, B, "bf16")
     assert np.array_equal(D.double().numpy(), ref)
 
 
+@pytest.mark.parametrize("tc", [False, True])
 @pytest.mark.parametrize("fmt,out", [("bf16", torch.bfloat16), ("f16", torch.float32)])
-def test_sparse_gemm_bound_with_beta(tcm, fmt, out):
+def test_sparse_gemm_bound_with_beta(tcm, fmt, out, tc):
     M, N, K = 640, 800, 1536
     g = si.generator(11)
     A = si.normal((M, K), g, dtype=fmt)
     B = si.normal((N, K), g, dtype=fmt)
     C = si.normal((M, N), g, dtype={torch.bfloat16: "bf16", torch.float32: "f32"}[out])
-    D, _, _ = run_sparse(tcm, A, B, out, C=C, alpha=0.75, beta=0.5)
+    D, _, _ = run_sparse(tcm, A, B, out, C=C, alpha=0.75, beta=0.5, tc=tc)
     ref, S = oracle_sparse(A, B, fmt, C=C, alpha=0.75, beta=0.5)
     assert ratio(D, ref, S, scale=0.75) <= 1.0
 
@@ -137,10 +146,27 @@ def test_sparse_matches_dense_on_decompressed(tcm):
     assert diff <= 2e-5 * float(np.max(S))
 
 
-def test_sparse_8192_sampled(tcm):
+@pytest.mark.parametrize("tc", [False, True])
+def test_sparse_8192_sampled(tcm, tc):
     case = si.sparse_case()
-    D, _, _ = run_sparse(tcm, case["A_logical"], case["B"], torch.bfloat16)
+    D, _, _ = run_sparse(tcm, case["A_logical"], case["B"], torch.bfloat16, tc=tc)
     rows, cols = sample_indices(8192, 8192)
     ref, S = oracle_sparse(case["A_logical"], case["B"], "bf16", rows=rows, cols=cols)
     assert ratio(D, ref, S, rows=rows, cols=cols) <= 1.0
     assert not torch.isnan(D).any()
+
+
+@pytest.mark.parametrize("M,K", [(1, 32), (130, 96), (300, 512), (8192, 8192)])
+def test_meta_pack_bit_exact(tcm, M, K):
+    g = si.generator(M + K)
+    meta = torch.randint(-2 ** 31, 2 ** 31 - 1, (M, K // 32), generator=g, dtype=torch.int64).to(torch.int32)
+    got = tcm.tcm_sp_meta_pack(meta.to(dev()), K).cpu().numpy()
+    assert np.array_equal(got, oracle.sp_meta_pack(meta.numpy().view(np.uint32), K))
+
+
+def test_sparse_tc_identical_to_canonical_path(tcm):
+    """Same MMAs in the same order: the two metadata paths give bit-identical D."""
+    case = si.sparse_case(1024, 768, 2048, seed=13)
+    D1, _, _ = run_sparse(tcm, case["A_logical"], case["B"], torch.float32, tc=False)
+    D2, _, _ = run_sparse(tcm, case["A_logical"], case["B"], torch.float32, tc=True)
+    assert torch.equal(D1, D2)
