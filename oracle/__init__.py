@@ -211,21 +211,23 @@ def gemm_mx(A, SA, B, SB, a_fmt, b_fmt, *, block=32, sf_fmt="e8m0", C=None, c_fm
     return ref, S
 
 
-def mx_pack_scales(SC, K, block=32, pad=127):
+def mx_pack_scales(SC, K, block=32, pad=127, reps=1):
     """Blocked layout of row-major scale codes ``SC`` (rows x K/block uint8).
 
     Code (r, j) goes to byte ``(r//128 * KT + j//4) * 512 + (r%32)*16 + ((r//32)%4)*4 + j%4``
     with ``KT = ceil(K / (4 block))``; every other byte of the ``ceil(rows/128) * KT * 512``
-    bytes holds ``pad`` (1.0: 127 for E8M0, 0x38 for UE4M3).  Written as a plain loop."""
+    bytes holds ``pad`` (1.0: 127 for E8M0, 0x38 for UE4M3).  With ``reps`` > 1 every
+    512-byte atom is stored ``reps`` times in a row (NVFP4: 4).  Written as plain loops."""
     SC = np.ascontiguousarray(SC, dtype=np.uint8)
     rows, nblk = SC.shape
     assert K % block == 0 and nblk == K // block
     kt = (nblk + 3) // 4
-    out = np.full(((rows + 127) // 128) * kt * 512, pad, dtype=np.uint8)
+    out = np.full(((rows + 127) // 128) * kt * 512 * reps, pad, dtype=np.uint8)
     for r in range(rows):
         for j in range(nblk):
             atom = (r // 128) * kt + j // 4
-            out[atom * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + j % 4] = SC[r, j]
+            for c in range(reps):
+                out[(atom * reps + c) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + j % 4] = SC[r, j]
     return out
 
 def sp_meta_pack(meta, K):

@@ -625,3 +625,14 @@ def test_sp_meta_pack_reads_back_to_the_canonical_words(M, K):
             hi = (int(words[base + 16 * a + 8 + r]) >> half) & 0xFFFF    # lane s = 1: nibbles 4..7
             back[R, q] = lo | (hi << 16)
     assert np.array_equal(back, meta)
+
+
+def test_pack_replicated_atoms_are_copies():
+    """reps = 4 (NVFP4): each 512-byte atom four times in a row, otherwise the reps = 1 layout."""
+    SC = _pack_source(130, 160)
+    one = oracle.mx_pack_scales(SC, 160)
+    four = oracle.mx_pack_scales(SC, 160, reps=4)
+    assert four.size == 4 * one.size
+    atoms = four.reshape(-1, 4, 512)
+    for c in range(4):
+        assert np.array_equal(atoms[:, c, :].reshape(-1), one)
