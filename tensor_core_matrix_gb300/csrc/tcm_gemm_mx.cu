@@ -33,11 +33,14 @@
 // Pipeline: the dense kernel's (TMA ring of 128-byte K stages = 128 FP8 values,
 // four MMAs of K = 32 per stage, one thread issuing, TMEM accumulators), with
 // the stage's scale atoms loaded by the same TMA producer onto the same
-// barrier, and the issuing thread copying them to tensor memory (tcgen05.cp,
-// ordered before the MMAs that read them), normally one atom after each MMA
-// of the previous stage -- no other warp touches the scales.  The scale columns of a
-// stage are rewritten only after the stage's barrier has completed again,
-// i.e. after the MMAs that read them have finished.
+// barrier.  A thread of its own (warp MX_COPY_WARP) copies them to tensor
+// memory (tcgen05.cp) as soon as the stage lands and commits the copies to the
+// stage's sfready barrier; the MMA thread waits on that barrier before the
+// stage's MMAs.  Copies issued by a separate thread proceed alongside the MMA
+// thread's MMAs (measured: NVFP4 +36 %, MXFP8 +9 % against the same copies
+// issued by the MMA thread between its MMAs).  The scale columns of a stage
+// are rewritten only after the stage's barrier has completed again, which the
+// producer allows only after the MMAs that read them have finished.
 //
 // One accumulator of 256 columns fills half of tensor memory and the scale
 // columns take part of the rest, so a 256-wide tile has a single accumulator
@@ -48,8 +51,9 @@
 
 namespace tcm {
 
-constexpr int MX_EPI_WARPS = 8;                    // two per TMEM lane quadrant, half the columns each
-constexpr int MX_THREADS = 32 * (2 + MX_EPI_WARPS); // TMA, MMA, epilogue
+constexpr int MX_EPI_WARPS = 8; // two per TMEM lane quadrant, half the columns each
+constexpr int MX_COPY_WARP = 2 + MX_EPI_WARPS;
+constexpr int MX_THREADS = 32 * (3 + MX_EPI_WARPS); // TMA, MMA, epilogue (warps 2..9), side-data copies
 constexpr int SF_ATOM = 512;                       // scales of 128 rows x one 128-value K stage
 
 // Formats of the kernel: MX (MXFP8), NV (NVFP4), SP (2:4-sparse bf16/fp16 A,
@@ -67,7 +71,8 @@ struct MxSmem {
     static constexpr int B_OFF = STAGES * A_STAGE_BYTES;
     static constexpr int SF_OFF = B_OFF + STAGES * B_STAGE;
     static constexpr int BAR_OFF = SF_OFF + STAGES * SF_STAGE;
-    static constexpr int NUM_BARS = 2 * STAGES + 5; // full, empty, tfull[2], tempty[2], drain
+    // full, empty, tfull[2], tempty[2], drain, sfready[STAGES], the copy thread's drain
+    static constexpr int NUM_BARS = 3 * STAGES + 6;
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
     static constexpr int BYTES = MISC_OFF + 16;
     static constexpr int ALLOC = BYTES + 1024;
@@ -270,6 +275,8 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
     uint64_t *tfull = empty + STAGES;
     uint64_t *tempty = tfull + 2;
     uint64_t *drain = tempty + 2;
+    uint64_t *sfready = drain + 1;       // a stage's side data copied to tensor memory
+    uint64_t *cdrain = sfready + STAGES; // the copy thread's last copies done
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::MISC_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::MISC_OFF + 4);
 
@@ -288,6 +295,8 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
             mbar_init(tempty + a, MX_EPI_WARPS * CG);
         }
         mbar_init(drain, 1);
+        for (int s = 0; s < STAGES; ++s) mbar_init(sfready + s, 1);
+        mbar_init(cdrain, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -376,60 +385,29 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
         }
     } else if (warp == 1) {
         if (lane == 0 && leader) {
-            // Item i = (tile, K block) in ring stage i % STAGES.  If the data of
-            // item i + 1 has already landed (a non-blocking test), its scale copies
-            // are issued between the four MMAs of item i; otherwise they go in
-            // front of item i + 1's own MMAs once its data arrives.  Measured:
-            // three copies back to back in front of the MMAs, or a blocking wait
-            // for the next stage, cost 16-35%.
-            const int my_tiles = first_tile < p.tile_end ? (p.tile_end - 1 - first_tile) / step + 1 : 0;
-            const long long items = static_cast<long long>(my_tiles) * p.num_kb;
+            // Item i = (tile, K block) in ring stage i % STAGES: wait until its data has
+            // landed and the copy thread's copies of its side data have completed.
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            if (items > 0) {
-                ok = wait_bar<CG>(full, 0, w, SITE_MMA_FULL, true);
-                if (ok) {
-                    tc_fence_after();
-                    const uint32_t sf0 = tmem_base + SF_COL;
-#pragma unroll
-                    for (int e = 0; e < SF::NCP; ++e)
-                        tmem_cp_side<FMT, CG>(sf0 + SF::col(e), sbase + L::SF_OFF + SF::src(e));
-                }
-            }
-            long long item = 0;
             int local = 0;
-            bool fetched = true; // stage 0: data seen and scales copied above
             for (int t = first_tile; ok && t < p.tile_end; t += step, ++local) {
                 const int acc = local % NACC;
                 const uint32_t acc_phase = (local / NACC) & 1;
                 if (!wait_bar<CG>(tempty + acc, acc_phase ^ 1u, w, SITE_MMA_ACC_EMPTY, true)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * ACC_STRIDE;
-                for (int kb = 0; kb < p.num_kb; ++kb, ++item) {
-                    const int next_stage = stage + 1 == STAGES ? 0 : stage + 1;
-                    const uint32_t next_phase = stage + 1 == STAGES ? phase ^ 1u : phase;
-                    if (!fetched) { // data not seen yet: wait for it, copy this stage's scales up front
-                        if (!wait_bar<CG>(full + stage, phase, w, SITE_MMA_FULL, true)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t ss = sbase + L::SF_OFF + stage * L::SF_STAGE;
-                        const uint32_t s0 = tmem_base + SF_COL + static_cast<uint32_t>(stage) * SF_STAGE_COLS;
-#pragma unroll
-                        for (int e = 0; e < SF::NCP; ++e) tmem_cp_side<FMT, CG>(s0 + SF::col(e), ss + SF::src(e));
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait_bar<CG>(sfready + stage, phase, w, SITE_MMA_META, true) ||
+                        !wait_bar<CG>(full + stage, phase, w, SITE_MMA_FULL, true)) {
+                        ok = false;
+                        break;
                     }
-                    // next stage already landed: interleave its copies with this stage's MMAs
-                    const bool has_next = item + 1 < items && mbar_try_wait(smem_u32(full + next_stage), next_phase);
-                    if (has_next) tc_fence_after();
-                    fetched = has_next;
+                    tc_fence_after();
                     const uint64_t ad = sdesc_kmajor_sw128(sbase + L::A_OFF + stage * A_STAGE_BYTES);
                     const uint64_t bd = sdesc_kmajor_sw128(sbase + L::B_OFF + stage * L::B_STAGE);
                     const uint64_t bd1 = sdesc_kmajor_sw128(sbase + L::B_OFF + stage * L::B_STAGE + BN_CTA * TILE_K_BYTES);
                     const uint32_t sf = tmem_base + SF_COL + static_cast<uint32_t>(stage) * SF_STAGE_COLS;
-                    const uint32_t nss = sbase + L::SF_OFF + next_stage * L::SF_STAGE;
-                    const uint32_t nsf = tmem_base + SF_COL + static_cast<uint32_t>(next_stage) * SF_STAGE_COLS;
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const uint32_t accum = (kb > 0 || k > 0) ? 1u : 0u;
@@ -444,17 +422,13 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
                             const uint32_t idesc = p.idesc | (static_cast<uint32_t>(k) << 29) | (static_cast<uint32_t>(k) << 4);
                             mma_mx<CG>(d_tmem, ad + 2 * k, bd + 2 * k, idesc, sf + SF::sfa(k), sf + SF::sfb(k), accum);
                         }
-                        // after MMA k: the next stage's copies [k*NCP/4, (k+1)*NCP/4), rounded up
-                        if (has_next) {
-#pragma unroll
-                            for (int e = (k * SF::NCP + 3) / 4; e < ((k + 1) * SF::NCP + 3) / 4; ++e)
-                                tmem_cp_side<FMT, CG>(nsf + SF::col(e), nss + SF::src(e));
-                        }
                     }
                     if (CG == 2) mma_commit_pair(empty + stage, 0x3);
                     else mma_commit(empty + stage);
-                    stage = next_stage;
-                    phase = next_phase;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
                 }
                 if (!ok) break;
                 if (CG == 2) mma_commit_pair(tfull + acc, 0x3);
@@ -464,7 +438,33 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
             else mma_commit(drain);
             wait_bar<CG>(drain, 0, w, SITE_DRAIN, false);
         }
-    } else {
+    } else if (warp == MX_COPY_WARP) {
+        if (lane == 0 && leader) {
+            const int my_tiles = first_tile < p.tile_end ? (p.tile_end - 1 - first_tile) / step + 1 : 0;
+            const long long items = static_cast<long long>(my_tiles) * p.num_kb;
+            int stage = 0;
+            uint32_t phase = 0;
+            for (long long item = 0; item < items; ++item) {
+                // the stage's data has landed; its TMEM slot's previous readers (the MMAs of
+                // item - STAGES) completed before the producer could refill the stage
+                if (!wait_bar<CG>(full + stage, phase, w, SITE_MMA_FULL, true)) break;
+                tc_fence_after();
+                const uint32_t ss = sbase + L::SF_OFF + stage * L::SF_STAGE;
+                const uint32_t s0 = tmem_base + SF_COL + static_cast<uint32_t>(stage) * SF_STAGE_COLS;
+#pragma unroll
+                for (int e = 0; e < SF::NCP; ++e) tmem_cp_side<FMT, CG>(s0 + SF::col(e), ss + SF::src(e));
+                if (CG == 2) mma_commit_pair(sfready + stage, 0x1);
+                else mma_commit(sfready + stage);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (CG == 2) mma_commit_pair(cdrain, 0x1);
+            else mma_commit(cdrain);
+            wait_bar<CG>(cdrain, 0, w, SITE_DRAIN, false);
+        }
+    } else if (warp < MX_COPY_WARP) {
         // Epilogue: warp quadrant (warp % 4) owns TMEM lanes / tile rows
         // 32q .. 32q + 31; the two warps of a quadrant split the columns.
         const int quad = warp & 3;
