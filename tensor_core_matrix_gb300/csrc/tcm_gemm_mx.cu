@@ -31,16 +31,20 @@
 // row-major codes.
 //
 // Pipeline: the dense kernel's (TMA ring of 128-byte K stages = 128 FP8 values,
-// four MMAs of K = 32 per stage, one thread issuing, TMEM accumulators), with
-// the stage's scale atoms loaded by the same TMA producer onto the same
-// barrier.  A thread of its own (warp MX_COPY_WARP) copies them to tensor
-// memory (tcgen05.cp) as soon as the stage lands and commits the copies to the
-// stage's sfready barrier; the MMA thread waits on that barrier before the
-// stage's MMAs.  Copies issued by a separate thread proceed alongside the MMA
-// thread's MMAs (measured: NVFP4 +36 %, MXFP8 +9 % against the same copies
-// issued by the MMA thread between its MMAs).  The scale columns of a stage
-// are rewritten only after the stage's barrier has completed again, which the
-// producer allows only after the MMAs that read them have finished.
+// four MMAs of K = 32 per stage, one thread issuing, TMEM accumulators).  The
+// same TMA producer loads the stage's scale atoms first, onto a barrier of
+// their own (sfull), then A and B onto the stage's full barrier.  Copy threads
+// (lane 0 of warps MX_COPY_WARP ..) copy the atoms to tensor memory
+// (tcgen05.cp) as soon as they land, while A and B are still in flight, and
+// commit their copies to the stage's sfready barrier; the MMA thread waits on
+// sfready and full before the stage's MMAs.  Copies issued by threads other
+// than the MMA thread proceed alongside the MMAs, and the issue of a copy
+// costs its thread tens of cycles, so NVFP4's twelve copies per stage are
+// split over three threads.  Measured at 8192^3 against one thread issuing
+// the copies between its MMAs: NVFP4 2913 -> 4605 TFLOP/s, MXFP8 2597 -> 2843.
+// The scale columns of a stage are rewritten only after the stage's sfull
+// barrier has completed again, which the producer allows only after the MMAs
+// that read them have finished.
 //
 // One accumulator of 256 columns fills half of tensor memory and the scale
 // columns take part of the rest, so a 256-wide tile has a single accumulator
@@ -52,14 +56,17 @@
 namespace tcm {
 
 constexpr int MX_EPI_WARPS = 8; // two per TMEM lane quadrant, half the columns each
-constexpr int MX_COPY_WARP = 2 + MX_EPI_WARPS;
-constexpr int MX_THREADS = 32 * (3 + MX_EPI_WARPS); // TMA, MMA, epilogue (warps 2..9), side-data copies
+constexpr int MX_COPY_WARP = 2 + MX_EPI_WARPS; // first copy warp
 constexpr int SF_ATOM = 512;                       // scales of 128 rows x one 128-value K stage
 
 // Formats of the kernel: MX (MXFP8), NV (NVFP4), SP (2:4-sparse bf16/fp16 A,
 // metadata in the hardware order -- the "side" data of a stage is then the
 // sparse metadata instead of block scales).
 enum SideFmt : int { FMT_MX = 0, FMT_NV = 1, FMT_SP = 2 };
+// copy warps per format (lane 0 of each issues the copies e with e % n == its index)
+__host__ __device__ constexpr int mx_copy_warps(int fmt) { return fmt == FMT_NV ? 3 : 1; }
+// TMA, MMA, epilogue (warps 2..9), copy warps
+__host__ __device__ constexpr int mx_threads(int fmt) { return 32 * (2 + MX_EPI_WARPS + mx_copy_warps(fmt)); }
 constexpr int SP_META_STAGE = 4 * 2048; // four 128-lane x 16-byte blocks, one per MMA
 
 template <int BN_CTA, int BN, int STAGES, int FMT>
@@ -71,8 +78,8 @@ struct MxSmem {
     static constexpr int B_OFF = STAGES * A_STAGE_BYTES;
     static constexpr int SF_OFF = B_OFF + STAGES * B_STAGE;
     static constexpr int BAR_OFF = SF_OFF + STAGES * SF_STAGE;
-    // full, empty, tfull[2], tempty[2], drain, sfready[STAGES], the copy thread's drain
-    static constexpr int NUM_BARS = 3 * STAGES + 6;
+    // full, empty, tfull[2], tempty[2], drain, sfready[STAGES], the copy threads' drain, sfull[STAGES]
+    static constexpr int NUM_BARS = 4 * STAGES + 6;
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
     static constexpr int BYTES = MISC_OFF + 16;
     static constexpr int ALLOC = BYTES + 1024;
@@ -246,7 +253,7 @@ __device__ __forceinline__ void tma_ld(uint32_t dst, const CUtensorMap *map, uin
 // pair per 256 x BN tile (each CTA loads 128 rows of A and BN/2 rows of B, its
 // own A scale atom and all BN/128 B scale atoms).
 template <int BN, int STAGES, int NACC, int CG, int FMT>
-__global__ void __launch_bounds__(MX_THREADS, 1)
+__global__ void __launch_bounds__(mx_threads(FMT), 1)
     gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                    const GemmParams p)
@@ -263,7 +270,9 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
     constexpr uint32_t SF_STAGE_COLS = SF::COLS;
     static_assert(SF_COL + SF_STAGE_COLS * STAGES <= 512, "tensor memory budget");
     constexpr uint32_t TMEM_COLS = 512;
-    constexpr uint32_t STAGE_TX = CG * (A_STAGE_BYTES + L::B_STAGE + L::SF_STAGE);
+    constexpr uint32_t STAGE_TX = CG * (A_STAGE_BYTES + L::B_STAGE); // A and B of both CTAs
+    constexpr uint32_t SIDE_TX = CG * L::SF_STAGE;                     // side data of both CTAs
+    constexpr int NCW = mx_copy_warps(FMT);
     constexpr int EPI_COLS = BN / (MX_EPI_WARPS / 4); // columns per epilogue warp
 
     extern __shared__ uint8_t smem_raw[];
@@ -276,7 +285,8 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
     uint64_t *tempty = tfull + 2;
     uint64_t *drain = tempty + 2;
     uint64_t *sfready = drain + 1;       // a stage's side data copied to tensor memory
-    uint64_t *cdrain = sfready + STAGES; // the copy thread's last copies done
+    uint64_t *cdrain = sfready + STAGES; // the copy threads' last copies done
+    uint64_t *sfull = cdrain + 1;        // a stage's side data landed in shared memory
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::MISC_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::MISC_OFF + 4);
 
@@ -295,8 +305,11 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
             mbar_init(tempty + a, MX_EPI_WARPS * CG);
         }
         mbar_init(drain, 1);
-        for (int s = 0; s < STAGES; ++s) mbar_init(sfready + s, 1);
-        mbar_init(cdrain, 1);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(sfready + s, NCW);
+            mbar_init(sfull + s, 1);
+        }
+        mbar_init(cdrain, NCW);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -328,6 +341,7 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
     if (warp == 0) {
         if (lane == 0) {
             const uint32_t full_cluster0 = CG == 2 ? mapa_shared(smem_u32(full), 0) : 0u;
+            const uint32_t sfull_cluster0 = CG == 2 ? mapa_shared(smem_u32(sfull), 0) : 0u;
             const int kt = p.num_kb * APT; // scale atoms per 128-row tile along K
             int stage = 0;
             uint32_t phase = 0;
@@ -347,26 +361,31 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
                     const uint32_t sa = sbase + L::A_OFF + stage * A_STAGE_BYTES;
                     const uint32_t sb = sbase + L::B_OFF + stage * L::B_STAGE;
                     const uint32_t ss = sbase + L::SF_OFF + stage * L::SF_STAGE;
-                    if (leader || CG == 1) mbar_arrive_expect_tx(full + stage, STAGE_TX);
+                    if (leader || CG == 1) {
+                        mbar_arrive_expect_tx(sfull + stage, SIDE_TX);
+                        mbar_arrive_expect_tx(full + stage, STAGE_TX);
+                    }
+                    // pair: both CTAs' loads complete on the even CTA's barriers (cluster addresses)
                     const uint32_t fb = CG == 2 ? full_cluster0 + static_cast<uint32_t>(stage) * 8u : 0u;
+                    const uint32_t sfb = CG == 2 ? sfull_cluster0 + static_cast<uint32_t>(stage) * 8u : 0u;
                     if constexpr (FMT == FMT_SP) {
-                        // compressed A: 64 kept values (128 bytes) of the stage's 128 logical K;
-                        // B: two 64-value atoms; metadata: the tile's four 2 KB blocks of this stage
+                        // metadata: the tile's four 2 KB blocks of this stage; compressed A: 64 kept
+                        // values (128 bytes) of the stage's 128 logical K; B: two 64-value atoms
                         const int ym = (a_tile * p.num_kb + kb) * 4 * 128;
+                        tma_ld<CG>(ss, &tmSA, sfull + stage, sfb, 0, ym);
+                        tma_ld<CG>(ss + 4096, &tmSA, sfull + stage, sfb, 0, ym + 256);
                         tma_ld<CG>(sa, &tmA, full + stage, fb, kb * 64, a_row);
                         tma_ld<CG>(sb, &tmB, full + stage, fb, kb * 128, b_row);
                         tma_ld<CG>(sb + BN_CTA * TILE_K_BYTES, &tmB, full + stage, fb, kb * 128 + 64, b_row);
-                        tma_ld<CG>(ss, &tmSA, full + stage, fb, 0, ym);
-                        tma_ld<CG>(ss + 4096, &tmSA, full + stage, fb, 0, ym + 256);
                     } else {
                         const int ya = (a_tile * kt + kb * APT) * 32;
-                        tma_ld<CG>(sa, &tmA, full + stage, fb, kb * 128, a_row);
-                        tma_ld<CG>(sb, &tmB, full + stage, fb, kb * 128, b_row);
-                        tma_ld<CG>(ss, &tmSA, full + stage, fb, 0, ya);
+                        tma_ld<CG>(ss, &tmSA, sfull + stage, sfb, 0, ya);
 #pragma unroll
                         for (int i = 0; i < SFB_ATOMS; ++i)
-                            tma_ld<CG>(ss + SF_ATOM * APT * (1 + i), &tmSB, full + stage, fb, 0,
+                            tma_ld<CG>(ss + SF_ATOM * APT * (1 + i), &tmSB, sfull + stage, sfb, 0,
                                        ((nb * SFB_ATOMS + i) * kt + kb * APT) * 32);
+                        tma_ld<CG>(sa, &tmA, full + stage, fb, kb * 128, a_row);
+                        tma_ld<CG>(sb, &tmB, full + stage, fb, kb * 128, b_row);
                     }
                     ++issued;
                     if (++stage == STAGES) {
@@ -379,14 +398,18 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
                 const long long n = issued > s ? (issued - s + STAGES - 1) / STAGES : 0;
                 if (n == 0) continue;
                 const uint32_t last = static_cast<uint32_t>((n - 1) & 1);
-                if (leader) wait_bar<CG>(full + s, last, w, SITE_DRAIN, false);
-                else wait_bar<CG>(empty + s, last, w, SITE_DRAIN, false);
+                if (leader) {
+                    wait_bar<CG>(sfull + s, last, w, SITE_DRAIN, false);
+                    wait_bar<CG>(full + s, last, w, SITE_DRAIN, false);
+                } else {
+                    wait_bar<CG>(empty + s, last, w, SITE_DRAIN, false);
+                }
             }
         }
     } else if (warp == 1) {
         if (lane == 0 && leader) {
             // Item i = (tile, K block) in ring stage i % STAGES: wait until its data has
-            // landed and the copy thread's copies of its side data have completed.
+            // landed and the copy threads' copies of its side data have completed.
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
@@ -438,21 +461,23 @@ __global__ void __launch_bounds__(MX_THREADS, 1)
             else mma_commit(drain);
             wait_bar<CG>(drain, 0, w, SITE_DRAIN, false);
         }
-    } else if (warp == MX_COPY_WARP) {
+    } else if (warp >= MX_COPY_WARP) {
+        const int cw = warp - MX_COPY_WARP; // this thread issues the copies e with e % NCW == cw
         if (lane == 0 && leader) {
             const int my_tiles = first_tile < p.tile_end ? (p.tile_end - 1 - first_tile) / step + 1 : 0;
             const long long items = static_cast<long long>(my_tiles) * p.num_kb;
             int stage = 0;
             uint32_t phase = 0;
             for (long long item = 0; item < items; ++item) {
-                // the stage's data has landed; its TMEM slot's previous readers (the MMAs of
-                // item - STAGES) completed before the producer could refill the stage
-                if (!wait_bar<CG>(full + stage, phase, w, SITE_MMA_FULL, true)) break;
+                // the stage's side data has landed; its TMEM slot's previous readers (the MMAs
+                // of item - STAGES) completed before the producer could refill the stage
+                if (!wait_bar<CG>(sfull + stage, phase, w, SITE_MMA_FULL, true)) break;
                 tc_fence_after();
                 const uint32_t ss = sbase + L::SF_OFF + stage * L::SF_STAGE;
                 const uint32_t s0 = tmem_base + SF_COL + static_cast<uint32_t>(stage) * SF_STAGE_COLS;
 #pragma unroll
-                for (int e = 0; e < SF::NCP; ++e) tmem_cp_side<FMT, CG>(s0 + SF::col(e), ss + SF::src(e));
+                for (int e = 0; e < SF::NCP; ++e)
+                    if (e % NCW == cw) tmem_cp_side<FMT, CG>(s0 + SF::col(e), ss + SF::src(e));
                 if (CG == 2) mma_commit_pair(sfready + stage, 0x1);
                 else mma_commit(sfready + stage);
                 if (++stage == STAGES) {
@@ -564,11 +589,12 @@ static cudaError_t launch_mx_one(const MxMaps &m, const GemmParams &p, int grid,
 {
     using L = MxSmem<BN / CG, BN, STAGES, FMT>;
     auto kern = gemm_mx_kernel<BN, STAGES, NACC, CG, FMT>;
+    static_assert(mx_threads(FMT) <= 1024, "block size");
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-    cfg.blockDim = dim3(MX_THREADS, 1, 1);
+    cfg.blockDim = dim3(mx_threads(FMT), 1, 1);
     cfg.dynamicSmemBytes = L::ALLOC;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
