@@ -98,9 +98,10 @@ def recorded_traffic():
         return None
     vals = {}
     for line in text.splitlines():
-        if "=" in line and line.strip().startswith(("dram_bytes_per_launch", "kernel_source_sha")):
-            k, v = line.split("=", 1)
-            vals[k.strip().strip("`- ")] = v.strip().strip("` ")
+        entry = line.strip().lstrip("-* ").strip("`")
+        if "=" in entry and entry.startswith(("dram_bytes_per_launch", "kernel_source_sha")):
+            k, v = entry.split("=", 1)
+            vals[k.strip().strip("`")] = v.strip().strip("` ")
     if vals.get("kernel_source_sha") != kernel_source_sha():
         return None
     try:
