@@ -96,6 +96,36 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, int fmt)
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
+// Stores a warp's 32 rows (lane l holds row row0 + l, NCH 16-byte chunks of packed
+// 16-bit outputs starting at column col0) so that each instruction writes whole
+// 32-byte sectors: lanes 2j and 2j + 1 exchange one chunk and then write chunks
+// q, q + 1 of row 2j together, then of row 2j + 1 (rows at or past kM are skipped).
+template <int NCH>
+__device__ __forceinline__ void store_rows_paired(uint16_t *D, long long ldd, int row, int kM, int col0,
+                                                  const uint32_t (&packed)[4 * NCH])
+{
+    static_assert(NCH % 2 == 0, "chunk pairs");
+    const int lane = threadIdx.x & 31;
+    const bool odd = lane & 1;
+    const int row_even = row - (odd ? 1 : 0);
+    uint16_t *const r0 = D + static_cast<long long>(row_even) * ldd + col0;
+    uint16_t *const r1 = r0 + ldd;
+#pragma unroll
+    for (int q = 0; q < NCH; q += 2) {
+        const uint4 c0 = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+        const uint4 c1 = make_uint4(packed[4 * q + 4], packed[4 * q + 5], packed[4 * q + 6], packed[4 * q + 7]);
+        const uint4 send = odd ? c0 : c1; // even lane gives its chunk q + 1, odd lane its chunk q
+        uint4 recv;
+        recv.x = __shfl_xor_sync(0xffffffffu, send.x, 1);
+        recv.y = __shfl_xor_sync(0xffffffffu, send.y, 1);
+        recv.z = __shfl_xor_sync(0xffffffffu, send.z, 1);
+        recv.w = __shfl_xor_sync(0xffffffffu, send.w, 1);
+        const int c = 8 * (q + (odd ? 1 : 0)); // column of this lane's chunk
+        if (row_even < kM) *reinterpret_cast<uint4 *>(r0 + c) = odd ? recv : c0;
+        if (row_even + 1 < kM) *reinterpret_cast<uint4 *>(r1 + c) = odd ? c1 : recv;
+    }
+}
+
 // Shared-memory descriptor of a 32-row x 16-byte block without swizzle:
 // core matrices of 8 rows x 16 bytes, 128 bytes apart.
 __device__ __forceinline__ uint64_t sdesc_sf_atom(uint32_t smem_addr)
@@ -542,12 +572,7 @@ __global__ void __launch_bounds__(mx_threads(FMT), 1)
                     if (CG == 2) mbar_arrive_cluster(tempty_cluster0 + static_cast<uint32_t>(acc) * 8u);
                     else mbar_arrive(tempty + acc);
                 }
-                if (row < p.kM) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.D) + static_cast<long long>(row) * p.ldd + col0);
-#pragma unroll
-                    for (int q = 0; q < EPI_COLS / 8; ++q)
-                        dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
-                }
+                store_rows_paired<EPI_COLS / 8>(static_cast<uint16_t *>(p.D), p.ldd, row, p.kM, col0, packed);
                 continue;
             }
 #pragma unroll 1
