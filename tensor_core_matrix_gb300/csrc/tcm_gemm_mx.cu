@@ -100,6 +100,8 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, int fmt)
 // 16-bit outputs starting at column col0) so that each instruction writes whole
 // 32-byte sectors: lanes 2j and 2j + 1 exchange one chunk and then write chunks
 // q, q + 1 of row 2j together, then of row 2j + 1 (rows at or past kM are skipped).
+// The stores are marked streaming (evict first), so that the output passing through
+// L2 displaces less of A and B (measured: NVFP4 8192^3 +5 %, sparse +2.4 %).
 template <int NCH>
 __device__ __forceinline__ void store_rows_paired(uint16_t *D, long long ldd, int row, int kM, int col0,
                                                   const uint32_t (&packed)[4 * NCH])
@@ -121,8 +123,8 @@ __device__ __forceinline__ void store_rows_paired(uint16_t *D, long long ldd, in
         recv.z = __shfl_xor_sync(0xffffffffu, send.z, 1);
         recv.w = __shfl_xor_sync(0xffffffffu, send.w, 1);
         const int c = 8 * (q + (odd ? 1 : 0)); // column of this lane's chunk
-        if (row_even < kM) *reinterpret_cast<uint4 *>(r0 + c) = odd ? recv : c0;
-        if (row_even + 1 < kM) *reinterpret_cast<uint4 *>(r1 + c) = odd ? c1 : recv;
+        if (row_even < kM) __stcs(reinterpret_cast<uint4 *>(r0 + c), odd ? recv : c0);
+        if (row_even + 1 < kM) __stcs(reinterpret_cast<uint4 *>(r1 + c), odd ? c1 : recv);
     }
 }
 
