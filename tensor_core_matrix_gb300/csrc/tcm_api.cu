@@ -123,10 +123,12 @@ static bool encode_sf_atoms(CUtensorMap *map, const void *base, uint64_t rows, u
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
+    // The atoms are contiguous 512-byte blocks; the map views them as rows of 128 bytes
+    // (4 per atom) so that a box of atoms moves in 128-byte requests, not 16-byte ones.
     const uint64_t atoms = ((rows + 127) / 128) * ((K + k_per_atom - 1) / k_per_atom);
-    const cuuint64_t dims[2] = {16, atoms * 32};
-    const cuuint64_t strides[1] = {16};
-    const cuuint32_t box[2] = {16, 32u * box_atoms};
+    const cuuint64_t dims[2] = {128, atoms * 4};
+    const cuuint64_t strides[1] = {128};
+    const cuuint32_t box[2] = {128, 4u * box_atoms};
     const cuuint32_t estr[2] = {1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
@@ -433,8 +435,8 @@ tcm_status tcm_gemm_sp_tc(int64_t M, int64_t N, int64_t K, tcm_dtype dtype, cons
     if (out_dtype != TCM_BF16 && out_dtype != TCM_F16 && out_dtype != TCM_F32) return TCM_ERR_UNSUPPORTED;
     if (M < 1 || N < 1 || K < 0 || K % 32 != 0) return TCM_ERR_INVALID_ARG;
     if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2) return TCM_ERR_UNSUPPORTED;
-    // metadata rows (128 per 2 KB block) are addressed with 32-bit coordinates
-    if (((M + 255) / 128) * ((K + 127) / 128) * 4 * 128 > INT32_MAX) return TCM_ERR_UNSUPPORTED;
+    // metadata rows (64 of 128 bytes per stage of 128 logical K) are addressed with 32-bit coordinates
+    if (((M + 255) / 128) * ((K + 127) / 128) * 64 > INT32_MAX) return TCM_ERR_UNSUPPORTED;
     if (!D || (K > 0 && (!A_comp || !meta_tc || !B)) || (beta != 0.f && !C)) return TCM_ERR_INVALID_ARG;
     const int eo = elem_bytes(out_dtype);
     if ((A_comp && !aligned16(A_comp)) || (B && !aligned16(B)) || (meta_tc && !aligned16(meta_tc)) || !aligned16(D) ||
@@ -458,11 +460,13 @@ tcm_status tcm_gemm_sp_tc(int64_t M, int64_t N, int64_t K, tcm_dtype dtype, cons
     MxMaps maps;
     std::memset(&maps, 0, sizeof maps);
     if (K > 0) {
-        const uint64_t meta_rows = static_cast<uint64_t>((M + 127) / 128) * static_cast<uint64_t>((K + 127) / 128) * 512u;
+        // a stage's 8 KB of metadata (four 2 KB MMA blocks) is contiguous: one box of 64
+        // rows of 128 bytes
+        const uint64_t meta_rows = static_cast<uint64_t>((M + 127) / 128) * static_cast<uint64_t>((K + 127) / 128) * 64u;
         EncodeTiledFn fn = encode_fn();
-        const cuuint64_t dims[2] = {16, meta_rows};
-        const cuuint64_t strides[1] = {16};
-        const cuuint32_t box[2] = {16, 256}; // two MMA blocks
+        const cuuint64_t dims[2] = {128, meta_rows};
+        const cuuint64_t strides[1] = {128};
+        const cuuint32_t box[2] = {128, 64};
         const cuuint32_t estr[2] = {1, 1};
         if (!fn || !encode_kmajor(&maps.a, A_comp, 2, static_cast<uint64_t>(K / 2), static_cast<uint64_t>(M),
                                   static_cast<uint64_t>(K / 2), 128) ||
@@ -603,9 +607,9 @@ static tcm_status block_scaled_impl(bool nv, int64_t M, int64_t N, int64_t K, tc
     const int64_t k_atom = nv ? 64 : 128;       // K values per scale atom
     if (M < 1 || N < 1 || K < 0 || K % (nv ? 256 : 32) != 0) return TCM_ERR_INVALID_ARG;
     if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2) return TCM_ERR_UNSUPPORTED;
-    // scale-atom rows (32 per atom) are addressed with 32-bit coordinates
-    if (((M + 255) / 128) * ((K + k_atom - 1) / k_atom) * 32 > INT32_MAX ||
-        ((N + 255) / 128) * ((K + k_atom - 1) / k_atom) * 32 > INT32_MAX)
+    // scale-atom rows (4 of 128 bytes per atom) are addressed with 32-bit coordinates
+    if (((M + 255) / 128) * ((K + k_atom - 1) / k_atom) * 4 > INT32_MAX ||
+        ((N + 255) / 128) * ((K + k_atom - 1) / k_atom) * 4 > INT32_MAX)
         return TCM_ERR_UNSUPPORTED;
     if (!D || (K > 0 && (!A || !B || !a_scales || !b_scales)) || (beta != 0.f && !C)) return TCM_ERR_INVALID_ARG;
     const int eo = elem_bytes(out_dtype);

@@ -401,21 +401,21 @@ __global__ void __launch_bounds__(mx_threads(FMT), 1)
                     const uint32_t fb = CG == 2 ? full_cluster0 + static_cast<uint32_t>(stage) * 8u : 0u;
                     const uint32_t sfb = CG == 2 ? sfull_cluster0 + static_cast<uint32_t>(stage) * 8u : 0u;
                     if constexpr (FMT == FMT_SP) {
-                        // metadata: the tile's four 2 KB blocks of this stage; compressed A: 64 kept
-                        // values (128 bytes) of the stage's 128 logical K; B: two 64-value atoms
-                        const int ym = (a_tile * p.num_kb + kb) * 4 * 128;
-                        tma_ld<CG>(ss, &tmSA, sfull + stage, sfb, 0, ym);
-                        tma_ld<CG>(ss + 4096, &tmSA, sfull + stage, sfb, 0, ym + 256);
+                        // metadata: the tile's four 2 KB blocks of this stage (64 rows of 128 bytes);
+                        // compressed A: 64 kept values (128 bytes) of the stage's 128 logical K; B:
+                        // two 64-value atoms
+                        tma_ld<CG>(ss, &tmSA, sfull + stage, sfb, 0, (a_tile * p.num_kb + kb) * 64);
                         tma_ld<CG>(sa, &tmA, full + stage, fb, kb * 64, a_row);
                         tma_ld<CG>(sb, &tmB, full + stage, fb, kb * 128, b_row);
                         tma_ld<CG>(sb + BN_CTA * TILE_K_BYTES, &tmB, full + stage, fb, kb * 128 + 64, b_row);
                     } else {
-                        const int ya = (a_tile * kt + kb * APT) * 32;
+                        // scale atoms: 512 bytes = 4 rows of 128 bytes each in the tensor maps
+                        const int ya = (a_tile * kt + kb * APT) * 4;
                         tma_ld<CG>(ss, &tmSA, sfull + stage, sfb, 0, ya);
 #pragma unroll
                         for (int i = 0; i < SFB_ATOMS; ++i)
                             tma_ld<CG>(ss + SF_ATOM * APT * (1 + i), &tmSB, sfull + stage, sfb, 0,
-                                       ((nb * SFB_ATOMS + i) * kt + kb * APT) * 32);
+                                       ((nb * SFB_ATOMS + i) * kt + kb * APT) * 4);
                         tma_ld<CG>(sa, &tmA, full + stage, fb, kb * 128, a_row);
                         tma_ld<CG>(sb, &tmB, full + stage, fb, kb * 128, b_row);
                     }
