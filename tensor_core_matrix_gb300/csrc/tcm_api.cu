@@ -114,8 +114,9 @@ static bool encode_kmajor(CUtensorMap *map, const void *base, int elem_bytes, ui
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Blocked E8M0 scales (see tcm_gemm_mx.cu) as a 2-D byte tensor of
-// ceil(rows / 128) * ceil(K / 128) * 32 rows of 16 bytes, boxes of one 512-byte atom.
+// Blocked scales (see tcm_gemm_mx.cu) as a 2-D byte tensor of 512-byte atoms, each
+// atom 4 rows of 128 bytes; a box holds the box_atoms atoms of one 128-row tile in one K
+// stage.
 // k_per_atom: K values covered by one atom (MX 128 = 4 blocks of 32, NVFP4 64 = 4 of 16);
 // box_atoms: atoms per TMA box (the atoms of one 128-row tile in one K stage).
 static bool encode_sf_atoms(CUtensorMap *map, const void *base, uint64_t rows, uint64_t K, uint64_t k_per_atom,
