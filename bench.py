@@ -265,8 +265,8 @@ def run_step(tcm, dev, stream, events=None):
 
 
 KERNELS_PER_STEP = 5
-# hardware-ordered metadata: ceil(M/128) * ceil(K/128) * 8192 bytes
-META_TC_BYTES = (SIZE // 128) * (SIZE // 128) * 8192
+# hardware-ordered metadata: ceil(M/128) * ceil(K/128) * 2048 bytes
+META_TC_BYTES = (SIZE // 128) * (SIZE // 128) * 2048
 GEMMS_PER_STEP = 3
 # compress (read A, write A_comp + canonical metadata) and metadata pack (read it, write meta_tc)
 COMPRESS_BYTES = SIZE * SIZE * 2 + SIZE * (SIZE // 2) * 2 + 2 * SIZE * (SIZE // 32) * 4 + META_TC_BYTES

@@ -205,18 +205,20 @@ tcm_status tcm_gemm_sp(int64_t M, int64_t N, int64_t K, tcm_dtype dtype,
  * Hardware-ordered 2:4 metadata.  "NVIDIA MMA", section "SM100：tcgen05.mma":
  * the sparse MMA reads its metadata from tensor memory; this layout is that
  * tensor-memory order (established on the GPU by a decoding probe), so the
- * kernel can copy it in with tcgen05.cp instead of assembling it.
+ * kernel moves it in with one vector load and one tensor-memory store per
+ * lane and stage instead of assembling it.
  *
- * For 128-row tile t, 128-logical-K stage kb and MMA k (logical K 32, i.e.
- * canonical word q = 4 kb + k of each row) a 2048-byte block at byte offset
- * ((t * KBS + kb) * 4 + k) * 2048, KBS = ceil(K / 128), holds for every lane
- * L = 16a + 8s + r (0 <= L < 128) at bytes 16 L .. 16 L + 3 the word
+ * For 128-row tile t and 128-logical-K stage kb a 2048-byte block at byte
+ * offset (t * KBS + kb) * 2048, KBS = ceil(K / 128), holds for every lane
+ * L = 16a + 8s + r (0 <= L < 128) at bytes 16 L + 4 k .. 16 L + 4 k + 3 the
+ * word that the stage's MMA k (logical K 32, i.e. canonical word q = 4 kb + k
+ * of each row) reads for lane L:
  *   bits  0..15 = nibbles 4s .. 4s+3 of row 128t + 16a + r's word q,
- *   bits 16..31 = the same nibbles of row 128t + 16a + 8 + r's word q,
- * and zeros at bytes 16 L + 4 .. 16 L + 15.  Rows past M and words past K/32
- * read 0x44444444 (positions {0, 1}).
+ *   bits 16..31 = the same nibbles of row 128t + 16a + 8 + r's word q.
+ * Rows past M and words past K/32 read 0x44444444 (positions {0, 1}).
  *
- * tcm_sp_meta_tc_bytes -- ceil(M/128) * ceil(K/128) * 8192; -1 if M < 0,
+ * tcm_sp_meta_tc_bytes -- ceil(M/128) * ceil(K/128) * 2048 (the size of the
+ * canonical metadata, rounded up to whole tiles and stages); -1 if M < 0,
  * K < 0 or K % 32 != 0.  Host only.
  * tcm_sp_meta_pack -- write that layout from the canonical metadata of
  * tcm_sp_compress (M x K/32 uint32, device) into meta_tc (device, 16-byte

@@ -233,14 +233,15 @@ def mx_pack_scales(SC, K, block=32, pad=127, reps=1):
 def sp_meta_pack(meta, K):
     """Hardware-ordered 2:4 metadata (the layout of ``tcm_sp_meta_pack`` in include/tcm.h) of
     canonical words ``meta`` (M x K/32 uint32), as bytes.  Plain loops over the definition:
-    block (t, kb, k), lane L = 16a + 8s + r gets bits 16s..16s+15 of row 128t+16a+r's word
+    stage (t, kb) holds 128 lanes of 16 bytes; word k of lane L = 16a + 8s + r is the word the
+    sparse MMA k of that stage reads for lane L: bits 16s..16s+15 of row 128t+16a+r's word
     q = 4kb+k in its low half and those of row 128t+16a+8+r in its high half."""
     meta = np.ascontiguousarray(meta).view(np.uint32)
     M, qn = meta.shape
     assert K % 32 == 0 and qn == K // 32
     kbs = (K + 127) // 128
     tiles = (M + 127) // 128
-    out = np.zeros(tiles * kbs * 4 * 128 * 4, dtype=np.uint32)  # 16-byte rows as 4 words
+    out = np.zeros(tiles * kbs * 128 * 4, dtype=np.uint32)  # per stage: 128 lanes x 4 words
     fill = 0x44444444
 
     def word(row, q):
@@ -248,13 +249,13 @@ def sp_meta_pack(meta, K):
 
     for t in range(tiles):
         for kb in range(kbs):
-            for k in range(4):
-                q = 4 * kb + k
-                for L in range(128):
-                    a, s, r = L // 16, (L // 8) % 2, L % 8
+            for L in range(128):
+                a, s, r = L // 16, (L // 8) % 2, L % 8
+                for k in range(4):
+                    q = 4 * kb + k
                     lo = (word(128 * t + 16 * a + r, q) >> (16 * s)) & 0xFFFF
                     hi = (word(128 * t + 16 * a + 8 + r, q) >> (16 * s)) & 0xFFFF
-                    out[(((t * kbs + kb) * 4 + k) * 128 + L) * 4] = lo | (hi << 16)
+                    out[((t * kbs + kb) * 128 + L) * 4 + k] = lo | (hi << 16)
     return out.view(np.uint8)
 
 

@@ -412,7 +412,7 @@ tcm_status tcm_sp_decompress(int64_t M, int64_t K, tcm_dtype dtype, const void *
 int64_t tcm_sp_meta_tc_bytes(int64_t M, int64_t K)
 {
     if (M < 0 || K < 0 || K % 32 != 0) return -1;
-    return ((M + 127) / 128) * ((K + 127) / 128) * 4 * 2048;
+    return ((M + 127) / 128) * ((K + 127) / 128) * 2048;
 }
 
 tcm_status tcm_sp_meta_pack(int64_t M, int64_t K, const uint32_t *meta, void *meta_tc, tcm_stream_t stream)
@@ -436,8 +436,8 @@ tcm_status tcm_gemm_sp_tc(int64_t M, int64_t N, int64_t K, tcm_dtype dtype, cons
     if (out_dtype != TCM_BF16 && out_dtype != TCM_F16 && out_dtype != TCM_F32) return TCM_ERR_UNSUPPORTED;
     if (M < 1 || N < 1 || K < 0 || K % 32 != 0) return TCM_ERR_INVALID_ARG;
     if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2) return TCM_ERR_UNSUPPORTED;
-    // metadata rows (64 of 128 bytes per stage of 128 logical K) are addressed with 32-bit coordinates
-    if (((M + 255) / 128) * ((K + 127) / 128) * 64 > INT32_MAX) return TCM_ERR_UNSUPPORTED;
+    // metadata rows (16 of 128 bytes per stage of 128 logical K) are addressed with 32-bit coordinates
+    if (((M + 255) / 128) * ((K + 127) / 128) * 16 > INT32_MAX) return TCM_ERR_UNSUPPORTED;
     if (!D || (K > 0 && (!A_comp || !meta_tc || !B)) || (beta != 0.f && !C)) return TCM_ERR_INVALID_ARG;
     const int eo = elem_bytes(out_dtype);
     if ((A_comp && !aligned16(A_comp)) || (B && !aligned16(B)) || (meta_tc && !aligned16(meta_tc)) || !aligned16(D) ||
@@ -461,13 +461,13 @@ tcm_status tcm_gemm_sp_tc(int64_t M, int64_t N, int64_t K, tcm_dtype dtype, cons
     MxMaps maps;
     std::memset(&maps, 0, sizeof maps);
     if (K > 0) {
-        // a stage's 8 KB of metadata (four 2 KB MMA blocks) is contiguous: one box of 64
+        // a stage's 2 KB of metadata (128 lanes x 16 bytes) is contiguous: one box of 16
         // rows of 128 bytes
-        const uint64_t meta_rows = static_cast<uint64_t>((M + 127) / 128) * static_cast<uint64_t>((K + 127) / 128) * 64u;
+        const uint64_t meta_rows = static_cast<uint64_t>((M + 127) / 128) * static_cast<uint64_t>((K + 127) / 128) * 16u;
         EncodeTiledFn fn = encode_fn();
         const cuuint64_t dims[2] = {128, meta_rows};
         const cuuint64_t strides[1] = {128};
-        const cuuint32_t box[2] = {128, 64};
+        const cuuint32_t box[2] = {128, 16};
         const cuuint32_t estr[2] = {1, 1};
         if (!fn || !encode_kmajor(&maps.a, A_comp, 2, static_cast<uint64_t>(K / 2), static_cast<uint64_t>(M),
                                   static_cast<uint64_t>(K / 2), 128) ||

@@ -63,11 +63,12 @@ constexpr int SF_ATOM = 512;                       // scales of 128 rows x one 1
 // metadata in the hardware order -- the "side" data of a stage is then the
 // sparse metadata instead of block scales).
 enum SideFmt : int { FMT_MX = 0, FMT_NV = 1, FMT_SP = 2 };
-// copy warps per format (lane 0 of each issues the copies e with e % n == its index)
-__host__ __device__ constexpr int mx_copy_warps(int fmt) { return fmt == FMT_NV ? 3 : 1; }
+// Side-data warps per format.  MX, NV: copy warps (lane 0 of each issues the copies e
+// with e % n == its index).  SP: one writer warp per TMEM lane quadrant (warp % 4).
+__host__ __device__ constexpr int mx_copy_warps(int fmt) { return fmt == FMT_NV ? 3 : fmt == FMT_SP ? 4 : 1; }
 // TMA, MMA, epilogue (warps 2..9), copy warps
 __host__ __device__ constexpr int mx_threads(int fmt) { return 32 * (2 + MX_EPI_WARPS + mx_copy_warps(fmt)); }
-constexpr int SP_META_STAGE = 4 * 2048; // four 128-lane x 16-byte blocks, one per MMA
+constexpr int SP_META_STAGE = 2048; // 128 lanes x 16 bytes: lane L's words for the stage's four MMAs
 
 template <int BN_CTA, int BN, int STAGES, int FMT>
 struct MxSmem {
@@ -201,52 +202,32 @@ __device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64
 // MMA, one E8M0 atom per 128 rows per stage shared by the stage's four MMAs
 // through scale-factor ids 0..3).  NV: NVFP4 (kind::mxf4nvf4.scale_vec::4X, packed
 // E2M1, K = 64 per MMA, one UE4M3 atom per 128 rows per MMA, scale-factor id 0).
-// SP: two tcgen05.cp.128x256b per stage, each moving the blocks of two MMAs
-// (lane l <- 16 bytes of block k at l*16 and 16 of block k+1, LBO 2048) to 8
-// columns, so MMA k finds its word at column 4k, a multiple of 4 as the
-// sparse MMA's metadata address requires.
+// SP: no copies; the stage's 16 columns hold MMA k's metadata word at column 4k,
+// a multiple of 4 as the sparse MMA's metadata address requires, written by the
+// writer warps with tcgen05.st.
 template <int FMT, int SFB_ATOMS>
 struct SfLayout {
     static constexpr bool NV = FMT == FMT_NV;
     static constexpr int APT = NV ? 4 : 1;             // atoms per 128-row tile per stage
-    static constexpr int NCP = FMT == FMT_SP ? 2 : APT * (1 + SFB_ATOMS);  // copies per stage
+    static constexpr int NCP = FMT == FMT_SP ? 0 : APT * (1 + SFB_ATOMS);  // copies per stage
     static constexpr uint32_t COLS = NV ? 16u + 16u * SFB_ATOMS : 16u;      // TMEM columns per stage
     // TMEM column (within the stage) of copy e: e = tile * APT + kk, tile 0 = A, 1.. = B row tiles
     __device__ static constexpr uint32_t col(int e)
     {
-        return FMT == FMT_SP ? 8u * e
-               : NV ? (e < APT ? 4u * e : 16u + 4u * SFB_ATOMS * static_cast<uint32_t>((e - APT) % APT) +
+        return NV ? (e < APT ? 4u * e : 16u + 4u * SFB_ATOMS * static_cast<uint32_t>((e - APT) % APT) +
                                              4u * static_cast<uint32_t>((e - APT) / APT))
                     : (e == 0 ? 0u : 4u + 4u * e);
     }
     // byte offset of copy e's source within the stage's side data
-    __device__ static constexpr uint32_t src(int e) { return FMT == FMT_SP ? 4096u * e : static_cast<uint32_t>(SF_ATOM) * e; }
+    __device__ static constexpr uint32_t src(int e) { return static_cast<uint32_t>(SF_ATOM) * e; }
     __device__ static constexpr uint32_t sfa(int k) { return NV ? 4u * k : 0u; }
     __device__ static constexpr uint32_t sfb(int k) { return NV ? 16u + 4u * SFB_ATOMS * k : 8u; }
 };
 
-// Shared-memory descriptor of two 128-row x 16-byte blocks 2048 bytes apart, no
-// swizzle: the source of one tcgen05.cp.128x256b (lane l <- row l of both).
-__device__ __forceinline__ uint64_t sdesc_meta_pair(uint32_t smem_addr)
-{
-    uint64_t d = 0;
-    d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
-    d |= static_cast<uint64_t>(2048 >> 4) << 16;
-    d |= static_cast<uint64_t>(128 >> 4) << 32;
-    d |= static_cast<uint64_t>(1) << 46;
-    return d;
-}
-
-template <int FMT, int CG>
+template <int CG>
 __device__ __forceinline__ void tmem_cp_side(uint32_t taddr, uint32_t smem_addr)
 {
-    if constexpr (FMT == FMT_SP) {
-        const uint64_t d = sdesc_meta_pair(smem_addr);
-        if constexpr (CG == 2) asm volatile("tcgen05.cp.cta_group::2.128x256b [%0], %1;" ::"r"(taddr), "l"(d) : "memory");
-        else asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(d) : "memory");
-    } else {
-        tmem_cp_sf<CG>(taddr, sdesc_sf_atom(smem_addr));
-    }
+    tmem_cp_sf<CG>(taddr, sdesc_sf_atom(smem_addr));
 }
 
 template <int CG>
@@ -338,7 +319,7 @@ __global__ void __launch_bounds__(mx_threads(FMT), 1)
         }
         mbar_init(drain, 1);
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(sfready + s, NCW);
+            mbar_init(sfready + s, FMT == FMT_SP ? NCW * CG : NCW); // SP: writer warps of both CTAs
             mbar_init(sfull + s, 1);
         }
         mbar_init(cdrain, NCW);
@@ -393,18 +374,19 @@ __global__ void __launch_bounds__(mx_threads(FMT), 1)
                     const uint32_t sa = sbase + L::A_OFF + stage * A_STAGE_BYTES;
                     const uint32_t sb = sbase + L::B_OFF + stage * L::B_STAGE;
                     const uint32_t ss = sbase + L::SF_OFF + stage * L::SF_STAGE;
-                    if (leader || CG == 1) {
-                        mbar_arrive_expect_tx(sfull + stage, SIDE_TX);
-                        mbar_arrive_expect_tx(full + stage, STAGE_TX);
-                    }
+                    // SP: each CTA's metadata lands on its own side-data barrier (its writer warps
+                    // wait there); scales: both CTAs' atoms on the even CTA's (its copy threads)
+                    if (FMT == FMT_SP) mbar_arrive_expect_tx(sfull + stage, L::SF_STAGE);
+                    else if (leader || CG == 1) mbar_arrive_expect_tx(sfull + stage, SIDE_TX);
+                    if (leader || CG == 1) mbar_arrive_expect_tx(full + stage, STAGE_TX);
                     // pair: both CTAs' loads complete on the even CTA's barriers (cluster addresses)
                     const uint32_t fb = CG == 2 ? full_cluster0 + static_cast<uint32_t>(stage) * 8u : 0u;
                     const uint32_t sfb = CG == 2 ? sfull_cluster0 + static_cast<uint32_t>(stage) * 8u : 0u;
                     if constexpr (FMT == FMT_SP) {
-                        // metadata: the tile's four 2 KB blocks of this stage (64 rows of 128 bytes);
-                        // compressed A: 64 kept values (128 bytes) of the stage's 128 logical K; B:
-                        // two 64-value atoms
-                        tma_ld<CG>(ss, &tmSA, sfull + stage, sfb, 0, (a_tile * p.num_kb + kb) * 64);
+                        // metadata: the tile's 2 KB block of this stage (16 rows of 128 bytes), onto
+                        // this CTA's own barrier; compressed A: 64 kept values (128 bytes) of the
+                        // stage's 128 logical K; B: two 64-value atoms
+                        tma_load_2d(ss, &tmSA, sfull + stage, 0, (a_tile * p.num_kb + kb) * 16);
                         tma_ld<CG>(sa, &tmA, full + stage, fb, kb * 64, a_row);
                         tma_ld<CG>(sb, &tmB, full + stage, fb, kb * 128, b_row);
                         tma_ld<CG>(sb + BN_CTA * TILE_K_BYTES, &tmB, full + stage, fb, kb * 128 + 64, b_row);
@@ -493,6 +475,40 @@ __global__ void __launch_bounds__(mx_threads(FMT), 1)
             else mma_commit(drain);
             wait_bar<CG>(drain, 0, w, SITE_DRAIN, false);
         }
+    } else if (FMT == FMT_SP && warp >= MX_COPY_WARP) {
+        // Metadata writer for TMEM lane quadrant warp % 4, in both CTAs of a pair (each CTA's
+        // MMA rows read their metadata from its own tensor memory): lane l loads the 16 bytes
+        // of TMEM lane 32q + l (the words of the stage's four MMAs) and stores word k at
+        // column 4k of the stage's slot.  The slot's previous readers (the MMAs of item -
+        // STAGES) completed before the producer could refill the stage's side data.
+        const int quad = warp & 3;
+        const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+        const uint32_t sfready0 = CG == 2 ? mapa_shared(smem_u32(sfready), 0) : smem_u32(sfready);
+        const int my_tiles = first_tile < p.tile_end ? (p.tile_end - 1 - first_tile) / step + 1 : 0;
+        const long long items = static_cast<long long>(my_tiles) * p.num_kb;
+        int stage = 0;
+        uint32_t phase = 0;
+        for (long long item = 0; item < items; ++item) {
+            if (!wait_bar<CG>(sfull + stage, phase, w, SITE_MMA_FULL, true)) break;
+            tc_fence_after();
+            const uint4 v = *reinterpret_cast<const uint4 *>(smem + L::SF_OFF + stage * L::SF_STAGE + (quad * 32 + lane) * 16);
+            const uint32_t t0 = tmem_base + lane_base + SF_COL + static_cast<uint32_t>(stage) * SF_STAGE_COLS;
+            tmem_st_32x32b_x1(t0, v.x);
+            tmem_st_32x32b_x1(t0 + 4u, v.y);
+            tmem_st_32x32b_x1(t0 + 8u, v.z);
+            tmem_st_32x32b_x1(t0 + 12u, v.w);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (CG == 2) mbar_arrive_cluster(sfready0 + static_cast<uint32_t>(stage) * 8u);
+                else mbar_arrive(sfready + stage);
+            }
+            if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
     } else if (warp >= MX_COPY_WARP) {
         const int cw = warp - MX_COPY_WARP; // this thread issues the copies e with e % NCW == cw
         if (lane == 0 && leader) {
@@ -509,7 +525,7 @@ __global__ void __launch_bounds__(mx_threads(FMT), 1)
                 const uint32_t s0 = tmem_base + SF_COL + static_cast<uint32_t>(stage) * SF_STAGE_COLS;
 #pragma unroll
                 for (int e = 0; e < SF::NCP; ++e)
-                    if (e % NCW == cw) tmem_cp_side<FMT, CG>(s0 + SF::col(e), ss + SF::src(e));
+                    if (e % NCW == cw) tmem_cp_side<CG>(s0 + SF::col(e), ss + SF::src(e));
                 if (CG == 2) mma_commit_pair(sfready + stage, 0x1);
                 else mma_commit(sfready + stage);
                 if (++stage == STAGES) {

@@ -164,11 +164,11 @@ cudaError_t launch_sp_decompress(int64_t M, int64_t K, int elem_bytes, const voi
 namespace tcm {
 
 // Hardware-ordered 2:4 metadata (see tcm_sp_meta_pack in tcm.h): one thread per
-// lane L of one MMA's 2 KB block.  Block (t, kb, k) holds, at byte 16 L, the word
-// the sparse MMA reads for lane L = 16a + 8s + r: bits 0..15 = nibbles 4s..4s+3 of
-// row 16a + r's word for logical K block q = 4 kb + k, bits 16..31 = the same of
-// row 16a + 8 + r; bytes 4..15 of the lane's row are 0.  Rows past M and K blocks
-// past K/32 read 0x44444444 (positions {0, 1}; their A values are zero).
+// lane L of one stage's 2 KB block.  Block (t, kb) holds, at byte 16 L + 4 k, the
+// word the stage's sparse MMA k reads for lane L = 16a + 8s + r: bits 0..15 =
+// nibbles 4s..4s+3 of row 16a + r's word for logical K block q = 4 kb + k, bits
+// 16..31 = the same of row 16a + 8 + r.  Rows past M and K blocks past K/32 read
+// 0x44444444 (positions {0, 1}; their A values are zero).
 __global__ void __launch_bounds__(256) sp_meta_pack_kernel(const uint32_t *__restrict__ meta, int64_t M,
                                                            int64_t qn, int64_t kbs, int64_t total,
                                                            uint4 *__restrict__ out)
@@ -176,25 +176,28 @@ __global__ void __launch_bounds__(256) sp_meta_pack_kernel(const uint32_t *__res
     const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (i >= total) return;
     const int64_t lane = i & 127;
-    const int64_t blk = i >> 7; // (t * kbs + kb) * 4 + k
-    const int64_t k = blk & 3;
-    const int64_t kb = (blk >> 2) % kbs;
-    const int64_t t = (blk >> 2) / kbs;
-    const int64_t q = kb * 4 + k;
+    const int64_t stage = i >> 7; // t * kbs + kb
+    const int64_t kb = stage % kbs;
+    const int64_t t = stage / kbs;
     const int64_t a = lane >> 4, s = (lane >> 3) & 1, r = lane & 7;
     const int64_t r0 = t * 128 + 16 * a + r, r1 = r0 + 8;
     const uint32_t fill = 0x44444444u;
-    const uint32_t m0 = (r0 < M && q < qn) ? __ldg(meta + r0 * qn + q) : fill;
-    const uint32_t m1 = (r1 < M && q < qn) ? __ldg(meta + r1 * qn + q) : fill;
-    const uint32_t word = s == 0 ? ((m0 & 0xFFFFu) | (m1 << 16)) : ((m0 >> 16) | (m1 & 0xFFFF0000u));
-    out[i] = make_uint4(word, 0u, 0u, 0u);
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int64_t q = kb * 4 + k;
+        const uint32_t m0 = (r0 < M && q < qn) ? __ldg(meta + r0 * qn + q) : fill;
+        const uint32_t m1 = (r1 < M && q < qn) ? __ldg(meta + r1 * qn + q) : fill;
+        w[k] = s == 0 ? ((m0 & 0xFFFFu) | (m1 << 16)) : ((m0 >> 16) | (m1 & 0xFFFF0000u));
+    }
+    out[i] = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 cudaError_t launch_sp_meta_pack(const uint32_t *meta, int64_t M, int64_t K, uint8_t *out, cudaStream_t stream)
 {
     const int64_t qn = K / 32;
     const int64_t kbs = (K + 127) / 128;
-    const int64_t total = ((M + 127) / 128) * kbs * 4 * 128;
+    const int64_t total = ((M + 127) / 128) * kbs * 128;
     if (total == 0) return cudaSuccess;
     sp_meta_pack_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, stream>>>(meta, M, qn, kbs, total,
                                                                                        reinterpret_cast<uint4 *>(out));

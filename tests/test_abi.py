@@ -149,7 +149,7 @@ def test_nvfp4_scales_bytes(lib):
 
 
 def test_sp_meta_tc_bytes_and_rejections(lib):
-    assert lib.tcm_sp_meta_tc_bytes(130, 160) == 2 * 2 * 8192
+    assert lib.tcm_sp_meta_tc_bytes(130, 160) == 2 * 2 * 2048
     assert lib.tcm_sp_meta_tc_bytes(1, 48) == -1
     assert lib.tcm_sp_meta_pack(64, 48, ALIGNED, ALIGNED, None) == 1
     assert lib.tcm_sp_meta_pack(64, 64, ALIGNED, ALIGNED + 4, None) == 3

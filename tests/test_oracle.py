@@ -596,23 +596,22 @@ def test_nvfp4_matches_numpy_expansion():
 def test_sp_meta_pack_hand_worked():
     """16 rows, K = 32: one canonical word per row, one stage, MMA 0 only; positions worked by hand."""
     meta = np.array([0xA0A1A2A3 + 0x01010101 * r for r in range(16)], dtype=np.uint32).reshape(16, 1)
-    out = oracle.sp_meta_pack(meta, 32).view(np.uint32).reshape(4, 128, 4)  # (MMA k, lane, word)
-    assert out.shape == (4, 128, 4)
-    assert out[0, 0, 0] == (0xA2A3 | (0xAAAB << 16))          # lane 0: low halves of rows 0 and 8
-    assert out[0, 8, 0] == (0xA0A1 | (0xA8A9 << 16))          # lane 8: high halves of rows 0 and 8
-    assert out[0, 3, 0] == (0xA5A6 | (0xADAE << 16))          # lane 3: rows 3 and 11
-    assert out[0, 15, 0] == (0xA7A8 | (0xAFB0 << 16))         # lane 15: high halves of rows 7 and 15
-    assert np.all(out[0, :, 1:] == 0)                          # bytes 4..15 of every lane are zero
-    assert np.all(out[0, 16:, 0] == 0x44444444)                # rows >= 16 read positions {0, 1}
-    assert np.all(out[1:, :, 0] == 0x44444444)                 # words past K/32
+    out = oracle.sp_meta_pack(meta, 32).view(np.uint32).reshape(128, 4)  # (lane, MMA k)
+    assert out[0, 0] == (0xA2A3 | (0xAAAB << 16))          # lane 0: low halves of rows 0 and 8
+    assert out[8, 0] == (0xA0A1 | (0xA8A9 << 16))          # lane 8: high halves of rows 0 and 8
+    assert out[3, 0] == (0xA5A6 | (0xADAE << 16))          # lane 3: rows 3 and 11
+    assert out[15, 0] == (0xA7A8 | (0xAFB0 << 16))         # lane 15: high halves of rows 7 and 15
+    assert np.all(out[16:, 0] == 0x44444444)                # rows >= 16 read positions {0, 1}
+    assert np.all(out[:, 1:] == 0x44444444)                 # MMAs 1..3: words past K/32
 
 
 @pytest.mark.parametrize("M,K", [(128, 128), (130, 96), (300, 512)])
 def test_sp_meta_pack_reads_back_to_the_canonical_words(M, K):
     g = np.random.default_rng(M + K)
     meta = g.integers(0, 2 ** 32, (M, K // 32), dtype=np.uint64).astype(np.uint32)
-    words = oracle.sp_meta_pack(meta, K).view(np.uint32).reshape(-1, 4)[:, 0]
+    words = oracle.sp_meta_pack(meta, K).view(np.uint32)
     kbs = (K + 127) // 128
+    assert words.size == ((M + 127) // 128) * kbs * 128 * 4
     back = np.zeros_like(meta)
     for R in range(M):
         t, i = divmod(R, 128)
@@ -620,9 +619,9 @@ def test_sp_meta_pack_reads_back_to_the_canonical_words(M, K):
         half = 16 * (rr // 8)         # rows 16a+8.. sit in the high halves
         r = rr % 8
         for q in range(K // 32):
-            base = ((t * kbs + q // 4) * 4 + q % 4) * 128
-            lo = (int(words[base + 16 * a + r]) >> half) & 0xFFFF        # lane s = 0: nibbles 0..3
-            hi = (int(words[base + 16 * a + 8 + r]) >> half) & 0xFFFF    # lane s = 1: nibbles 4..7
+            base = (t * kbs + q // 4) * 128
+            lo = (int(words[(base + 16 * a + r) * 4 + q % 4]) >> half) & 0xFFFF      # lane s = 0: nibbles 0..3
+            hi = (int(words[(base + 16 * a + 8 + r) * 4 + q % 4]) >> half) & 0xFFFF  # lane s = 1: nibbles 4..7
             back[R, q] = lo | (hi << 16)
     assert np.array_equal(back, meta)
 
