@@ -1,7 +1,9 @@
-// tcm_gemm_mx.cu -- block-scaled FP8 GEMM (MXFP8: E4M3/E5M2 elements, one E8M0
-// scale per 32 consecutive K elements of every row of A and of B) on
-// tcgen05.mma.kind::mxf8f6f4.block_scale, and the packing of row-major scales
-// into the blocked layout the kernel reads.
+// tcm_gemm_mx.cu -- block-scaled GEMM (MXFP8: E4M3/E5M2 elements, one E8M0
+// scale per 32 consecutive K elements of every row of A and of B, on
+// tcgen05.mma.kind::mxf8f6f4.block_scale; NVFP4: packed E2M1 with UE4M3 scales
+// per 16, on kind::mxf4nvf4.block_scale.scale_vec::4X), the same pipeline with
+// 2:4-sparse A and hardware-ordered metadata (tcgen05.mma.sp), and the packing
+// of row-major scales into the blocked layout the kernel reads.
 //
 // "NVIDIA MMA", section "SM100：tcgen05.mma": the block-scaled form reads the
 // scales of A and B from tensor memory ([scale-A-tmem], [scale-B-tmem]) and
@@ -32,8 +34,10 @@
 //
 // Pipeline: the dense kernel's (TMA ring of 128-byte K stages = 128 FP8 values,
 // four MMAs of K = 32 per stage, one thread issuing, TMEM accumulators).  The
-// same TMA producer loads the stage's scale atoms first, onto a barrier of
-// their own (sfull), then A and B onto the stage's full barrier.  Copy threads
+// same TMA producer loads the stage's scale atoms first (in 128-byte rows: the
+// atoms are contiguous, and 16-byte rows made hundreds of small TMA requests per
+// stage), onto a barrier of their own (sfull), then A and B onto the stage's full
+// barrier.  Copy threads
 // (lane 0 of warps MX_COPY_WARP ..) copy the atoms to tensor memory
 // (tcgen05.cp) as soon as they land, while A and B are still in flight, and
 // commit their copies to the stage's sfready barrier; the MMA thread waits on
@@ -44,7 +48,9 @@
 // the copies between its MMAs: NVFP4 2913 -> 4605 TFLOP/s, MXFP8 2597 -> 2843.
 // The scale columns of a stage are rewritten only after the stage's sfull
 // barrier has completed again, which the producer allows only after the MMAs
-// that read them have finished.
+// that read them have finished.  The sparse format has no copies: four writer
+// warps per CTA, one per TMEM lane quadrant, store each stage's compact
+// metadata with tcgen05.st (see FMT_SP below).
 //
 // One accumulator of 256 columns fills half of tensor memory and the scale
 // columns take part of the rest, so a 256-wide tile has a single accumulator
@@ -56,7 +62,7 @@
 namespace tcm {
 
 constexpr int MX_EPI_WARPS = 8; // two per TMEM lane quadrant, half the columns each
-constexpr int MX_COPY_WARP = 2 + MX_EPI_WARPS; // first copy warp
+constexpr int MX_COPY_WARP = 2 + MX_EPI_WARPS; // first side-data (copy or writer) warp
 constexpr int SF_ATOM = 512;                       // scales of 128 rows x one 128-value K stage
 
 // Formats of the kernel: MX (MXFP8), NV (NVFP4), SP (2:4-sparse bf16/fp16 A,
