@@ -365,7 +365,8 @@ inline cudaError_t launch_one(const CUtensorMap &a, const CUtensorMap &b, const 
 {
     using L = Smem<BN / CG, STAGES, (KS - 1) * BM * BN * 4, KATOMS>;
     auto kern = gemm_kernel<KIND, BN, STAGES, CG, KS, KATOMS>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+    static std::atomic<unsigned long long> smem_limit_set{0};
+    cudaError_t e = ensure_max_smem(reinterpret_cast<const void *>(kern), L::ALLOC, smem_limit_set);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);

@@ -639,7 +639,8 @@ static cudaError_t launch_mx_one(const MxMaps &m, const GemmParams &p, int grid,
     using L = MxSmem<BN / CG, BN, STAGES, FMT>;
     auto kern = gemm_mx_kernel<BN, STAGES, NACC, CG, FMT>;
     static_assert(mx_threads(FMT) <= 1024, "block size");
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+    static std::atomic<unsigned long long> smem_limit_set{0};
+    cudaError_t e = ensure_max_smem(reinterpret_cast<const void *>(kern), L::ALLOC, smem_limit_set);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);

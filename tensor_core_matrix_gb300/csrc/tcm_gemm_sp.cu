@@ -374,7 +374,8 @@ static cudaError_t launch_sp_one(const CUtensorMap &a, const CUtensorMap &b, con
 {
     using L = SpSmem<BN / CG, STAGES>;
     auto kern = gemm_sp_kernel<BN, STAGES, CG, NACC>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+    static std::atomic<unsigned long long> smem_limit_set{0};
+    cudaError_t e = ensure_max_smem(reinterpret_cast<const void *>(kern), L::ALLOC, smem_limit_set);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);

@@ -5,6 +5,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstdint>
+#include <atomic>
 
 namespace tcm {
 
@@ -107,5 +108,19 @@ cudaError_t launch_sp_decompress(int64_t M, int64_t K, int elem_bytes, const voi
                                  int64_t lda, cudaStream_t stream);
 
 int *device_status_ptr(); // address of this device's status words (per current device)
+
+// Raise a kernel's dynamic shared-memory limit once per device instead of on every
+// launch; `done` is the launching function's own flag word (bit d = device d, d < 64).
+inline cudaError_t ensure_max_smem(const void *kern, int bytes, std::atomic<unsigned long long> &done)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
 
 } // namespace tcm
