@@ -169,8 +169,9 @@ namespace tcm {
 // nibbles 4s..4s+3 of row 16a + r's word for logical K block q = 4 kb + k, bits
 // 16..31 = the same of row 16a + 8 + r.  Rows past M and K blocks past K/32 read
 // 0x44444444 (positions {0, 1}; their A values are zero).
+// vec: every row holds whole stages of 4 words (qn % 4 == 0) at a 16-byte-aligned base.
 __global__ void __launch_bounds__(256) sp_meta_pack_kernel(const uint32_t *__restrict__ meta, int64_t M,
-                                                           int64_t qn, int64_t kbs, int64_t total,
+                                                           int64_t qn, int64_t kbs, int64_t total, bool vec,
                                                            uint4 *__restrict__ out)
 {
     const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -182,14 +183,24 @@ __global__ void __launch_bounds__(256) sp_meta_pack_kernel(const uint32_t *__res
     const int64_t a = lane >> 4, s = (lane >> 3) & 1, r = lane & 7;
     const int64_t r0 = t * 128 + 16 * a + r, r1 = r0 + 8;
     const uint32_t fill = 0x44444444u;
+    const int64_t q0 = kb * 4;
+    uint32_t m0[4], m1[4];
+    if (vec) { // the stage's four words of each row in one 16-byte load
+        const uint4 v0 = r0 < M ? __ldg(reinterpret_cast<const uint4 *>(meta + r0 * qn + q0)) : make_uint4(fill, fill, fill, fill);
+        const uint4 v1 = r1 < M ? __ldg(reinterpret_cast<const uint4 *>(meta + r1 * qn + q0)) : make_uint4(fill, fill, fill, fill);
+        m0[0] = v0.x; m0[1] = v0.y; m0[2] = v0.z; m0[3] = v0.w;
+        m1[0] = v1.x; m1[1] = v1.y; m1[2] = v1.z; m1[3] = v1.w;
+    } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            m0[k] = (r0 < M && q0 + k < qn) ? __ldg(meta + r0 * qn + q0 + k) : fill;
+            m1[k] = (r1 < M && q0 + k < qn) ? __ldg(meta + r1 * qn + q0 + k) : fill;
+        }
+    }
     uint32_t w[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const int64_t q = kb * 4 + k;
-        const uint32_t m0 = (r0 < M && q < qn) ? __ldg(meta + r0 * qn + q) : fill;
-        const uint32_t m1 = (r1 < M && q < qn) ? __ldg(meta + r1 * qn + q) : fill;
-        w[k] = s == 0 ? ((m0 & 0xFFFFu) | (m1 << 16)) : ((m0 >> 16) | (m1 & 0xFFFF0000u));
-    }
+    for (int k = 0; k < 4; ++k)
+        w[k] = s == 0 ? ((m0[k] & 0xFFFFu) | (m1[k] << 16)) : ((m0[k] >> 16) | (m1[k] & 0xFFFF0000u));
     out[i] = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
@@ -199,7 +210,8 @@ cudaError_t launch_sp_meta_pack(const uint32_t *meta, int64_t M, int64_t K, uint
     const int64_t kbs = (K + 127) / 128;
     const int64_t total = ((M + 127) / 128) * kbs * 128;
     if (total == 0) return cudaSuccess;
-    sp_meta_pack_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, stream>>>(meta, M, qn, kbs, total,
+    const bool vec = qn % 4 == 0 && (reinterpret_cast<uintptr_t>(meta) & 15u) == 0;
+    sp_meta_pack_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, stream>>>(meta, M, qn, kbs, total, vec,
                                                                                        reinterpret_cast<uint4 *>(out));
     return cudaGetLastError();
 }
