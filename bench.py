@@ -553,38 +553,46 @@ def main():
     if args.e2e_steps > 0:
         sets = [dev, {k: torch.empty_like(v) for k, v in dev.items()}]
         s_in, s_out = torch.cuda.Stream(device=device), torch.cuda.Stream(device=device)
-        ev_in = [torch.cuda.Event() for _ in range(args.e2e_steps)]
-        ev_comp = [torch.cuda.Event() for _ in range(args.e2e_steps)]
-        ev_out = [torch.cuda.Event() for _ in range(args.e2e_steps)]
+
+        def e2e_steps(n):
+            """n pipelined end-to-end steps; returns their total time in ms (s_in start to s_out end)."""
+            ev_in = [torch.cuda.Event() for _ in range(n)]
+            ev_comp = [torch.cuda.Event() for _ in range(n)]
+            ev_out = [torch.cuda.Event() for _ in range(n)]
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(s_in)
+            for i in range(n):
+                d = sets[i % 2]
+                with torch.cuda.stream(s_in):
+                    if i >= 2:
+                        s_in.wait_event(ev_comp[i - 2])  # the GEMMs of step i-2 finished reading this set
+                    for k in pinned:
+                        d[k].copy_(pinned[k], non_blocking=True)
+                    ev_in[i].record(s_in)
+                with torch.cuda.stream(stream):
+                    stream.wait_event(ev_in[i])
+                    if i >= 2:
+                        stream.wait_event(ev_out[i - 2])  # results of step i-2 copied out of this set
+                    run_step(tcm, d, stream)
+                    ev_comp[i].record(stream)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(ev_comp[i])
+                    for k in outs[i % 2]:
+                        outs[i % 2][k].copy_(d[k], non_blocking=True)
+                    ev_out[i].record(s_out)
+            s_out.wait_event(ev_out[-1])
+            e1.record(s_out)
+            e1.synchronize()
+            return e0.elapsed_time(e1)
+
+        # untimed warm-up of the copy path: after the seconds-long device-only loop above, the
+        # first host copies run far slower (measured: 111 ms for one step's 671 MB in)
+        e2e_steps(max(8, args.warmup))
         if pg:
             pg.barrier()
         torch.cuda.synchronize(device)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(s_in)
-        for i in range(args.e2e_steps):
-            d = sets[i % 2]
-            with torch.cuda.stream(s_in):
-                if i >= 2:
-                    s_in.wait_event(ev_comp[i - 2])  # the GEMMs of step i-2 finished reading this set
-                for k in pinned:
-                    d[k].copy_(pinned[k], non_blocking=True)
-                ev_in[i].record(s_in)
-            with torch.cuda.stream(stream):
-                stream.wait_event(ev_in[i])
-                if i >= 2:
-                    stream.wait_event(ev_out[i - 2])  # results of step i-2 copied out of this set
-                run_step(tcm, d, stream)
-                ev_comp[i].record(stream)
-            with torch.cuda.stream(s_out):
-                s_out.wait_event(ev_comp[i])
-                for k in outs[i % 2]:
-                    outs[i % 2][k].copy_(d[k], non_blocking=True)
-                ev_out[i].record(s_out)
-        s_out.wait_event(ev_out[-1])
-        e1.record(s_out)
-        e1.synchronize()
-        e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+        e2e_ms = e2e_steps(args.e2e_steps) / args.e2e_steps
 
     elapsed_ms, e2e_max = slowest_rank(pg, [elapsed_ms, e2e_ms or 0.0], device)
 
@@ -629,7 +637,8 @@ def main():
         if e2e_ms:
             line["e2e"] = {"value": whole_job_rate(world, flop_step, e2e_max * 1e-3) / 1e12, "unit": "TFLOP/s",
                            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                           "note": f"{args.e2e_steps} steps; every step copies all inputs in from pinned host "
+                           "note": f"{args.e2e_steps} steps after {max(8, args.warmup)} untimed ones; every step "
+                                   f"copies all inputs in from pinned host "
                                    f"memory and all three D out; copies overlap the GEMMs of neighbouring steps; "
                                    f"pinned buffers allocated from "
                                    f"{'GPU-local CPUs ' + str(len(local)) if local else 'the default CPU set'}"}
