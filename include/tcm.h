@@ -366,12 +366,15 @@ void tcm_set_config_override(int cta_group, int tile_n, int stages, int group_m,
 
 /*
  * Test hook for the device-side failure path: with mask bit 1 set, the next
- * dense GEMM launch (only that one) has its loader skip the first shared-
- * memory stage, so the waits for that stage run out after the time limit
- * (tcm_set_timeout_ns): the kernel records TCM_ERR_TIMEOUT at the site of the
- * first wait to give up (2, the MMA issuer, or 4, the epilogue waiting for
- * the same tile), winds down and returns.  D is left partly unwritten.  No memory outside
- * the kernel's own buffers is touched.
+ * GEMM launch of tcm_gemm / tcm_gemm_ex / tcm_gemm_fused, tcm_gemm_mx,
+ * tcm_gemm_nvfp4 or tcm_gemm_sp_tc (only that one) has its loader skip the
+ * first shared-memory stage, so the waits for that stage run out after the
+ * time limit (tcm_set_timeout_ns): the kernel records TCM_ERR_TIMEOUT at the
+ * site of the first wait to give up (2: the MMA issuer or a side-data thread
+ * waiting for data; 4: the epilogue waiting for the same tile; 6: the MMA
+ * issuer waiting for the stage's scales or metadata in tensor memory), winds
+ * down and returns.  D is left partly unwritten.  No memory outside the
+ * kernel's own buffers is touched.
  */
 void tcm_debug_fail_next_launch(int mask);
 

@@ -507,7 +507,7 @@ tcm_status tcm_gemm_sp_tc(int64_t M, int64_t N, int64_t K, tcm_dtype dtype, cons
     p.timeout_ns = timeout_ns();
     p.status = device_status_ptr();
     if (!p.status) return TCM_ERR_CUDA;
-    p.fault_inject = 0;
+    p.fault_inject = g_fault_once.exchange(0);
     const int64_t clusters = sms / cfg.cta_group;
     const int grid = static_cast<int>((p.num_tiles < clusters ? p.num_tiles : clusters) * cfg.cta_group);
     const cudaError_t e = launch_gemm_mx(cfg, maps, p, grid, reinterpret_cast<cudaStream_t>(stream));
@@ -679,7 +679,7 @@ static tcm_status block_scaled_impl(bool nv, int64_t M, int64_t N, int64_t K, tc
     p.timeout_ns = timeout_ns();
     p.status = device_status_ptr();
     if (!p.status) return TCM_ERR_CUDA;
-    p.fault_inject = 0;
+    p.fault_inject = g_fault_once.exchange(0);
     const int64_t clusters = sms / cfg.cta_group;
     const int grid = static_cast<int>((p.num_tiles < clusters ? p.num_tiles : clusters) * cfg.cta_group);
     const cudaError_t e = launch_gemm_mx(cfg, maps, p, grid, reinterpret_cast<cudaStream_t>(stream));

@@ -380,6 +380,15 @@ __global__ void __launch_bounds__(mx_threads(FMT), 1)
                     const uint32_t sa = sbase + L::A_OFF + stage * A_STAGE_BYTES;
                     const uint32_t sb = sbase + L::B_OFF + stage * L::B_STAGE;
                     const uint32_t ss = sbase + L::SF_OFF + stage * L::SF_STAGE;
+                    // test hook: the first stage is never issued nor announced, so its waits run out
+                    if ((p.fault_inject & FAULT_SKIP_FIRST_LOAD) && issued == 0) {
+                        ++issued;
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                        continue;
+                    }
                     // SP: each CTA's metadata lands on its own side-data barrier (its writer warps
                     // wait there); scales: both CTAs' atoms on the even CTA's (its copy threads)
                     if (FMT == FMT_SP) mbar_arrive_expect_tx(sfull + stage, L::SF_STAGE);
@@ -422,6 +431,8 @@ __global__ void __launch_bounds__(mx_threads(FMT), 1)
                     wait_bar<CG>(sfull + s, last, w, SITE_DRAIN, false);
                     wait_bar<CG>(full + s, last, w, SITE_DRAIN, false);
                 } else {
+                    // SP: this CTA's metadata lands on its own side-data barrier
+                    if (FMT == FMT_SP) wait_bar<CG>(sfull + s, last, w, SITE_DRAIN, false);
                     wait_bar<CG>(empty + s, last, w, SITE_DRAIN, false);
                 }
             }
