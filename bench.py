@@ -419,7 +419,7 @@ def run_shapes(args, tcm, device, peaks_used):
             launch = lambda: tcm.tcm_gemm_fused(A, B, D, act=case["fused"], d_scale=d_scale, amax=amax, **kw)
         else:
             launch = lambda: tcm.tcm_gemm_ex(A, B, D, **kw)
-        for _ in range(3):
+        for _ in range(5):
             launch()
         in_bytes_total = sum(t.numel() * t.element_size() for t in (A, B) if t is not None)
         needs_flush = in_bytes_total < L2_BYTES  # inputs larger than L2 are not flushed
@@ -433,8 +433,19 @@ def run_shapes(args, tcm, device, peaks_used):
             e1.record(stream)
             e1.synchronize()
             times.append(e0.elapsed_time(e1))
-        ms_b2b = None
+        ms_b2b = ms_flushed = None
         if not needs_flush:
+            # also with L2 flushed before each launch (the inputs exceed L2, so this changes little)
+            flushed = []
+            for _ in range(args.shape_iters):
+                flush.fill_(1)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                launch()
+                e1.record(stream)
+                e1.synchronize()
+                flushed.append(e0.elapsed_time(e1))
+            ms_flushed = statistics.median(flushed)
             # the same launches back to back (inputs exceed L2 anyway): the host-side cost of
             # each call (tensor maps, launch) overlaps the previous kernel instead of adding to it
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -456,8 +467,8 @@ def run_shapes(args, tcm, device, peaks_used):
         line = {"kind": "shape", "workload": name, "M": M, "N": N, "K": K, "ms_median": ms, "ms_min": min(times),
                 "tflops": tf, "frac_of_tensor_peak": tf / peak, "algorithmic_bytes": byts, "gbs": gbs,
                 "frac_of_hbm": gbs / hbm_peak, "bound": "hbm" if M <= 64 else "tensor", "device_status": code,
-                "ms_back_to_back": ms_b2b,
-                "timing": f"median of {args.shape_iters} launches, each synchronised; " + (
+                "ms_back_to_back": ms_b2b, "ms_median_l2_flushed": ms_flushed,
+                "timing": f"5 warm-up launches, then the median of {args.shape_iters} launches, each synchronised; " + (
                     "L2 flushed (256 MiB write) before each" if needs_flush else "inputs larger than L2, no flush"),
                 "peak_source": src}
         print(json.dumps(line), flush=True)
