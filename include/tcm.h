@@ -76,7 +76,8 @@ typedef enum {
  * (D_{m,n} = sum_k A_{m,k} B_{k,n} + C_{m,n}); accumulation in fp32 as in
  * section "输入/累加/输出"; the output cast is round-to-nearest-even.
  *
- *  M, N, K    problem size; M, N >= 1, K >= 0 (K == 0 gives beta*C).
+ *  M, N, K    problem size; M, N >= 1, K >= 0 (K == 0 gives beta*C; A and B
+ *             are then not read, and their pointers are not checked).
  *  in_dtype   TCM_BF16 or TCM_F16 for both A and B (the FP8 types go
  *             through tcm_gemm_ex, which carries their scales).
  *  A          M x K, row-major, leading dimension K (densely packed).
@@ -193,8 +194,13 @@ tcm_status tcm_sp_decompress(int64_t M, int64_t K, tcm_dtype dtype,
  * "NVIDIA MMA", section "稠密乘法与 2:4 结构化稀疏乘法": only A is compressed;
  * B, C and D are dense; shapes are stated on the logical K.
  *  dtype      TCM_BF16 or TCM_F16 (A_comp and B); K % 32 == 0.
- *  A_comp     M x K/2 row-major, meta M x K/32 uint32 (as tcm_sp_compress).
+ *  A_comp     M x K/2 row-major, meta M x K/32 uint32 (as tcm_sp_compress),
+ *             both 16-byte aligned.
  *  B, C, D    as in tcm_gemm.
+ * The kernel reads `meta` in this canonical layout and puts each stage's words
+ * into the sparse MMA's tensor-memory order itself (the order described below
+ * for tcm_sp_meta_pack), so no second metadata buffer is needed; the result is
+ * bit-identical to tcm_gemm_sp_tc on the packed copy of the same metadata.
  */
 tcm_status tcm_gemm_sp(int64_t M, int64_t N, int64_t K, tcm_dtype dtype,
                        const void *A_comp, const uint32_t *meta, const void *B,
@@ -331,7 +337,9 @@ tcm_status tcm_nvfp4_pack_scales(int64_t rows, int64_t K, const uint8_t *scales,
  * *code = TCM_OK or TCM_ERR_TIMEOUT, *site = which pipeline wait gave up
  * (1 = loader waiting for a free stage, 2 = MMA issuer waiting for data,
  * 3 = MMA issuer waiting for a free accumulator, 4 = epilogue waiting for
- * an accumulator, 5 = drain at exit).  Returns TCM_ERR_CUDA if the
+ * an accumulator, 5 = drain at exit, 6 = MMA issuer waiting for a stage's
+ * scales or sparse metadata, 7 = sparse metadata writer waiting for a free
+ * stage).  Returns TCM_ERR_CUDA if the
  * synchronisation itself failed.  Either output pointer may be NULL.
  */
 tcm_status tcm_get_device_status(tcm_stream_t stream, int32_t *code, int32_t *site);
@@ -367,12 +375,13 @@ void tcm_set_config_override(int cta_group, int tile_n, int stages, int group_m,
 /*
  * Test hook for the device-side failure path: with mask bit 1 set, the next
  * GEMM launch of tcm_gemm / tcm_gemm_ex / tcm_gemm_fused, tcm_gemm_mx,
- * tcm_gemm_nvfp4 or tcm_gemm_sp_tc (only that one) has its loader skip the
- * first shared-memory stage, so the waits for that stage run out after the
- * time limit (tcm_set_timeout_ns): the kernel records TCM_ERR_TIMEOUT at the
+ * tcm_gemm_nvfp4, tcm_gemm_sp or tcm_gemm_sp_tc (only that one) has its loader
+ * skip the first shared-memory stage, so the waits for that stage run out after
+ * the time limit (tcm_set_timeout_ns): the kernel records TCM_ERR_TIMEOUT at the
  * site of the first wait to give up (2: the MMA issuer or a side-data thread
  * waiting for data; 4: the epilogue waiting for the same tile; 6: the MMA
- * issuer waiting for the stage's scales or metadata in tensor memory), winds
+ * issuer waiting for the stage's scales or metadata in tensor memory; 7: a
+ * metadata writer of tcm_gemm_sp waiting for a stage's previous MMAs), winds
  * down and returns.  D is left partly unwritten.  No memory outside the
  * kernel's own buffers is touched.
  */

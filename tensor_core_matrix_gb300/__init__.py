@@ -120,10 +120,78 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
 
-def _row_pitch(t, name):
-    if t.dim() != 2 or t.stride(1) != 1:
-        raise ValueError(f"{name} must be a 2-D tensor with unit column stride")
-    return t.stride(0)
+# ------------------------------------------------------------------ argument checks
+# Every wrapper checks shapes, dtypes and layouts first and device placement last,
+# before anything reaches the library: the C ABI receives raw pointers and pitches
+# and cannot tell a host pointer or an undersized buffer from a valid one.
+
+F16_TYPES = (torch.bfloat16, torch.float16)
+F8_TYPES = (torch.float8_e4m3fn, torch.float8_e5m2)
+OUT_TYPES = (torch.bfloat16, torch.float16, torch.float32)
+INDEX_TYPES = tuple(t for t in (torch.int32, getattr(torch, "uint32", None)) if t is not None)
+
+
+def _mat(t, name, rows=None, cols=None, dtypes=None, contiguous=False):
+    """``t`` must be a 2-D tensor of shape (rows, cols) (None: any) with unit column
+    stride and a row pitch >= its row length, densely packed if ``contiguous``."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
+    if t.dim() != 2:
+        raise ValueError(f"{name} must be 2-D, got shape {tuple(t.shape)}")
+    if (rows is not None and t.shape[0] != rows) or (cols is not None and t.shape[1] != cols):
+        want = f"{'any' if rows is None else rows} x {'any' if cols is None else cols}"
+        raise ValueError(f"{name} must be {want}, got {t.shape[0]} x {t.shape[1]}")
+    if dtypes is not None and t.dtype not in dtypes:
+        raise ValueError(f"{name}: dtype {t.dtype} not accepted here (expected one of {list(dtypes)})")
+    if contiguous:
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous (rows densely packed)")
+    elif t.stride(1) != 1 or t.stride(0) < t.shape[1]:
+        raise ValueError(f"{name} must have unit column stride and a row pitch >= its row length")
+    return t
+
+
+def _vec(t, name, n, dtypes):
+    """``t`` must hold exactly ``n`` contiguous elements of one of ``dtypes``."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
+    if t.numel() != n or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous tensor of {n} elements, got shape {tuple(t.shape)}")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name}: dtype {t.dtype} not accepted here (expected one of {list(dtypes)})")
+    return t
+
+
+def _scalar(t, name):
+    """``t``: None or a tensor whose first element is the fp32 value the kernel reads."""
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or t.numel() < 1 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous fp32 tensor of at least one element")
+    return t
+
+
+def _bytes(t, name, nbytes):
+    """``t`` must be a contiguous uint8 tensor of at least ``nbytes`` bytes."""
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.uint8 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous uint8 tensor")
+    if t.numel() < nbytes:
+        raise ValueError(f"{name} holds {t.numel()} bytes, {nbytes} needed")
+    return t
+
+
+def _on_device(**named):
+    """Every given tensor must live in device memory of the current CUDA device."""
+    cur = None
+    for name, t in named.items():
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor (device memory), got device {t.device}")
+        if cur is None:
+            cur = torch.cuda.current_device()
+        if t.device.index != cur:
+            raise ValueError(f"{name} is on {t.device} but the current device is cuda:{cur}")
 
 
 def _code(t, name):
@@ -139,13 +207,24 @@ TCM_E2M1 = 5
 def _operand(t, fmt, name):
     """(dtype code, element columns, pitch in elements) of a GEMM operand; fmt="e2m1"
     marks a uint8 tensor of packed FP4 (two elements per byte)."""
+    _mat(t, name)
     if fmt == "e2m1":
         if t.dtype != torch.uint8:
             raise ValueError(f"{name}: packed E2M1 operands are uint8 tensors")
-        return TCM_E2M1, 2 * t.shape[1], 2 * _row_pitch(t, name)
+        return TCM_E2M1, 2 * t.shape[1], 2 * t.stride(0)
     if fmt is not None:
         raise ValueError(f"{name}: unknown format {fmt!r}")
-    return _code(t, name), t.shape[1], _row_pitch(t, name)
+    if t.dtype not in F16_TYPES + F8_TYPES:
+        raise ValueError(f"{name}: unsupported operand dtype {t.dtype}")
+    return _code(t, name), t.shape[1], t.stride(0)
+
+
+def _epilogue_args(D, C, bias, M, N, out_types, bias_types):
+    _mat(D, "D", M, N, out_types)
+    if C is not None:
+        _mat(C, "C", M, N, (D.dtype,))
+    if bias is not None:
+        _vec(bias, "bias", N, bias_types)
 
 
 def tcm_gemm_ex(A, B, D, *, C=None, alpha=1.0, beta=0.0, a_scale=None, b_scale=None, bias=None, stream=None,
@@ -153,19 +232,23 @@ def tcm_gemm_ex(A, B, D, *, C=None, alpha=1.0, beta=0.0, a_scale=None, b_scale=N
     """D = alpha * a_scale * b_scale * (A @ B_stored.T) + beta * C + bias.
 
     A: M x K (row-major, pitch = A.stride(0)); B: N x K (K-major storage of
-    the K x N operand); C, D: M x N; bias: N; a_scale, b_scale: one-element
-    fp32 CUDA tensors or None.  a_fmt / b_fmt = "e2m1": that operand is a
-    uint8 tensor of packed FP4 (M x K/2 or N x K/2 bytes).
+    the K x N operand); C, D: M x N (C of D's dtype); bias: N elements of D's
+    dtype; a_scale, b_scale: one-element fp32 CUDA tensors or None.
+    a_fmt / b_fmt = "e2m1": that operand is a uint8 tensor of packed FP4
+    (M x K/2 or N x K/2 bytes).
     """
-    lib = load_library()
     ca, K, lda = _operand(A, a_fmt, "A")
     cb, Kb, ldb = _operand(B, b_fmt, "B")
     M, N = A.shape[0], B.shape[0]
-    if Kb != K or tuple(D.shape) != (M, N):
-        raise ValueError("shape mismatch")
+    if Kb != K:
+        raise ValueError(f"A has K = {K}, B has K = {Kb}")
+    _epilogue_args(D, C, bias, M, N, OUT_TYPES, (D.dtype,))
+    _scalar(a_scale, "a_scale"), _scalar(b_scale, "b_scale")
+    _on_device(A=A, B=B, D=D, C=C, bias=bias, a_scale=a_scale, b_scale=b_scale)
+    lib = load_library()
     st = lib.tcm_gemm_ex(M, N, K, ca, _ptr(A), lda, cb, _ptr(B),
-                         ldb, _ptr(C), _row_pitch(C, "C") if C is not None else 0,
-                         _ptr(D), _row_pitch(D, "D"), _code(D, "D"), float(alpha), float(beta),
+                         ldb, _ptr(C), C.stride(0) if C is not None else 0,
+                         _ptr(D), D.stride(0), _code(D, "D"), float(alpha), float(beta),
                          _ptr(a_scale), _ptr(b_scale), _ptr(bias), _stream(stream))
     _check(st, "tcm_gemm_ex")
     return D
@@ -176,19 +259,25 @@ def tcm_gemm_fused(A, B, D, *, C=None, alpha=1.0, beta=0.0, a_scale=None, b_scal
     """y = act(alpha * a_scale * b_scale * (A @ B_stored.T) + beta * C + bias); D = y / d_scale in D's
     dtype (FP8 outputs saturate); amax (one-element fp32 CUDA tensor or None) receives max |y|.
 
-    act: None/"none", "relu" or "gelu"; d_scale: one-element fp32 CUDA tensor or None (FP8 D only).
+    act: None/"none", "relu" or "gelu"; d_scale: one-element fp32 CUDA tensor or None (FP8 D only);
+    bias: N elements, bf16 for an FP8 D, else D's dtype.
     """
-    lib = load_library()
     ca, K, lda = _operand(A, a_fmt, "A")
     cb, Kb, ldb = _operand(B, b_fmt, "B")
     M, N = A.shape[0], B.shape[0]
-    if Kb != K or tuple(D.shape) != (M, N):
-        raise ValueError("shape mismatch")
+    if Kb != K:
+        raise ValueError(f"A has K = {K}, B has K = {Kb}")
     if act not in ACT_CODE:
         raise ValueError(f"unknown activation {act!r}")
+    out8 = D.dtype in F8_TYPES
+    _epilogue_args(D, C, bias, M, N, OUT_TYPES + F8_TYPES, (torch.bfloat16,) if out8 else (D.dtype,))
+    for name, t in (("a_scale", a_scale), ("b_scale", b_scale), ("d_scale", d_scale), ("amax", amax)):
+        _scalar(t, name)
+    _on_device(A=A, B=B, D=D, C=C, bias=bias, a_scale=a_scale, b_scale=b_scale, d_scale=d_scale, amax=amax)
+    lib = load_library()
     st = lib.tcm_gemm_fused(M, N, K, ca, _ptr(A), lda, cb, _ptr(B),
-                            ldb, _ptr(C), _row_pitch(C, "C") if C is not None else 0,
-                            _ptr(D), _row_pitch(D, "D"), _code(D, "D"), float(alpha), float(beta),
+                            ldb, _ptr(C), C.stride(0) if C is not None else 0,
+                            _ptr(D), D.stride(0), _code(D, "D"), float(alpha), float(beta),
                             _ptr(a_scale), _ptr(b_scale), _ptr(bias), ACT_CODE[act], _ptr(d_scale), _ptr(amax),
                             _stream(stream))
     _check(st, "tcm_gemm_fused")
@@ -196,15 +285,16 @@ def tcm_gemm_fused(A, B, D, *, C=None, alpha=1.0, beta=0.0, a_scale=None, b_scal
 
 
 def tcm_gemm(A, B, D, *, C=None, alpha=1.0, beta=0.0, stream=None):
-    """D = alpha * (A @ B_stored.T) + beta * C for bf16/fp16 A, B (densely packed)."""
-    lib = load_library()
+    """D = alpha * (A @ B_stored.T) + beta * C for bf16/fp16 A, B; all densely packed."""
+    _mat(A, "A", dtypes=F16_TYPES, contiguous=True)
     M, K = A.shape
-    N = B.shape[0]
-    for t, n in ((A, "A"), (B, "B"), (D, "D")):
-        if not t.is_contiguous():
-            raise ValueError(f"{n} must be contiguous")
-    if C is not None and not C.is_contiguous():
-        raise ValueError("C must be contiguous")
+    N = B.shape[0] if isinstance(B, torch.Tensor) and B.dim() == 2 else None
+    _mat(B, "B", N, K, (A.dtype,), contiguous=True)
+    _mat(D, "D", M, N, OUT_TYPES, contiguous=True)
+    if C is not None:
+        _mat(C, "C", M, N, (D.dtype,), contiguous=True)
+    _on_device(A=A, B=B, D=D, C=C)
+    lib = load_library()
     st = lib.tcm_gemm(M, N, K, _code(A, "A"), _ptr(A), _ptr(B), _ptr(C), _ptr(D), float(alpha),
                       float(beta), _code(D, "D"), _stream(stream))
     _check(st, "tcm_gemm")
@@ -213,13 +303,21 @@ def tcm_gemm(A, B, D, *, C=None, alpha=1.0, beta=0.0, stream=None):
 
 def tcm_sp_compress(A, A_comp=None, meta=None, *, stream=None):
     """2:4 prune + compress of logical A (M x K, K % 32 == 0) -> (A_comp M x K/2, meta M x K/32 int32)."""
-    lib = load_library()
+    _mat(A, "A", dtypes=F16_TYPES)
     M, K = A.shape
+    if K % 32:
+        raise ValueError(f"K = {K} must be a multiple of 32")
+    if A_comp is not None:
+        _mat(A_comp, "A_comp", M, K // 2, (A.dtype,), contiguous=True)
+    if meta is not None:
+        _mat(meta, "meta", M, K // 32, INDEX_TYPES, contiguous=True)
+    _on_device(A=A, A_comp=A_comp, meta=meta)
     if A_comp is None:
         A_comp = torch.empty((M, K // 2), dtype=A.dtype, device=A.device)
     if meta is None:
         meta = torch.empty((M, K // 32), dtype=torch.int32, device=A.device)
-    st = lib.tcm_sp_compress(M, K, _code(A, "A"), _ptr(A), _row_pitch(A, "A"), _ptr(A_comp), _ptr(meta),
+    lib = load_library()
+    st = lib.tcm_sp_compress(M, K, _code(A, "A"), _ptr(A), A.stride(0), _ptr(A_comp), _ptr(meta),
                              _stream(stream))
     _check(st, "tcm_sp_compress")
     return A_comp, meta
@@ -227,23 +325,40 @@ def tcm_sp_compress(A, A_comp=None, meta=None, *, stream=None):
 
 def tcm_sp_decompress(A_comp, meta, A=None, *, stream=None):
     """Logical M x K matrix from (A_comp, meta) with zeros at the dropped positions."""
-    lib = load_library()
+    _mat(A_comp, "A_comp", dtypes=F16_TYPES, contiguous=True)
     M, Kh = A_comp.shape
     K = 2 * Kh
+    if K % 32:
+        raise ValueError(f"K = {K} must be a multiple of 32")
+    _mat(meta, "meta", M, K // 32, INDEX_TYPES, contiguous=True)
+    if A is not None:
+        _mat(A, "A", M, K, (A_comp.dtype,))
+    _on_device(A_comp=A_comp, meta=meta, A=A)
     if A is None:
         A = torch.empty((M, K), dtype=A_comp.dtype, device=A_comp.device)
+    lib = load_library()
     st = lib.tcm_sp_decompress(M, K, _code(A_comp, "A_comp"), _ptr(A_comp), _ptr(meta), _ptr(A),
-                               _row_pitch(A, "A"), _stream(stream))
+                               A.stride(0), _stream(stream))
     _check(st, "tcm_sp_decompress")
     return A
 
 
 def tcm_gemm_sp(A_comp, meta, B, D, *, C=None, alpha=1.0, beta=0.0, stream=None):
-    """D = alpha * (A' @ B_stored.T) + beta * C, A' the 2:4 matrix held by (A_comp, meta)."""
-    lib = load_library()
+    """D = alpha * (A' @ B_stored.T) + beta * C, A' the 2:4 matrix held by (A_comp, meta)
+    (A_comp M x K/2, meta M x K/32 int32, B N x K, C and D M x N; all densely packed)."""
+    _mat(A_comp, "A_comp", dtypes=F16_TYPES, contiguous=True)
     M, Kh = A_comp.shape
     K = 2 * Kh
+    if K % 32:
+        raise ValueError(f"K = {K} must be a multiple of 32")
+    _mat(meta, "meta", M, K // 32, INDEX_TYPES, contiguous=True)
+    _mat(B, "B", None, K, (A_comp.dtype,), contiguous=True)
     N = B.shape[0]
+    _mat(D, "D", M, N, OUT_TYPES, contiguous=True)
+    if C is not None:
+        _mat(C, "C", M, N, (D.dtype,), contiguous=True)
+    _on_device(A_comp=A_comp, meta=meta, B=B, D=D, C=C)
+    lib = load_library()
     st = lib.tcm_gemm_sp(M, N, K, _code(A_comp, "A_comp"), _ptr(A_comp), _ptr(meta), _ptr(B), _ptr(C),
                          _ptr(D), float(alpha), float(beta), _code(D, "D"), _stream(stream))
     _check(st, "tcm_gemm_sp")
@@ -258,29 +373,36 @@ def tcm_mx_scales_bytes(rows: int, K: int) -> int:
 def tcm_mx_pack_scales(scales, K: int, packed=None, stream=None):
     """Blocked layout of row-major E8M0 codes `scales` (rows x K/32 uint8, CUDA);
     allocates `packed` (uint8, tcm_mx_scales_bytes(rows, K) bytes) if not given."""
-    import torch
-    lib = load_library()
+    if K % 32:
+        raise ValueError(f"K = {K} must be a multiple of 32")
+    _mat(scales, "scales", None, K // 32, (torch.uint8,), contiguous=True)
     rows = scales.shape[0]
-    if tuple(scales.shape) != (rows, K // 32) or not scales.is_contiguous():
-        raise ValueError("scales must be a contiguous rows x K/32 tensor")
+    nbytes = max(tcm_mx_scales_bytes(rows, K), 0)
+    if packed is not None:
+        _bytes(packed, "packed", nbytes)
+    _on_device(scales=scales, packed=packed)
     if packed is None:
-        packed = torch.empty(max(tcm_mx_scales_bytes(rows, K), 0), dtype=torch.uint8, device=scales.device)
+        packed = torch.empty(nbytes, dtype=torch.uint8, device=scales.device)
+    lib = load_library()
     _check(lib.tcm_mx_pack_scales(rows, K, _ptr(scales), _ptr(packed), _stream(stream)), "tcm_mx_pack_scales")
     return packed
 
 
 def tcm_gemm_mx(A, a_scales, B, b_scales, D, *, C=None, alpha=1.0, beta=0.0, bias=None, stream=None):
     """Block-scaled FP8 GEMM: A (M x K) and B (N x K) in E4M3/E5M2; a_scales and
-    b_scales the blocked E8M0 arrays of tcm_mx_pack_scales; D (M x N); all
-    contiguous CUDA tensors."""
-    lib = load_library()
+    b_scales the blocked E8M0 arrays of tcm_mx_pack_scales; D (M x N), C of D's
+    dtype, bias N elements of D's dtype; all contiguous CUDA tensors."""
+    _mat(A, "A", dtypes=F8_TYPES, contiguous=True)
     M, K = A.shape
+    _mat(B, "B", None, K, F8_TYPES, contiguous=True)
     N = B.shape[0]
-    for t, n in ((A, "A"), (B, "B"), (a_scales, "a_scales"), (b_scales, "b_scales"), (D, "D")):
-        if not t.is_contiguous():
-            raise ValueError(f"{n} must be contiguous")
-    if a_scales.numel() < tcm_mx_scales_bytes(M, K) or b_scales.numel() < tcm_mx_scales_bytes(N, K):
-        raise ValueError("scales must be blocked arrays of tcm_mx_scales_bytes(rows, K) bytes")
+    _bytes(a_scales, "a_scales", tcm_mx_scales_bytes(M, K))
+    _bytes(b_scales, "b_scales", tcm_mx_scales_bytes(N, K))
+    _epilogue_args(D, C, bias, M, N, OUT_TYPES, (D.dtype,))
+    if not D.is_contiguous() or (C is not None and not C.is_contiguous()):
+        raise ValueError("C and D must be contiguous")
+    _on_device(A=A, a_scales=a_scales, B=B, b_scales=b_scales, D=D, C=C, bias=bias)
+    lib = load_library()
     st = lib.tcm_gemm_mx(M, N, K, _code(A, "A"), _ptr(A), _ptr(a_scales), _code(B, "B"), _ptr(B), _ptr(b_scales),
                          _ptr(C), _ptr(D), float(alpha), float(beta), _ptr(bias), _code(D, "D"), _stream(stream))
     _check(st, "tcm_gemm_mx")
@@ -294,26 +416,34 @@ def tcm_sp_meta_tc_bytes(M: int, K: int) -> int:
 
 def tcm_sp_meta_pack(meta, K: int, meta_tc=None, stream=None):
     """Hardware-ordered copy of canonical metadata `meta` (M x K/32 int32/uint32, CUDA)."""
-    lib = load_library()
+    if K % 32:
+        raise ValueError(f"K = {K} must be a multiple of 32")
+    _mat(meta, "meta", None, K // 32, INDEX_TYPES, contiguous=True)
     M = meta.shape[0]
-    if tuple(meta.shape) != (M, K // 32) or not meta.is_contiguous():
-        raise ValueError("meta must be a contiguous M x K/32 tensor")
+    nbytes = max(tcm_sp_meta_tc_bytes(M, K), 0)
+    if meta_tc is not None:
+        _bytes(meta_tc, "meta_tc", nbytes)
+    _on_device(meta=meta, meta_tc=meta_tc)
     if meta_tc is None:
-        meta_tc = torch.empty(max(tcm_sp_meta_tc_bytes(M, K), 0), dtype=torch.uint8, device=meta.device)
+        meta_tc = torch.empty(nbytes, dtype=torch.uint8, device=meta.device)
+    lib = load_library()
     _check(lib.tcm_sp_meta_pack(M, K, _ptr(meta), _ptr(meta_tc), _stream(stream)), "tcm_sp_meta_pack")
     return meta_tc
 
 
 def tcm_gemm_sp_tc(A_comp, meta_tc, B, D, *, C=None, alpha=1.0, beta=0.0, stream=None):
     """tcm_gemm_sp with hardware-ordered metadata (tcm_sp_meta_pack); A_comp M x K/2, B N x K."""
+    _mat(A_comp, "A_comp", dtypes=F16_TYPES, contiguous=True)
+    _mat(B, "B", dtypes=(A_comp.dtype,), contiguous=True)
+    M, K, N = A_comp.shape[0], B.shape[1], B.shape[0]
+    if A_comp.shape[1] * 2 != K or K % 32:
+        raise ValueError(f"A_comp holds K/2 = {A_comp.shape[1]} columns but B has K = {K} (a multiple of 32)")
+    _bytes(meta_tc, "meta_tc", tcm_sp_meta_tc_bytes(M, K))
+    _mat(D, "D", M, N, OUT_TYPES, contiguous=True)
+    if C is not None:
+        _mat(C, "C", M, N, (D.dtype,), contiguous=True)
+    _on_device(A_comp=A_comp, meta_tc=meta_tc, B=B, D=D, C=C)
     lib = load_library()
-    M, K = A_comp.shape[0], B.shape[1]
-    N = B.shape[0]
-    for t, n in ((A_comp, "A_comp"), (meta_tc, "meta_tc"), (B, "B"), (D, "D")):
-        if not t.is_contiguous():
-            raise ValueError(f"{n} must be contiguous")
-    if A_comp.shape[1] * 2 != K or tuple(D.shape) != (M, N) or meta_tc.numel() < tcm_sp_meta_tc_bytes(M, K):
-        raise ValueError("shape mismatch")
     st = lib.tcm_gemm_sp_tc(M, N, K, _code(A_comp, "A_comp"), _ptr(A_comp), _ptr(meta_tc), _ptr(B), _ptr(C), _ptr(D),
                             float(alpha), float(beta), _code(D, "D"), _stream(stream))
     _check(st, "tcm_gemm_sp_tc")
@@ -327,29 +457,36 @@ def tcm_nvfp4_scales_bytes(rows: int, K: int) -> int:
 
 def tcm_nvfp4_pack_scales(scales, K: int, packed=None, stream=None):
     """Blocked layout of row-major UE4M3 codes `scales` (rows x K/16 uint8, CUDA)."""
-    import torch
-    lib = load_library()
+    if K % 16:
+        raise ValueError(f"K = {K} must be a multiple of 16")
+    _mat(scales, "scales", None, K // 16, (torch.uint8,), contiguous=True)
     rows = scales.shape[0]
-    if tuple(scales.shape) != (rows, K // 16) or not scales.is_contiguous():
-        raise ValueError("scales must be a contiguous rows x K/16 tensor")
+    nbytes = max(tcm_nvfp4_scales_bytes(rows, K), 0)
+    if packed is not None:
+        _bytes(packed, "packed", nbytes)
+    _on_device(scales=scales, packed=packed)
     if packed is None:
-        packed = torch.empty(max(tcm_nvfp4_scales_bytes(rows, K), 0), dtype=torch.uint8, device=scales.device)
+        packed = torch.empty(nbytes, dtype=torch.uint8, device=scales.device)
+    lib = load_library()
     _check(lib.tcm_nvfp4_pack_scales(rows, K, _ptr(scales), _ptr(packed), _stream(stream)), "tcm_nvfp4_pack_scales")
     return packed
 
 
 def tcm_gemm_nvfp4(A, a_scales, B, b_scales, D, *, C=None, alpha=1.0, beta=0.0, bias=None, stream=None):
     """NVFP4 GEMM: A (M x K/2 bytes) and B (N x K/2 bytes) packed E2M1, a_scales / b_scales the
-    blocked UE4M3 arrays of tcm_nvfp4_pack_scales, D (M x N); alpha = product of the per-tensor scales."""
+    blocked UE4M3 arrays of tcm_nvfp4_pack_scales, D (M x N), C of D's dtype, bias N elements of
+    D's dtype; alpha = product of the per-tensor scales.  All contiguous CUDA tensors."""
+    _mat(A, "A", dtypes=(torch.uint8,), contiguous=True)
+    M, K = A.shape[0], 2 * A.shape[1]
+    _mat(B, "B", None, K // 2, (torch.uint8,), contiguous=True)
+    N = B.shape[0]
+    _bytes(a_scales, "a_scales", tcm_nvfp4_scales_bytes(M, K))
+    _bytes(b_scales, "b_scales", tcm_nvfp4_scales_bytes(N, K))
+    _epilogue_args(D, C, bias, M, N, OUT_TYPES, (D.dtype,))
+    if not D.is_contiguous() or (C is not None and not C.is_contiguous()):
+        raise ValueError("C and D must be contiguous")
+    _on_device(A=A, a_scales=a_scales, B=B, b_scales=b_scales, D=D, C=C, bias=bias)
     lib = load_library()
-    M, N, K = A.shape[0], B.shape[0], 2 * A.shape[1]
-    for t, n in ((A, "A"), (B, "B"), (a_scales, "a_scales"), (b_scales, "b_scales"), (D, "D")):
-        if not t.is_contiguous():
-            raise ValueError(f"{n} must be contiguous")
-    if A.dtype != torch.uint8 or B.dtype != torch.uint8 or 2 * B.shape[1] != K or tuple(D.shape) != (M, N):
-        raise ValueError("A, B must be packed uint8 rows of K/2 bytes; D M x N")
-    if a_scales.numel() < tcm_nvfp4_scales_bytes(M, K) or b_scales.numel() < tcm_nvfp4_scales_bytes(N, K):
-        raise ValueError("scales must be blocked arrays of tcm_nvfp4_scales_bytes(rows, K) bytes")
     st = lib.tcm_gemm_nvfp4(M, N, K, _ptr(A), _ptr(a_scales), _ptr(B), _ptr(b_scales), _ptr(C), _ptr(D),
                             float(alpha), float(beta), _ptr(bias), _code(D, "D"), _stream(stream))
     _check(st, "tcm_gemm_nvfp4")

@@ -37,15 +37,15 @@ int *device_status_ptr()
 
 static int sm_count()
 {
-    static int counts[kMaxDevices] = {};
+    static std::atomic<int> counts[kMaxDevices] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
-    if (counts[dev] == 0) {
-        int n = 0;
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        counts[dev] = n;
+    int n = counts[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        counts[dev].store(n, std::memory_order_relaxed);
     }
-    return counts[dev];
+    return n;
 }
 
 static std::atomic<unsigned long long> g_timeout_ns{0};
@@ -217,16 +217,19 @@ static tcm_status gemm_impl(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, 
     if (beta != 0.f && !C) return TCM_ERR_INVALID_ARG;
     if (lda < K || ldb < K || ldd < N || (C && ldc < N)) return TCM_ERR_INVALID_ARG;
     const int ea = elem_bytes(a_dtype), eb = elem_bytes(b_dtype), eo = elem_bytes(out_dtype);
-    if ((A && !aligned16(A)) || (B && !aligned16(B)) || !aligned16(D) || (C && !aligned16(C)) ||
+    // A and B are not read when K == 0: their pointers and pitches are then not checked
+    const bool reads_ab = K > 0;
+    if ((reads_ab && (!aligned16(A) || !aligned16(B))) || !aligned16(D) || (C && !aligned16(C)) ||
         (bias && !aligned16(bias)))
         return TCM_ERR_MISALIGNED;
-    if ((!a4 && (lda * ea) % 16) || (!b4 && (ldb * eb) % 16) || (ldd * eo) % 16 || (C && (ldc * eo) % 16))
+    if ((reads_ab && ((!a4 && (lda * ea) % 16) || (!b4 && (ldb * eb) % 16))) || (ldd * eo) % 16 ||
+        (C && (ldc * eo) % 16))
         return TCM_ERR_MISALIGNED;
     // packed FP4 operands (16U4_ALIGN16B tensor maps): K a multiple of 128, rows of a
     // multiple of 32 bytes (64 elements) starting on 32-byte boundaries
     if ((a4 || b4) && K % 128 != 0) return TCM_ERR_UNSUPPORTED;
-    if ((a4 && (lda % 64 || (reinterpret_cast<uintptr_t>(A) & 31u))) ||
-        (b4 && (ldb % 64 || (reinterpret_cast<uintptr_t>(B) & 31u))))
+    if (reads_ab && ((a4 && (lda % 64 || (reinterpret_cast<uintptr_t>(A) & 31u))) ||
+                     (b4 && (ldb % 64 || (reinterpret_cast<uintptr_t>(B) & 31u)))))
         return TCM_ERR_MISALIGNED;
 
     // ---- configuration: swap A and B for skinny M so the weight fills the 128-row MMA
@@ -428,19 +431,26 @@ tcm_status tcm_sp_meta_pack(int64_t M, int64_t K, const uint32_t *meta, void *me
                : TCM_ERR_CUDA;
 }
 
-tcm_status tcm_gemm_sp_tc(int64_t M, int64_t N, int64_t K, tcm_dtype dtype, const void *A_comp, const void *meta_tc,
-                          const void *B, const void *C, void *D, float alpha, float beta, tcm_dtype out_dtype,
-                          tcm_stream_t stream)
+} // extern "C"
+
+// 2:4-sparse GEMM on the block-scaled kernel's sparse formats.  canonical: `meta` is the
+// M x K/32-word layout of tcm_sp_compress, which the kernel's writer warps read and
+// reorder themselves; otherwise it is the hardware-ordered layout of tcm_sp_meta_pack,
+// loaded by TMA.
+static tcm_status sparse_impl(bool canonical, int64_t M, int64_t N, int64_t K, tcm_dtype dtype, const void *A_comp,
+                              const void *meta, const void *B, const void *C, void *D, float alpha, float beta,
+                              tcm_dtype out_dtype, tcm_stream_t stream)
 {
     if (dtype != TCM_BF16 && dtype != TCM_F16) return TCM_ERR_UNSUPPORTED;
     if (out_dtype != TCM_BF16 && out_dtype != TCM_F16 && out_dtype != TCM_F32) return TCM_ERR_UNSUPPORTED;
     if (M < 1 || N < 1 || K < 0 || K % 32 != 0) return TCM_ERR_INVALID_ARG;
     if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2) return TCM_ERR_UNSUPPORTED;
-    // metadata rows (16 of 128 bytes per stage of 128 logical K) are addressed with 32-bit coordinates
-    if (((M + 255) / 128) * ((K + 127) / 128) * 16 > INT32_MAX) return TCM_ERR_UNSUPPORTED;
-    if (!D || (K > 0 && (!A_comp || !meta_tc || !B)) || (beta != 0.f && !C)) return TCM_ERR_INVALID_ARG;
+    // hardware-ordered metadata rows (16 of 128 bytes per stage of 128 logical K) are
+    // addressed with 32-bit coordinates
+    if (!canonical && ((M + 255) / 128) * ((K + 127) / 128) * 16 > INT32_MAX) return TCM_ERR_UNSUPPORTED;
+    if (!D || (K > 0 && (!A_comp || !meta || !B)) || (beta != 0.f && !C)) return TCM_ERR_INVALID_ARG;
     const int eo = elem_bytes(out_dtype);
-    if ((A_comp && !aligned16(A_comp)) || (B && !aligned16(B)) || (meta_tc && !aligned16(meta_tc)) || !aligned16(D) ||
+    if ((A_comp && !aligned16(A_comp)) || (B && !aligned16(B)) || (meta && !aligned16(meta)) || !aligned16(D) ||
         (C && !aligned16(C)))
         return TCM_ERR_MISALIGNED;
     if ((N * eo) % 16) return TCM_ERR_MISALIGNED;
@@ -448,7 +458,7 @@ tcm_status tcm_gemm_sp_tc(int64_t M, int64_t N, int64_t K, tcm_dtype dtype, cons
     if (sms <= 0) return TCM_ERR_CUDA;
 
     GemmConfig cfg{};
-    cfg.kind = 5;
+    cfg.kind = canonical ? 2 : 5;
     cfg.ksplit = 1;
     cfg.katoms = 1;
     const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
@@ -461,23 +471,26 @@ tcm_status tcm_gemm_sp_tc(int64_t M, int64_t N, int64_t K, tcm_dtype dtype, cons
     MxMaps maps;
     std::memset(&maps, 0, sizeof maps);
     if (K > 0) {
-        // a stage's 2 KB of metadata (128 lanes x 16 bytes) is contiguous: one box of 16
-        // rows of 128 bytes
-        const uint64_t meta_rows = static_cast<uint64_t>((M + 127) / 128) * static_cast<uint64_t>((K + 127) / 128) * 16u;
-        EncodeTiledFn fn = encode_fn();
-        const cuuint64_t dims[2] = {128, meta_rows};
-        const cuuint64_t strides[1] = {128};
-        const cuuint32_t box[2] = {128, 16};
-        const cuuint32_t estr[2] = {1, 1};
-        if (!fn || !encode_kmajor(&maps.a, A_comp, 2, static_cast<uint64_t>(K / 2), static_cast<uint64_t>(M),
-                                  static_cast<uint64_t>(K / 2), 128) ||
+        if (!encode_kmajor(&maps.a, A_comp, 2, static_cast<uint64_t>(K / 2), static_cast<uint64_t>(M),
+                           static_cast<uint64_t>(K / 2), 128) ||
             !encode_kmajor(&maps.b, B, 2, static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(K),
-                           static_cast<uint32_t>(cfg.bn / cfg.cta_group)) ||
-            fn(&maps.sa, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(meta_tc), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                           static_cast<uint32_t>(cfg.bn / cfg.cta_group)))
             return TCM_ERR_CUDA;
-        maps.sb = maps.sa;
+        if (!canonical) {
+            // a stage's 2 KB of metadata (128 lanes x 16 bytes) is contiguous: one box of 16
+            // rows of 128 bytes
+            const uint64_t meta_rows = static_cast<uint64_t>((M + 127) / 128) * static_cast<uint64_t>((K + 127) / 128) * 16u;
+            EncodeTiledFn fn = encode_fn();
+            const cuuint64_t dims[2] = {128, meta_rows};
+            const cuuint64_t strides[1] = {128};
+            const cuuint32_t box[2] = {128, 16};
+            const cuuint32_t estr[2] = {1, 1};
+            if (!fn || fn(&maps.sa, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(meta), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                return TCM_ERR_CUDA;
+            maps.sb = maps.sa;
+        }
     }
     GemmParams p{};
     p.kM = static_cast<int>(M);
@@ -508,87 +521,30 @@ tcm_status tcm_gemm_sp_tc(int64_t M, int64_t N, int64_t K, tcm_dtype dtype, cons
     p.status = device_status_ptr();
     if (!p.status) return TCM_ERR_CUDA;
     p.fault_inject = g_fault_once.exchange(0);
+    if (canonical) {
+        p.meta = static_cast<const uint32_t *>(meta);
+        p.meta_ld = K / 32;
+    }
     const int64_t clusters = sms / cfg.cta_group;
     const int grid = static_cast<int>((p.num_tiles < clusters ? p.num_tiles : clusters) * cfg.cta_group);
     const cudaError_t e = launch_gemm_mx(cfg, maps, p, grid, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TCM_OK : TCM_ERR_CUDA;
 }
 
+extern "C" {
+
+tcm_status tcm_gemm_sp_tc(int64_t M, int64_t N, int64_t K, tcm_dtype dtype, const void *A_comp, const void *meta_tc,
+                          const void *B, const void *C, void *D, float alpha, float beta, tcm_dtype out_dtype,
+                          tcm_stream_t stream)
+{
+    return sparse_impl(false, M, N, K, dtype, A_comp, meta_tc, B, C, D, alpha, beta, out_dtype, stream);
+}
+
 tcm_status tcm_gemm_sp(int64_t M, int64_t N, int64_t K, tcm_dtype dtype, const void *A_comp, const uint32_t *meta,
                        const void *B, const void *C, void *D, float alpha, float beta, tcm_dtype out_dtype,
                        tcm_stream_t stream)
 {
-    if (dtype != TCM_BF16 && dtype != TCM_F16) return TCM_ERR_UNSUPPORTED;
-    if (out_dtype != TCM_BF16 && out_dtype != TCM_F16 && out_dtype != TCM_F32) return TCM_ERR_UNSUPPORTED;
-    if (M < 1 || N < 1 || K < 0 || K % 32 != 0) return TCM_ERR_INVALID_ARG;
-    if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2) return TCM_ERR_UNSUPPORTED;
-    if (!D || (K > 0 && (!A_comp || !meta || !B)) || (beta != 0.f && !C)) return TCM_ERR_INVALID_ARG;
-    const int eo = elem_bytes(out_dtype);
-    if ((A_comp && !aligned16(A_comp)) || (B && !aligned16(B)) || (meta && !aligned16(meta)) || !aligned16(D) ||
-        (C && !aligned16(C)))
-        return TCM_ERR_MISALIGNED;
-    if ((N * eo) % 16) return TCM_ERR_MISALIGNED;
-    const int64_t sms = sm_count();
-    if (sms <= 0) return TCM_ERR_CUDA;
-
-    GemmConfig cfg{};
-    cfg.kind = 2;
-    cfg.ksplit = 1;
-    cfg.katoms = 1;
-    const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
-    cfg.cta_group = (M > 128 && N > 128 && pair_tiles >= sms / 2) ? 2 : 1;
-    const int force_cg = g_force_cta_group.load();
-    if (force_cg == 1 || force_cg == 2) cfg.cta_group = force_cg;
-    cfg.bn = cfg.cta_group == 2 ? 256 : 128;
-    if (cfg.cta_group == 2 && g_force_bn.load() == 128) cfg.bn = 128;
-    cfg.stages = g_force_stages.load();
-
-    CUtensorMap tmA, tmB;
-    std::memset(&tmA, 0, sizeof tmA);
-    std::memset(&tmB, 0, sizeof tmB);
-    if (K > 0) {
-        if (!encode_kmajor(&tmA, A_comp, 2, static_cast<uint64_t>(K / 2), static_cast<uint64_t>(M),
-                           static_cast<uint64_t>(K / 2), 128))
-            return TCM_ERR_CUDA;
-        if (!encode_kmajor(&tmB, B, 2, static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint64_t>(K),
-                           static_cast<uint32_t>(cfg.bn / cfg.cta_group)))
-            return TCM_ERR_CUDA;
-    }
-    GemmParams p{};
-    p.kM = static_cast<int>(M);
-    p.kN = static_cast<int>(N);
-    p.K = static_cast<int>(K);
-    p.num_kb = static_cast<int>((K + 127) / 128);
-    p.tiles_m = static_cast<int>((M + 128 * cfg.cta_group - 1) / (128 * cfg.cta_group));
-    p.tiles_n = static_cast<int>((N + cfg.bn - 1) / cfg.bn);
-    p.num_tiles = p.tiles_m * p.tiles_n;
-    p.group_m = g_force_group_m.load() > 0 ? g_force_group_m.load() : 16;
-    p.tile_begin = 0;
-    p.tile_end = p.num_tiles;
-    p.D = D;
-    p.ldd = N;
-    p.C = beta != 0.f ? C : nullptr;
-    p.ldc = N;
-    p.bias = nullptr;
-    p.a_scale = p.b_scale = nullptr;
-    p.alpha = alpha;
-    p.beta = beta;
-    p.out_fmt = static_cast<int>(out_dtype);
-    p.bias_fmt = p.out_fmt;
-    p.swap_ab = 0;
-    const uint32_t code = dtype == TCM_BF16 ? 1u : 0u;
-    p.idesc = make_idesc(code, code, 128u * static_cast<uint32_t>(cfg.cta_group), static_cast<uint32_t>(cfg.bn)) |
-              (1u << 2); // sparsity enabled
-    p.timeout_ns = timeout_ns();
-    p.status = device_status_ptr();
-    if (!p.status) return TCM_ERR_CUDA;
-    p.fault_inject = 0;
-    p.meta = meta;
-    p.meta_ld = K / 32;
-    const int64_t clusters = sms / cfg.cta_group;
-    const int grid = static_cast<int>((p.num_tiles < clusters ? p.num_tiles : clusters) * cfg.cta_group);
-    const cudaError_t e = launch_gemm_sp(cfg, tmA, tmB, p, grid, reinterpret_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? TCM_OK : TCM_ERR_CUDA;
+    return sparse_impl(true, M, N, K, dtype, A_comp, meta, B, C, D, alpha, beta, out_dtype, stream);
 }
 
 // Block-scaled GEMM (nv = false: MXFP8, E8M0 per 32, kind::mxf8f6f4; nv = true: NVFP4,

@@ -115,7 +115,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 0 && lane == 0) {
+    if (warp == 0 && lane == 0 && p.num_kb > 0) { // K == 0: the maps are not encoded
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
     }

@@ -68,18 +68,22 @@ constexpr int SF_ATOM = 512;                       // scales of 128 rows x one 1
 // Formats of the kernel: MX (MXFP8), NV (NVFP4), SP (2:4-sparse bf16/fp16 A,
 // metadata in the hardware order -- the "side" data of a stage is then the
 // sparse metadata instead of block scales).
-enum SideFmt : int { FMT_MX = 0, FMT_NV = 1, FMT_SP = 2 };
+// SPC: 2:4-sparse A with the canonical metadata of tcm_sp_compress, which the writer
+// warps read from global memory and put into the hardware order themselves.
+enum SideFmt : int { FMT_MX = 0, FMT_NV = 1, FMT_SP = 2, FMT_SPC = 3 };
+__host__ __device__ constexpr bool is_sparse(int fmt) { return fmt == FMT_SP || fmt == FMT_SPC; }
 // Side-data warps per format.  MX, NV: copy warps (lane 0 of each issues the copies e
-// with e % n == its index).  SP: one writer warp per TMEM lane quadrant (warp % 4).
-__host__ __device__ constexpr int mx_copy_warps(int fmt) { return fmt == FMT_NV ? 3 : fmt == FMT_SP ? 4 : 1; }
+// with e % n == its index).  SP, SPC: one writer warp per TMEM lane quadrant (warp % 4).
+__host__ __device__ constexpr int mx_copy_warps(int fmt) { return fmt == FMT_NV ? 3 : is_sparse(fmt) ? 4 : 1; }
+constexpr uint32_t SP_META_FILL = 0x44444444u; // positions {0, 1} in every group (rows / words past the matrix)
 // TMA, MMA, epilogue (warps 2..9), copy warps
 __host__ __device__ constexpr int mx_threads(int fmt) { return 32 * (2 + MX_EPI_WARPS + mx_copy_warps(fmt)); }
 constexpr int SP_META_STAGE = 2048; // 128 lanes x 16 bytes: lane L's words for the stage's four MMAs
 
 template <int BN_CTA, int BN, int STAGES, int FMT>
 struct MxSmem {
-    static constexpr int B_STAGE = BN_CTA * TILE_K_BYTES * (FMT == FMT_SP ? 2 : 1); // SP: 128 logical K = 2 atoms
-    static constexpr int SF_STAGE = FMT == FMT_SP ? SP_META_STAGE
+    static constexpr int B_STAGE = BN_CTA * TILE_K_BYTES * (is_sparse(FMT) ? 2 : 1); // 128 logical K = 2 atoms
+    static constexpr int SF_STAGE = FMT == FMT_SPC ? 0 : FMT == FMT_SP ? SP_META_STAGE
                                                   : SF_ATOM * (FMT == FMT_NV ? 4 : 1) * (1 + BN / 128);
     static constexpr int A_OFF = 0;
     static constexpr int B_OFF = STAGES * A_STAGE_BYTES;
@@ -215,7 +219,7 @@ template <int FMT, int SFB_ATOMS>
 struct SfLayout {
     static constexpr bool NV = FMT == FMT_NV;
     static constexpr int APT = NV ? 4 : 1;             // atoms per 128-row tile per stage
-    static constexpr int NCP = FMT == FMT_SP ? 0 : APT * (1 + SFB_ATOMS);  // copies per stage
+    static constexpr int NCP = is_sparse(FMT) ? 0 : APT * (1 + SFB_ATOMS);  // copies per stage
     static constexpr uint32_t COLS = NV ? 16u + 16u * SFB_ATOMS : 16u;      // TMEM columns per stage
     // TMEM column (within the stage) of copy e: e = tile * APT + kk, tile 0 = A, 1.. = B row tiles
     __device__ static constexpr uint32_t col(int e)
@@ -258,6 +262,22 @@ __device__ __forceinline__ void mma_sp16(uint32_t d_tmem, uint64_t adesc, uint64
             "}\n" ::"r"(d_tmem),
             "l"(adesc), "l"(bdesc), "r"(meta_tmem), "r"(idesc), "r"(accumulate)
             : "memory");
+}
+
+// The four canonical 2:4 metadata words of `row` for 128-logical-K stage kb (words
+// 4kb .. 4kb+3 of the row, tcm_sp_compress layout: qn words per row), the fill code
+// for rows or words past the matrix.  vec: rows hold whole stages (qn % 4 == 0, the
+// base 16-byte aligned), so the four words are one 16-byte load.
+__device__ __forceinline__ uint4 sp_meta_words(const uint32_t *meta, long long qn, int rows, int row, int kb, bool vec)
+{
+    const long long q0 = 4ll * kb;
+    if (row >= rows) return make_uint4(SP_META_FILL, SP_META_FILL, SP_META_FILL, SP_META_FILL);
+    const uint32_t *src = meta + static_cast<long long>(row) * qn + q0;
+    if (vec) return __ldg(reinterpret_cast<const uint4 *>(src));
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) w[k] = q0 + k < qn ? __ldg(src + k) : SP_META_FILL;
+    return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 // One TMA tile load onto this stage's barrier (pair: the even CTA's barrier, cluster address fb).
@@ -325,18 +345,18 @@ __global__ void __launch_bounds__(mx_threads(FMT), 1)
         }
         mbar_init(drain, 1);
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(sfready + s, FMT == FMT_SP ? NCW * CG : NCW); // SP: writer warps of both CTAs
+            mbar_init(sfready + s, is_sparse(FMT) ? NCW * CG : NCW); // sparse: writer warps of both CTAs
             mbar_init(sfull + s, 1);
         }
         mbar_init(cdrain, NCW);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 0 && lane == 0) {
+    if (warp == 0 && lane == 0 && p.num_kb > 0) { // K == 0: the maps are not encoded
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
-        tma_prefetch_desc(&tmSA);
-        tma_prefetch_desc(&tmSB);
+        if (FMT != FMT_SPC) tma_prefetch_desc(&tmSA);
+        if (!is_sparse(FMT)) tma_prefetch_desc(&tmSB);
     }
     if (warp == 1) {
         if (CG == 2) {
@@ -392,16 +412,18 @@ __global__ void __launch_bounds__(mx_threads(FMT), 1)
                     // SP: each CTA's metadata lands on its own side-data barrier (its writer warps
                     // wait there); scales: both CTAs' atoms on the even CTA's (its copy threads)
                     if (FMT == FMT_SP) mbar_arrive_expect_tx(sfull + stage, L::SF_STAGE);
-                    else if (leader || CG == 1) mbar_arrive_expect_tx(sfull + stage, SIDE_TX);
+                    else if (FMT != FMT_SPC && (leader || CG == 1)) mbar_arrive_expect_tx(sfull + stage, SIDE_TX);
                     if (leader || CG == 1) mbar_arrive_expect_tx(full + stage, STAGE_TX);
                     // pair: both CTAs' loads complete on the even CTA's barriers (cluster addresses)
                     const uint32_t fb = CG == 2 ? full_cluster0 + static_cast<uint32_t>(stage) * 8u : 0u;
                     const uint32_t sfb = CG == 2 ? sfull_cluster0 + static_cast<uint32_t>(stage) * 8u : 0u;
-                    if constexpr (FMT == FMT_SP) {
-                        // metadata: the tile's 2 KB block of this stage (16 rows of 128 bytes), onto
-                        // this CTA's own barrier; compressed A: 64 kept values (128 bytes) of the
-                        // stage's 128 logical K; B: two 64-value atoms
-                        tma_load_2d(ss, &tmSA, sfull + stage, 0, (a_tile * p.num_kb + kb) * 16);
+                    if constexpr (is_sparse(FMT)) {
+                        // SP metadata: the tile's 2 KB block of this stage (16 rows of 128 bytes), onto
+                        // this CTA's own barrier (SPC: the writer warps read it themselves);
+                        // compressed A: 64 kept values (128 bytes) of the stage's 128 logical K;
+                        // B: two 64-value atoms
+                        if constexpr (FMT == FMT_SP)
+                            tma_load_2d(ss, &tmSA, sfull + stage, 0, (a_tile * p.num_kb + kb) * 16);
                         tma_ld<CG>(sa, &tmA, full + stage, fb, kb * 64, a_row);
                         tma_ld<CG>(sb, &tmB, full + stage, fb, kb * 128, b_row);
                         tma_ld<CG>(sb + BN_CTA * TILE_K_BYTES, &tmB, full + stage, fb, kb * 128 + 64, b_row);
@@ -428,7 +450,7 @@ __global__ void __launch_bounds__(mx_threads(FMT), 1)
                 if (n == 0) continue;
                 const uint32_t last = static_cast<uint32_t>((n - 1) & 1);
                 if (leader) {
-                    wait_bar<CG>(sfull + s, last, w, SITE_DRAIN, false);
+                    if (FMT != FMT_SPC) wait_bar<CG>(sfull + s, last, w, SITE_DRAIN, false);
                     wait_bar<CG>(full + s, last, w, SITE_DRAIN, false);
                 } else {
                     // SP: this CTA's metadata lands on its own side-data barrier
@@ -465,7 +487,7 @@ __global__ void __launch_bounds__(mx_threads(FMT), 1)
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const uint32_t accum = (kb > 0 || k > 0) ? 1u : 0u;
-                        if constexpr (FMT == FMT_SP) {
+                        if constexpr (is_sparse(FMT)) {
                             // logical K 32 per MMA: A +32 bytes (16 kept values), B +64 bytes within its
                             // atom (atom k / 2); metadata word of MMA k at column 4k
                             mma_sp16<CG>(d_tmem, ad + 2 * k, (k < 2 ? bd : bd1) + 4 * (k & 1), sf + 4u * k, p.idesc, accum);
@@ -491,6 +513,90 @@ __global__ void __launch_bounds__(mx_threads(FMT), 1)
             if (CG == 2) mma_commit_pair(drain, 0x1);
             else mma_commit(drain);
             wait_bar<CG>(drain, 0, w, SITE_DRAIN, false);
+        }
+    } else if (FMT == FMT_SPC && warp >= MX_COPY_WARP) {
+        // Metadata writer for TMEM lane quadrant q = warp % 4 (in both CTAs of a pair): lane l
+        // reads, SPC_PREFETCH stages ahead, the stage's four canonical words of its tile row
+        // 32q + l from global memory, exchanges half-words with lane l ^ 8 -- the sparse MMA
+        // reads, in TMEM lane 16a + 8s + r, bits 16s .. 16s+15 of the words of rows 16a + r
+        // (low half) and 16a + 8 + r (high half) -- and stores word k at column 4k of the
+        // stage's slot.  A slot is rewritten only after its previous readers (the MMAs of
+        // item - STAGES) completed, which the stage's empty barrier records.
+        constexpr int SPC_PREFETCH = 4;
+        const int quad = warp & 3;
+        const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+        const uint32_t sfready0 = CG == 2 ? mapa_shared(smem_u32(sfready), 0) : smem_u32(sfready);
+        const int my_tiles = first_tile < p.tile_end ? (p.tile_end - 1 - first_tile) / step + 1 : 0;
+        const long long items = static_cast<long long>(my_tiles) * p.num_kb;
+        const long long qn = p.meta_ld;
+        const bool vec = (qn & 3) == 0;
+        const bool upper = (lane & 8) != 0;
+        const int row_in_tile = quad * 32 + lane;
+        // fetch cursor: the (tile, stage) of the next item to load
+        int f_t = first_tile, f_kb = 0, f_row = 0;
+        long long fetched = 0;
+        uint4 buf[SPC_PREFETCH];
+#pragma unroll
+        for (int j = 0; j < SPC_PREFETCH; ++j) {
+            buf[j] = make_uint4(SP_META_FILL, SP_META_FILL, SP_META_FILL, SP_META_FILL);
+            if (fetched < items) {
+                if (f_kb == 0) {
+                    int mb, nb;
+                    tile_coords(p, f_t, mb, nb);
+                    f_row = (mb * CG + static_cast<int>(rank)) * BM + row_in_tile;
+                }
+                buf[j] = sp_meta_words(p.meta, qn, p.kM, f_row, f_kb, vec);
+                ++fetched;
+                if (++f_kb == p.num_kb) f_kb = 0, f_t += step;
+            }
+        }
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (long long item = 0; ok && item < items; item += SPC_PREFETCH) {
+#pragma unroll
+            for (int j = 0; j < SPC_PREFETCH; ++j) {
+                if (item + j >= items) break;
+                const uint4 cur = buf[j];
+                if (fetched < items) {
+                    if (f_kb == 0) {
+                        int mb, nb;
+                        tile_coords(p, f_t, mb, nb);
+                        f_row = (mb * CG + static_cast<int>(rank)) * BM + row_in_tile;
+                    }
+                    buf[j] = sp_meta_words(p.meta, qn, p.kM, f_row, f_kb, vec);
+                    ++fetched;
+                    if (++f_kb == p.num_kb) f_kb = 0, f_t += step;
+                }
+                int free_ok = 1;
+                if (lane == 0) free_ok = wait_bar<CG>(empty + stage, phase ^ 1u, w, SITE_META_EMPTY, true);
+                free_ok = __shfl_sync(0xffffffffu, free_ok, 0);
+                if (!free_ok) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t words[4] = {cur.x, cur.y, cur.z, cur.w};
+                const uint32_t t0 = tmem_base + lane_base + SF_COL + static_cast<uint32_t>(stage) * SF_STAGE_COLS;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint32_t other = __shfl_xor_sync(0xffffffffu, words[k], 8);
+                    const uint32_t hw = upper ? ((other >> 16) | (words[k] & 0xFFFF0000u))
+                                              : ((words[k] & 0xFFFFu) | (other << 16));
+                    tmem_st_32x32b_x1(t0 + 4u * static_cast<uint32_t>(k), hw);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if (CG == 2) mbar_arrive_cluster(sfready0 + static_cast<uint32_t>(stage) * 8u);
+                    else mbar_arrive(sfready + stage);
+                }
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
         }
     } else if (FMT == FMT_SP && warp >= MX_COPY_WARP) {
         // Metadata writer for TMEM lane quadrant warp % 4, in both CTAs of a pair (each CTA's
@@ -678,6 +784,15 @@ cudaError_t launch_gemm_mx(const GemmConfig &cfg, const MxMaps &maps, const Gemm
             return cudaErrorInvalidValue;
         }
         if (cfg.bn == 128) return launch_mx_one<128, 4, 2, 1, FMT_SP>(maps, p, grid, stream);
+        return cudaErrorInvalidValue;
+    }
+    if (cfg.kind == 2) { // 2:4-sparse A with canonical metadata (read by the writer warps)
+        if (cfg.cta_group == 2) {
+            if (cfg.bn == 256) return launch_mx_one<256, 4, 1, 2, FMT_SPC>(maps, p, grid, stream);
+            if (cfg.bn == 128) return launch_mx_one<128, 5, 2, 2, FMT_SPC>(maps, p, grid, stream);
+            return cudaErrorInvalidValue;
+        }
+        if (cfg.bn == 128) return launch_mx_one<128, 4, 2, 1, FMT_SPC>(maps, p, grid, stream);
         return cudaErrorInvalidValue;
     }
     if (cfg.kind == 4) { // NVFP4

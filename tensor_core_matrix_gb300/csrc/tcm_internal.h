@@ -68,7 +68,8 @@ enum FaultBits : int {
 
 // Which kernel variant a launch uses.
 struct GemmConfig {
-    int kind;      // 0 = kind::f16, 1 = kind::f8f6f4, 2 = sparse kind::f16
+    int kind;      // 0 = kind::f16, 1 = kind::f8f6f4, 2 = sparse kind::f16 (canonical metadata),
+                   // 3 = MXFP8, 4 = NVFP4, 5 = sparse kind::f16 (hardware-ordered metadata)
     int bn;        // N tile (columns of the accumulator)
     int cta_group; // 1 = one CTA per 128-row tile, 2 = CTA pair per 256-row tile
     int stages;    // 0 = the variant's default ring depth
@@ -99,8 +100,6 @@ cudaError_t launch_sp_meta_pack(const uint32_t *meta, int64_t M, int64_t K, uint
 cudaError_t launch_mx_pack_scales(const uint8_t *src, int64_t rows, int64_t nblk, uint32_t pad, uint8_t *dst,
                                   cudaStream_t stream);
 
-cudaError_t launch_gemm_sp(const GemmConfig &cfg, const CUtensorMap &tmA, const CUtensorMap &tmB,
-                           const GemmParams &p, int grid, cudaStream_t stream);
 
 cudaError_t launch_sp_compress(int64_t M, int64_t K, int elem_bytes, const void *A, int64_t lda, void *Ac,
                                uint32_t *meta, cudaStream_t stream);

@@ -1,5 +1,5 @@
 """Failure path of the block-scaled and sparse kernels (MXFP8, NVFP4, 2:4 sparse with
-hardware-ordered metadata): a stage whose loads are never issued makes its waits run out,
+hardware-ordered or canonical metadata): a stage whose loads are never issued makes its waits run out,
 the status names a pipeline wait, the kernel winds down, and the next launch computes the
 same result as an unstarved one."""
 import pytest
@@ -11,8 +11,9 @@ from parity import dev
 pytestmark = pytest.mark.gpu
 
 # 2: the MMA issuer or a side-data thread waiting for data; 4: the epilogue waiting for the
-# tile; 6: the MMA issuer waiting for the stage's scales or metadata in tensor memory
-SITES = (2, 4, 6)
+# tile; 6: the MMA issuer waiting for the stage's scales or metadata in tensor memory;
+# 7: a metadata writer waiting for a stage's previous MMAs (canonical sparse path)
+SITES = (2, 4, 6, 7)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -90,3 +91,14 @@ def test_sparse_tc_starved_stage(tcm, cg, bn):
     B = s["B"].to(d)
     D = torch.empty((512, 512), dtype=torch.bfloat16, device=d)
     starve_then_recover(tcm, lambda: tcm.tcm_gemm_sp_tc(Ac, meta_tc, B, D), D)
+
+
+@pytest.mark.parametrize("cg,bn", [(2, 256), (1, 128)])
+def test_sparse_canonical_starved_stage(tcm, cg, bn):
+    tcm.tcm_set_config_override(cg, bn, 0, 0, 0)
+    d = dev()
+    s = si.sparse_case(512, 512, 512, seed=93)
+    Ac, meta = tcm.tcm_sp_compress(s["A_logical"].to(d))
+    B = s["B"].to(d)
+    D = torch.empty((512, 512), dtype=torch.bfloat16, device=d)
+    starve_then_recover(tcm, lambda: tcm.tcm_gemm_sp(Ac, meta, B, D), D)
