@@ -1,25 +1,35 @@
 """Throughput of the tcgen05 GEMM hot path on GB300, one JSON line per run.
 
-A step is one pass of the hot path over one batch of resident synthetic
-input at M = N = K = 8192:
+A step is one pass of the hot path over one batch of resident synthetic input
+at M = N = K = 8192:
   * bf16 x bf16 -> fp32 accumulate -> bf16 D (alpha = 1, beta = 0)
   * E4M3 x E4M3 with per-tensor fp32 dequantisation scales and a bf16 bias
     -> bf16 D
   * 2:4 structured-sparse bf16 A: compress of the logical A (keep the two
-    largest of every four along K, ordered metadata), a copy of the metadata
-    into the sparse MMA's tensor-memory order, and the sparse GEMM, counted
-    at its logical 2*M*N*K
-value = sum of 2*M*N*K over the step's three GEMMs / step time (TFLOP/s).
+    largest of every four along K, ordered metadata) and the sparse GEMM on
+    the compressed A and its canonical metadata
+value = 2*M*N*K of the step's two dense GEMMs (the bf16 and FP8 GEMMs the
+metric names) / step time, in TFLOP/s.  The sparse GEMM runs inside the step
+but its (logical) FLOPs are reported only in its own part.
+
+Besides the step, the default run times every configured workload as a part
+outside `value` (512^3 with C, 4096^3 fp16 and bf16, the three LLM shapes, the
+skinny 16 x 28672 x 8192 decode shape against HBM bandwidth, E4M3 x E5M2) and,
+in the CPU-baseline leg, checks the timed step's outputs against the CPU
+oracle on whole output rows (exit status 1 if any exceeds the bound).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tcm|reference]
 
 With torchrun (N > 1) every rank runs an independent replica on its own GPU
 (weak scaling); the slowest rank's time counts.  ``--impl reference`` times
 the CPU oracle instead (rank 0 only), on bounded samples of the same work.
+``--shapes`` times a longer list of workloads (block-scaled, fused, FP4), one
+JSON line each, instead of the step.
 """
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import math
@@ -27,6 +37,7 @@ import os
 import statistics
 import subprocess
 import sys
+import threading
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -39,14 +50,20 @@ import synth_inputs as si  # noqa: E402
 
 SIZE = 8192
 FLOP_PER_GEMM = 2.0 * SIZE ** 3
-METRIC = "GEMM TFLOP/s (2MNK/t) at 8192^3 bf16 and FP8; % of GB300 dense tensor peak"
+DENSE_GEMMS_PER_STEP = 2  # bf16 and E4M3: the FLOPs `value` counts
+METRIC = "GEMM TFLOP/s (2MNK/t) at 8192³ bf16 and FP8; % of GB300 dense tensor peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense FP4 / bf16 tensor rates (GB300)
 FP8_OVER_BF16 = 4.5 / 2.25  # nominal dense ratio
+# dense bf16 tcgen05 rate of one SM per clock (the ncu tensor-pipe utilisation of the
+# bf16 8192^3 kernel, 88.8 % of elapsed cycles at 1.647 GHz for 1822 TFLOP/s, gives 8197)
+BF16_FLOP_PER_CLK_PER_SM = 8192
 L2_BYTES = 129 * 10 ** 6
+SUSTAINED_AFTER_S = 1.0  # timed regions at least this long are compared with the sustained peak
 KERNEL_SOURCES = ["tensor_core_matrix_gb300/csrc/tcm_gemm_kernel.cuh", "tensor_core_matrix_gb300/csrc/tcm_kernel_common.cuh",
                   "tensor_core_matrix_gb300/csrc/tcm_ptx.cuh", "tensor_core_matrix_gb300/csrc/tcm_gemm_pair.cu"]
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_kernel_bf16_8192cubed.md")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_kernel_bf16_8192cubed.json")
+SLEEP_CYCLES = 400_000  # ~0.2 ms: lets the host enqueue a launch before its start event
 
 
 def parse_args():
@@ -58,6 +75,8 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-parts", action="store_true", help="skip the per-config parts")
+    ap.add_argument("--part-iters", type=int, default=20)
     ap.add_argument("--shapes", action="store_true",
                     help="instead of the step, time every configured workload shape (one JSON line each)")
     ap.add_argument("--shape-iters", type=int, default=20)
@@ -82,6 +101,17 @@ def peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def bf16_peak_for(region_s, peaks_used):
+    """(peak TFLOP/s, label): the burst figure for a timed region shorter than a second,
+    the figure measured over a seconds-long loop otherwise."""
+    p, src = peaks_used
+    if region_s >= SUSTAINED_AFTER_S:
+        return (float(p.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])),
+                f"{src} bf16_tflops_sustained (timed region {region_s:.3f} s, seconds-long)")
+    return (float(p.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])),
+            f"{src} bf16_tflops burst (timed region {region_s:.3f} s, under {SUSTAINED_AFTER_S:g} s)")
+
+
 def kernel_source_sha():
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
@@ -91,28 +121,24 @@ def kernel_source_sha():
 
 
 def recorded_traffic():
-    """dram bytes per launch of the bf16 8192^3 kernel from the committed ncu summary, if still current."""
+    """DRAM bytes per launch of the bf16 8192^3 kernel from the committed ncu record, if the
+    kernel sources are still the ones it was captured from (else None)."""
     try:
-        text = open(TRAFFIC_FILE).read()
-    except OSError:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
         return None
-    vals = {}
-    for line in text.splitlines():
-        entry = line.strip().lstrip("-* ").strip("`")
-        if "=" in entry and entry.startswith(("dram_bytes_per_launch", "kernel_source_sha")):
-            k, v = entry.split("=", 1)
-            vals[k.strip().strip("`")] = v.strip().strip("` ")
-    if vals.get("kernel_source_sha") != kernel_source_sha():
+    if rec.get("kernel_source_sha") != kernel_source_sha():
         return None
     try:
-        return float(vals["dram_bytes_per_launch"])
-    except (KeyError, ValueError):
+        return float(rec["dram_bytes_per_launch"])
+    except (KeyError, TypeError, ValueError):
         return None
 
 
 def smi_gpu_id(dev_index):
-    """nvidia-smi's name for CUDA device `dev_index`: its UUID (nvidia-smi numbers the
-    machine's GPUs itself and ignores CUDA_VISIBLE_DEVICES, so an index may name another GPU)."""
+    """The NVML / nvidia-smi name of CUDA device `dev_index`: its UUID (they number the
+    machine's GPUs themselves and ignore CUDA_VISIBLE_DEVICES, so an index may name another GPU)."""
     try:
         u = str(torch.cuda.get_device_properties(dev_index).uuid)
         if u:
@@ -123,73 +149,121 @@ def smi_gpu_id(dev_index):
     return vis[dev_index].strip() if dev_index < len(vis) else str(dev_index)
 
 
+# NVML clock-event reason bits (nvmlClocksEventReason*), the ones a timing must report
+REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+
 class ClockSampler:
-    """nvidia-smi clock / throttle samples taken while the timed region runs."""
+    """SM clock, power and clock-event reasons of one GPU, polled every `period` seconds
+    while a timed region runs.  Read-only NVML queries through ctypes (libnvidia-ml ships
+    with the driver); falls back to `nvidia-smi -lms` if NVML cannot be opened.  Each
+    sample carries a host timestamp so that summaries can keep only the samples taken
+    inside given windows (the timed regions)."""
 
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
-
-    def __init__(self, index):
+    def __init__(self, index, period=0.001):
         self.index = index
-        self.proc = None
-        self.path = os.path.join("/tmp", f"tcm_clocks_{os.getpid()}.csv")
+        self.period = period
+        self.samples = []  # (t, sm_mhz, max_mhz, power_w, reasons)
+        self.source = None
+        self.error = ""
+        self._stop = threading.Event()
+        self._thread = None
+        self._proc = None
+
+    def _open_nvml(self):
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if nv.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit_v2 failed")
+        h = ctypes.c_void_p()
+        if nv.nvmlDeviceGetHandleByUUID(ctypes.c_char_p(smi_gpu_id(self.index).encode()), ctypes.byref(h)) != 0:
+            raise OSError("nvmlDeviceGetHandleByUUID failed")
+        reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))  # NVML_CLOCK_SM = 1
+        return nv, h, reasons, float(mx.value)
+
+    def _poll_nvml(self, nv, h, reasons, max_mhz):
+        clk, pw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            t = time.perf_counter()
+            ok = nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0
+            nv.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw))
+            reasons(h, ctypes.byref(rs))
+            if ok:
+                self.samples.append((t, float(clk.value), max_mhz, pw.value / 1000.0, int(rs.value)))
+            time.sleep(self.period)
 
     def __enter__(self):
         try:
-            self.out = open(self.path, "w")
-            self.err = open(self.path + ".err", "w")
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", smi_gpu_id(self.index), f"--query-gpu={self.QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
-                                         stdout=self.out, stderr=self.err)
-        except (OSError, FileNotFoundError):
-            self.proc = None
+            nv, h, reasons, max_mhz = self._open_nvml()
+            self.source = f"nvml every {self.period * 1e3:g} ms"
+            self._thread = threading.Thread(target=self._poll_nvml, args=(nv, h, reasons, max_mhz), daemon=True)
+            self._thread.start()
+            while not self.samples and self._thread.is_alive():
+                time.sleep(0.001)
             return self
-        # do not start the timed region before the sampler is producing samples
-        deadline = time.time() + 15.0
-        while time.time() < deadline and self.proc.poll() is None:
-            if os.path.getsize(self.path) > 0:
-                break
-            time.sleep(0.05)
+        except (OSError, AttributeError) as e:
+            self.error = f"nvml: {e}"
+        try:
+            self._path = os.path.join("/tmp", f"tcm_clocks_{os.getpid()}.csv")
+            self._out = open(self._path, "w")
+            q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+                 "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_power_cap")
+            self._proc = subprocess.Popen(["nvidia-smi", "-i", smi_gpu_id(self.index), f"--query-gpu={q}",
+                                           "--format=csv,noheader,nounits", "-lms", "20"],
+                                          stdout=self._out, stderr=subprocess.DEVNULL)
+            self.source = "nvidia-smi -lms 20"
+            self._t_start = time.perf_counter()
+            deadline = time.time() + 15.0
+            while time.time() < deadline and self._proc.poll() is None and os.path.getsize(self._path) == 0:
+                time.sleep(0.05)
+        except (OSError, FileNotFoundError) as e:
+            self.error += f"; nvidia-smi: {e}"
+            self._proc = None
         return self
 
     def __exit__(self, *exc):
-        if self.proc is not None:
-            self.proc.terminate()
+        self._stop.set()
+        if self._thread is not None:
+            self._thread.join(timeout=5)
+        if self._proc is not None:
+            t_end = time.perf_counter()
+            self._proc.terminate()
             try:
-                self.proc.wait(timeout=5)
+                self._proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
-                self.proc.kill()
-            self.out.close()
-            self.err.close()
+                self._proc.kill()
+            self._out.close()
+            rows = []
+            for line in open(self._path):
+                f = [x.strip() for x in line.split(",")]
+                try:
+                    bits = sum(b for b, v in zip((0x8, 0x40, 0x20, 0x4), f[3:7]) if v.lower() == "active")
+                    rows.append((float(f[0]), float(f[1]), float(f[2]), bits))
+                except (ValueError, IndexError):
+                    continue
+            os.unlink(self._path)
+            # nvidia-smi rows carry no timestamps: spread them evenly over the sampling period
+            n = len(rows)
+            for i, r in enumerate(rows):
+                t = self._t_start + (t_end - self._t_start) * (i + 0.5) / max(n, 1)
+                self.samples.append((t, r[0], r[1], r[2], r[3]))
 
-    def summary(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        rows = []
-        for line in open(self.path):
-            parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
-            except ValueError:
-                continue
-        os.unlink(self.path)
-        err = ""
-        if os.path.exists(self.path + ".err"):
-            err = open(self.path + ".err").read().strip().splitlines()[:1]
-            err = err[0][:200] if err else ""
-            os.unlink(self.path + ".err")
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples" + (f": {err}" if err else "")],
-                    "samples": 0}
-        loaded = [r for r in rows if r[2] > 300.0] or rows
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[3]) if v.lower() == "active"})
-        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": reasons, "samples": len(rows), "samples_under_load": len(loaded),
-                "power_w_max": max(r[2] for r in rows)}
+    def summary(self, windows=None):
+        """Median SM clock etc. over the samples inside `windows` ([(t0, t1), ...]; all if None)."""
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0,
+                    "source": self.source, "error": self.error}
+        inside = [s for s in self.samples if windows is None or any(a <= s[0] <= b for a, b in windows)]
+        use = inside or self.samples
+        reasons = sorted({name for s in use for bit, name in REASON_BITS.items() if s[4] & bit})
+        return {"sm_mhz": statistics.median(s[1] for s in use), "sm_mhz_min": min(s[1] for s in use),
+                "sm_max_mhz": max(s[2] for s in self.samples), "reasons": reasons,
+                "samples": len(self.samples), "samples_under_load": len(inside),
+                "power_w_max": max(s[3] for s in use), "source": self.source}
 
 
 def gpu_local_cpus(device_index):
@@ -225,24 +299,27 @@ def local_rank_index(device):
     return device.index if device.index is not None else torch.cuda.current_device()
 
 
-def make_inputs(device):
-    """Resident device inputs of one step plus their pinned host copies (for the end-to-end leg)."""
+def step_host_inputs():
     dense = si.llm_case(SIZE, SIZE, SIZE, seed=2)  # bf16 A ~ N(0,1), B ~ N(0, 0.02)
     f8 = si.fp8_case(SIZE, SIZE, SIZE, b_fmt="e4m3", seed=3)
     sp = si.sparse_case(SIZE, SIZE, SIZE, seed=4)
-    host = {
+    return {
         "A": dense["A"], "B": dense["B"],
         "A8": f8["A"], "B8": f8["B"], "bias": f8["bias"],
         "sa": torch.tensor([f8["sa"]], dtype=torch.float32), "sb": torch.tensor([f8["sb"]], dtype=torch.float32),
         "Asp": sp["A_logical"], "Bsp": sp["B"],
     }
+
+
+def make_inputs(device):
+    """Resident device inputs of one step plus their pinned host copies (for the end-to-end leg)."""
+    host = step_host_inputs()
     pinned = {k: v.pin_memory() for k, v in host.items()}
     dev = {k: v.to(device) for k, v in host.items()}
     for k in ("D", "D8", "Dsp"):
         dev[k] = torch.empty((SIZE, SIZE), dtype=torch.bfloat16, device=device)
     dev["Ac"] = torch.empty((SIZE, SIZE // 2), dtype=torch.bfloat16, device=device)
     dev["meta"] = torch.empty((SIZE, SIZE // 32), dtype=torch.int32, device=device)
-    dev["meta_tc"] = torch.empty(META_TC_BYTES, dtype=torch.uint8, device=device)
     return host, pinned, dev
 
 
@@ -258,22 +335,19 @@ def run_step(tcm, dev, stream, events=None):
                     stream=stream)
     mark(2)
     tcm.tcm_sp_compress(dev["Asp"], dev["Ac"], dev["meta"], stream=stream)
-    tcm.tcm_sp_meta_pack(dev["meta"], SIZE, dev["meta_tc"], stream=stream)
     mark(3)
-    tcm.tcm_gemm_sp_tc(dev["Ac"], dev["meta_tc"], dev["Bsp"], dev["Dsp"], stream=stream)
+    tcm.tcm_gemm_sp(dev["Ac"], dev["meta"], dev["Bsp"], dev["Dsp"], stream=stream)
     mark(4)
 
 
-KERNELS_PER_STEP = 5
-# hardware-ordered metadata: ceil(M/128) * ceil(K/128) * 2048 bytes
-META_TC_BYTES = (SIZE // 128) * (SIZE // 128) * 2048
-GEMMS_PER_STEP = 3
-# compress (read A, write A_comp + canonical metadata) and metadata pack (read it, write meta_tc)
-COMPRESS_BYTES = SIZE * SIZE * 2 + SIZE * (SIZE // 2) * 2 + 2 * SIZE * (SIZE // 32) * 4 + META_TC_BYTES
+KERNELS_PER_STEP = 4
+# compress: read A, write A_comp and the canonical metadata
+COMPRESS_BYTES = SIZE * SIZE * 2 + SIZE * (SIZE // 2) * 2 + SIZE * (SIZE // 32) * 4
 
 
 class OracleSample:
-    """The CPU oracle on whole output rows of the step's three GEMMs (and the 2:4 compress of those rows)."""
+    """The CPU oracle on whole output rows of the step's three GEMMs (and the 2:4 compress of
+    those rows); keeps its results so that the GPU's outputs of the same rows can be checked."""
 
     def __init__(self, host):
         import oracle
@@ -283,17 +357,23 @@ class OracleSample:
         self.a8, self.b8, self.bias = si.codes(host["A8"]), si.codes(host["B8"]), si.codes(host["bias"])
         self.sa, self.sb = float(host["sa"][0]), float(host["sb"][0])
         self.asp, self.bsp = si.codes(host["Asp"]), si.codes(host["Bsp"])
+        self.last = None
 
     def rows(self, r):
+        """Rows 0 .. r-1 of every GEMM of the step; returns (dense FLOPs, all FLOPs) computed."""
         import numpy as np
         o = self.oracle
         rows = np.repeat(np.arange(r, dtype=np.int64), SIZE)
         cols = np.tile(np.arange(SIZE, dtype=np.int64), r)
-        o.gemm(self.a, self.b, "bf16", "bf16", rows=rows, cols=cols)
-        o.gemm(self.a8, self.b8, "e4m3", "e4m3", bias=self.bias, sa=self.sa, sb=self.sb, rows=rows, cols=cols)
+        out = {"D": o.gemm(self.a, self.b, "bf16", "bf16", rows=rows, cols=cols),
+               "D8": o.gemm(self.a8, self.b8, "e4m3", "e4m3", bias=self.bias, sa=self.sa, sb=self.sb,
+                            rows=rows, cols=cols)}
         ac, meta = o.sp_compress(np.ascontiguousarray(self.asp[:r]), "bf16")
-        o.gemm(o.sp_decompress(ac, meta, "bf16"), self.bsp, "bf16", "bf16", rows=rows, cols=cols)
-        return GEMMS_PER_STEP * 2.0 * r * SIZE * SIZE
+        out["Dsp"] = o.gemm(o.sp_decompress(ac, meta, "bf16"), self.bsp, "bf16", "bf16", rows=rows, cols=cols)
+        out["Ac"], out["meta"] = ac, meta
+        self.last = (r, out)
+        flop = 2.0 * r * SIZE * SIZE
+        return DENSE_GEMMS_PER_STEP * flop, 3 * flop
 
     def calibrate(self, seconds):
         t0 = time.perf_counter()
@@ -301,32 +381,49 @@ class OracleSample:
         per_row = max(time.perf_counter() - t0, 1e-6)
         return max(1, int(seconds / per_row))
 
+    def check(self, gpu):
+        """max err / bound of the GPU's rows of each GEMM and bit-equality of the compress;
+        `gpu` holds CPU copies of the first r rows of D, D8, Dsp, Ac and meta."""
+        import numpy as np
+        o = self.oracle
+        r, out = self.last
+        res = {"rows": r}
+        for key, name, scale in (("D", "bf16_dense", 1.0), ("D8", "e4m3_scaled_bias", self.sa * self.sb),
+                                 ("Dsp", "sp24_gemm_bf16", 1.0)):
+            ref, S = out[key]
+            res[name] = o.err_over_bound(si.codes(gpu[key][:r]).reshape(-1), "bf16", ref, S, scale)
+        res["sp24_compress_bit_exact"] = bool(
+            np.array_equal(si.codes(gpu["Ac"][:r]), out["Ac"]) and
+            np.array_equal(si.codes(gpu["meta"][:r]).view(np.uint32), out["meta"]))
+        res["ok"] = all(res[k] <= 1.0 for k in ("bf16_dense", "e4m3_scaled_bias", "sp24_gemm_bf16")) and \
+            res["sp24_compress_bit_exact"]
+        return res
 
-def cpu_baseline_sample(host, seconds):
-    """Time the CPU oracle on about `seconds` of whole output rows of the step's GEMMs."""
+
+def cpu_baseline_sample(host, seconds, gpu_rows):
+    """Time the CPU oracle on about `seconds` of whole output rows of the step's GEMMs and check
+    the GPU's outputs of the same rows against it.  Returns (baseline, check)."""
     o = OracleSample(host)
-    r = o.calibrate(seconds)
+    r = min(o.calibrate(seconds), min(t.shape[0] for t in gpu_rows.values()))
     t0 = time.perf_counter()
-    flop = o.rows(r)
+    dense_flop, flop = o.rows(r)
     t = time.perf_counter() - t0
     cores = len(os.sched_getaffinity(0))
-    return {"value": flop / t / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+    base = {"value": dense_flop / t / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "sample": f"{r} full output rows (8192 outputs of K=8192 each) of each of the step's three GEMMs "
                       f"(bf16, E4M3 with scales+bias, 2:4-sparse bf16 incl. compress of those rows), "
-                      f"{t:.1f} s on {cores} host threads (OpenMP)"}
+                      f"{t:.1f} s on {cores} host threads (OpenMP); value counts the two dense GEMMs' FLOPs "
+                      f"like the GPU line",
+            "extrapolated_full_step_s": t * SIZE / r,
+            "extrapolated_note": "extrapolated: sample time x M / rows (per-MAC time x M*N*K of each GEMM)"}
+    return base, o.check(gpu_rows)
 
 
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    dense = si.llm_case(SIZE, SIZE, SIZE, seed=2)
-    f8 = si.fp8_case(SIZE, SIZE, SIZE, b_fmt="e4m3", seed=3)
-    sp = si.sparse_case(SIZE, SIZE, SIZE, seed=4)
-    host = {"A": dense["A"], "B": dense["B"], "A8": f8["A"], "B8": f8["B"], "bias": f8["bias"],
-            "sa": torch.tensor([f8["sa"]]), "sb": torch.tensor([f8["sb"]]),
-            "Asp": sp["A_logical"], "Bsp": sp["B"]}
-    o = OracleSample(host)
+    o = OracleSample(step_host_inputs())
     cores = len(os.sched_getaffinity(0))
     r = o.calibrate(90.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
@@ -334,7 +431,7 @@ def run_reference(args):
     t0 = time.perf_counter()
     flop = 0.0
     for _ in range(args.steps):
-        flop += o.rows(r)
+        flop += o.rows(r)[0]
     t = time.perf_counter() - t0
     value = flop / t / 1e12
     line = {
@@ -344,11 +441,138 @@ def run_reference(args):
         "data": "synthetic", "config": config_block(world),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": f"each step: {r} full output rows of each of the three 8192^3 GEMMs "
-                                   f"(fp64 CPU oracle, {cores} host threads)"},
+                                   f"(fp64 CPU oracle, {cores} host threads); value counts the two dense "
+                                   f"GEMMs' FLOPs"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
+
+# ------------------------------------------------------------------ per-config parts
+
+class LaunchTimer:
+    """Device time of single launches and of back-to-back runs on one stream.
+
+    single(): before each launch the stream sleeps ~0.2 ms (torch's device-side sleep)
+    so that the host has enqueued the launch before its start event is reached: the
+    event pair then brackets the kernel alone, not the host-side cost of the call.
+    `flush` writes 256 MiB (more than L2) before each launch."""
+
+    def __init__(self, device, stream):
+        self.stream = stream
+        self.flush_buf = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=device)
+        self.windows = []
+
+    def single(self, launch, iters, flush, sleep=True):
+        times = []
+        t0 = time.perf_counter()
+        for _ in range(iters):
+            with torch.cuda.stream(self.stream):
+                if flush:
+                    self.flush_buf.fill_(1)
+                if sleep and hasattr(torch.cuda, "_sleep"):
+                    torch.cuda._sleep(SLEEP_CYCLES)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(self.stream)
+                launch()
+                e1.record(self.stream)
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1))
+        self.windows.append((t0, time.perf_counter()))
+        return times
+
+    def back_to_back(self, launch, iters):
+        t0 = time.perf_counter()
+        with torch.cuda.stream(self.stream):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(self.stream)
+            for _ in range(iters):
+                launch()
+            e1.record(self.stream)
+        e1.synchronize()
+        self.windows.append((t0, time.perf_counter()))
+        return e0.elapsed_time(e1) / iters
+
+
+def part_cases():
+    """(name, builder, bound) of every configured workload besides the step's."""
+    return [
+        ("c1_bf16_512_C_f32", lambda: si.small_case(), "launch"),
+        ("c2_f16_4096", lambda: si.square_case(4096, "f16"), "tensor"),
+        ("c2_bf16_4096", lambda: si.square_case(4096, "bf16"), "tensor"),
+        ("c3_bf16_8192x28672x8192", lambda: si.llm_case(8192, 28672, 8192), "tensor"),
+        ("c3_bf16_8192x8192x28672", lambda: si.llm_case(8192, 8192, 28672), "tensor"),
+        ("c3_bf16_8192x24576x8192", lambda: si.llm_case(8192, 24576, 8192), "tensor"),
+        ("c3_skinny_bf16_16x28672x8192", lambda: si.llm_case(16, 28672, 8192), "hbm"),
+        ("c4_e4m3xe5m2_8192", lambda: si.fp8_case(b_fmt="e5m2"), "tensor"),
+    ]
+
+
+def run_parts(tcm, device, iters, peaks_used):
+    """Each configured workload timed on its own, outside `value`: median device time of
+    single launches (L2 flushed first when the inputs fit in it), the mean of back-to-back
+    launches, TFLOP/s against the burst tensor peak and, for the HBM-bound skinny shape,
+    GB/s of its algorithmic bytes against the measured copy bandwidth."""
+    p, src = peaks_used
+    bf16_peak = float(p.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    hbm_peak = float(p.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    stream = torch.cuda.Stream(device=device)
+    timer = LaunchTimer(device, stream)
+    parts = {}
+    for name, build, bound in part_cases():
+        case = build()
+        A, B = case["A"].to(device), case["B"].to(device)
+        M, K = A.shape
+        N = B.shape[0]
+        out = torch.float32 if case.get("out_fmt") == "f32" else torch.bfloat16
+        D = torch.empty((M, N), dtype=out, device=device)
+        C = case["C"].to(device) if case.get("C") is not None else None
+        kw = dict(C=C, alpha=case.get("alpha", 1.0), beta=case.get("beta", 0.0), stream=stream)
+        if "sa" in case:
+            kw.update(a_scale=torch.tensor([case["sa"]], device=device),
+                      b_scale=torch.tensor([case["sb"]], device=device), bias=case["bias"].to(device))
+
+        def launch():
+            tcm.tcm_gemm_ex(A, B, D, **kw)
+
+        for _ in range(5):
+            launch()
+        in_bytes = A.numel() * A.element_size() + B.numel() * B.element_size()
+        alg_bytes = in_bytes + D.numel() * D.element_size() + (C.numel() * C.element_size() if C is not None else 0)
+        flush = in_bytes < L2_BYTES
+        t_single = timer.single(launch, iters, flush)
+        t_b2b = timer.back_to_back(launch, iters)
+        ms = statistics.median(t_single)
+        flop = 2.0 * M * N * K
+        peak = bf16_peak * (FP8_OVER_BF16 if "e4m3" in name else 1.0)
+        rec = {"M": M, "N": N, "K": K, "ms": ms, "ms_min": min(t_single), "ms_back_to_back": t_b2b,
+               "tflops": flop / (ms * 1e-3) / 1e12, "tflops_back_to_back": flop / (t_b2b * 1e-3) / 1e12,
+               "frac_of_tensor_peak": flop / (ms * 1e-3) / 1e12 / peak, "bound": bound,
+               "timing": f"median of {iters} single launches (device sleep before each start event, "
+                         f"{'L2 flushed before each' if flush else 'inputs larger than L2, no flush'}); "
+                         f"mean of {iters} back-to-back launches"}
+        if bound == "hbm":
+            t_flushed = timer.single(launch, iters, True)
+            t_call = timer.single(launch, iters, False, sleep=False)
+            msf = statistics.median(t_flushed)
+            rec.update({"algorithmic_bytes": alg_bytes,
+                        "gbs": alg_bytes / (ms * 1e-3) / 1e9, "frac_of_hbm": alg_bytes / (ms * 1e-3) / 1e9 / hbm_peak,
+                        "ms_l2_flushed": msf, "gbs_l2_flushed": alg_bytes / (msf * 1e-3) / 1e9,
+                        "frac_of_hbm_l2_flushed": alg_bytes / (msf * 1e-3) / 1e9 / hbm_peak,
+                        "gbs_back_to_back": alg_bytes / (t_b2b * 1e-3) / 1e9,
+                        "frac_of_hbm_back_to_back": alg_bytes / (t_b2b * 1e-3) / 1e9 / hbm_peak,
+                        "ms_per_call_synchronised": statistics.median(t_call),
+                        "host_call_us": 1e3 * (statistics.median(t_call) - ms)})
+        parts[name] = rec
+        del A, B, C, D, case
+    torch.cuda.synchronize(device)
+    code, site = tcm.tcm_get_device_status(stream)
+    if code != 0:
+        raise SystemExit(f"device status {code} at site {site} in the per-config parts")
+    return parts, timer.windows, f"{src} bf16_tflops burst (single launches); FP8 x{FP8_OVER_BF16:g}; hbm_gbs"
+
+
+# ------------------------------------------------------------------ --shapes (extended list)
 
 def shape_cases():
     """(name, builder) for every configured workload shape; builders return CPU inputs."""
@@ -363,6 +587,7 @@ def shape_cases():
         ("fp8 e4m3xe4m3 8192^3 +scales+bias", lambda: si.fp8_case(b_fmt="e4m3")),
         ("fp8 e4m3xe5m2 8192^3 +scales+bias", lambda: si.fp8_case(b_fmt="e5m2")),
         ("sparse 2:4 bf16 8192^3", lambda: si.sparse_case()),
+        ("sparse-tc 2:4 bf16 8192^3 (hardware-ordered metadata)", lambda: dict(si.sparse_case(), tc=True)),
         ("mxfp8 e4m3 8192^3 (E8M0 scales per 32)", lambda: si.mx_case()),
         ("nvfp4 e2m1 8192^3 (UE4M3 scales per 16, per-tensor scales in alpha)", lambda: dict(si.nvfp4_case(), nv=True)),
         ("w4a8 fp8 e4m3 x fp4 e2m1 8192^3 +scales", lambda: si.w4a8_case()),
@@ -372,12 +597,13 @@ def shape_cases():
 
 
 def run_shapes(args, tcm, device, peaks_used):
-    """Median device time of each configured shape, L2 flushed before every timed launch."""
+    """Median device time of each configured shape (single launches, L2 flushed when the
+    inputs fit in it) and the mean of back-to-back launches; one JSON line each."""
     p, src = peaks_used
-    bf16_peak = float(p.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    bf16_peak = float(p.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     hbm_peak = float(p.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=device)
-    stream = torch.cuda.current_stream(device)
+    stream = torch.cuda.Stream(device=device)
+    timer = LaunchTimer(device, stream)
     for name, build in shape_cases():
         if args.only and args.only not in name:
             continue
@@ -392,7 +618,7 @@ def run_shapes(args, tcm, device, peaks_used):
             out_dtype = torch.float8_e4m3fn
         D = torch.empty((M, N), dtype=out_dtype, device=device)
         C = case["C"].to(device) if case.get("C") is not None else None
-        kw = dict(C=C, alpha=case.get("alpha", 1.0), beta=case.get("beta", 0.0))
+        kw = dict(C=C, alpha=case.get("alpha", 1.0), beta=case.get("beta", 0.0), stream=stream)
         if "sa" in case:
             kw.update(a_scale=torch.tensor([case["sa"]], device=device), b_scale=torch.tensor([case["sb"]], device=device))
             if case.get("bias") is not None:
@@ -401,61 +627,37 @@ def run_shapes(args, tcm, device, peaks_used):
             kw.update(b_fmt="e2m1")  # B holds N x K/2 bytes of packed FP4
         if sparse:
             Ac, meta = tcm.tcm_sp_compress(A)
-            meta_tc = tcm.tcm_sp_meta_pack(meta, K)
-            launch = lambda: tcm.tcm_gemm_sp_tc(Ac, meta_tc, B, D, C=C, alpha=kw["alpha"], beta=kw["beta"])
+            if case.get("tc"):
+                meta_tc = tcm.tcm_sp_meta_pack(meta, K)
+                launch = lambda: tcm.tcm_gemm_sp_tc(Ac, meta_tc, B, D, C=C, alpha=kw["alpha"], beta=kw["beta"],
+                                                    stream=stream)
+            else:
+                launch = lambda: tcm.tcm_gemm_sp(Ac, meta, B, D, C=C, alpha=kw["alpha"], beta=kw["beta"],
+                                                 stream=stream)
         elif case.get("nv"):
             SA = tcm.tcm_nvfp4_pack_scales(case["SA"].to(device), 2 * K)
             SB = tcm.tcm_nvfp4_pack_scales(case["SB"].to(device), 2 * K)
             K = 2 * K  # A holds K/2 bytes per row
-            launch = lambda: tcm.tcm_gemm_nvfp4(A, SA, B, SB, D, alpha=case["alpha"])
+            launch = lambda: tcm.tcm_gemm_nvfp4(A, SA, B, SB, D, alpha=case["alpha"], stream=stream)
         elif "SA" in case:
             # scales packed once into the blocked layout (as a quantiser would emit them)
             SA = tcm.tcm_mx_pack_scales(case["SA"].to(device), K)
             SB = tcm.tcm_mx_pack_scales(case["SB"].to(device), K)
-            launch = lambda: tcm.tcm_gemm_mx(A, SA, B, SB, D)
+            launch = lambda: tcm.tcm_gemm_mx(A, SA, B, SB, D, stream=stream)
         elif case.get("fused"):
             d_scale = torch.tensor([2.0], device=device)
             amax = torch.zeros(1, device=device)
             launch = lambda: tcm.tcm_gemm_fused(A, B, D, act=case["fused"], d_scale=d_scale, amax=amax, **kw)
         else:
             launch = lambda: tcm.tcm_gemm_ex(A, B, D, **kw)
+        torch.cuda.synchronize(device)
         for _ in range(5):
             launch()
         in_bytes_total = sum(t.numel() * t.element_size() for t in (A, B) if t is not None)
-        needs_flush = in_bytes_total < L2_BYTES  # inputs larger than L2 are not flushed
-        times = []
-        for _ in range(args.shape_iters):
-            if needs_flush:
-                flush.fill_(1)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            launch()
-            e1.record(stream)
-            e1.synchronize()
-            times.append(e0.elapsed_time(e1))
-        ms_b2b = ms_flushed = None
-        if not needs_flush:
-            # also with L2 flushed before each launch (the inputs exceed L2, so this changes little)
-            flushed = []
-            for _ in range(args.shape_iters):
-                flush.fill_(1)
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                launch()
-                e1.record(stream)
-                e1.synchronize()
-                flushed.append(e0.elapsed_time(e1))
-            ms_flushed = statistics.median(flushed)
-            # the same launches back to back (inputs exceed L2 anyway): the host-side cost of
-            # each call (tensor maps, launch) overlaps the previous kernel instead of adding to it
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(args.shape_iters):
-                launch()
-            e1.record(stream)
-            e1.synchronize()
-            ms_b2b = e0.elapsed_time(e1) / args.shape_iters
-        code, site = tcm.tcm_get_device_status()
+        flush = in_bytes_total < L2_BYTES
+        times = timer.single(launch, args.shape_iters, flush)
+        ms_b2b = timer.back_to_back(launch, args.shape_iters)
+        code, site = tcm.tcm_get_device_status(stream)
         ms = statistics.median(times)
         flop = 2.0 * M * N * K
         in_bytes = (A.numel() // (2 if sparse else 1)) * A.element_size() + B.numel() * B.element_size()
@@ -467,19 +669,23 @@ def run_shapes(args, tcm, device, peaks_used):
         line = {"kind": "shape", "workload": name, "M": M, "N": N, "K": K, "ms_median": ms, "ms_min": min(times),
                 "tflops": tf, "frac_of_tensor_peak": tf / peak, "algorithmic_bytes": byts, "gbs": gbs,
                 "frac_of_hbm": gbs / hbm_peak, "bound": "hbm" if M <= 64 else "tensor", "device_status": code,
-                "ms_back_to_back": ms_b2b, "ms_median_l2_flushed": ms_flushed,
-                "timing": f"5 warm-up launches, then the median of {args.shape_iters} launches, each synchronised; " + (
-                    "L2 flushed (256 MiB write) before each" if needs_flush else "inputs larger than L2, no flush"),
-                "peak_source": src}
+                "ms_back_to_back": ms_b2b, "tflops_back_to_back": flop / (ms_b2b * 1e-3) / 1e12,
+                "timing": f"5 warm-up launches, then the median of {args.shape_iters} single launches (device "
+                          f"sleep before each start event; " + (
+                              "L2 flushed before each)" if flush else "inputs larger than L2, no flush)") +
+                          f"; mean of {args.shape_iters} back-to-back launches",
+                "peak_source": f"{src} bf16_tflops burst"}
         print(json.dumps(line), flush=True)
         del A, B, D, C, case
 
 
 def config_block(world):
     return {"workload": "GEMM 8192^3 (M=N=K=8192): bf16 x bf16 -> bf16; E4M3 x E4M3 with per-tensor "
-                        "scales + bf16 bias -> bf16; 2:4-sparse bf16 A (compress + metadata pack + sparse GEMM) -> bf16; "
-                        "A row-major, B K-major, fp32 accumulate",
+                        "scales + bf16 bias -> bf16; 2:4-sparse bf16 A (compress + sparse GEMM on canonical "
+                        "metadata) -> bf16; A row-major, B K-major, fp32 accumulate",
             "M": SIZE, "N": SIZE, "K": SIZE,
+            "value_counts": "2*M*N*K of the bf16 and E4M3 GEMMs per step (the sparse GEMM runs in the step; "
+                            "its logical FLOPs are reported in parts.sp24_gemm_bf16 only)",
             "inputs": "bf16 A ~ N(0,1), B ~ N(0,0.02) (seed 2); E4M3 A, B ~ N(0,1) scaled so amax = 448 (seed 3); "
                       "sparse: logical A, B ~ N(0,1) bf16 (seed 4)",
             "l2": "no flush: each GEMM's inputs (256 MiB bf16, 128 MiB E4M3) exceed the 129 MB L2",
@@ -517,9 +723,9 @@ def main():
     # allocate (first-touch) the pinned host buffers from CPUs local to the GPU,
     # so host<->device copies do not cross the CPU-to-CPU link
     saved_affinity = os.sched_getaffinity(0)
-    local = gpu_local_cpus(local_rank_index(device))
-    if local:
-        os.sched_setaffinity(0, local)
+    local_cpus = gpu_local_cpus(local_rank_index(device))
+    if local_cpus:
+        os.sched_setaffinity(0, local_cpus)
     host, pinned, dev = make_inputs(device)
     # the end-to-end results' pinned buffers (two sets), first-touched here as well
     outs = [{k: torch.empty((SIZE, SIZE), dtype=torch.bfloat16).pin_memory() for k in ("D", "D8", "Dsp")}
@@ -536,15 +742,17 @@ def main():
     if pg:
         pg.barrier()
     torch.cuda.synchronize(device)
-    with ClockSampler(local) as clocks:
+    with ClockSampler(local_rank_index(device)) as clocks:
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
+        h0 = time.perf_counter()
         with torch.cuda.stream(stream):
             t_start.record(stream)
             for i in range(args.steps):
                 run_step(tcm, dev, stream, ev[i])
             t_end.record(stream)
         t_end.synchronize()
+        h1 = time.perf_counter()
     torch.cuda.synchronize(device)
     elapsed_ms = t_start.elapsed_time(t_end)
     bf16_ms = [e[0].elapsed_time(e[1]) for e in ev]
@@ -554,6 +762,12 @@ def main():
     code, site = tcm.tcm_get_device_status(stream)
     if code != 0:
         raise SystemExit(f"device status {code} at site {site}")
+    step_clocks = clocks.summary([(h0, h1)])
+    # the last timed step's outputs, for the oracle check of the CPU-baseline leg
+    check_rows = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n = 1024
+        check_rows = {k: dev[k][:n].cpu() for k in ("D", "D8", "Dsp", "Ac", "meta")}
 
     # end-to-end: every step copies all of its inputs in from pinned host memory
     # and all three results back out.  Copies run on their own streams and are
@@ -597,21 +811,32 @@ def main():
             e1.synchronize()
             return e0.elapsed_time(e1)
 
-        # untimed warm-up of the copy path: after the seconds-long device-only loop above, the
-        # first host copies run far slower (measured: 111 ms for one step's 671 MB in)
+        # untimed warm-up of the copy path: after the device-only loop above, the first
+        # host copies run far slower (measured: 111 ms for one step's 671 MB in)
         e2e_steps(max(8, args.warmup))
         if pg:
             pg.barrier()
         torch.cuda.synchronize(device)
         e2e_ms = e2e_steps(args.e2e_steps) / args.e2e_steps
+        del sets
 
     elapsed_ms, e2e_max = slowest_rank(pg, [elapsed_ms, e2e_ms or 0.0], device)
 
+    parts_cfg, parts_clocks, parts_peak = {}, None, None
+    if not args.no_parts and rank == 0:
+        del dev
+        torch.cuda.empty_cache()
+        with ClockSampler(local_rank_index(device)) as pclocks:
+            parts_cfg, windows, parts_peak = run_parts(tcm, device, args.part_iters, peaks())
+        parts_clocks = pclocks.summary(windows)
+
+    exit_code = 0
     if rank == 0:
         p, src = peaks()
-        bf16_peak = float(p.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+        region_s = elapsed_ms * 1e-3
+        bf16_peak, peak_label = bf16_peak_for(region_s, (p, src))
         ms_step = elapsed_ms / args.steps
-        flop_step = GEMMS_PER_STEP * FLOP_PER_GEMM
+        flop_step = DENSE_GEMMS_PER_STEP * FLOP_PER_GEMM
         value = whole_job_rate(world, flop_step * args.steps, elapsed_ms * 1e-3) / 1e12
         t_bf16 = statistics.mean(bf16_ms)
         t_fp8 = statistics.mean(fp8_ms)
@@ -623,7 +848,9 @@ def main():
         ach_sp = FLOP_PER_GEMM / (t_sp * 1e-3) / 1e12
         hbm_peak = float(p.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
         cmp_gbs = COMPRESS_BYTES / (t_cmp * 1e-3) / 1e9
-        traffic = recorded_traffic()
+        sms = torch.cuda.get_device_properties(device).multi_processor_count
+        mhz = step_clocks.get("sm_mhz")
+        clock_peak = sms * BF16_FLOP_PER_CLK_PER_SM * mhz * 1e6 / 1e12 if mhz else None
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -631,20 +858,30 @@ def main():
             "parts": {
                 "bf16_dense": {"tflops": ach_bf16, "ms": t_bf16, "frac_of_bf16_peak": ach_bf16 / bf16_peak},
                 "e4m3_scaled_bias": {"tflops": ach_fp8, "ms": t_fp8, "frac_of_fp8_peak": ach_fp8 / fp8_peak},
-                "sp24_compress_and_meta_pack": {"gbs": cmp_gbs, "ms": t_cmp, "frac_of_hbm": cmp_gbs / hbm_peak,
-                                                "bytes": COMPRESS_BYTES},
+                "sp24_compress": {"gbs": cmp_gbs, "ms": t_cmp, "frac_of_hbm": cmp_gbs / hbm_peak,
+                                  "bytes": COMPRESS_BYTES},
                 "sp24_gemm_bf16": {"tflops_logical": ach_sp, "ms": t_sp,
-                                   "frac_of_dense_bf16_peak": ach_sp / bf16_peak},
+                                   "frac_of_2to4_peak": ach_sp / (2 * bf16_peak),
+                                   "note": "logical 2*M*N*K (twice the issued MMA work); peak = 2 x dense bf16"},
+                "peak_source": peak_label,
+                **parts_cfg,
             },
             "roofline": {"bound": "tensor", "achieved": ach_bf16, "peak": bf16_peak, "unit": "TFLOP/s",
-                         "frac": ach_bf16 / bf16_peak, "traffic": traffic,
+                         "frac": ach_bf16 / bf16_peak, "traffic": recorded_traffic(),
                          "kernel": "gemm_kernel<kind::f16, 256x256 CTA-pair tile, 6 stages> bf16 8192^3",
-                         "peak_source": f"{src} bf16_tflops_sustained (kernel timed inside a multi-second "
-                                        f"back-to-back loop)",
+                         "peak_source": peak_label, "timed_region_s": region_s,
                          "algorithmic_flop_per_launch": FLOP_PER_GEMM},
             "gpu_launches": KERNELS_PER_STEP * args.steps,
-            "clocks": clocks.summary(),
+            "clocks": step_clocks,
         }
+        if clock_peak:
+            line["roofline"]["clock_derived"] = {
+                "sm_mhz_median": mhz, "sms": sms, "flop_per_clk_per_sm": BF16_FLOP_PER_CLK_PER_SM,
+                "peak_tflops": clock_peak, "frac": ach_bf16 / clock_peak,
+                "note": "SMs x dense bf16 FLOP per clock per SM x median SM clock sampled in the timed region"}
+        if parts_clocks is not None:
+            line["parts"]["clocks"] = parts_clocks
+            line["parts"]["config_peak_source"] = parts_peak
         if e2e_ms:
             line["e2e"] = {"value": whole_job_rate(world, flop_step, e2e_max * 1e-3) / 1e12, "unit": "TFLOP/s",
                            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -652,13 +889,19 @@ def main():
                                    f"copies all inputs in from pinned host "
                                    f"memory and all three D out; copies overlap the GEMMs of neighbouring steps; "
                                    f"pinned buffers allocated from "
-                                   f"{'GPU-local CPUs ' + str(len(local)) if local else 'the default CPU set'}"}
-        if not args.no_cpu_baseline and world == 1:
-            line["cpu_baseline"] = cpu_baseline_sample(host, args.cpu_seconds)
+                                   f"{'GPU-local CPUs ' + str(len(local_cpus)) if local_cpus else 'the default CPU set'}"}
+        if check_rows is not None:
+            base, check = cpu_baseline_sample(host, args.cpu_seconds, check_rows)
+            line["cpu_baseline"] = base
+            line["check"] = check
+            if not check["ok"]:
+                exit_code = 1
         print(json.dumps(line), flush=True)
     if pg:
         pg.barrier()
         pg.destroy_process_group()
+    if exit_code:
+        raise SystemExit(f"timed outputs outside the oracle bound: {line['check']}")
 
 
 if __name__ == "__main__":
