@@ -320,24 +320,45 @@ def make_inputs(device):
         dev[k] = torch.empty((SIZE, SIZE), dtype=torch.bfloat16, device=device)
     dev["Ac"] = torch.empty((SIZE, SIZE // 2), dtype=torch.bfloat16, device=device)
     dev["meta"] = torch.empty((SIZE, SIZE // 32), dtype=torch.int32, device=device)
+    # workspace of the dense GEMMs (tail tiles split over K); one buffer serves both, in turn
+    import tensor_core_matrix_gb300 as tcm
+    ws = max(tcm.tcm_gemm_workspace_bytes(SIZE, SIZE, SIZE, torch.bfloat16),
+             tcm.tcm_gemm_workspace_bytes(SIZE, SIZE, SIZE, torch.float8_e4m3fn))
+    dev["ws"] = torch.empty(max(ws, 16), dtype=torch.uint8, device=device)
     return host, pinned, dev
 
 
-def run_step(tcm, dev, stream, events=None):
-    """One pass of the hot path; events[0..4] bracket the four launches on `stream`."""
+def run_step(tcm, dev, stream, events=None, probes=None):
+    """One pass of the hot path; events[0..4] bracket the four launches on `stream`;
+    probes: per-GEMM clock-probe counters (tcm_set_clock_probe) or None."""
     def mark(i):
         if events:
             events[i].record(stream)
+
+    def probe(key):
+        if probes is not None:
+            tcm.tcm_set_clock_probe(probes.get(key))
     mark(0)
-    tcm.tcm_gemm_ex(dev["A"], dev["B"], dev["D"], stream=stream)
+    probe("bf16_dense")
+    tcm.tcm_gemm_ex(dev["A"], dev["B"], dev["D"], workspace=dev["ws"], stream=stream)
     mark(1)
+    probe("e4m3_scaled_bias")
     tcm.tcm_gemm_ex(dev["A8"], dev["B8"], dev["D8"], a_scale=dev["sa"], b_scale=dev["sb"], bias=dev["bias"],
-                    stream=stream)
+                    workspace=dev["ws"], stream=stream)
     mark(2)
+    probe(None)
     tcm.tcm_sp_compress(dev["Asp"], dev["Ac"], dev["meta"], stream=stream)
     mark(3)
+    probe("sp24_gemm_bf16")
     tcm.tcm_gemm_sp(dev["Ac"], dev["meta"], dev["Bsp"], dev["Dsp"], stream=stream)
     mark(4)
+    probe(None)
+
+
+def probe_mhz(counters):
+    """SM clock (MHz) of the launches a clock probe saw: cycles / global-timer ns of their first CTA."""
+    c = counters.cpu().tolist()
+    return 1e3 * c[0] / c[1] if c[1] > 0 else None
 
 
 KERNELS_PER_STEP = 4
@@ -531,6 +552,9 @@ def run_parts(tcm, device, iters, peaks_used):
         if "sa" in case:
             kw.update(a_scale=torch.tensor([case["sa"]], device=device),
                       b_scale=torch.tensor([case["sb"]], device=device), bias=case["bias"].to(device))
+        ws_bytes = tcm.tcm_gemm_workspace_bytes(M, N, K, A.dtype, B.dtype)
+        if ws_bytes > 0:
+            kw.update(workspace=torch.empty(ws_bytes, dtype=torch.uint8, device=device))
 
         def launch():
             tcm.tcm_gemm_ex(A, B, D, **kw)
@@ -540,14 +564,18 @@ def run_parts(tcm, device, iters, peaks_used):
         in_bytes = A.numel() * A.element_size() + B.numel() * B.element_size()
         alg_bytes = in_bytes + D.numel() * D.element_size() + (C.numel() * C.element_size() if C is not None else 0)
         flush = in_bytes < L2_BYTES
+        probe = torch.zeros(3, dtype=torch.int64, device=device)
+        tcm.tcm_set_clock_probe(probe)
         t_single = timer.single(launch, iters, flush)
         t_b2b = timer.back_to_back(launch, iters)
+        tcm.tcm_set_clock_probe(None)
         ms = statistics.median(t_single)
         flop = 2.0 * M * N * K
         peak = bf16_peak * (FP8_OVER_BF16 if "e4m3" in name else 1.0)
         rec = {"M": M, "N": N, "K": K, "ms": ms, "ms_min": min(t_single), "ms_back_to_back": t_b2b,
                "tflops": flop / (ms * 1e-3) / 1e12, "tflops_back_to_back": flop / (t_b2b * 1e-3) / 1e12,
                "frac_of_tensor_peak": flop / (ms * 1e-3) / 1e12 / peak, "bound": bound,
+               "device_measured_mhz": probe_mhz(probe), "workspace_bytes": ws_bytes,
                "timing": f"median of {iters} single launches (device sleep before each start event, "
                          f"{'L2 flushed before each' if flush else 'inputs larger than L2, no flush'}); "
                          f"mean of {iters} back-to-back launches"}
@@ -681,8 +709,9 @@ def run_shapes(args, tcm, device, peaks_used):
 
 def config_block(world):
     return {"workload": "GEMM 8192^3 (M=N=K=8192): bf16 x bf16 -> bf16; E4M3 x E4M3 with per-tensor "
-                        "scales + bf16 bias -> bf16; 2:4-sparse bf16 A (compress + sparse GEMM on canonical "
-                        "metadata) -> bf16; A row-major, B K-major, fp32 accumulate",
+                        "scales + bf16 bias -> bf16 (both through tcm_gemm_ex_ws: the last round's tiles split "
+                        "over K); 2:4-sparse bf16 A (compress + sparse GEMM on canonical metadata) -> bf16; "
+                        "A row-major, B K-major, fp32 accumulate",
             "M": SIZE, "N": SIZE, "K": SIZE,
             "value_counts": "2*M*N*K of the bf16 and E4M3 GEMMs per step (the sparse GEMM runs in the step; "
                             "its logical FLOPs are reported in parts.sp24_gemm_bf16 only)",
@@ -739,6 +768,9 @@ def main():
     stream.synchronize()
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    # SM clock measured on the device: each GEMM's first CTA adds its cycles and ns
+    probes = {k: torch.zeros(3, dtype=torch.int64, device=device)
+              for k in ("bf16_dense", "e4m3_scaled_bias", "sp24_gemm_bf16")}
     if pg:
         pg.barrier()
     torch.cuda.synchronize(device)
@@ -749,11 +781,12 @@ def main():
         with torch.cuda.stream(stream):
             t_start.record(stream)
             for i in range(args.steps):
-                run_step(tcm, dev, stream, ev[i])
+                run_step(tcm, dev, stream, ev[i], probes)
             t_end.record(stream)
         t_end.synchronize()
         h1 = time.perf_counter()
     torch.cuda.synchronize(device)
+    device_mhz = {k: probe_mhz(v) for k, v in probes.items()}
     elapsed_ms = t_start.elapsed_time(t_end)
     bf16_ms = [e[0].elapsed_time(e[1]) for e in ev]
     fp8_ms = [e[1].elapsed_time(e[2]) for e in ev]
@@ -849,8 +882,11 @@ def main():
         hbm_peak = float(p.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
         cmp_gbs = COMPRESS_BYTES / (t_cmp * 1e-3) / 1e9
         sms = torch.cuda.get_device_properties(device).multi_processor_count
-        mhz = step_clocks.get("sm_mhz")
+        mhz = device_mhz.get("bf16_dense")
         clock_peak = sms * BF16_FLOP_PER_CLK_PER_SM * mhz * 1e6 / 1e12 if mhz else None
+        step_clocks["device_measured_mhz"] = device_mhz
+        step_clocks["device_measured_note"] = ("SM clock during each GEMM of the timed region, measured on the "
+                                               "device: %clock64 cycles / %globaltimer ns of each launch's first CTA")
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -876,9 +912,11 @@ def main():
         }
         if clock_peak:
             line["roofline"]["clock_derived"] = {
-                "sm_mhz_median": mhz, "sms": sms, "flop_per_clk_per_sm": BF16_FLOP_PER_CLK_PER_SM,
+                "sm_mhz": mhz, "sms": sms, "flop_per_clk_per_sm": BF16_FLOP_PER_CLK_PER_SM,
                 "peak_tflops": clock_peak, "frac": ach_bf16 / clock_peak,
-                "note": "SMs x dense bf16 FLOP per clock per SM x median SM clock sampled in the timed region"}
+                "kernel_time_x_mhz_mcycles": t_bf16 * 1e-3 * mhz,
+                "note": "SMs x dense bf16 FLOP per clock per SM x the SM clock measured on the device during "
+                        "the bf16 launches of the timed region"}
         if parts_clocks is not None:
             line["parts"]["clocks"] = parts_clocks
             line["parts"]["config_peak_source"] = parts_peak

@@ -126,6 +126,40 @@ tcm_status tcm_gemm_ex(int64_t M, int64_t N, int64_t K,
                        tcm_stream_t stream);
 
 /*
+ * tcm_gemm_ex_ws -- tcm_gemm_ex with a caller-provided device workspace, which lets
+ * the persistent kernel balance its last round.  The CTA pairs of the kernel take
+ * 256 x 256 output tiles in rounds; when the last round is only partly filled
+ * (e.g. 8192^3: 1024 tiles = 13 rounds of 76 pairs + 36 tiles) and at most half
+ * full, and K is long enough for it to pay (at least 64 K blocks of 128 bytes),
+ * each of its tiles is split into two halves along K, computed by two pairs
+ * at once: the second half stores its fp32 partial sums in the workspace and the
+ * first adds them before the epilogue.  Same results as tcm_gemm_ex up to the
+ * order of the fp32 accumulation (integer-valued sums stay exact).
+ *  workspace        DEVICE memory, 16-byte aligned, caller-owned, at least
+ *                   tcm_gemm_workspace_bytes(M, N, K, a_dtype, b_dtype) bytes
+ *                   (else TCM_ERR_INVALID_ARG); NULL with workspace_bytes 0 gives
+ *                   tcm_gemm_ex.  Its contents are scratch: the call zeroes its
+ *                   counters on `stream` first.  Two calls that may run at the same
+ *                   time on the GPU must not share a workspace.
+ *  other arguments  as tcm_gemm_ex.
+ * A launch that splits tiles is cooperative (all its CTAs resident at once); the
+ * wait of part 0 for the other parts is bounded like every pipeline wait (site 10).
+ *
+ * tcm_gemm_workspace_bytes -- bytes of workspace tcm_gemm_ex_ws uses for this
+ * problem on the current device (0: no split; -1: arguments tcm_gemm_ex would
+ * reject).  Depends on the device's SM count and on tcm_set_config_override.
+ * Host only.
+ */
+tcm_status tcm_gemm_ex_ws(int64_t M, int64_t N, int64_t K,
+                          tcm_dtype a_dtype, const void *A, int64_t lda,
+                          tcm_dtype b_dtype, const void *B, int64_t ldb,
+                          const void *C, int64_t ldc, void *D, int64_t ldd,
+                          tcm_dtype out_dtype, float alpha, float beta,
+                          const float *a_scale, const float *b_scale, const void *bias,
+                          void *workspace, int64_t workspace_bytes, tcm_stream_t stream);
+int64_t tcm_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, tcm_dtype b_dtype);
+
+/*
  * tcm_gemm_fused -- tcm_gemm_ex with the rest of the epilogue chain:
  *   y   = act(alpha * sA * sB * (A . B) + beta * C + bias)
  *   D   = y / d_scale, cast to out_dtype (FP8: round to nearest even, saturating to
@@ -339,7 +373,8 @@ tcm_status tcm_nvfp4_pack_scales(int64_t rows, int64_t K, const uint8_t *scales,
  * 3 = MMA issuer waiting for a free accumulator, 4 = epilogue waiting for
  * an accumulator, 5 = drain at exit, 6 = MMA issuer waiting for a stage's
  * scales or sparse metadata, 7 = sparse metadata writer waiting for a free
- * stage).  Returns TCM_ERR_CUDA if the
+ * stage, 10 = tcm_gemm_ex_ws part 0 waiting for the other parts' partial sums).
+ * Returns TCM_ERR_CUDA if the
  * synchronisation itself failed.  Either output pointer may be NULL.
  */
 tcm_status tcm_get_device_status(tcm_stream_t stream, int32_t *code, int32_t *site);
@@ -367,10 +402,24 @@ void tcm_set_timeout_ns(uint64_t ns);
  *   ksplit     1, 2 or 4 CTAs of a cluster sharing each tile's K range, their
  *              partial sums added through distributed shared memory (dense
  *              single-CTA tiles of width 32 or 64, e.g. skinny M)
+ *   tail_split tcm_gemm_ex_ws with a workspace: 1 = never split the last round's
+ *              CTA-pair tiles over K; 2 = split them whenever every pair then gets
+ *              at most one half (automatic: also only when a tile has at least 64
+ *              K blocks of 128 bytes, i.e. K >= 4096 for 16-bit, K >= 8192 for FP8)
  * Combinations the kernels do not provide fall back to the automatic choice.
  * Results are the same either way, up to the order of the fp32 accumulation.
  */
-void tcm_set_config_override(int cta_group, int tile_n, int stages, int group_m, int ksplit);
+void tcm_set_config_override(int cta_group, int tile_n, int stages, int group_m, int ksplit, int tail_split);
+
+/*
+ * Measurement hook: while `counters` is set, every GEMM launch made afterwards
+ * adds, from its first CTA, the SM clock cycles (%clock64) and global-timer
+ * nanoseconds between that CTA's start and end to counters[0] and counters[1],
+ * and 1 to counters[2] (atomically; DEVICE memory, three uint64, caller-owned).
+ * counters[0] / counters[1] is then the SM clock in GHz during those launches.
+ * NULL turns it off.  The pointer is read when a launch is made.
+ */
+void tcm_set_clock_probe(unsigned long long *counters);
 
 /*
  * Test hook for the device-side failure path: with mask bit 1 set, the next
@@ -382,7 +431,9 @@ void tcm_set_config_override(int cta_group, int tile_n, int stages, int group_m,
  * waiting for data; 4: the epilogue waiting for the same tile; 6: the MMA
  * issuer waiting for the stage's scales or metadata in tensor memory; 7: a
  * metadata writer of tcm_gemm_sp waiting for a stage's previous MMAs), winds
- * down and returns.  D is left partly unwritten.  No memory outside the
+ * down and returns.  With mask bit 2 set, the next tcm_gemm_ex_ws launch that
+ * splits tiles has its helper parts skip announcing their partial sums, so each
+ * owner's wait runs out (site 10).  D is left partly unwritten.  No memory outside the
  * kernel's own buffers is touched.
  */
 void tcm_debug_fail_next_launch(int mask);

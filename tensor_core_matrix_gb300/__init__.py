@@ -33,7 +33,8 @@ EXPORTS = ("tcm_gemm", "tcm_gemm_ex", "tcm_gemm_fused", "tcm_sp_compress", "tcm_
            "tcm_mx_scales_bytes", "tcm_mx_pack_scales", "tcm_gemm_nvfp4", "tcm_nvfp4_scales_bytes",
            "tcm_nvfp4_pack_scales",
            "tcm_get_device_status", "tcm_clear_device_status", "tcm_set_timeout_ns",
-           "tcm_status_string", "tcm_version", "tcm_set_config_override", "tcm_debug_fail_next_launch")
+           "tcm_status_string", "tcm_version", "tcm_set_config_override", "tcm_debug_fail_next_launch",
+           "tcm_set_clock_probe", "tcm_gemm_ex_ws", "tcm_gemm_workspace_bytes")
 
 
 class TcmError(RuntimeError):
@@ -60,6 +61,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.tcm_gemm_ex.restype = i32
     lib.tcm_gemm_ex.argtypes = [i64, i64, i64, i32, vp, i64, i32, vp, i64, vp, i64, vp, i64,
                                 i32, f32, f32, vp, vp, vp, vp]
+    lib.tcm_gemm_ex_ws.restype = i32
+    lib.tcm_gemm_ex_ws.argtypes = [i64, i64, i64, i32, vp, i64, i32, vp, i64, vp, i64, vp, i64,
+                                   i32, f32, f32, vp, vp, vp, vp, i64, vp]
+    lib.tcm_gemm_workspace_bytes.restype = i64
+    lib.tcm_gemm_workspace_bytes.argtypes = [i64, i64, i64, i32, i32]
     lib.tcm_gemm_fused.restype = i32
     lib.tcm_gemm_fused.argtypes = [i64, i64, i64, i32, vp, i64, i32, vp, i64, vp, i64, vp, i64,
                                    i32, f32, f32, vp, vp, vp, i32, vp, vp, vp]
@@ -94,7 +100,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.tcm_set_timeout_ns.restype = None
     lib.tcm_set_timeout_ns.argtypes = [ctypes.c_uint64]
     lib.tcm_set_config_override.restype = None
-    lib.tcm_set_config_override.argtypes = [i32, i32, i32, i32, i32]
+    lib.tcm_set_config_override.argtypes = [i32, i32, i32, i32, i32, i32]
+    lib.tcm_set_clock_probe.restype = None
+    lib.tcm_set_clock_probe.argtypes = [vp]
     lib.tcm_debug_fail_next_launch.restype = None
     lib.tcm_debug_fail_next_launch.argtypes = [i32]
     lib.tcm_status_string.restype = ctypes.c_char_p
@@ -227,15 +235,29 @@ def _epilogue_args(D, C, bias, M, N, out_types, bias_types):
         _vec(bias, "bias", N, bias_types)
 
 
+def tcm_gemm_workspace_bytes(M: int, N: int, K: int, a_dtype, b_dtype=None) -> int:
+    """Workspace bytes tcm_gemm_ex needs to balance its last round for this problem on the
+    current device (0: none); dtypes as torch dtypes or "e2m1"."""
+    def code(d):
+        return TCM_E2M1 if d == "e2m1" else DTYPE_CODE[d]
+    n = int(load_library().tcm_gemm_workspace_bytes(int(M), int(N), int(K), code(a_dtype),
+                                                    code(a_dtype if b_dtype is None else b_dtype)))
+    if n < 0:
+        raise ValueError("unsupported problem")
+    return n
+
+
 def tcm_gemm_ex(A, B, D, *, C=None, alpha=1.0, beta=0.0, a_scale=None, b_scale=None, bias=None, stream=None,
-                a_fmt=None, b_fmt=None):
+                a_fmt=None, b_fmt=None, workspace=None):
     """D = alpha * a_scale * b_scale * (A @ B_stored.T) + beta * C + bias.
 
     A: M x K (row-major, pitch = A.stride(0)); B: N x K (K-major storage of
     the K x N operand); C, D: M x N (C of D's dtype); bias: N elements of D's
     dtype; a_scale, b_scale: one-element fp32 CUDA tensors or None.
     a_fmt / b_fmt = "e2m1": that operand is a uint8 tensor of packed FP4
-    (M x K/2 or N x K/2 bytes).
+    (M x K/2 or N x K/2 bytes).  workspace: a contiguous uint8 CUDA tensor of at
+    least tcm_gemm_workspace_bytes(...) bytes, or None (then the C ABI's
+    tcm_gemm_ex; with it, tcm_gemm_ex_ws).
     """
     ca, K, lda = _operand(A, a_fmt, "A")
     cb, Kb, ldb = _operand(B, b_fmt, "B")
@@ -244,13 +266,17 @@ def tcm_gemm_ex(A, B, D, *, C=None, alpha=1.0, beta=0.0, a_scale=None, b_scale=N
         raise ValueError(f"A has K = {K}, B has K = {Kb}")
     _epilogue_args(D, C, bias, M, N, OUT_TYPES, (D.dtype,))
     _scalar(a_scale, "a_scale"), _scalar(b_scale, "b_scale")
-    _on_device(A=A, B=B, D=D, C=C, bias=bias, a_scale=a_scale, b_scale=b_scale)
+    if workspace is not None:
+        _bytes(workspace, "workspace", 0)
+    _on_device(A=A, B=B, D=D, C=C, bias=bias, a_scale=a_scale, b_scale=b_scale, workspace=workspace)
     lib = load_library()
-    st = lib.tcm_gemm_ex(M, N, K, ca, _ptr(A), lda, cb, _ptr(B),
-                         ldb, _ptr(C), C.stride(0) if C is not None else 0,
-                         _ptr(D), D.stride(0), _code(D, "D"), float(alpha), float(beta),
-                         _ptr(a_scale), _ptr(b_scale), _ptr(bias), _stream(stream))
-    _check(st, "tcm_gemm_ex")
+    args = (M, N, K, ca, _ptr(A), lda, cb, _ptr(B), ldb, _ptr(C), C.stride(0) if C is not None else 0,
+            _ptr(D), D.stride(0), _code(D, "D"), float(alpha), float(beta),
+            _ptr(a_scale), _ptr(b_scale), _ptr(bias))
+    if workspace is None:
+        _check(lib.tcm_gemm_ex(*args, _stream(stream)), "tcm_gemm_ex")
+    else:
+        _check(lib.tcm_gemm_ex_ws(*args, _ptr(workspace), workspace.numel(), _stream(stream)), "tcm_gemm_ex_ws")
     return D
 
 
@@ -511,13 +537,25 @@ def tcm_set_timeout_ns(ns: int):
 
 
 def tcm_set_config_override(cta_group: int = 0, tile_n: int = 0, stages: int = 0, group_m: int = 0,
-                            ksplit: int = 0):
+                            ksplit: int = 0, tail_split: int = 0):
     """Force kernel-variant fields of later GEMMs (see include/tcm.h); zeros restore the automatic choice."""
-    load_library().tcm_set_config_override(int(cta_group), int(tile_n), int(stages), int(group_m), int(ksplit))
+    load_library().tcm_set_config_override(int(cta_group), int(tile_n), int(stages), int(group_m), int(ksplit),
+                                           int(tail_split))
+
+
+def tcm_set_clock_probe(counters=None):
+    """Measurement hook: later GEMM launches add their first CTA's SM cycles, global-timer ns and 1
+    to ``counters`` (a CUDA int64 tensor of >= 3 elements); None turns it off."""
+    if counters is not None:
+        if counters.dtype != torch.int64 or counters.numel() < 3 or not counters.is_contiguous():
+            raise ValueError("counters must be a contiguous int64 tensor of at least 3 elements")
+        _on_device(counters=counters)
+    load_library().tcm_set_clock_probe(_ptr(counters))
 
 
 def tcm_debug_fail_next_launch(mask: int = 1):
-    """Test hook: the next GEMM launch skips its first load and times out (see include/tcm.h)."""
+    """Test hook: bit 1 -- the next GEMM launch skips its first load and times out; bit 2 -- the
+    next split tcm_gemm_ex_ws launch's helper parts never announce their partials (see include/tcm.h)."""
     load_library().tcm_debug_fail_next_launch(int(mask))
 
 

@@ -54,6 +54,8 @@ static std::atomic<int> g_force_bn{0};
 static std::atomic<int> g_force_stages{0};
 static std::atomic<int> g_force_group_m{0};
 static std::atomic<int> g_force_ksplit{0};
+static std::atomic<int> g_force_split{0};
+static std::atomic<unsigned long long *> g_clock_probe{nullptr};
 
 static std::atomic<int> g_fault_once{0};
 
@@ -174,25 +176,132 @@ int tcm_version(void) { return 100; }
 
 void tcm_set_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns); }
 
-void tcm_set_config_override(int cta_group, int tile_n, int stages, int group_m, int ksplit)
+void tcm_set_config_override(int cta_group, int tile_n, int stages, int group_m, int ksplit, int tail_split)
 {
     g_force_cta_group.store(cta_group);
     g_force_bn.store(tile_n);
     g_force_stages.store(stages);
     g_force_group_m.store(group_m);
     g_force_ksplit.store(ksplit);
+    g_force_split.store(tail_split);
 }
+
+void tcm_set_clock_probe(unsigned long long *counters) { g_clock_probe.store(counters); }
 
 void tcm_debug_fail_next_launch(int mask) { g_fault_once.store(mask); }
 
+} // extern "C"
+
+namespace tcm {
+
+// Kernel variant, tile grid and work units of a dense GEMM (shared by the launch and by
+// tcm_gemm_workspace_bytes, so that the size query and the launch always agree).
+struct DensePlan {
+    GemmConfig cfg;
+    bool swap;                  // skinny M: the kernel computes D^T (weights as the 128-row operand)
+    int64_t kM, kN;             // kernel-space rows and columns
+    int64_t tiles_m, tiles_n, num_tiles;
+    int64_t per_cluster, clusters;
+    int split;                  // K parts per tile of the last, partly filled round (1: none)
+    int64_t split_begin, units;
+    int64_t flag_bytes, ws_bytes; // workspace: counters, then fp32 partial slots
+};
+
+static DensePlan plan_dense(int64_t M, int64_t N, int64_t K, int kind, int64_t sms, bool allow_split)
+{
+    DensePlan d{};
+    // swap A and B for skinny M so the weight fills the 128-row MMA
+    d.swap = M <= 64 && N >= 128;
+    d.kM = d.swap ? N : M;
+    d.kN = d.swap ? M : N;
+    const int64_t kM = d.kM, kN = d.kN;
+    GemmConfig &cfg = d.cfg;
+    cfg.kind = kind;
+    cfg.cta_group = 1;
+    if (d.swap) cfg.bn = kN <= 32 ? 32 : 64;
+    else if (kN <= 32) cfg.bn = 32;
+    else if (kN <= 64) cfg.bn = 64;
+    else if (kN <= 128) cfg.bn = 128;
+    else {
+        cfg.bn = 256;
+        // 256 x 256 pair tiles when they still give every CTA pair work
+        const int64_t pair_tiles = ((kM + 255) / 256) * ((kN + 255) / 256);
+        const int64_t t128 = ((kM + 127) / 128) * ((kN + 127) / 128);
+        if (kM > 128 && pair_tiles >= sms / 2) cfg.cta_group = 2;
+        else if (((kM + 127) / 128) * ((kN + 255) / 256) < sms / 2 && t128 > pair_tiles) cfg.bn = 128;
+    }
+    const int force_cg = g_force_cta_group.load(), force_bn = g_force_bn.load();
+    if (force_cg == 1 || force_cg == 2) cfg.cta_group = force_cg;
+    if (force_bn == 32 || force_bn == 64 || force_bn == 128 || force_bn == 256) cfg.bn = force_bn;
+    if (cfg.cta_group == 2 && (cfg.bn != 256 || d.swap)) cfg.cta_group = 1;
+    cfg.stages = g_force_stages.load();
+    cfg.ksplit = 1;
+    const int64_t kbs = (K + (kind == 1 ? 127 : 63)) / (kind == 1 ? 128 : 64);
+    {
+        // K split across a cluster when single-CTA tiles leave SMs idle: pick the
+        // split (1, 2, 4) whose last round of tiles is fullest, keeping >= 8 K
+        // blocks per CTA; tiles of width 32 and 64 only.
+        const int64_t tiles = ((kM + 127) / 128) * ((kN + cfg.bn - 1) / cfg.bn);
+        if (cfg.cta_group == 1 && (cfg.bn == 32 || cfg.bn == 64)) {
+            double best = 0.0;
+            for (int ks = 1; ks <= 4; ks *= 2) {
+                if (ks > 1 && kbs / ks < 8) break;
+                const int64_t clusters = sms / ks;
+                const int64_t rounds = (tiles + clusters - 1) / clusters;
+                const double eff = static_cast<double>(tiles) / static_cast<double>(rounds * clusters) / (ks > 1 ? 1.02 : 1.0);
+                if (eff > best + 0.05) best = eff, cfg.ksplit = ks;
+            }
+        }
+        const int fk = g_force_ksplit.load();
+        if (fk == 1 || ((fk == 2 || fk == 4) && cfg.cta_group == 1 && (cfg.bn == 32 || cfg.bn == 64))) cfg.ksplit = fk;
+    }
+    // two 128-byte K atoms per stage for 32-wide single-CTA tiles (the skinny,
+    // HBM-bound shapes): longer contiguous reads of each weight row
+    cfg.katoms = (cfg.cta_group == 1 && cfg.bn == 32 && cfg.ksplit <= 2) ? 2 : 1;
+
+    d.tiles_m = (kM + 128 * cfg.cta_group - 1) / (128 * cfg.cta_group);
+    d.tiles_n = (kN + cfg.bn - 1) / cfg.bn;
+    d.num_tiles = d.tiles_m * d.tiles_n;
+    d.per_cluster = static_cast<int64_t>(cfg.cta_group) * cfg.ksplit;
+    d.clusters = sms / d.per_cluster;
+    // Tail K split (CTA-pair tiles, with a workspace): the R tiles of the last, partly
+    // filled round become 2R half-K units when every pair then gets at most one of them
+    // (2R <= clusters).  Handing the second half's partial sums to the first costs
+    // ~6 us (stage, bulk store, counter, bulk load; measured), so only tiles of at least
+    // SPLIT_MIN_KB K blocks are split (measured at 4096^3: bf16, 64 blocks, 2.6 % faster;
+    // E4M3, 32 blocks, 7.6 % slower).  tail_split 2 in the config override lowers the
+    // limit to 2 blocks, 1 turns the split off.
+    constexpr int64_t SPLIT_MIN_KB = 64;
+    d.split = 1;
+    const int64_t rem = d.num_tiles % d.clusters;
+    const int fs = g_force_split.load();
+    const int64_t min_kb = fs == 2 ? 2 : SPLIT_MIN_KB;
+    if (allow_split && cfg.cta_group == 2 && cfg.ksplit == 1 && rem > 0 && 2 * rem <= d.clusters && kbs >= min_kb &&
+        fs != 1)
+        d.split = 2;
+    d.split_begin = d.split > 1 ? d.num_tiles - rem : d.num_tiles;
+    d.units = d.split_begin + (d.num_tiles - d.split_begin) * d.split;
+    if (d.split > 1) {
+        const int64_t nsplit = d.num_tiles - d.split_begin;
+        d.flag_bytes = ((nsplit * cfg.cta_group * 4 + 255) / 256) * 256;
+        d.ws_bytes = d.flag_bytes + nsplit * (d.split - 1) * cfg.cta_group * 128 * cfg.bn * 4;
+    }
+    return d;
+}
+
+} // namespace tcm
+
+extern "C" {
+
 // Dense GEMM with the full epilogue: y = act(alpha * sa * sb * acc + beta * C + bias),
 // D = y / d_scale cast to out_dtype (FP8 outputs: saturating), amax = max |y|.
-// tcm_gemm_ex is the act = none, 16/32-bit-output case.
+// tcm_gemm_ex is the act = none, 16/32-bit-output case.  With a workspace (ws,
+// ws_bytes >= tcm_gemm_workspace_bytes) the last round of CTA-pair tiles may be split over K.
 static tcm_status gemm_impl(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const void *A, int64_t lda,
                             tcm_dtype b_dtype, const void *B, int64_t ldb, const void *C, int64_t ldc, void *D,
                             int64_t ldd, tcm_dtype out_dtype, float alpha, float beta, const float *a_scale,
                             const float *b_scale, const void *bias, int act, const float *d_scale, float *amax,
-                            bool fused, tcm_stream_t stream)
+                            bool fused, void *ws, int64_t ws_bytes, tcm_stream_t stream)
 {
     // ---- argument checks (nothing is launched on failure)
     const bool a16 = a_dtype == TCM_BF16 || a_dtype == TCM_F16;
@@ -232,54 +341,16 @@ static tcm_status gemm_impl(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, 
                      (b4 && (ldb % 64 || (reinterpret_cast<uintptr_t>(B) & 31u)))))
         return TCM_ERR_MISALIGNED;
 
-    // ---- configuration: swap A and B for skinny M so the weight fills the 128-row MMA
-    const bool swap = M <= 64 && N >= 128;
-    const int64_t kM = swap ? N : M, kN = swap ? M : N;
+    if (ws_bytes < 0 || (ws_bytes > 0 && !ws)) return TCM_ERR_INVALID_ARG;
+    if (ws && !aligned16(ws)) return TCM_ERR_MISALIGNED;
+
     const int64_t sms = sm_count();
     if (sms <= 0) return TCM_ERR_CUDA;
-    GemmConfig cfg{};
-    cfg.kind = kind;
-    cfg.cta_group = 1;
-    if (swap) cfg.bn = kN <= 32 ? 32 : 64;
-    else if (kN <= 32) cfg.bn = 32;
-    else if (kN <= 64) cfg.bn = 64;
-    else if (kN <= 128) cfg.bn = 128;
-    else {
-        cfg.bn = 256;
-        // 256 x 256 pair tiles when they still give every CTA pair work
-        const int64_t pair_tiles = ((kM + 255) / 256) * ((kN + 255) / 256);
-        const int64_t t128 = ((kM + 127) / 128) * ((kN + 127) / 128);
-        if (kM > 128 && pair_tiles >= sms / 2) cfg.cta_group = 2;
-        else if (((kM + 127) / 128) * ((kN + 255) / 256) < sms / 2 && t128 > pair_tiles) cfg.bn = 128;
-    }
-    const int force_cg = g_force_cta_group.load(), force_bn = g_force_bn.load();
-    if (force_cg == 1 || force_cg == 2) cfg.cta_group = force_cg;
-    if (force_bn == 32 || force_bn == 64 || force_bn == 128 || force_bn == 256) cfg.bn = force_bn;
-    if (cfg.cta_group == 2 && (cfg.bn != 256 || swap)) cfg.cta_group = 1;
-    cfg.stages = g_force_stages.load();
-    cfg.ksplit = 1;
-    {
-        // K split across a cluster when single-CTA tiles leave SMs idle: pick the
-        // split (1, 2, 4) whose last round of tiles is fullest, keeping >= 8 K
-        // blocks per CTA; tiles of width 32 and 64 only.
-        const int64_t kbs = (K + (kind == 1 ? 127 : 63)) / (kind == 1 ? 128 : 64);
-        const int64_t tiles = ((kM + 127) / 128) * ((kN + cfg.bn - 1) / cfg.bn);
-        if (cfg.cta_group == 1 && (cfg.bn == 32 || cfg.bn == 64)) {
-            double best = 0.0;
-            for (int ks = 1; ks <= 4; ks *= 2) {
-                if (ks > 1 && kbs / ks < 8) break;
-                const int64_t clusters = sms / ks;
-                const int64_t rounds = (tiles + clusters - 1) / clusters;
-                const double eff = static_cast<double>(tiles) / static_cast<double>(rounds * clusters) / (ks > 1 ? 1.02 : 1.0);
-                if (eff > best + 0.05) best = eff, cfg.ksplit = ks;
-            }
-        }
-        const int fk = g_force_ksplit.load();
-        if (fk == 1 || ((fk == 2 || fk == 4) && cfg.cta_group == 1 && (cfg.bn == 32 || cfg.bn == 64))) cfg.ksplit = fk;
-    }
-    // two 128-byte K atoms per stage for 32-wide single-CTA tiles (the skinny,
-    // HBM-bound shapes): longer contiguous reads of each weight row
-    cfg.katoms = (cfg.cta_group == 1 && cfg.bn == 32 && cfg.ksplit <= 2) ? 2 : 1;
+    const DensePlan plan = plan_dense(M, N, K, kind, sms, ws != nullptr && ws_bytes > 0);
+    const GemmConfig &cfg = plan.cfg;
+    const bool swap = plan.swap;
+    const int64_t kM = plan.kM, kN = plan.kN;
+    if (plan.split > 1 && ws_bytes < plan.ws_bytes) return TCM_ERR_INVALID_ARG;
 
     // ---- tensor maps (the kernel's "A" operand is the swapped one when swap)
     const int k_elems_stage = kind == 1 ? 128 : 64;
@@ -305,12 +376,18 @@ static tcm_status gemm_impl(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, 
     p.kN = static_cast<int>(kN);
     p.K = static_cast<int>(K);
     p.num_kb = static_cast<int>((K + k_elems_stage * cfg.katoms - 1) / (k_elems_stage * cfg.katoms));
-    p.tiles_m = static_cast<int>((kM + 128 * cfg.cta_group - 1) / (128 * cfg.cta_group));
-    p.tiles_n = static_cast<int>((kN + cfg.bn - 1) / cfg.bn);
-    p.num_tiles = p.tiles_m * p.tiles_n;
+    p.tiles_m = static_cast<int>(plan.tiles_m);
+    p.tiles_n = static_cast<int>(plan.tiles_n);
+    p.num_tiles = static_cast<int>(plan.num_tiles);
     p.group_m = g_force_group_m.load() > 0 ? g_force_group_m.load() : 16;
+    p.split = plan.split;
+    p.split_begin = static_cast<int>(plan.split_begin);
+    if (plan.split > 1) {
+        p.ws_flag = static_cast<int *>(ws);
+        p.ws_part = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + plan.flag_bytes);
+    }
     p.tile_begin = 0;
-    p.tile_end = p.num_tiles;
+    p.tile_end = static_cast<int>(plan.units);
     p.D = D;
     p.ldd = ldd;
     p.C = beta != 0.f ? C : nullptr;
@@ -332,6 +409,7 @@ static tcm_status gemm_impl(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, 
     const uint32_t codeA = kind == 0 ? (fa == TCM_BF16 ? 1u : 0u) : f8code(fa);
     const uint32_t codeB = kind == 0 ? (fb == TCM_BF16 ? 1u : 0u) : f8code(fb);
     p.idesc = make_idesc(codeA, codeB, 128u * static_cast<uint32_t>(cfg.cta_group), static_cast<uint32_t>(cfg.bn));
+    p.clock_probe = g_clock_probe.load();
     p.timeout_ns = timeout_ns();
     p.status = device_status_ptr();
     if (!p.status) return TCM_ERR_CUDA;
@@ -345,13 +423,29 @@ static tcm_status gemm_impl(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, 
                      (row_a * 128u + row_b * static_cast<uint32_t>(cfg.bn / cfg.cta_group));
     }
     p.fault_inject = g_fault_once.exchange(0);
-    const int64_t per_cluster = static_cast<int64_t>(cfg.cta_group) * cfg.ksplit;
-    const int64_t clusters = sms / per_cluster;
-    const int grid = static_cast<int>((p.num_tiles < clusters ? p.num_tiles : clusters) * per_cluster);
-    if (amax && cudaMemsetAsync(amax, 0, sizeof(float), reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    const int grid = static_cast<int>((plan.units < plan.clusters ? plan.units : plan.clusters) * plan.per_cluster);
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (amax && cudaMemsetAsync(amax, 0, sizeof(float), st) != cudaSuccess) return TCM_ERR_CUDA;
+    // the split tiles' counters start at zero in every launch
+    if (plan.split > 1 && cudaMemsetAsync(ws, 0, static_cast<size_t>(plan.flag_bytes), st) != cudaSuccess)
         return TCM_ERR_CUDA;
-    const cudaError_t e = launch_gemm(cfg, tmA, tmB, nullptr, p, grid, reinterpret_cast<cudaStream_t>(stream));
+    const cudaError_t e = launch_gemm(cfg, tmA, tmB, p, grid, st);
     return e == cudaSuccess ? TCM_OK : TCM_ERR_CUDA;
+}
+
+int64_t tcm_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, tcm_dtype b_dtype)
+{
+    const bool a16 = a_dtype == TCM_BF16 || a_dtype == TCM_F16;
+    const bool a8 = a_dtype == TCM_E4M3 || a_dtype == TCM_E5M2 || a_dtype == TCM_E2M1;
+    const bool b8 = b_dtype == TCM_E4M3 || b_dtype == TCM_E5M2 || b_dtype == TCM_E2M1;
+    int kind;
+    if (a16 && b_dtype == a_dtype) kind = 0;
+    else if (a8 && b8) kind = 1;
+    else return -1;
+    if (M < 1 || N < 1 || K < 0 || M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2) return -1;
+    const int64_t sms = sm_count();
+    if (sms <= 0) return -1;
+    return plan_dense(M, N, K, kind, sms, true).ws_bytes;
 }
 
 tcm_status tcm_gemm_ex(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const void *A, int64_t lda,
@@ -360,7 +454,17 @@ tcm_status tcm_gemm_ex(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const
                        const float *b_scale, const void *bias, tcm_stream_t stream)
 {
     return gemm_impl(M, N, K, a_dtype, A, lda, b_dtype, B, ldb, C, ldc, D, ldd, out_dtype, alpha, beta, a_scale,
-                     b_scale, bias, TCM_ACT_NONE, nullptr, nullptr, false, stream);
+                     b_scale, bias, TCM_ACT_NONE, nullptr, nullptr, false, nullptr, 0, stream);
+}
+
+tcm_status tcm_gemm_ex_ws(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const void *A, int64_t lda,
+                          tcm_dtype b_dtype, const void *B, int64_t ldb, const void *C, int64_t ldc, void *D,
+                          int64_t ldd, tcm_dtype out_dtype, float alpha, float beta, const float *a_scale,
+                          const float *b_scale, const void *bias, void *workspace, int64_t workspace_bytes,
+                          tcm_stream_t stream)
+{
+    return gemm_impl(M, N, K, a_dtype, A, lda, b_dtype, B, ldb, C, ldc, D, ldd, out_dtype, alpha, beta, a_scale,
+                     b_scale, bias, TCM_ACT_NONE, nullptr, nullptr, false, workspace, workspace_bytes, stream);
 }
 
 tcm_status tcm_gemm_fused(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const void *A, int64_t lda,
@@ -370,7 +474,7 @@ tcm_status tcm_gemm_fused(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, co
                           float *amax, tcm_stream_t stream)
 {
     return gemm_impl(M, N, K, a_dtype, A, lda, b_dtype, B, ldb, C, ldc, D, ldd, out_dtype, alpha, beta, a_scale,
-                     b_scale, bias, static_cast<int>(act), d_scale, amax, true, stream);
+                     b_scale, bias, static_cast<int>(act), d_scale, amax, true, nullptr, 0, stream);
 }
 
 tcm_status tcm_gemm(int64_t M, int64_t N, int64_t K, tcm_dtype in_dtype, const void *A, const void *B,
@@ -501,8 +605,11 @@ static tcm_status sparse_impl(bool canonical, int64_t M, int64_t N, int64_t K, t
     p.tiles_n = static_cast<int>((N + cfg.bn - 1) / cfg.bn);
     p.num_tiles = p.tiles_m * p.tiles_n;
     p.group_m = g_force_group_m.load() > 0 ? g_force_group_m.load() : 16;
+    p.split = 1;
+    p.split_begin = p.num_tiles;
     p.tile_begin = 0;
     p.tile_end = p.num_tiles;
+    p.clock_probe = g_clock_probe.load();
     p.D = D;
     p.ldd = N;
     p.C = beta != 0.f ? C : nullptr;
@@ -611,8 +718,11 @@ static tcm_status block_scaled_impl(bool nv, int64_t M, int64_t N, int64_t K, tc
     p.tiles_n = static_cast<int>((N + cfg.bn - 1) / cfg.bn);
     p.num_tiles = p.tiles_m * p.tiles_n;
     p.group_m = g_force_group_m.load() > 0 ? g_force_group_m.load() : 16;
+    p.split = 1;
+    p.split_begin = p.num_tiles;
     p.tile_begin = 0;
     p.tile_end = p.num_tiles;
+    p.clock_probe = g_clock_probe.load();
     p.D = D;
     p.ldd = N;
     p.C = beta != 0.f ? C : nullptr;

@@ -5,7 +5,7 @@
 namespace tcm {
 
 cudaError_t launch_gemm(const GemmConfig &cfg, const CUtensorMap &tmA, const CUtensorMap &tmB,
-                        const CUtensorMap * /*tmMeta*/, const GemmParams &p, int grid, cudaStream_t stream)
+                        const GemmParams &p, int grid, cudaStream_t stream)
 {
     if (cfg.ksplit > 1) return launch_gemm_ksplit(cfg, tmA, tmB, p, grid, stream);
     if (cfg.cta_group == 2) return launch_gemm_pair(cfg, tmA, tmB, p, grid, stream);

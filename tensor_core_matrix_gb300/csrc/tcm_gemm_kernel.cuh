@@ -46,6 +46,15 @@ __device__ __forceinline__ uint32_t red_offset(int slot, int row, int c, int j)
     return static_cast<uint32_t>(slot * (BM * BN * 4) + row * BN * 4 + c * 4 + ((j ^ (row & 7)) * 16));
 }
 
+// Tail K split (two parts): the workspace slot of split tile j for CTA `rank` of the pair,
+// the helper part's 128 x BN fp32 partial sums as the byte image of its shared-memory
+// staging (red_offset layout, rows bank-swizzled).
+template <int CG, int BN>
+__device__ __forceinline__ float *part_slot(const GemmParams &p, int j, uint32_t rank)
+{
+    return p.ws_part + (static_cast<size_t>(j) * CG + rank) * (BM * BN);
+}
+
 // KIND: 0 = kind::f16, 1 = kind::f8f6f4.  BN: N extent of the (pair) tile.
 // CG: 1 = one CTA computes a 128 x BN tile; 2 = a cluster of two CTAs
 // computes a 256 x BN tile with cta_group::2 (each CTA loads its own 128
@@ -58,10 +67,21 @@ __device__ __forceinline__ uint32_t red_offset(int slot, int row, int c, int j)
 // problem has fewer tiles than the GPU has SMs (skinny M after the swap).
 // KATOMS: 128-byte K atoms per stage; more than one gives each weight row
 // a longer contiguous run per stage (skinny, HBM-bound shapes).
+// Work units (unit_coords): whole tiles, and -- when p.split == 2 -- the two K halves
+// of each tile of the last, partly filled round (CTA pairs only).  That round is each
+// CTA's last unit, so its shared-memory ring is idle by then: the helper half stages its
+// fp32 accumulator there (128 x BN per CTA), bulk-copies the image to its workspace slot
+// and release-adds 1 to the slot's counter; the owner half waits (bounded) for the
+// counter, bulk-copies the image into its own ring and adds it before its epilogue.
+// Such launches are cooperative, so every pair is resident and the waits end.
+// (Register loads of the partials, chunk by chunk, cost the owner ~15 us of L2
+// latency at 4096^3; one bulk copy each way does not.)
 template <int KIND, int BN, int STAGES, int CG, int KS, int KATOMS = 1>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GemmParams p)
 {
+    const unsigned long long clk0 = clock64(); // clock probe (CTA 0, thread 0 only)
+    const unsigned long long gt0 = globaltimer_ns();
     constexpr int RED_SLOT = BM * BN * 4; // one CTA's fp32 partial tile
     using L = Smem<BN / CG, STAGES, (KS - 1) * RED_SLOT, KATOMS>;
     static_assert(CG == 1 || CG == 2, "CTA group of 1 or 2");
@@ -87,6 +107,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint64_t *drain = tempty + 2;
     uint64_t *red_full = drain + 1;
     uint64_t *red_empty = drain + 2;
+    uint64_t *part_full = drain + 3;   // tail K split: the helper's partial sums landed in the ring
+    uint64_t *part_staged = drain + 4; // tail K split: every epilogue warp staged its rows
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::MISC_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::MISC_OFF + 4);
     constexpr bool CLUSTERED = CG == 2 || KS > 1;
@@ -108,6 +130,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(tempty + a, EPI_WARPS * CG);
         }
         mbar_init(drain, 1);
+        mbar_init(part_full, 1);
+        mbar_init(part_staged, EPI_WARPS);
         if constexpr (KS > 1) {
             mbar_init(red_full, (KS - 1) * EPI_WARPS);
             mbar_init(red_empty, EPI_WARPS);
@@ -138,7 +162,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int cluster_id = static_cast<int>(blockIdx.x) / (CG * KS);
     const int num_clusters = static_cast<int>(gridDim.x) / (CG * KS);
     const int first_tile = p.tile_begin + cluster_id;
-    // this CTA's share of each tile's K blocks
+    // K-split clusters: this CTA's share of each tile's K blocks (else a unit's own range)
     const int kb0 = static_cast<int>((static_cast<long long>(p.num_kb) * krank) / KS);
     const int kb1 = static_cast<int>((static_cast<long long>(p.num_kb) * (krank + 1)) / KS);
 
@@ -151,11 +175,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             long long issued = 0;
             bool ok = true;
             for (int t = first_tile; ok && t < p.tile_end; t += num_clusters) {
-                int mb, nb;
-                tile_coords(p, t, mb, nb);
-                const int a_row = mb * (BM * CG) + static_cast<int>(rank) * BM;
-                const int b_row = nb * BN + static_cast<int>(rank) * BN_CTA;
-                for (int kb = kb0; kb < kb1; ++kb) {
+                const Unit u = unit_coords(p, t);
+                const int ukb0 = KS > 1 ? kb0 : u.kb0, ukb1 = KS > 1 ? kb1 : u.kb1;
+                const int a_row = u.mb * (BM * CG) + static_cast<int>(rank) * BM;
+                const int b_row = u.nb * BN + static_cast<int>(rank) * BN_CTA;
+                for (int kb = ukb0; kb < ukb1; ++kb) {
                     if (!wait_bar<CG>(empty + stage, phase ^ 1u, w, SITE_LOAD_EMPTY, true)) {
                         ok = false;
                         break;
@@ -208,10 +232,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int t = first_tile; ok && t < p.tile_end; t += num_clusters, ++local) {
                 const int acc = local & 1;
                 const uint32_t acc_phase = (local >> 1) & 1;
+                const uint32_t idesc = p.idesc;
+                const Unit u = unit_coords(p, t);
+                const int ukb0 = KS > 1 ? kb0 : u.kb0, ukb1 = KS > 1 ? kb1 : u.kb1;
                 if (!wait_bar<CG>(tempty + acc, acc_phase ^ 1u, w, SITE_MMA_ACC_EMPTY, true)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                for (int kb = kb0; kb < kb1; ++kb) {
+                for (int kb = ukb0; kb < ukb1; ++kb) {
                     if (!wait_bar<CG>(full + stage, phase, w, SITE_MMA_FULL, true)) {
                         ok = false;
                         break;
@@ -226,13 +253,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
                             // +32 bytes of K per instruction = +2 in the descriptor's address field
-                            const uint32_t accum = (kb > kb0 || a > 0 || k > 0) ? 1u : 0u;
+                            const uint32_t accum = (kb > ukb0 || a > 0 || k > 0) ? 1u : 0u;
                             if (CG == 2) {
-                                if (KIND == 1) mma_f8_pair(d_tmem, ad + 2 * k, bd + 2 * k, p.idesc, accum);
-                                else mma_f16_pair(d_tmem, ad + 2 * k, bd + 2 * k, p.idesc, accum);
+                                if (KIND == 1) mma_f8_pair(d_tmem, ad + 2 * k, bd + 2 * k, idesc, accum);
+                                else mma_f16_pair(d_tmem, ad + 2 * k, bd + 2 * k, idesc, accum);
                             } else {
-                                if (KIND == 1) mma_f8(d_tmem, ad + 2 * k, bd + 2 * k, p.idesc, accum);
-                                else mma_f16(d_tmem, ad + 2 * k, bd + 2 * k, p.idesc, accum);
+                                if (KIND == 1) mma_f8(d_tmem, ad + 2 * k, bd + 2 * k, idesc, accum);
+                                else mma_f16(d_tmem, ad + 2 * k, bd + 2 * k, idesc, accum);
                             }
                         }
                     }
@@ -258,7 +285,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const float scale = p.alpha * (p.a_scale ? *p.a_scale : 1.f) * (p.b_scale ? *p.b_scale : 1.f);
         // the issuer's "accumulator free" barrier lives in the even CTA
         const uint32_t tempty_cluster0 = CG == 2 ? mapa_shared(smem_u32(tempty), 0) : 0u;
-        const bool has_acc = kb1 > kb0;
         // K split: partial sums of CTA r go to slot r-1 of CTA 0's buffer (red_offset)
         uint32_t red_cluster0 = 0u, red_full_cluster0 = 0u;
         if constexpr (KS > 1) {
@@ -283,10 +309,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after();
-            int mb, nb;
-            tile_coords(p, t, mb, nb);
-            const int row = mb * (BM * CG) + static_cast<int>(rank) * BM + row_in_tile;
+            const Unit u = unit_coords(p, t);
+            const bool has_acc = KS > 1 ? kb1 > kb0 : u.kb1 > u.kb0;
+            const int row = u.mb * (BM * CG) + static_cast<int>(rank) * BM + row_in_tile;
             const uint32_t tbase = tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(quad * 32) << 16);
+            const bool helper = CG == 2 && u.part > 0;
+            const bool owner = CG == 2 && u.j >= 0 && u.part == 0;
+            constexpr uint32_t PART_BYTES = BM * BN * 4;
+            constexpr uint32_t PART_PIECE = 16384;
+            static_assert(CG == 1 || PART_BYTES <= STAGES * (L::A_STAGE + L::B_STAGE), "partial sums fit the ring");
+            bool add_parts = false;
+            if (owner) {
+                int got = 1;
+                if (warp == 2 && lane == 0) {
+                    // the helper CTA's image is in the workspace: bring it into this CTA's ring
+                    got = wait_count(p.ws_flag + u.j * CG + static_cast<int>(rank), 1, w, SITE_PART_WAIT);
+                    if (got) {
+                        fence_proxy_async_global();
+                        mbar_arrive_expect_tx(part_full, PART_BYTES);
+                        const uint8_t *src = reinterpret_cast<const uint8_t *>(part_slot<CG, BN>(p, u.j, rank));
+                        for (uint32_t q = 0; q < PART_BYTES; q += PART_PIECE)
+                            bulk_load_g2s(sbase + q, src + q, PART_PIECE, smem_u32(part_full));
+                    }
+                }
+                if (lane == 0 && got) got = wait_bar<CG>(part_full, 0, w, SITE_PART_WAIT, true);
+                add_parts = __shfl_sync(0xffffffffu, got, 0) != 0;
+            }
 #pragma unroll 1
             for (int c = 0; c < BN; c += 32) {
                 uint32_t r[32];
@@ -329,8 +377,41 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                     for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(sum[j]);
                 }
-                const float m = epilogue_row32(p, scale, row, nb * BN + c, r);
+                if (helper) {
+                    // stage the partial sums in the idle ring, rows bank-swizzled
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        *reinterpret_cast<uint4 *>(smem + red_offset<BN>(0, row_in_tile, c, j)) =
+                            make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+                    continue;
+                }
+                if (add_parts) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float4 v = *reinterpret_cast<const float4 *>(smem + red_offset<BN>(0, row_in_tile, c, j));
+                        r[4 * j] = __float_as_uint(__uint_as_float(r[4 * j]) + v.x);
+                        r[4 * j + 1] = __float_as_uint(__uint_as_float(r[4 * j + 1]) + v.y);
+                        r[4 * j + 2] = __float_as_uint(__uint_as_float(r[4 * j + 2]) + v.z);
+                        r[4 * j + 3] = __float_as_uint(__uint_as_float(r[4 * j + 3]) + v.w);
+                    }
+                }
+                const float m = epilogue_row32(p, scale, row, u.nb * BN + c, r);
                 if (p.amax) amax_local = amax_combine(amax_local, m);
+            }
+            if (helper) {
+                // publish: the staged image to the workspace in one bulk copy, then the counter
+                // (every wait here is bounded: the first epilogue warp waits for the others)
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(part_staged);
+                if (warp == 2 && lane == 0 && wait_bar<CG>(part_staged, 0, w, SITE_PART_WAIT, true)) {
+                    uint8_t *dst = reinterpret_cast<uint8_t *>(part_slot<CG, BN>(p, u.j, rank));
+                    for (uint32_t q = 0; q < PART_BYTES; q += PART_PIECE) bulk_store_s2g(dst + q, sbase + q, PART_PIECE);
+                    bulk_commit_wait_all();
+                    fence_proxy_async_global();
+                    if (!(p.fault_inject & FAULT_SKIP_PUBLISH))
+                        red_release_gpu_add(p.ws_flag + u.j * CG + static_cast<int>(rank), 1);
+                }
             }
             if constexpr (KS > 1) {
                 __syncwarp();
@@ -357,6 +438,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (CG == 2) tmem_dealloc_pair(tmem_base, TMEM_COLS);
         else tmem_dealloc(tmem_base, TMEM_COLS);
     }
+    clock_probe_add(p, clk0, gt0);
 }
 
 template <int KIND, int BN, int STAGES, int CG, int KS = 1, int KATOMS = 1>
@@ -373,13 +455,16 @@ inline cudaError_t launch_one(const CUtensorMap &a, const CUtensorMap &b, const 
     cfg.blockDim = dim3(NUM_THREADS, 1, 1);
     cfg.dynamicSmemBytes = L::ALLOC;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CG * KS;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // owners of split tiles wait for helper pairs: all CTAs must be resident at once
+    attr[1].id = cudaLaunchAttributeCooperative;
+    attr[1].val.cooperative = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = p.split > 1 ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kern, a, b, p);
 }
 

@@ -297,6 +297,8 @@ __global__ void __launch_bounds__(mx_threads(FMT), 1)
                    const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                    const GemmParams p)
 {
+    const unsigned long long clk0 = clock64(); // clock probe (CTA 0, thread 0 only)
+    const unsigned long long gt0 = globaltimer_ns();
     constexpr int BN_CTA = BN / CG;
     constexpr int SFB_ATOMS = BN / 128;
     using SF = SfLayout<FMT, SFB_ATOMS>;
@@ -748,6 +750,7 @@ __global__ void __launch_bounds__(mx_threads(FMT), 1)
         if (CG == 2) tmem_dealloc_pair(tmem_base, TMEM_COLS);
         else tmem_dealloc(tmem_base, TMEM_COLS);
     }
+    clock_probe_add(p, clk0, gt0);
 }
 
 template <int BN, int STAGES, int NACC, int CG, int FMT>

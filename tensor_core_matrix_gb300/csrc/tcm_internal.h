@@ -27,6 +27,7 @@ enum WaitSite : int {
     SITE_META_EMPTY = 7, // sparse: metadata warps waiting for a free stage
     SITE_RED_FULL = 8,   // K-split: leader waiting for the other CTAs' partial sums
     SITE_RED_EMPTY = 9,  // K-split: CTA waiting for the leader to consume its previous partials
+    SITE_PART_WAIT = 10, // tail K split: the tile's owner waiting for the other parts' partial sums
 };
 
 // Everything a GEMM kernel needs besides its tensor maps.  "Kernel" rows and
@@ -37,7 +38,12 @@ struct GemmParams {
     int num_kb;               // number of K blocks of the tile loop
     int tiles_m, tiles_n, num_tiles;
     int group_m;              // rasterisation: tiles of this many row blocks share B in L2
-    int tile_begin, tile_end; // the linear tile range this launch covers
+    int tile_begin, tile_end; // the range of work units this launch covers (see split_begin)
+    int split_begin;          // units below are whole tiles (unit = tile index); from here on each
+                              // tile of the last, partly filled round is `split` K parts
+    int split;                // K parts per tile of that round (1: none)
+    float *ws_part;           // split > 1: fp32 partial accumulators of parts 1 .. split-1
+    int *ws_flag;             // split > 1: per (tail tile, CTA of the pair): epilogue warps done storing
     void *D;
     long long ldd;
     const void *C;
@@ -53,6 +59,7 @@ struct GemmParams {
     float *amax;              // if set: max |y| over the launch, max-combined as fp32 bits
     int swap_ab;
     uint32_t stage_tx;        // bytes a stage's TMA loads complete (all CTAs of a pair); 0 = from the tile sizes
+    unsigned long long *clock_probe; // if set: CTA 0 adds its SM cycles, global-timer ns and 1 to [0..2]
     uint32_t idesc;
     unsigned long long timeout_ns;
     int *status;              // device status word pair {code, site}
@@ -64,6 +71,7 @@ struct GemmParams {
 // Test hook bits: make a pipeline wait run out without touching memory.
 enum FaultBits : int {
     FAULT_SKIP_FIRST_LOAD = 1, // the loader never issues (nor announces) its first stage
+    FAULT_SKIP_PUBLISH = 2,    // tail K split: helper parts never count their stored partials
 };
 
 // Which kernel variant a launch uses.
@@ -78,7 +86,7 @@ struct GemmConfig {
 };
 
 cudaError_t launch_gemm(const GemmConfig &cfg, const CUtensorMap &tmA, const CUtensorMap &tmB,
-                        const CUtensorMap *tmMeta, const GemmParams &p, int grid, cudaStream_t stream);
+                        const GemmParams &p, int grid, cudaStream_t stream);
 
 
 cudaError_t launch_gemm_pair(const GemmConfig &cfg, const CUtensorMap &tmA, const CUtensorMap &tmB,

@@ -30,7 +30,8 @@ struct Smem {
     static constexpr int B_OFF = STAGES * A_STAGE;
     static constexpr int RED_OFF = B_OFF + STAGES * B_STAGE; // K-split partial sums (leader CTA)
     static constexpr int BAR_OFF = RED_OFF + RED_BYTES;
-    static constexpr int NUM_BARS = 2 * STAGES + 7; // full, empty, tfull[2], tempty[2], drain, red_full, red_empty
+    // full, empty, tfull[2], tempty[2], drain, red_full, red_empty, part_full, part_staged
+    static constexpr int NUM_BARS = 2 * STAGES + 9;
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
     static constexpr int BYTES = MISC_OFF + 16;
     static constexpr int ALLOC = BYTES + 1024; // slack to align the base to 1024
@@ -76,6 +77,29 @@ __device__ __noinline__ bool bounded_wait(uint64_t *bar, uint32_t parity, const 
     return false;
 }
 
+__device__ __forceinline__ int ld_acquire_gpu(const int *addr)
+{
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+    return v;
+}
+
+// Wait until the counter in global memory written by other CTAs reaches `target`; false
+// if the CTA is aborting or the limit expired (then the timeout is recorded at `site`).
+static __device__ __noinline__ bool wait_count(const int *counter, int target, const Waiter &w, int site)
+{
+    const uint64_t t0 = globaltimer_ns();
+    for (unsigned long long it = 0; it < kMaxSpin; ++it) {
+        if (ld_acquire_gpu(counter) >= target) return true;
+        if ((it & 31ull) == 0) {
+            if (*w.abort_flag) return false;
+            if (globaltimer_ns() - t0 > w.timeout_ns) break;
+        }
+    }
+    record_timeout(w, site);
+    return false;
+}
+
 __device__ __forceinline__ void tile_coords(const GemmParams &p, int t, int &mb, int &nb)
 {
     const int group = p.group_m * p.tiles_n;
@@ -85,6 +109,51 @@ __device__ __forceinline__ void tile_coords(const GemmParams &p, int t, int &mb,
     const int r = t - gid * group;
     mb = first + r % gm;
     nb = r / gm;
+}
+
+// Work unit u of a launch: a whole tile (u < split_begin), or part `part` of the `split`
+// K parts of tile split_begin + j of the last, partly filled round (j = (u - split_begin) /
+// split).  Splitting that round over K lets more CTA pairs share it at full tile width:
+// at 8192^3 with 76 pairs, the 36 leftover 256 x 256 tiles become 72 half-K units, so
+// the launch takes 13.5 tile times instead of 14.  Part 0 owns the tile: it adds the
+// other parts' fp32 partial sums (in part order) before its epilogue.
+struct Unit {
+    int mb, nb;   // the tile's row and column block
+    int kb0, kb1; // K blocks of this unit
+    int part;     // 0: whole tile or owner of a split tile; 1 .. split-1: helper
+    int j;        // index of a split tile among the split ones; -1 for a whole tile
+};
+
+__device__ __forceinline__ Unit unit_coords(const GemmParams &p, int u)
+{
+    Unit r;
+    int t = u;
+    r.part = 0;
+    r.j = -1;
+    r.kb0 = 0;
+    r.kb1 = p.num_kb;
+    if (u >= p.split_begin) {
+        const int q = u - p.split_begin;
+        r.j = q / p.split;
+        r.part = q - r.j * p.split;
+        t = p.split_begin + r.j;
+        r.kb0 = static_cast<int>((static_cast<long long>(p.num_kb) * r.part) / p.split);
+        r.kb1 = static_cast<int>((static_cast<long long>(p.num_kb) * (r.part + 1)) / p.split);
+    }
+    tile_coords(p, t, r.mb, r.nb);
+    return r;
+}
+
+// Clock probe: CTA 0's SM cycles and global-timer nanoseconds from its start to its end.
+__device__ __forceinline__ void clock_probe_add(const GemmParams &p, unsigned long long c0, unsigned long long g0)
+{
+    if (p.clock_probe && blockIdx.x == 0 && threadIdx.x == 0) {
+        const unsigned long long c1 = clock64();
+        const unsigned long long g1 = globaltimer_ns();
+        atomicAdd(p.clock_probe, c1 - c0);
+        atomicAdd(p.clock_probe + 1, g1 - g0);
+        atomicAdd(p.clock_probe + 2, 1ull);
+    }
 }
 
 __device__ __forceinline__ float ld_elem(const void *base, long long i, int fmt)

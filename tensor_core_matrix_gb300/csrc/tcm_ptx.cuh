@@ -48,6 +48,39 @@ __device__ __forceinline__ void fence_proxy_async_smem()
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory to global
+// memory, in the executing thread's current bulk group.
+__device__ __forceinline__ void bulk_store_s2g(void *gdst, uint32_t smem_src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_src), "r"(bytes)
+                 : "memory");
+}
+
+// Commit the executing thread's bulk copies and wait until all of them have completed.
+__device__ __forceinline__ void bulk_commit_wait_all()
+{
+    asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// Bulk copy of `bytes` (a multiple of 16) from global memory into this CTA's shared
+// memory, counted on `bar`'s transaction bytes.
+__device__ __forceinline__ void bulk_load_g2s(uint32_t smem_dst, const void *gsrc, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_dst),
+                 "l"(gsrc), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// Order this thread's generic-proxy and async-proxy accesses to global memory.
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+// Release-add to a counter in global memory, visible GPU-wide.
+__device__ __forceinline__ void red_release_gpu_add(int *addr, int v)
+{
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
 {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)

@@ -26,9 +26,16 @@ def padded(t, device):
     return buf[:, :cols]
 
 
+def workspace_for(M, N, K, a_dtype, b_dtype, device):
+    """A workspace of the size tcm_gemm_ex_ws asks for (at least 16 bytes)."""
+    n = tcm.tcm_gemm_workspace_bytes(M, N, K, a_dtype, b_dtype)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device)
+
+
 def run_gemm_ex(A, B, out_dtype, *, C=None, alpha=1.0, beta=0.0, sa=None, sb=None, bias=None,
-                fill=float("nan")):
-    """Run tcm_gemm_ex on CPU tensors moved to the GPU; D is pre-filled with NaN."""
+                fill=float("nan"), workspace=False):
+    """Run tcm_gemm_ex (tcm_gemm_ex_ws with a workspace of the queried size if `workspace`) on
+    CPU tensors moved to the GPU; D is pre-filled with NaN."""
     d = dev()
     Ad, Bd = padded(A, d), padded(B, d)
     M, N = A.shape[0], B.shape[0]
@@ -37,7 +44,8 @@ def run_gemm_ex(A, B, out_dtype, *, C=None, alpha=1.0, beta=0.0, sa=None, sb=Non
     sad = None if sa is None else torch.tensor([sa], dtype=torch.float32, device=d)
     sbd = None if sb is None else torch.tensor([sb], dtype=torch.float32, device=d)
     biasd = None if bias is None else bias.to(d)
-    tcm.tcm_gemm_ex(Ad, Bd, D, C=Cd, alpha=alpha, beta=beta, a_scale=sad, b_scale=sbd, bias=biasd)
+    ws = workspace_for(M, N, A.shape[1], A.dtype, B.dtype, d) if workspace else None
+    tcm.tcm_gemm_ex(Ad, Bd, D, C=Cd, alpha=alpha, beta=beta, a_scale=sad, b_scale=sbd, bias=biasd, workspace=ws)
     code, site = tcm.tcm_get_device_status()
     assert code == 0, f"device status {code} at site {site}"
     return D.cpu()

@@ -117,6 +117,115 @@ def test_each_variant_fp8_bound(override, cg, bn, stages, fb):
     assert ratio(D, ref, S, scale=case["sa"] * case["sb"]) <= 1.0
 
 
+@pytest.mark.parametrize("split", [1, 2])
+@pytest.mark.parametrize("M,N,K", [(512, 768, 320), (300, 520, 136), (4096, 2560, 256), (4000, 2600, 200),
+                                   (1024, 1024, 1000)])
+def test_pair_tail_k_split_integer_exact(override, split, M, N, K):
+    """tcm_gemm_ex_ws: the tiles of the last, partly filled round of CTA pairs split into two K
+    halves (split 2: whenever each pair gets at most one half) or not (1); 4096 x 2560 has two full
+    rounds of 76 pairs plus 8 tiles.  Integer sums are exact whatever the order."""
+    override.tcm_set_config_override(2, 256, 0, 0, 0, split)
+    g = si.generator(M + 2 * N + K + split)
+    A = si.integers((M, K), g)
+    B = si.integers((N, K), g)
+    D = run_gemm_ex(A, B, torch.float32, workspace=True)
+    ref, _ = oracle_ref(A, B)
+    assert np.array_equal(D.double().numpy(), ref)
+
+
+@pytest.mark.parametrize("in_fmt", ["bf16", "e4m3"])
+def test_pair_tail_k_split_with_epilogue(override, in_fmt):
+    """Split tail tiles with the whole epilogue (alpha, scales, beta * C, bias): within the bound of the
+    oracle on sampled outputs of every tile, and within it of the unsplit launch (3 rounds + 28 tiles)."""
+    M = N = 4096
+    K = 512
+    g = si.generator(31)
+    if in_fmt == "e4m3":
+        c = si.fp8_case(M, N, K, seed=32)
+        A, B, kw = c["A"], c["B"], dict(sa=c["sa"], sb=c["sb"], bias=c["bias"])
+    else:
+        A, B = si.normal((M, K), g), si.normal((N, K), g)
+        kw = dict(bias=si.normal((N,), g))
+    C = si.normal((M, N), g)
+    override.tcm_set_config_override(0, 0, 0, 0, 0, 2)  # split the 28 tail tiles whatever K
+    out = [run_gemm_ex(A, B, torch.bfloat16, C=C, alpha=0.5, beta=0.25, workspace=ws, **kw) for ws in (False, True)]
+    rows, cols = sample_indices(M, N, per_tile=2)
+    ref, S = oracle_ref(A, B, C=C, alpha=0.5, beta=0.25, rows=rows, cols=cols, **kw)
+    scale = 0.5 * kw.get("sa", 1.0) * kw.get("sb", 1.0)
+    for D in out:
+        assert ratio(D, ref, S, scale=scale, rows=rows, cols=cols) <= 1.0
+
+
+def test_workspace_size_and_rejection(override):
+    """The workspace query matches the plan (36 split tiles at 8192^3 on 76 pairs: flags plus one
+    128 x 256 fp32 slot per CTA per helper part); a smaller workspace is rejected before launch."""
+    import tensor_core_matrix_gb300 as tcm
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    pairs = sms // 2
+    rem = 1024 % pairs
+    n = tcm.tcm_gemm_workspace_bytes(8192, 8192, 8192, torch.bfloat16, torch.bfloat16)
+    if rem == 0:
+        assert n == 0
+        return
+    assert 2 * rem <= pairs  # 36 leftover tiles on 76 pairs: split in two K halves
+    assert n == -(-(rem * 2 * 4) // 256) * 256 + rem * 2 * 128 * 256 * 4
+    assert tcm.tcm_gemm_workspace_bytes(16, 28672, 8192, torch.bfloat16, torch.bfloat16) == 0  # no pair tiles
+    d = dev()
+    A = torch.zeros((8192, 8192), dtype=torch.bfloat16, device=d)
+    D = torch.empty((8192, 8192), dtype=torch.bfloat16, device=d)
+    small = torch.empty(n - 256, dtype=torch.uint8, device=d)
+    with pytest.raises(tcm.TcmError, match="INVALID_ARG"):
+        tcm.tcm_gemm_ex(A, A, D, workspace=small)
+
+
+def test_tail_k_split_wait_times_out_and_context_stays_usable(override):
+    """Helper parts that never announce their partial sums: each owner's bounded wait runs out
+    (site 10), the kernel returns, and the next launch is correct."""
+    tcm = override
+    d = dev()
+    M, N, K = 4096, 2560, 512
+    g = si.generator(78)
+    A = si.integers((M, K), g)
+    B = si.integers((N, K), g)
+    Ad, Bd = A.to(d), B.to(d)
+    tcm.tcm_set_config_override(0, 0, 0, 0, 0, 2)  # split the 8 tail tiles whatever K
+    ws = torch.empty(tcm.tcm_gemm_workspace_bytes(M, N, K, torch.bfloat16), dtype=torch.uint8, device=d)
+    assert ws.numel() > 0
+    D = torch.zeros((M, N), dtype=torch.float32, device=d)
+    tcm.tcm_clear_device_status()
+    tcm.tcm_set_timeout_ns(50_000_000)
+    try:
+        tcm.tcm_debug_fail_next_launch(2)
+        tcm.tcm_gemm_ex(Ad, Bd, D, workspace=ws)
+        code, site = tcm.tcm_get_device_status()
+        assert (code, site) == (5, 10)
+    finally:
+        tcm.tcm_set_timeout_ns(0)
+        tcm.tcm_clear_device_status()
+    D.fill_(float("nan"))
+    tcm.tcm_gemm_ex(Ad, Bd, D, workspace=ws)
+    assert tcm.tcm_get_device_status() == (0, 0)
+    ref, _ = oracle_ref(A, B)
+    assert np.array_equal(D.cpu().double().numpy(), ref)
+
+
+@pytest.mark.parametrize("in_fmt", ["bf16", "e4m3"])
+def test_8192_cubed_with_workspace_sampled(in_fmt):
+    """The bench's two dense GEMMs through tcm_gemm_ex_ws at full size (tail tiles split over K),
+    sampled outputs of every 128 x 128 block against the oracle."""
+    if in_fmt == "bf16":
+        c = si.llm_case(8192, 8192, 8192, seed=2)
+        kw = {}
+    else:
+        c = si.fp8_case(seed=3)
+        kw = dict(sa=c["sa"], sb=c["sb"], bias=c["bias"])
+    D = run_gemm_ex(c["A"], c["B"], torch.bfloat16, workspace=True, **kw)
+    rows, cols = sample_indices(8192, 8192)
+    ref, S = oracle_ref(c["A"], c["B"], rows=rows, cols=cols, **kw)
+    assert ratio(D, ref, S, scale=kw.get("sa", 1.0) * kw.get("sb", 1.0), rows=rows, cols=cols) <= 1.0
+    assert not torch.isnan(D).any()
+
+
 @pytest.mark.parametrize("ks", [2, 4])
 @pytest.mark.parametrize("M,N,K", [(16, 1024, 2048), (64, 384, 1000), (1, 256, 512), (16, 512, 64), (40, 300, 4096)])
 def test_k_split_cluster_integer_exact(override, ks, M, N, K):
