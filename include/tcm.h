@@ -160,6 +160,37 @@ tcm_status tcm_gemm_ex_ws(int64_t M, int64_t N, int64_t K,
 int64_t tcm_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, tcm_dtype b_dtype);
 
 /*
+ * tcm_gemm_ex_builtin_ws -- tcm_gemm_ex_ws for callers that cannot allocate device
+ * memory.  The pages have no counterpart: this is a service of the library.
+ *
+ * Some callers have no way to provide tcm_gemm_ex_ws's workspace: code that runs
+ * inside another framework's device-memory manager, where every allocation must go
+ * through that manager, or a latency-critical path where cudaMalloc (which may
+ * synchronise the device) is not allowed.  This entry point takes the same
+ * arguments as tcm_gemm_ex (the caller still passes A, B, C, D, scales and bias)
+ * and allocates nothing: its workspace is a 10 MiB array inside the library, one
+ * copy on every GPU that loads the library, held until the process exits.
+ *  - Size limit: a problem whose tcm_gemm_workspace_bytes exceeds 10 MiB
+ *    (10485760 bytes) returns TCM_ERR_UNSUPPORTED before anything is launched.
+ *    On a 152-SM GB300 no problem needs more than about 9.5 MiB.
+ *  - Set-up: the first call on a device looks up that device's copy of the array
+ *    (with the device current); make that first call before any stream capture.
+ *  - Sharing: every call on a device uses the same array, which keeps the last
+ *    call's contents; each call clears what must start at zero (its counters) on
+ *    `stream` before its kernel.  Calls that may run at the same time on the GPU
+ *    (different streams without ordering between them) race on the array and
+ *    must not be made; calls ordered on one stream are safe.
+ * Results are those of tcm_gemm_ex_ws with a workspace of its own.
+ */
+tcm_status tcm_gemm_ex_builtin_ws(int64_t M, int64_t N, int64_t K,
+                                  tcm_dtype a_dtype, const void *A, int64_t lda,
+                                  tcm_dtype b_dtype, const void *B, int64_t ldb,
+                                  const void *C, int64_t ldc, void *D, int64_t ldd,
+                                  tcm_dtype out_dtype, float alpha, float beta,
+                                  const float *a_scale, const float *b_scale, const void *bias,
+                                  tcm_stream_t stream);
+
+/*
  * tcm_gemm_fused -- tcm_gemm_ex with the rest of the epilogue chain:
  *   y   = act(alpha * sA * sB * (A . B) + beta * C + bias)
  *   D   = y / d_scale, cast to out_dtype (FP8: round to nearest even, saturating to

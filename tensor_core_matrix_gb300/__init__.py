@@ -34,7 +34,7 @@ EXPORTS = ("tcm_gemm", "tcm_gemm_ex", "tcm_gemm_fused", "tcm_sp_compress", "tcm_
            "tcm_nvfp4_pack_scales",
            "tcm_get_device_status", "tcm_clear_device_status", "tcm_set_timeout_ns",
            "tcm_status_string", "tcm_version", "tcm_set_config_override", "tcm_debug_fail_next_launch",
-           "tcm_set_clock_probe", "tcm_gemm_ex_ws", "tcm_gemm_workspace_bytes")
+           "tcm_set_clock_probe", "tcm_gemm_ex_ws", "tcm_gemm_workspace_bytes", "tcm_gemm_ex_builtin_ws")
 
 
 class TcmError(RuntimeError):
@@ -64,6 +64,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.tcm_gemm_ex_ws.restype = i32
     lib.tcm_gemm_ex_ws.argtypes = [i64, i64, i64, i32, vp, i64, i32, vp, i64, vp, i64, vp, i64,
                                    i32, f32, f32, vp, vp, vp, vp, i64, vp]
+    lib.tcm_gemm_ex_builtin_ws.restype = i32
+    lib.tcm_gemm_ex_builtin_ws.argtypes = [i64, i64, i64, i32, vp, i64, i32, vp, i64, vp, i64, vp, i64,
+                                           i32, f32, f32, vp, vp, vp, vp]
     lib.tcm_gemm_workspace_bytes.restype = i64
     lib.tcm_gemm_workspace_bytes.argtypes = [i64, i64, i64, i32, i32]
     lib.tcm_gemm_fused.restype = i32

@@ -433,6 +433,52 @@ static tcm_status gemm_impl(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, 
     return e == cudaSuccess ? TCM_OK : TCM_ERR_CUDA;
 }
 
+} // extern "C"
+
+namespace tcm {
+
+// Workspace of tcm_gemm_ex_builtin_ws, inside the library: one copy on every device that
+// loads it, kept until the process exits.  10 MiB holds the largest workspace a
+// 256 x 256 CTA-pair split can ask for on a GB300 (152 SMs: at most 38 split tiles of
+// two 128 KB slots each, plus their counters, 9.5 MiB); larger requests are refused.
+constexpr int64_t kBuiltinWsBytes = 10ll << 20;
+static __device__ __align__(256) uint8_t g_builtin_ws[kBuiltinWsBytes];
+
+// Device address of this device's copy of g_builtin_ws.  The first call on a device
+// looks it up (with that device current) and keeps it; the array's name in host code
+// is only a stand-in for the symbol, never a usable address.
+static void *builtin_ws_ptr()
+{
+    static void *ptrs[kMaxDevices] = {};
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ptrs[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_builtin_ws) != cudaSuccess) return nullptr;
+        ptrs[dev] = p;
+    }
+    return ptrs[dev];
+}
+
+} // namespace tcm
+
+extern "C" {
+
+tcm_status tcm_gemm_ex_builtin_ws(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const void *A, int64_t lda,
+                                  tcm_dtype b_dtype, const void *B, int64_t ldb, const void *C, int64_t ldc, void *D,
+                                  int64_t ldd, tcm_dtype out_dtype, float alpha, float beta, const float *a_scale,
+                                  const float *b_scale, const void *bias, tcm_stream_t stream)
+{
+    const int64_t need = tcm_gemm_workspace_bytes(M, N, K, a_dtype, b_dtype);
+    if (need > kBuiltinWsBytes) return TCM_ERR_UNSUPPORTED; // larger than the built-in workspace
+    void *ws = builtin_ws_ptr();
+    if (!ws) return TCM_ERR_CUDA;
+    return gemm_impl(M, N, K, a_dtype, A, lda, b_dtype, B, ldb, C, ldc, D, ldd, out_dtype, alpha, beta, a_scale,
+                     b_scale, bias, TCM_ACT_NONE, nullptr, nullptr, false, ws, kBuiltinWsBytes, stream);
+}
+
 int64_t tcm_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, tcm_dtype b_dtype)
 {
     const bool a16 = a_dtype == TCM_BF16 || a_dtype == TCM_F16;
