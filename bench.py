@@ -515,8 +515,78 @@ class LaunchTimer:
         return e0.elapsed_time(e1) / iters
 
 
+class Workload:
+    """One GEMM workload on the device: its launch closure (on `stream`), sizes, algorithmic
+    bytes and the tensor-peak multiple of its input format (bf16 = 1)."""
+
+    def __init__(self, name, case, tcm, device, stream):
+        self.name = name
+        sparse = "A_logical" in case
+        A = (case["A_logical"] if sparse else case["A"]).to(device)
+        B = case["B"].to(device)
+        M = A.shape[0]
+        N = B.shape[0]
+        fp4 = case.get("nv") or case.get("a_fmt") == "e2m1"          # packed operands: K/2 bytes per row
+        K = A.shape[1] * (2 if fp4 else 1)
+        out_dtype = torch.float32 if case.get("out_fmt") == "f32" else torch.bfloat16
+        if case.get("fused"):
+            out_dtype = torch.float8_e4m3fn
+        D = torch.empty((M, N), dtype=out_dtype, device=device)
+        C = case["C"].to(device) if case.get("C") is not None else None
+        kw = dict(C=C, alpha=case.get("alpha", 1.0), beta=case.get("beta", 0.0), stream=stream)
+        self.workspace_bytes = 0
+        self.peak_mult = 1.0
+        if "sa" in case:
+            kw.update(a_scale=torch.tensor([case["sa"]], device=device), b_scale=torch.tensor([case["sb"]], device=device))
+            if case.get("bias") is not None:
+                kw.update(bias=case["bias"].to(device))
+        if case.get("b_fmt") == "e2m1" and case.get("a_fmt") != "e2m1":
+            kw.update(b_fmt="e2m1")  # W4A8: B holds N x K/2 bytes of packed FP4
+        if sparse:
+            self.peak_mult = 2.0  # logical FLOPs against the 2:4 rate
+            Ac, meta = tcm.tcm_sp_compress(A)
+            if case.get("tc"):
+                meta_tc = tcm.tcm_sp_meta_pack(meta, K)
+                self.launch = lambda: tcm.tcm_gemm_sp_tc(Ac, meta_tc, B, D, C=C, alpha=kw["alpha"], beta=kw["beta"],
+                                                         stream=stream)
+            else:
+                self.launch = lambda: tcm.tcm_gemm_sp(Ac, meta, B, D, C=C, alpha=kw["alpha"], beta=kw["beta"],
+                                                      stream=stream)
+        elif case.get("nv"):
+            self.peak_mult = FP4_OVER_BF16
+            SA = tcm.tcm_nvfp4_pack_scales(case["SA"].to(device), K)
+            SB = tcm.tcm_nvfp4_pack_scales(case["SB"].to(device), K)
+            self.launch = lambda: tcm.tcm_gemm_nvfp4(A, SA, B, SB, D, alpha=case["alpha"], stream=stream)
+        elif "SA" in case:
+            # scales packed once into the blocked layout (as a quantiser would emit them)
+            self.peak_mult = FP4_OVER_BF16 if fp4 else FP8_OVER_BF16
+            SA = tcm.tcm_mx_pack_scales(case["SA"].to(device), K)
+            SB = tcm.tcm_mx_pack_scales(case["SB"].to(device), K)
+            fmt = "e2m1" if fp4 else None
+            self.launch = lambda: tcm.tcm_gemm_mx(A, SA, B, SB, D, stream=stream, fmt=fmt)
+        elif case.get("fused"):
+            self.peak_mult = FP8_OVER_BF16
+            d_scale = torch.tensor([2.0], device=device)
+            amax = torch.zeros(1, device=device)
+            self.launch = lambda: tcm.tcm_gemm_fused(A, B, D, act=case["fused"], d_scale=d_scale, amax=amax, **kw)
+        else:
+            if A.dtype in (torch.float8_e4m3fn, torch.float8_e5m2):
+                self.peak_mult = FP8_OVER_BF16
+            if kw.get("b_fmt") is None:
+                self.workspace_bytes = tcm.tcm_gemm_workspace_bytes(M, N, K, A.dtype, B.dtype)
+                if self.workspace_bytes > 0:
+                    kw.update(workspace=torch.empty(self.workspace_bytes, dtype=torch.uint8, device=device))
+            self.launch = lambda: tcm.tcm_gemm_ex(A, B, D, **kw)
+        self.M, self.N, self.K = M, N, K
+        self.in_bytes = (A.numel() // (2 if sparse else 1)) * A.element_size() + B.numel() * B.element_size()
+        self.bytes = self.in_bytes + D.numel() * D.element_size() + (C.numel() * C.element_size() if C is not None else 0)
+        self.flop = 2.0 * M * N * K
+        self.tensors = (A, B, C, D)
+
+
 def part_cases():
-    """(name, builder, bound) of every configured workload besides the step's."""
+    """(name, builder, bound) of every configured workload besides the step's, then the
+    block-scaled, fused and FP4 workloads of the library."""
     return [
         ("c1_bf16_512_C_f32", lambda: si.small_case(), "launch"),
         ("c2_f16_4096", lambda: si.square_case(4096, "f16"), "tensor"),
@@ -526,14 +596,19 @@ def part_cases():
         ("c3_bf16_8192x24576x8192", lambda: si.llm_case(8192, 24576, 8192), "tensor"),
         ("c3_skinny_bf16_16x28672x8192", lambda: si.llm_case(16, 28672, 8192), "hbm"),
         ("c4_e4m3xe5m2_8192", lambda: si.fp8_case(b_fmt="e5m2"), "tensor"),
+        ("f1_mxfp8_e4m3_8192", lambda: si.mx_case(), "tensor"),
+        ("f1_nvfp4_8192", lambda: dict(si.nvfp4_case(), nv=True), "tensor"),
+        ("f1_mxfp4_8192", lambda: si.mxfp4_case(), "tensor"),
+        ("f2_fused_e4m3_gelu_e4m3out_amax_8192", lambda: dict(si.fp8_case(b_fmt="e4m3"), fused="gelu"), "tensor"),
+        ("f3_w4a8_e4m3xe2m1_8192", lambda: si.w4a8_case(), "tensor"),
     ]
 
 
 def run_parts(tcm, device, iters, peaks_used):
     """Each configured workload timed on its own, outside `value`: median device time of
     single launches (L2 flushed first when the inputs fit in it), the mean of back-to-back
-    launches, TFLOP/s against the burst tensor peak and, for the HBM-bound skinny shape,
-    GB/s of its algorithmic bytes against the measured copy bandwidth."""
+    launches, TFLOP/s against the burst tensor peak of its input format and, for the
+    HBM-bound skinny shape, GB/s of its algorithmic bytes against the measured copy bandwidth."""
     p, src = peaks_used
     bf16_peak = float(p.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     hbm_peak = float(p.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
@@ -541,63 +616,43 @@ def run_parts(tcm, device, iters, peaks_used):
     timer = LaunchTimer(device, stream)
     parts = {}
     for name, build, bound in part_cases():
-        case = build()
-        A, B = case["A"].to(device), case["B"].to(device)
-        M, K = A.shape
-        N = B.shape[0]
-        out = torch.float32 if case.get("out_fmt") == "f32" else torch.bfloat16
-        D = torch.empty((M, N), dtype=out, device=device)
-        C = case["C"].to(device) if case.get("C") is not None else None
-        kw = dict(C=C, alpha=case.get("alpha", 1.0), beta=case.get("beta", 0.0), stream=stream)
-        if "sa" in case:
-            kw.update(a_scale=torch.tensor([case["sa"]], device=device),
-                      b_scale=torch.tensor([case["sb"]], device=device), bias=case["bias"].to(device))
-        ws_bytes = tcm.tcm_gemm_workspace_bytes(M, N, K, A.dtype, B.dtype)
-        if ws_bytes > 0:
-            kw.update(workspace=torch.empty(ws_bytes, dtype=torch.uint8, device=device))
-
-        def launch():
-            tcm.tcm_gemm_ex(A, B, D, **kw)
-
+        w = Workload(name, build(), tcm, device, stream)
         for _ in range(5):
-            launch()
-        in_bytes = A.numel() * A.element_size() + B.numel() * B.element_size()
-        alg_bytes = in_bytes + D.numel() * D.element_size() + (C.numel() * C.element_size() if C is not None else 0)
-        flush = in_bytes < L2_BYTES
+            w.launch()
+        flush = w.in_bytes < L2_BYTES
         probe = torch.zeros(3, dtype=torch.int64, device=device)
         tcm.tcm_set_clock_probe(probe)
-        t_single = timer.single(launch, iters, flush)
-        t_b2b = timer.back_to_back(launch, iters)
+        t_single = timer.single(w.launch, iters, flush)
+        t_b2b = timer.back_to_back(w.launch, iters)
         tcm.tcm_set_clock_probe(None)
         ms = statistics.median(t_single)
-        flop = 2.0 * M * N * K
-        peak = bf16_peak * (FP8_OVER_BF16 if "e4m3" in name else 1.0)
-        rec = {"M": M, "N": N, "K": K, "ms": ms, "ms_min": min(t_single), "ms_back_to_back": t_b2b,
-               "tflops": flop / (ms * 1e-3) / 1e12, "tflops_back_to_back": flop / (t_b2b * 1e-3) / 1e12,
-               "frac_of_tensor_peak": flop / (ms * 1e-3) / 1e12 / peak, "bound": bound,
-               "device_measured_mhz": probe_mhz(probe), "workspace_bytes": ws_bytes,
+        peak = bf16_peak * w.peak_mult
+        tf = w.flop / (ms * 1e-3) / 1e12
+        rec = {"M": w.M, "N": w.N, "K": w.K, "ms": ms, "ms_min": min(t_single), "ms_back_to_back": t_b2b,
+               "tflops": tf, "tflops_back_to_back": w.flop / (t_b2b * 1e-3) / 1e12,
+               "frac_of_tensor_peak": tf / peak, "peak_tflops": peak, "bound": bound,
+               "device_measured_mhz": probe_mhz(probe), "workspace_bytes": w.workspace_bytes,
                "timing": f"median of {iters} single launches (device sleep before each start event, "
                          f"{'L2 flushed before each' if flush else 'inputs larger than L2, no flush'}); "
                          f"mean of {iters} back-to-back launches"}
         if bound == "hbm":
-            t_flushed = timer.single(launch, iters, True)
-            t_call = timer.single(launch, iters, False, sleep=False)
+            t_flushed = timer.single(w.launch, iters, True)
+            t_call = timer.single(w.launch, iters, False, sleep=False)
             msf = statistics.median(t_flushed)
-            rec.update({"algorithmic_bytes": alg_bytes,
-                        "gbs": alg_bytes / (ms * 1e-3) / 1e9, "frac_of_hbm": alg_bytes / (ms * 1e-3) / 1e9 / hbm_peak,
-                        "ms_l2_flushed": msf, "gbs_l2_flushed": alg_bytes / (msf * 1e-3) / 1e9,
-                        "frac_of_hbm_l2_flushed": alg_bytes / (msf * 1e-3) / 1e9 / hbm_peak,
-                        "gbs_back_to_back": alg_bytes / (t_b2b * 1e-3) / 1e9,
-                        "frac_of_hbm_back_to_back": alg_bytes / (t_b2b * 1e-3) / 1e9 / hbm_peak,
+            gbs = lambda t: w.bytes / (t * 1e-3) / 1e9
+            rec.update({"algorithmic_bytes": w.bytes, "gbs": gbs(ms), "frac_of_hbm": gbs(ms) / hbm_peak,
+                        "ms_l2_flushed": msf, "gbs_l2_flushed": gbs(msf), "frac_of_hbm_l2_flushed": gbs(msf) / hbm_peak,
+                        "gbs_back_to_back": gbs(t_b2b), "frac_of_hbm_back_to_back": gbs(t_b2b) / hbm_peak,
                         "ms_per_call_synchronised": statistics.median(t_call),
                         "host_call_us": 1e3 * (statistics.median(t_call) - ms)})
         parts[name] = rec
-        del A, B, C, D, case
+        del w
     torch.cuda.synchronize(device)
     code, site = tcm.tcm_get_device_status(stream)
     if code != 0:
         raise SystemExit(f"device status {code} at site {site} in the per-config parts")
-    return parts, timer.windows, f"{src} bf16_tflops burst (single launches); FP8 x{FP8_OVER_BF16:g}; hbm_gbs"
+    return parts, timer.windows, (f"{src} bf16_tflops burst (single launches) x the format's nominal dense "
+                                  f"ratio: FP8 x{FP8_OVER_BF16:g}, FP4 x{FP4_OVER_BF16:g}, 2:4 logical x2; hbm_gbs")
 
 
 # ------------------------------------------------------------------ --shapes (extended list)
@@ -618,6 +673,7 @@ def shape_cases():
         ("sparse-tc 2:4 bf16 8192^3 (hardware-ordered metadata)", lambda: dict(si.sparse_case(), tc=True)),
         ("mxfp8 e4m3 8192^3 (E8M0 scales per 32)", lambda: si.mx_case()),
         ("nvfp4 e2m1 8192^3 (UE4M3 scales per 16, per-tensor scales in alpha)", lambda: dict(si.nvfp4_case(), nv=True)),
+        ("mxfp4 e2m1 8192^3 (E8M0 scales per 32)", lambda: si.mxfp4_case()),
         ("w4a8 fp8 e4m3 x fp4 e2m1 8192^3 +scales", lambda: si.w4a8_case()),
         ("fused fp8 e4m3 8192^3 +scales+bias -> GELU -> e4m3 out (d_scale 2) + amax",
          lambda: dict(si.fp8_case(b_fmt="e4m3"), fused="gelu")),
@@ -635,76 +691,33 @@ def run_shapes(args, tcm, device, peaks_used):
     for name, build in shape_cases():
         if args.only and args.only not in name:
             continue
-        case = build()
-        sparse = "A_logical" in case
-        A = (case["A_logical"] if sparse else case["A"]).to(device)
-        B = case["B"].to(device)
-        M, K = A.shape
-        N = B.shape[0]
-        out_dtype = torch.float32 if case.get("out_fmt") == "f32" else torch.bfloat16
-        if case.get("fused"):
-            out_dtype = torch.float8_e4m3fn
-        D = torch.empty((M, N), dtype=out_dtype, device=device)
-        C = case["C"].to(device) if case.get("C") is not None else None
-        kw = dict(C=C, alpha=case.get("alpha", 1.0), beta=case.get("beta", 0.0), stream=stream)
-        if "sa" in case:
-            kw.update(a_scale=torch.tensor([case["sa"]], device=device), b_scale=torch.tensor([case["sb"]], device=device))
-            if case.get("bias") is not None:
-                kw.update(bias=case["bias"].to(device))
-        if case.get("b_fmt") == "e2m1":
-            kw.update(b_fmt="e2m1")  # B holds N x K/2 bytes of packed FP4
-        if sparse:
-            Ac, meta = tcm.tcm_sp_compress(A)
-            if case.get("tc"):
-                meta_tc = tcm.tcm_sp_meta_pack(meta, K)
-                launch = lambda: tcm.tcm_gemm_sp_tc(Ac, meta_tc, B, D, C=C, alpha=kw["alpha"], beta=kw["beta"],
-                                                    stream=stream)
-            else:
-                launch = lambda: tcm.tcm_gemm_sp(Ac, meta, B, D, C=C, alpha=kw["alpha"], beta=kw["beta"],
-                                                 stream=stream)
-        elif case.get("nv"):
-            SA = tcm.tcm_nvfp4_pack_scales(case["SA"].to(device), 2 * K)
-            SB = tcm.tcm_nvfp4_pack_scales(case["SB"].to(device), 2 * K)
-            K = 2 * K  # A holds K/2 bytes per row
-            launch = lambda: tcm.tcm_gemm_nvfp4(A, SA, B, SB, D, alpha=case["alpha"], stream=stream)
-        elif "SA" in case:
-            # scales packed once into the blocked layout (as a quantiser would emit them)
-            SA = tcm.tcm_mx_pack_scales(case["SA"].to(device), K)
-            SB = tcm.tcm_mx_pack_scales(case["SB"].to(device), K)
-            launch = lambda: tcm.tcm_gemm_mx(A, SA, B, SB, D, stream=stream)
-        elif case.get("fused"):
-            d_scale = torch.tensor([2.0], device=device)
-            amax = torch.zeros(1, device=device)
-            launch = lambda: tcm.tcm_gemm_fused(A, B, D, act=case["fused"], d_scale=d_scale, amax=amax, **kw)
-        else:
-            launch = lambda: tcm.tcm_gemm_ex(A, B, D, **kw)
+        w = Workload(name, build(), tcm, device, stream)
         torch.cuda.synchronize(device)
         for _ in range(5):
-            launch()
-        in_bytes_total = sum(t.numel() * t.element_size() for t in (A, B) if t is not None)
-        flush = in_bytes_total < L2_BYTES
-        times = timer.single(launch, args.shape_iters, flush)
-        ms_b2b = timer.back_to_back(launch, args.shape_iters)
+            w.launch()
+        flush = w.in_bytes < L2_BYTES
+        probe = torch.zeros(3, dtype=torch.int64, device=device)
+        tcm.tcm_set_clock_probe(probe)
+        times = timer.single(w.launch, args.shape_iters, flush)
+        ms_b2b = timer.back_to_back(w.launch, args.shape_iters)
+        tcm.tcm_set_clock_probe(None)
         code, site = tcm.tcm_get_device_status(stream)
         ms = statistics.median(times)
-        flop = 2.0 * M * N * K
-        in_bytes = (A.numel() // (2 if sparse else 1)) * A.element_size() + B.numel() * B.element_size()
-        byts = in_bytes + D.numel() * D.element_size() + (C.numel() * C.element_size() if C is not None else 0)
-        tf = flop / (ms * 1e-3) / 1e12
-        gbs = byts / (ms * 1e-3) / 1e9
-        peak = bf16_peak * (FP4_OVER_BF16 if "nvfp4" in name else
-                            FP8_OVER_BF16 if ("fp8" in name or "mx" in name) else 1.0)  # fused, w4a8: FP8 rate
-        line = {"kind": "shape", "workload": name, "M": M, "N": N, "K": K, "ms_median": ms, "ms_min": min(times),
-                "tflops": tf, "frac_of_tensor_peak": tf / peak, "algorithmic_bytes": byts, "gbs": gbs,
-                "frac_of_hbm": gbs / hbm_peak, "bound": "hbm" if M <= 64 else "tensor", "device_status": code,
-                "ms_back_to_back": ms_b2b, "tflops_back_to_back": flop / (ms_b2b * 1e-3) / 1e12,
+        tf = w.flop / (ms * 1e-3) / 1e12
+        gbs = w.bytes / (ms * 1e-3) / 1e9
+        peak = bf16_peak * w.peak_mult
+        line = {"kind": "shape", "workload": name, "M": w.M, "N": w.N, "K": w.K, "ms_median": ms, "ms_min": min(times),
+                "tflops": tf, "frac_of_tensor_peak": tf / peak, "algorithmic_bytes": w.bytes, "gbs": gbs,
+                "frac_of_hbm": gbs / hbm_peak, "bound": "hbm" if w.M <= 64 else "tensor", "device_status": code,
+                "ms_back_to_back": ms_b2b, "tflops_back_to_back": w.flop / (ms_b2b * 1e-3) / 1e12,
+                "device_measured_mhz": probe_mhz(probe), "workspace_bytes": w.workspace_bytes,
                 "timing": f"5 warm-up launches, then the median of {args.shape_iters} single launches (device "
                           f"sleep before each start event; " + (
                               "L2 flushed before each)" if flush else "inputs larger than L2, no flush)") +
                           f"; mean of {args.shape_iters} back-to-back launches",
-                "peak_source": f"{src} bf16_tflops burst"}
+                "peak_source": f"{src} bf16_tflops burst x {w.peak_mult:g}"}
         print(json.dumps(line), flush=True)
-        del A, B, D, C, case
+        del w
 
 
 def config_block(world):

@@ -193,8 +193,9 @@ tcm_status tcm_gemm_ex_builtin_ws(int64_t M, int64_t N, int64_t K,
 /*
  * tcm_gemm_fused -- tcm_gemm_ex with the rest of the epilogue chain:
  *   y   = act(alpha * sA * sB * (A . B) + beta * C + bias)
- *   D   = y / d_scale, cast to out_dtype (FP8: round to nearest even, saturating to
- *         the largest finite value; 16/32-bit: RNE, d_scale not used)
+ *   D   = y * r, r = 1 / d_scale rounded once to fp32 (round to nearest even), then
+ *         cast to out_dtype (FP8: round to nearest even, saturating to the largest
+ *         finite value; 16/32-bit: RNE, d_scale not used)
  *   amax = max over all M x N outputs of |y| (before the division and the cast)
  *
  * "NVIDIA MMA", section "输入/累加/输出": the epilogue does scale / bias /
@@ -207,8 +208,11 @@ tcm_status tcm_gemm_ex_builtin_ws(int64_t M, int64_t N, int64_t K,
  *  act               TCM_ACT_NONE, TCM_ACT_RELU or TCM_ACT_GELU; else
  *                    TCM_ERR_INVALID_ARG.
  *  d_scale           DEVICE pointer to one fp32 (dequantisation factor of D:
- *                    real value = stored value * d_scale), or NULL for 1.0.
- *                    Read only for FP8 outputs.
+ *                    real value ~= stored value * d_scale), or NULL for 1.0.
+ *                    Read only for FP8 outputs; D is y times its rounded
+ *                    reciprocal (one reciprocal per launch, not one division
+ *                    per element).
+ *  The device product y * r is rounded to fp32 before the FP8 cast.
  *  amax              DEVICE pointer to one fp32, 4-byte aligned, or NULL.  The
  *                    call sets it to 0 on `stream` before the GEMM, then to the
  *                    maximum |y| (NaN if any y is NaN).
@@ -305,15 +309,20 @@ tcm_status tcm_gemm_sp_tc(int64_t M, int64_t N, int64_t K, tcm_dtype dtype,
                           tcm_dtype out_dtype, tcm_stream_t stream);
 
 /*
- * tcm_gemm_mx -- block-scaled FP8 GEMM (MXFP8):
+ * tcm_gemm_mx -- block-scaled GEMM in an MX format, MXFP8 or MXFP4:
  *   D = alpha * sum_g (A_g * 2^(sa_g - 127)) . (B_g * 2^(sb_g - 127)) + beta * C + bias
  *
  * "NVIDIA MMA", section "SM100：tcgen05.mma" (block-scaled form: each K block's
  * partial sum is scaled by the A and B block scales before it is accumulated)
  * and section "MXFP4 与 NVFP4" (MX formats: one UE8M0 scale per 32 elements;
  * kernels follow a scale layout contract, which is the blocked layout below).
- *  a_dtype, b_dtype  TCM_E4M3 or TCM_E5M2 (any pair).
- *  A                 M x K row-major (pitch K), B N x K (pitch K): the elements.
+ *  a_dtype, b_dtype  MXFP8: TCM_E4M3 or TCM_E5M2 (any pair).  MXFP4: both TCM_E2M1
+ *                    (packed two per byte, element 2i in the low nibble; section "MXFP4
+ *                    与 NVFP4": MXFP4 = E2M1 elements with a UE8M0 scale per 32), then K
+ *                    must be a multiple of 256 (else TCM_ERR_INVALID_ARG).  E2M1 with an
+ *                    FP8 type: TCM_ERR_UNSUPPORTED.
+ *  A                 M x K row-major (pitch K), B N x K (pitch K): the elements (E2M1:
+ *                    rows of K/2 bytes).
  *  a_scales          E8M0 scale codes (value 2^(code - 127); 255 is NaN) of the
  *                    32-element blocks of the rows of A, in the BLOCKED layout
  *                    written by tcm_mx_pack_scales (tcm_mx_scales_bytes(M, K)

@@ -291,6 +291,17 @@ def activate(x, act):
     return y
 
 
+def fp32_reciprocal(d):
+    """1 / d rounded to the nearest fp32 value, ties to even, decided exactly: the float
+    candidates around fp32(1 / d) are compared with the rational 1 / d."""
+    from fractions import Fraction
+    exact = 1 / Fraction(float(d))
+    c = np.float32(1.0 / float(d))
+    cands = [np.nextafter(c, np.float32(-np.inf)), c, np.nextafter(c, np.float32(np.inf))]
+    best = min(cands, key=lambda v: (abs(Fraction(float(v)) - exact), int(np.float32(v).view(np.uint32)) & 1))
+    return float(best)
+
+
 def fused_reference(ref, S, act, out_fmt, scale=1.0, d_scale=1.0):
     """Expected outputs of the fused epilogue and their bounds.
 
@@ -299,8 +310,9 @@ def fused_reference(ref, S, act, out_fmt, scale=1.0, d_scale=1.0):
     ``bound_y`` on |y_gpu - y| (accumulation allowance and the fp32 epilogue
     arithmetic, stretched by the activation's Lipschitz constant, plus the
     device GELU's own evaluation error), and the stored value's target -- y,
-    or y / d_scale saturated for FP8 outputs -- with the bound on the decoded
-    output (bound_y carried through d_scale, plus one RNE cast of the format)."""
+    or y * RN32(1 / d_scale) saturated for FP8 outputs (the library's documented
+    rule) -- with the bound on the decoded output (bound_y carried through the
+    multiplier, the fp32 rounding of the device's product, then one RNE cast)."""
     ref = np.asarray(ref, dtype=np.float64)
     y = activate(ref, act)
     lip = GELU_LIPSCHITZ if ACT[act] == 2 else 1.0
@@ -308,8 +320,9 @@ def fused_reference(ref, S, act, out_fmt, scale=1.0, d_scale=1.0):
     e_y = lip * e_pre + (2.0 ** -20 * np.abs(ref) if ACT[act] == 2 else 0.0)
     if out_fmt in ("e4m3", "e5m2"):
         target = np.empty_like(y)
-        _load().orc_fp8_target(y.size, _ptr(np.ascontiguousarray(y)), float(d_scale), FMT[out_fmt], _ptr(target))
-        e_t = e_y / abs(d_scale) + 2.0 ** -23 * np.abs(target)
+        mult = fp32_reciprocal(d_scale)
+        _load().orc_fp8_target(y.size, _ptr(np.ascontiguousarray(y)), mult, FMT[out_fmt], _ptr(target))
+        e_t = e_y * abs(mult) + 2.0 ** -23 * np.abs(target)
     else:
         target, e_t = y, e_y
     return target, e_t + 2.0 ** -PRECISION[out_fmt] * np.abs(target) + MIN_SUBNORMAL[out_fmt], y, e_y

@@ -362,7 +362,8 @@ int orc_gemm_mx(int64_t M, int64_t N, int64_t K, int64_t blk, int sf_fmt,
  *   RELU(x) = x if x > 0 else 0 (a NaN gives 0),
  *   GELU(x) = x * Phi(x) = 0.5 * x * (1 + erf(x / sqrt 2)), Phi the standard
  *             normal distribution function;
- * an FP8 output holds y / d_scale rounded to nearest even and saturated to
+ * an FP8 output holds y * RN32(1 / d_scale) (the library's documented rule: one
+ * reciprocal rounded to fp32, then a product) rounded to nearest even and saturated to
  * the format's largest finite value (E4M3 448 = 1.75 * 2^8, E5M2 57344 =
  * 1.75 * 2^15); amax = max |y| over the outputs.
  */
@@ -380,15 +381,17 @@ int orc_activate(int64_t n, const double *x, int act, double *y)
     return 0;
 }
 
-/* The unrounded value an FP8 output element targets: y / d_scale, saturated. */
-int orc_fp8_target(int64_t n, const double *y, double d_scale, int fmt, double *out)
+/* The unrounded value an FP8 output element targets: y * mult, saturated, where mult is
+ * the library's documented multiplier 1 / d_scale rounded to fp32 (computed exactly by
+ * the caller). */
+int orc_fp8_target(int64_t n, const double *y, double mult, int fmt, double *out)
 {
     double top;
     if (fmt == ORC_E4M3) top = ldexp(1.75, 8);
     else if (fmt == ORC_E5M2) top = ldexp(1.75, 15);
     else return -1;
     for (int64_t i = 0; i < n; ++i) {
-        const double t = y[i] / d_scale;
+        const double t = y[i] * mult;
         out[i] = t > top ? top : (t < -top ? -top : t); /* a NaN passes through */
     }
     return 0;

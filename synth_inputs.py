@@ -160,6 +160,33 @@ def nvfp4_case(M=8192, N=8192, K=8192, seed=7):
     return dict(A=A, SA=SA, B=B, SB=SB, alpha=float(torch.tensor(ga * gb, dtype=torch.float32)), out_fmt="bf16")
 
 
+FP4_EMAX = 2  # exponent of E2M1's largest finite value (6 = 1.5 * 2^2)
+
+
+def mxfp4_quantize(x: torch.Tensor, block: int = 32):
+    """MXFP4 storage of fp32 ``x`` (rows x K): per ``block`` consecutive K elements one
+    E8M0 scale 2^e with e = floor(log2(amax)) - emax(E2M1) (the OCP MX conversion; an
+    all-zero block gets e = -127), elements E2M1 rounded to nearest (ties to the even
+    code) of x / 2^e, saturated at +-6.  Returns (packed E2M1 rows x K/2, scale codes
+    uint8 rows x K/block)."""
+    rows, K = x.shape
+    xb = x.reshape(rows, K // block, block).to(torch.float32)
+    amax = xb.abs().amax(dim=2)
+    e = torch.floor(torch.log2(torch.where(amax > 0, amax, torch.ones_like(amax)))) - FP4_EMAX
+    e = torch.where(amax > 0, e, torch.full_like(e, -127.0)).clamp(-127, 127)
+    q = fp4_e2m1((xb / torch.exp2(e)[..., None]).reshape(rows, K))
+    return pack_fp4(q), (e + 127).to(torch.uint8)
+
+
+def mxfp4_case(M=8192, N=8192, K=8192, seed=8):
+    g = generator(seed)
+    xa = torch.randn((M, K), generator=g, dtype=torch.float32)
+    xb = torch.randn((N, K), generator=g, dtype=torch.float32)
+    A, SA = mxfp4_quantize(xa)
+    B, SB = mxfp4_quantize(xb)
+    return dict(A=A, SA=SA, B=B, SB=SB, a_fmt="e2m1", b_fmt="e2m1", out_fmt="bf16")
+
+
 def w4a8_case(M=8192, N=8192, K=8192, a_fmt="e4m3", seed=6):
     """FP8 activations A (M x K) times FP4 E2M1 weights B (N x K, packed: N x K/2 bytes)."""
     g = generator(seed)

@@ -417,13 +417,17 @@ def tcm_mx_pack_scales(scales, K: int, packed=None, stream=None):
     return packed
 
 
-def tcm_gemm_mx(A, a_scales, B, b_scales, D, *, C=None, alpha=1.0, beta=0.0, bias=None, stream=None):
-    """Block-scaled FP8 GEMM: A (M x K) and B (N x K) in E4M3/E5M2; a_scales and
+def tcm_gemm_mx(A, a_scales, B, b_scales, D, *, C=None, alpha=1.0, beta=0.0, bias=None, stream=None, fmt=None):
+    """Block-scaled MX GEMM: A (M x K) and B (N x K) in E4M3/E5M2 (MXFP8), or, with
+    fmt="e2m1", packed E2M1 uint8 tensors of K/2 bytes per row (MXFP4); a_scales and
     b_scales the blocked E8M0 arrays of tcm_mx_pack_scales; D (M x N), C of D's
     dtype, bias N elements of D's dtype; all contiguous CUDA tensors."""
-    _mat(A, "A", dtypes=F8_TYPES, contiguous=True)
-    M, K = A.shape
-    _mat(B, "B", None, K, F8_TYPES, contiguous=True)
+    if fmt not in (None, "e2m1"):
+        raise ValueError(f"unknown format {fmt!r}")
+    el = (torch.uint8,) if fmt == "e2m1" else F8_TYPES
+    _mat(A, "A", dtypes=el, contiguous=True)
+    M, K = A.shape[0], A.shape[1] * (2 if fmt == "e2m1" else 1)
+    _mat(B, "B", None, A.shape[1], el, contiguous=True)
     N = B.shape[0]
     _bytes(a_scales, "a_scales", tcm_mx_scales_bytes(M, K))
     _bytes(b_scales, "b_scales", tcm_mx_scales_bytes(N, K))
@@ -432,7 +436,8 @@ def tcm_gemm_mx(A, a_scales, B, b_scales, D, *, C=None, alpha=1.0, beta=0.0, bia
         raise ValueError("C and D must be contiguous")
     _on_device(A=A, a_scales=a_scales, B=B, b_scales=b_scales, D=D, C=C, bias=bias)
     lib = load_library()
-    st = lib.tcm_gemm_mx(M, N, K, _code(A, "A"), _ptr(A), _ptr(a_scales), _code(B, "B"), _ptr(B), _ptr(b_scales),
+    ca, cb = (TCM_E2M1, TCM_E2M1) if fmt == "e2m1" else (_code(A, "A"), _code(B, "B"))
+    st = lib.tcm_gemm_mx(M, N, K, ca, _ptr(A), _ptr(a_scales), cb, _ptr(B), _ptr(b_scales),
                          _ptr(C), _ptr(D), float(alpha), float(beta), _ptr(bias), _code(D, "D"), _stream(stream))
     _check(st, "tcm_gemm_mx")
     return D

@@ -700,22 +700,26 @@ tcm_status tcm_gemm_sp(int64_t M, int64_t N, int64_t K, tcm_dtype dtype, const v
     return sparse_impl(true, M, N, K, dtype, A_comp, meta, B, C, D, alpha, beta, out_dtype, stream);
 }
 
-// Block-scaled GEMM (nv = false: MXFP8, E8M0 per 32, kind::mxf8f6f4; nv = true: NVFP4,
-// packed E2M1 with UE4M3 per 16, kind::mxf4nvf4.scale_vec::4X).
-static tcm_status block_scaled_impl(bool nv, int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const void *A,
+// Block-scaled GEMM: MXFP8 (E4M3/E5M2 elements, E8M0 per 32, kind::mxf8f6f4), NVFP4
+// (packed E2M1, UE4M3 per 16, kind::mxf4nvf4.scale_vec::4X) or MXFP4 (packed E2M1, E8M0
+// per 32, kind::mxf4nvf4.scale_vec::2X).
+enum BlockFmt { BF_MXFP8 = 0, BF_NVFP4 = 1, BF_MXFP4 = 2 };
+
+static tcm_status block_scaled_impl(int bfmt, int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const void *A,
                                     const uint8_t *a_scales, tcm_dtype b_dtype, const void *B, const uint8_t *b_scales,
                                     const void *C, void *D, float alpha, float beta, const void *bias,
                                     tcm_dtype out_dtype, tcm_stream_t stream)
 {
-    if (!nv) {
+    if (bfmt == BF_MXFP8) {
         const bool a8 = a_dtype == TCM_E4M3 || a_dtype == TCM_E5M2;
         const bool b8 = b_dtype == TCM_E4M3 || b_dtype == TCM_E5M2;
         if (!a8 || !b8) return TCM_ERR_UNSUPPORTED;
     }
+    const bool fp4 = bfmt != BF_MXFP8; // packed E2M1 operands, 256 K values per 128-byte stage
     if (out_dtype != TCM_BF16 && out_dtype != TCM_F16 && out_dtype != TCM_F32) return TCM_ERR_UNSUPPORTED;
-    const int64_t k_stage = nv ? 256 : 128;     // K values per 128-byte stage
-    const int64_t k_atom = nv ? 64 : 128;       // K values per scale atom
-    if (M < 1 || N < 1 || K < 0 || K % (nv ? 256 : 32) != 0) return TCM_ERR_INVALID_ARG;
+    const int64_t k_stage = fp4 ? 256 : 128;                  // K values per 128-byte stage
+    const int64_t k_atom = bfmt == BF_NVFP4 ? 64 : 128;       // K values per scale atom
+    if (M < 1 || N < 1 || K < 0 || K % (fp4 ? 256 : 32) != 0) return TCM_ERR_INVALID_ARG;
     if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2) return TCM_ERR_UNSUPPORTED;
     // scale-atom rows (4 of 128 bytes per atom) are addressed with 32-bit coordinates
     if (((M + 255) / 128) * ((K + k_atom - 1) / k_atom) * 4 > INT32_MAX ||
@@ -731,7 +735,7 @@ static tcm_status block_scaled_impl(bool nv, int64_t M, int64_t N, int64_t K, tc
     if (sms <= 0) return TCM_ERR_CUDA;
 
     GemmConfig cfg{};
-    cfg.kind = nv ? 4 : 3;
+    cfg.kind = bfmt == BF_NVFP4 ? 4 : bfmt == BF_MXFP4 ? 6 : 3;
     cfg.cta_group = 1;
     cfg.ksplit = 1;
     cfg.katoms = 1;
@@ -746,7 +750,7 @@ static tcm_status block_scaled_impl(bool nv, int64_t M, int64_t N, int64_t K, tc
     std::memset(&maps, 0, sizeof maps);
     if (K > 0) {
         const uint64_t uK = static_cast<uint64_t>(K);
-        const uint64_t row_bytes = nv ? uK / 2 : uK; // packed E2M1: two values per byte
+        const uint64_t row_bytes = fp4 ? uK / 2 : uK; // packed E2M1: two values per byte
         const uint32_t box_atoms = static_cast<uint32_t>(k_stage / k_atom);
         if (!encode_kmajor(&maps.a, A, 1, row_bytes, static_cast<uint64_t>(M), row_bytes, 128) ||
             !encode_kmajor(&maps.b, B, 1, row_bytes, static_cast<uint64_t>(N), row_bytes,
@@ -783,11 +787,14 @@ static tcm_status block_scaled_impl(bool nv, int64_t M, int64_t N, int64_t K, tc
     // block-scaled instruction descriptor: [7,10) A format, [10,13) B format, [17,23) N >> 3,
     // [23] scale type, [24,29) M >> 4.  kind::mxf8f6f4: E4M3 = 0, E5M2 = 1, scale UE8M0 (1);
     // the per-MMA scale-factor ids ([4,6) B, [29,31) A) are added by the kernel.
-    // kind::mxf4nvf4: E2M1 = 1, scale UE4M3 (0), ids 0 (probed on the GPU).
+    // kind::mxf4nvf4: E2M1 = 1; NVFP4 scale UE4M3 (0), ids 0 (probed on the GPU); MXFP4
+    // scale UE8M0 (1), ids 0 or 2 (scale_vec::2X, added by the kernel).
     const uint32_t dims = ((static_cast<uint32_t>(cfg.bn) >> 3) << 17) |
                           (((128u * static_cast<uint32_t>(cfg.cta_group)) >> 4) << 24);
-    p.idesc = nv ? ((1u << 7) | (1u << 10) | dims)
-                 : (((a_dtype == TCM_E5M2 ? 1u : 0u) << 7) | ((b_dtype == TCM_E5M2 ? 1u : 0u) << 10) | (1u << 23) | dims);
+    if (bfmt == BF_NVFP4) p.idesc = (1u << 7) | (1u << 10) | dims;
+    else if (bfmt == BF_MXFP4) p.idesc = (1u << 7) | (1u << 10) | (1u << 23) | dims;
+    else
+        p.idesc = ((a_dtype == TCM_E5M2 ? 1u : 0u) << 7) | ((b_dtype == TCM_E5M2 ? 1u : 0u) << 10) | (1u << 23) | dims;
     p.timeout_ns = timeout_ns();
     p.status = device_status_ptr();
     if (!p.status) return TCM_ERR_CUDA;
@@ -802,16 +809,18 @@ tcm_status tcm_gemm_mx(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, const
                        tcm_dtype b_dtype, const void *B, const uint8_t *b_scales, const void *C, void *D,
                        float alpha, float beta, const void *bias, tcm_dtype out_dtype, tcm_stream_t stream)
 {
-    return block_scaled_impl(false, M, N, K, a_dtype, A, a_scales, b_dtype, B, b_scales, C, D, alpha, beta, bias,
-                             out_dtype, stream);
+    const bool a4 = a_dtype == TCM_E2M1, b4 = b_dtype == TCM_E2M1;
+    if (a4 != b4) return TCM_ERR_UNSUPPORTED; // E2M1 with E2M1 only (MXFP4)
+    return block_scaled_impl(a4 ? BF_MXFP4 : BF_MXFP8, M, N, K, a_dtype, A, a_scales, b_dtype, B, b_scales, C, D,
+                             alpha, beta, bias, out_dtype, stream);
 }
 
 tcm_status tcm_gemm_nvfp4(int64_t M, int64_t N, int64_t K, const void *A, const uint8_t *a_scales, const void *B,
                           const uint8_t *b_scales, const void *C, void *D, float alpha, float beta, const void *bias,
                           tcm_dtype out_dtype, tcm_stream_t stream)
 {
-    return block_scaled_impl(true, M, N, K, TCM_E2M1, A, a_scales, TCM_E2M1, B, b_scales, C, D, alpha, beta, bias,
-                             out_dtype, stream);
+    return block_scaled_impl(BF_NVFP4, M, N, K, TCM_E2M1, A, a_scales, TCM_E2M1, B, b_scales, C, D, alpha, beta,
+                             bias, out_dtype, stream);
 }
 
 int64_t tcm_mx_scales_bytes(int64_t rows, int64_t K)

@@ -70,11 +70,19 @@ constexpr int SF_ATOM = 512;                       // scales of 128 rows x one 1
 // sparse metadata instead of block scales).
 // SPC: 2:4-sparse A with the canonical metadata of tcm_sp_compress, which the writer
 // warps read from global memory and put into the hardware order themselves.
-enum SideFmt : int { FMT_MX = 0, FMT_NV = 1, FMT_SP = 2, FMT_SPC = 3 };
+// MXF4: MXFP4, packed E2M1 with one E8M0 scale per 32 (kind::mxf4nvf4.scale_vec::2X).
+enum SideFmt : int { FMT_MX = 0, FMT_NV = 1, FMT_SP = 2, FMT_SPC = 3, FMT_MXF4 = 4 };
 __host__ __device__ constexpr bool is_sparse(int fmt) { return fmt == FMT_SP || fmt == FMT_SPC; }
 // Side-data warps per format.  MX, NV: copy warps (lane 0 of each issues the copies e
 // with e % n == its index).  SP, SPC: one writer warp per TMEM lane quadrant (warp % 4).
-__host__ __device__ constexpr int mx_copy_warps(int fmt) { return fmt == FMT_NV ? 3 : is_sparse(fmt) ? 4 : 1; }
+__host__ __device__ constexpr int mx_copy_warps(int fmt)
+{
+    return fmt == FMT_NV ? 3 : is_sparse(fmt) ? 4 : fmt == FMT_MXF4 ? 2 : 1;
+}
+// scale atoms per 128-row tile per stage: MX one (4 blocks of 32 over 128 FP8 values),
+// NVFP4 four (one per K = 64 MMA, blocks of 16), MXFP4 two (4 blocks of 32 each; a stage
+// is 256 packed E2M1 values)
+__host__ __device__ constexpr int mx_atoms_per_tile(int fmt) { return fmt == FMT_NV ? 4 : fmt == FMT_MXF4 ? 2 : 1; }
 constexpr uint32_t SP_META_FILL = 0x44444444u; // positions {0, 1} in every group (rows / words past the matrix)
 // TMA, MMA, epilogue (warps 2..9), copy warps
 __host__ __device__ constexpr int mx_threads(int fmt) { return 32 * (2 + MX_EPI_WARPS + mx_copy_warps(fmt)); }
@@ -84,7 +92,7 @@ template <int BN_CTA, int BN, int STAGES, int FMT>
 struct MxSmem {
     static constexpr int B_STAGE = BN_CTA * TILE_K_BYTES * (is_sparse(FMT) ? 2 : 1); // 128 logical K = 2 atoms
     static constexpr int SF_STAGE = FMT == FMT_SPC ? 0 : FMT == FMT_SP ? SP_META_STAGE
-                                                  : SF_ATOM * (FMT == FMT_NV ? 4 : 1) * (1 + BN / 128);
+                                                  : SF_ATOM * mx_atoms_per_tile(FMT) * (1 + BN / 128);
     static constexpr int A_OFF = 0;
     static constexpr int B_OFF = STAGES * A_STAGE_BYTES;
     static constexpr int SF_OFF = B_OFF + STAGES * B_STAGE;
@@ -215,23 +223,28 @@ __device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64
 // SP: no copies; the stage's 16 columns hold MMA k's metadata word at column 4k,
 // a multiple of 4 as the sparse MMA's metadata address requires, written by the
 // writer warps with tcgen05.st.
+// MXF4: two atoms per tile per stage; MMA k (K = 64, blocks 2k and 2k + 1 of the stage)
+// reads atom k / 2, scale-factor id 2 (k % 2) selecting bytes 2 (k % 2) .. +1 of each
+// row's scale word (scale_vec::2X), the atoms laid out as NVFP4's.
 template <int FMT, int SFB_ATOMS>
 struct SfLayout {
-    static constexpr bool NV = FMT == FMT_NV;
-    static constexpr int APT = NV ? 4 : 1;             // atoms per 128-row tile per stage
+    static constexpr int APT = mx_atoms_per_tile(FMT); // atoms per 128-row tile per stage
+    static constexpr bool MA = APT > 1;                // NVFP4, MXFP4: several atoms per stage
     static constexpr int NCP = is_sparse(FMT) ? 0 : APT * (1 + SFB_ATOMS);  // copies per stage
-    static constexpr uint32_t COLS = NV ? 16u + 16u * SFB_ATOMS : 16u;      // TMEM columns per stage
+    static constexpr uint32_t COLS = MA ? 4u * APT * (1u + SFB_ATOMS) : 16u; // TMEM columns per stage
     // TMEM column (within the stage) of copy e: e = tile * APT + kk, tile 0 = A, 1.. = B row tiles
     __device__ static constexpr uint32_t col(int e)
     {
-        return NV ? (e < APT ? 4u * e : 16u + 4u * SFB_ATOMS * static_cast<uint32_t>((e - APT) % APT) +
+        return MA ? (e < APT ? 4u * e : 4u * APT + 4u * SFB_ATOMS * static_cast<uint32_t>((e - APT) % APT) +
                                              4u * static_cast<uint32_t>((e - APT) / APT))
-                    : (e == 0 ? 0u : 4u + 4u * e);
+                  : (e == 0 ? 0u : 4u + 4u * e);
     }
     // byte offset of copy e's source within the stage's side data
     __device__ static constexpr uint32_t src(int e) { return static_cast<uint32_t>(SF_ATOM) * e; }
-    __device__ static constexpr uint32_t sfa(int k) { return NV ? 4u * k : 0u; }
-    __device__ static constexpr uint32_t sfb(int k) { return NV ? 16u + 4u * SFB_ATOMS * k : 8u; }
+    // atom of the stage that MMA k reads
+    __device__ static constexpr uint32_t atom(int k) { return FMT == FMT_NV ? k : FMT == FMT_MXF4 ? k / 2 : 0; }
+    __device__ static constexpr uint32_t sfa(int k) { return MA ? 4u * atom(k) : 0u; }
+    __device__ static constexpr uint32_t sfb(int k) { return MA ? 4u * APT + 4u * SFB_ATOMS * atom(k) : 8u; }
 };
 
 template <int CG>
@@ -278,6 +291,30 @@ __device__ __forceinline__ uint4 sp_meta_words(const uint32_t *meta, long long q
 #pragma unroll
     for (int k = 0; k < 4; ++k) w[k] = q0 + k < qn ? __ldg(src + k) : SP_META_FILL;
     return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <int CG>
+__device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
+{
+    if constexpr (CG == 2)
+        asm volatile(
+            "{\n"
+            ".reg .pred p;\n"
+            "setp.ne.b32 p, %6, 0;\n"
+            "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n"
+            "}\n" ::"r"(d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+            : "memory");
+    else
+        asm volatile(
+            "{\n"
+            ".reg .pred p;\n"
+            "setp.ne.b32 p, %6, 0;\n"
+            "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n"
+            "}\n" ::"r"(d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+            : "memory");
 }
 
 // One TMA tile load onto this stage's barrier (pair: the even CTA's barrier, cluster address fb).
@@ -495,6 +532,11 @@ __global__ void __launch_bounds__(mx_threads(FMT), 1)
                             mma_sp16<CG>(d_tmem, ad + 2 * k, (k < 2 ? bd : bd1) + 4 * (k & 1), sf + 4u * k, p.idesc, accum);
                         } else if constexpr (FMT == FMT_NV) {
                             mma_nvf4<CG>(d_tmem, ad + 2 * k, bd + 2 * k, p.idesc, sf + SF::sfa(k), sf + SF::sfb(k), accum);
+                        } else if constexpr (FMT == FMT_MXF4) {
+                            // scale-factor id 2 (k % 2): bytes 2 (k % 2) .. +1 of the atom's scale words
+                            const uint32_t id = 2u * static_cast<uint32_t>(k & 1);
+                            const uint32_t idesc = p.idesc | (id << 29) | (id << 4);
+                            mma_mxf4<CG>(d_tmem, ad + 2 * k, bd + 2 * k, idesc, sf + SF::sfa(k), sf + SF::sfb(k), accum);
                         } else {
                             // scale-factor ids: byte k of the stage's scale words (A bits [29,31), B bits [4,6))
                             const uint32_t idesc = p.idesc | (static_cast<uint32_t>(k) << 29) | (static_cast<uint32_t>(k) << 4);
@@ -796,6 +838,13 @@ cudaError_t launch_gemm_mx(const GemmConfig &cfg, const MxMaps &maps, const Gemm
             return cudaErrorInvalidValue;
         }
         if (cfg.bn == 128) return launch_mx_one<128, 4, 2, 1, FMT_SPC>(maps, p, grid, stream);
+        return cudaErrorInvalidValue;
+    }
+    if (cfg.kind == 6) { // MXFP4
+        if (cfg.cta_group == 2) return cfg.bn == 256 ? launch_mx_one<256, 6, 1, 2, FMT_MXF4>(maps, p, grid, stream)
+                                                     : cudaErrorInvalidValue;
+        if (cfg.bn == 256) return launch_mx_one<256, 4, 1, 1, FMT_MXF4>(maps, p, grid, stream);
+        if (cfg.bn == 128) return launch_mx_one<128, 6, 2, 1, FMT_MXF4>(maps, p, grid, stream);
         return cudaErrorInvalidValue;
     }
     if (cfg.kind == 4) { // NVFP4

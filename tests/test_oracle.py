@@ -635,3 +635,61 @@ def test_pack_replicated_atoms_are_copies():
     atoms = four.reshape(-1, 4, 512)
     for c in range(4):
         assert np.array_equal(atoms[:, c, :].reshape(-1), one)
+
+
+# ---- MXFP4: E8M0 block scales per 32 over E2M1 elements
+
+def test_mxfp4_ones_closed_form():
+    """a = b = 1 (E2M1 code 2) everywhere, block scales 2^u, 2^v per 32: D = sum_g 32 * 2^(u + v)."""
+    M, N, K = 5, 6, 256
+    g = np.random.default_rng(19)
+    u = g.integers(-6, 7, (M, K // 32))
+    v = g.integers(-6, 7, (N, K // 32))
+    ones_a = np.full((M, K // 2), 0x22, dtype=np.uint8)
+    ones_b = np.full((N, K // 2), 0x22, dtype=np.uint8)
+    ref, S = oracle.gemm_mx(ones_a, (u + 127).astype(np.uint8), ones_b, (v + 127).astype(np.uint8),
+                            "e2m1", "e2m1", block=32, sf_fmt="e8m0")
+    expect = (32.0 * 2.0 ** (u[:, None, :] + v[None, :, :])).sum(axis=2)
+    assert np.array_equal(ref, expect) and np.array_equal(S, expect)
+
+
+def test_mxfp4_matches_numpy_expansion():
+    c = si.mxfp4_case(40, 24, 256, seed=3)
+    ref, S = oracle.gemm_mx(c["A"].numpy(), c["SA"].numpy(), c["B"].numpy(), c["SB"].numpy(), "e2m1", "e2m1",
+                            block=32, sf_fmt="e8m0")
+    ea = oracle.decode(c["A"].numpy(), "e2m1") * np.repeat(oracle.decode(c["SA"].numpy(), "e8m0"), 32, axis=1)
+    eb = oracle.decode(c["B"].numpy(), "e2m1") * np.repeat(oracle.decode(c["SB"].numpy(), "e8m0"), 32, axis=1)
+    assert np.all(np.abs(ref - ea @ eb.T) <= 1e-12 * np.maximum(S, 1e-300))
+
+
+def test_mxfp4_quantize_scale_rule_worked_by_hand():
+    """OCP MX conversion with emax(E2M1) = 2: block amax 3 -> e = floor(log2 3) - 2 = -1 (code 126),
+    elements x / 2^-1 rounded to E2M1; amax 40 -> e = 3 (code 130), 40 / 8 = 5 -> 4 (ties to even);
+    an all-zero block -> code 0 (2^-127) and zero elements."""
+    x = torch.zeros((1, 96))
+    x[0, 0], x[0, 1], x[0, 2] = 3.0, -0.75, 1.25     # block 0: amax 3
+    x[0, 32], x[0, 33] = 40.0, 7.0                    # block 1: amax 40
+    q, sc = si.mxfp4_quantize(x)
+    assert sc.tolist() == [[126, 130, 0]]
+    vals = oracle.decode(q.numpy(), "e2m1")[0]
+    assert vals[:3].tolist() == [6.0, -1.5, 2.0]      # 3/0.5 = 6; -0.75/0.5 = -1.5; 1.25/0.5 = 2.5 -> 2 (even)
+    assert vals[32:34].tolist() == [4.0, 1.0]         # 40/8 = 5 -> 4 (tie to even), 7/8 = 0.875 -> 1
+    assert not vals[64:].any()
+
+
+def test_fp8_target_multiplies_by_the_rounded_reciprocal():
+    """FP8 outputs hold y * RN32(1 / d_scale): for d_scale = 3 the multiplier is the fp32 value
+    nearest 1/3 (0x3EAAAAAB = 11184811 * 2^-25), so y = 3 targets 3 * that, just above 1."""
+    r = oracle.fp32_reciprocal(3.0)
+    assert r == 11184811 * 2.0 ** -25 and np.float32(r).view(np.uint32) == 0x3EAAAAAB
+    t, *_ = oracle.fused_reference(np.array([3.0, -6.0]), np.zeros(2), None, "e4m3", d_scale=3.0)
+    assert list(t) == [3.0 * r, -6.0 * r] and t[0] > 1.0
+    # exact reciprocals are unchanged; ties between fp32 neighbours cannot occur for 1/d, but
+    # the choice between the neighbours is the nearest one
+    for d in (2.0, 0.25, 448.0, 1e-3, 7.0, 1.0 / 3.0):
+        rr = oracle.fp32_reciprocal(d)
+        c = np.float32(rr)
+        lo, hi = np.nextafter(c, np.float32(0)), np.nextafter(c, np.float32(np.inf))
+        from fractions import Fraction
+        ex = 1 / Fraction(d)
+        assert abs(Fraction(float(c)) - ex) <= min(abs(Fraction(float(lo)) - ex), abs(Fraction(float(hi)) - ex))

@@ -102,3 +102,15 @@ def test_sparse_canonical_starved_stage(tcm, cg, bn):
     B = s["B"].to(d)
     D = torch.empty((512, 512), dtype=torch.bfloat16, device=d)
     starve_then_recover(tcm, lambda: tcm.tcm_gemm_sp(Ac, meta, B, D), D)
+
+
+@pytest.mark.parametrize("cg,bn", [(2, 256), (1, 128)])
+def test_mxfp4_starved_stage(tcm, cg, bn):
+    tcm.tcm_set_config_override(cg, bn, 0, 0, 0)
+    d = dev()
+    c = si.mxfp4_case(512, 512, 1024, seed=94)
+    A, B = c["A"].to(d), c["B"].to(d)
+    SA = tcm.tcm_mx_pack_scales(c["SA"].to(d), 1024)
+    SB = tcm.tcm_mx_pack_scales(c["SB"].to(d), 1024)
+    D = torch.empty((512, 512), dtype=torch.bfloat16, device=d)
+    starve_then_recover(tcm, lambda: tcm.tcm_gemm_mx(A, SA, B, SB, D, fmt="e2m1"), D)
