@@ -101,6 +101,8 @@ def _load():
     lib.orc_sp_compress.argtypes = [i64, i64, i32, vp, i64, vp, vp]
     lib.orc_sp_decompress.restype = i32
     lib.orc_sp_decompress.argtypes = [i64, i64, i32, vp, vp, vp, i64]
+    lib.orc_gemm_i8.restype = i32
+    lib.orc_gemm_i8.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, i64, vp, vp, vp]
     _lib = lib
     return lib
 
@@ -280,6 +282,29 @@ def sp_decompress(Ac, meta, fmt):
     if _load().orc_sp_decompress(M, K, FMT[fmt], _ptr(Ac), _ptr(meta), _ptr(A), K) != 0:
         raise ValueError("orc_sp_decompress rejected its arguments")
     return A
+
+
+def gemm_i8(A, B, C=None, rows=None, cols=None):
+    """Exact integer GEMM with .satfinite (``oracle.c``): int8 A (M x K), int8 B (N x K),
+    optional int32 C (M x N); returns int32 outputs, clamped to the 32-bit range, of every
+    (row, col) -- M x N -- or of the sampled (rows[t], cols[t])."""
+    A = np.ascontiguousarray(A, dtype=np.int8)
+    B = np.ascontiguousarray(B, dtype=np.int8)
+    M, K = A.shape
+    N = B.shape[0]
+    assert B.shape[1] == K
+    Cc = None if C is None else np.ascontiguousarray(C, dtype=np.int32)
+    if rows is None:
+        n, r, c = M * N, None, None
+    else:
+        r = np.ascontiguousarray(rows, dtype=np.int64)
+        c = np.ascontiguousarray(cols, dtype=np.int64)
+        n = r.size
+    out = np.empty(n, dtype=np.int32)
+    if _load().orc_gemm_i8(M, N, K, _ptr(A), K, _ptr(B), K, _ptr(Cc), N if Cc is not None else 0, n,
+                           _ptr(r), _ptr(c), _ptr(out)) != 0:
+        raise ValueError("orc_gemm_i8 rejected its arguments")
+    return out.reshape(M, N) if rows is None else out
 
 
 def activate(x, act):

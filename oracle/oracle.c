@@ -396,3 +396,31 @@ int orc_fp8_target(int64_t n, const double *y, double mult, int fmt, double *out
     }
     return 0;
 }
+
+/*
+ * Integer GEMM, "NVIDIA MMA" page, section "Ampere：FP16/BF16 与整数 MMA 基线": signed
+ * 8-bit A and B, 32-bit integer accumulator and output, .satfinite: the result is
+ * clamped to the 32-bit range instead of wrapping.  Reading where the page is silent:
+ * the exact sum sum_k a_mk b_nk + c_mn is formed first (64-bit, exact for any K below
+ * 2^48) and clamped once at the end.  B is stored N x K (K-major) like the other GEMMs;
+ * C (int32, pitch ldc) may be NULL.  Outputs (i, j) for t in [0, n) of rows[t], cols[t]
+ * (all M x N in row-major order when rows == NULL) go to out[t].
+ */
+int orc_gemm_i8(int64_t M, int64_t N, int64_t K, const int8_t *A, int64_t lda, const int8_t *B, int64_t ldb,
+                const int32_t *C, int64_t ldc, int64_t n, const int64_t *rows, const int64_t *cols, int32_t *out)
+{
+    if (M < 0 || N < 0 || K < 0 || lda < K || ldb < K || (C && ldc < N)) return -1;
+    if (!rows && n != M * N) return -1;
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < n; ++t) {
+        const int64_t i = rows ? rows[t] : t / N;
+        const int64_t j = rows ? cols[t] : t % N;
+        int64_t acc = 0;
+        for (int64_t k = 0; k < K; ++k) acc += (int64_t)A[i * lda + k] * (int64_t)B[j * ldb + k];
+        if (C) acc += C[i * ldc + j];
+        if (acc > INT32_MAX) acc = INT32_MAX;
+        if (acc < INT32_MIN) acc = INT32_MIN;
+        out[t] = (int32_t)acc;
+    }
+    return 0;
+}

@@ -693,3 +693,47 @@ def test_fp8_target_multiplies_by_the_rounded_reciprocal():
         from fractions import Fraction
         ex = 1 / Fraction(d)
         assert abs(Fraction(float(c)) - ex) <= min(abs(Fraction(float(lo)) - ex), abs(Fraction(float(hi)) - ex))
+
+
+# ---- INT8 x INT8 -> INT32 with .satfinite
+
+def test_gemm_i8_brute_force_python_ints():
+    """Every output of a ragged 7 x 5 x 37 case against a Python-integer triple loop, with C."""
+    g = np.random.default_rng(21)
+    A = g.integers(-128, 128, (7, 37), dtype=np.int8)
+    B = g.integers(-128, 128, (5, 37), dtype=np.int8)
+    C = g.integers(-2 ** 31, 2 ** 31, (7, 5), dtype=np.int64).astype(np.int32)
+    got = oracle.gemm_i8(A, B, C)
+    for i in range(7):
+        for j in range(5):
+            exact = sum(int(A[i, k]) * int(B[j, k]) for k in range(37)) + int(C[i, j])
+            assert got[i, j] == max(-2 ** 31, min(2 ** 31 - 1, exact))
+
+
+def test_gemm_i8_matches_numpy_int64_and_samples():
+    g = np.random.default_rng(22)
+    A = g.integers(-128, 128, (64, 300), dtype=np.int8)
+    B = g.integers(-128, 128, (48, 300), dtype=np.int8)
+    ref = A.astype(np.int64) @ B.astype(np.int64).T
+    got = oracle.gemm_i8(A, B)
+    assert np.array_equal(got, ref.astype(np.int32))
+    rows, cols = g.integers(0, 64, 50), g.integers(0, 48, 50)
+    assert np.array_equal(oracle.gemm_i8(A, B, rows=rows, cols=cols), got[rows, cols])
+
+
+def test_gemm_i8_closed_forms_and_saturation():
+    """a = b = -128: each output is 16384 K; at K = 131072 that is 2^31, clamped to 2^31 - 1.
+    a = -128, b = 127: -16256 K; with C = -2^31 the sum clamps to -2^31.  Identity A picks rows of B."""
+    K = 1024
+    A = np.full((2, K), -128, dtype=np.int8)
+    assert np.all(oracle.gemm_i8(A, A[:1]) == 16384 * K)
+    K = 131072
+    A = np.full((1, K), -128, dtype=np.int8)
+    assert oracle.gemm_i8(A, A)[0, 0] == 2 ** 31 - 1
+    B = np.full((1, 8), 127, dtype=np.int8)
+    C = np.array([[-2 ** 31]], dtype=np.int32)
+    assert oracle.gemm_i8(np.full((1, 8), -128, dtype=np.int8), B, C)[0, 0] == -2 ** 31
+    assert oracle.gemm_i8(np.full((1, 8), -128, dtype=np.int8), B)[0, 0] == -16256 * 8
+    I = np.eye(16, dtype=np.int8)
+    Bm = np.random.default_rng(23).integers(-128, 128, (16, 16), dtype=np.int8)
+    assert np.array_equal(oracle.gemm_i8(I, Bm), Bm.T.astype(np.int32))
