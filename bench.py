@@ -531,6 +531,8 @@ class Workload:
         out_dtype = torch.float32 if case.get("out_fmt") == "f32" else torch.bfloat16
         if case.get("fused"):
             out_dtype = torch.float8_e4m3fn
+        if case.get("i8"):
+            out_dtype = torch.int32
         D = torch.empty((M, N), dtype=out_dtype, device=device)
         C = case["C"].to(device) if case.get("C") is not None else None
         kw = dict(C=C, alpha=case.get("alpha", 1.0), beta=case.get("beta", 0.0), stream=stream)
@@ -542,7 +544,13 @@ class Workload:
                 kw.update(bias=case["bias"].to(device))
         if case.get("b_fmt") == "e2m1" and case.get("a_fmt") != "e2m1":
             kw.update(b_fmt="e2m1")  # W4A8: B holds N x K/2 bytes of packed FP4
-        if sparse:
+        if case.get("i8"):
+            # exact INT8 on the bf16 tensor path: 2MNK integer ops against the bf16 rate, the
+            # int8 -> bf16 conversion of A and B included
+            self.workspace_bytes = tcm.tcm_gemm_i8_workspace_bytes(M, N, K)
+            ws = torch.empty(self.workspace_bytes, dtype=torch.uint8, device=device)
+            self.launch = lambda: tcm.tcm_gemm_i8(A, B, D, workspace=ws, stream=stream)
+        elif sparse:
             self.peak_mult = 2.0  # logical FLOPs against the 2:4 rate
             Ac, meta = tcm.tcm_sp_compress(A)
             if case.get("tc"):
@@ -601,6 +609,7 @@ def part_cases():
         ("f1_mxfp4_8192", lambda: si.mxfp4_case(), "tensor"),
         ("f2_fused_e4m3_gelu_e4m3out_amax_8192", lambda: dict(si.fp8_case(b_fmt="e4m3"), fused="gelu"), "tensor"),
         ("f3_w4a8_e4m3xe2m1_8192", lambda: si.w4a8_case(), "tensor"),
+        ("f4_int8_exact_bf16path_8192", lambda: si.int8_case(), "tensor"),
     ]
 
 
@@ -675,6 +684,7 @@ def shape_cases():
         ("nvfp4 e2m1 8192^3 (UE4M3 scales per 16, per-tensor scales in alpha)", lambda: dict(si.nvfp4_case(), nv=True)),
         ("mxfp4 e2m1 8192^3 (E8M0 scales per 32)", lambda: si.mxfp4_case()),
         ("w4a8 fp8 e4m3 x fp4 e2m1 8192^3 +scales", lambda: si.w4a8_case()),
+        ("int8 exact (bf16 tensor path, int32 out, conversions included) 8192^3", lambda: si.int8_case()),
         ("fused fp8 e4m3 8192^3 +scales+bias -> GELU -> e4m3 out (d_scale 2) + amax",
          lambda: dict(si.fp8_case(b_fmt="e4m3"), fused="gelu")),
     ]

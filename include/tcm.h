@@ -406,6 +406,35 @@ tcm_status tcm_nvfp4_pack_scales(int64_t rows, int64_t K, const uint8_t *scales,
                                  tcm_stream_t stream);
 
 /*
+ * tcm_gemm_i8 -- D = satfinite_int32(A . B + C) for signed 8-bit A and B, exact.
+ *
+ * "NVIDIA MMA", section "SM100：tcgen05.mma" lists kind::i8 (8-bit integer operands,
+ * 32-bit integer accumulator) and section "Ampere：FP16/BF16 与整数 MMA 基线" the
+ * integer semantics (.satfinite: the result clamped to the int32 range instead of
+ * wrapping).  ptxas does not accept kind::i8 for sm_103a, so this runs on the bf16
+ * tensor path with the same results: int8 values are exact in bf16, and every 1024-long
+ * K chunk is accumulated in fp32 on its own (its partial sums are integers below 2^24,
+ * exact), converted to int32 and added; + C saturates.
+ *  M, N >= 1; 0 <= K <= 131071 (else TCM_ERR_UNSUPPORTED: the int32 sums of A . B
+ *              alone then cannot overflow).
+ *  A           M x K int8, row pitch lda bytes (>= K, any alignment).
+ *  B           N x K int8 (the K x N operand stored K-major), pitch ldb bytes (>= K).
+ *  C           M x N int32, pitch ldc elements (multiple of 4, base 16-byte aligned), or NULL.
+ *  D           M x N int32, pitch ldd elements (multiple of 4, base 16-byte aligned).
+ *  workspace   DEVICE memory, 16-byte aligned, at least tcm_gemm_i8_workspace_bytes(M, N, K)
+ *              bytes (the bf16 copies of A and B, rows of K rounded up to 64); scratch.
+ * Three launches on `stream`: the two conversions and the GEMM (256 x 256 CTA-pair tiles).
+ *
+ * tcm_gemm_i8_workspace_bytes -- (M + N) * ceil(K / 64) * 64 * 2; -1 if the sizes are
+ * rejected.  Host only.
+ */
+int64_t tcm_gemm_i8_workspace_bytes(int64_t M, int64_t N, int64_t K);
+tcm_status tcm_gemm_i8(int64_t M, int64_t N, int64_t K, const int8_t *A, int64_t lda,
+                       const int8_t *B, int64_t ldb, const int32_t *C, int64_t ldc,
+                       int32_t *D, int64_t ldd, void *workspace, int64_t workspace_bytes,
+                       tcm_stream_t stream);
+
+/*
  * tcm_get_device_status -- synchronise `stream`, then report the first
  * device-side failure recorded since the last tcm_clear_device_status():
  * *code = TCM_OK or TCM_ERR_TIMEOUT, *site = which pipeline wait gave up

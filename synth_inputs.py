@@ -197,6 +197,14 @@ def w4a8_case(M=8192, N=8192, K=8192, a_fmt="e4m3", seed=6):
     return dict(A=A, B=B, sa=sa, sb=sb, a_fmt=a_fmt, b_fmt="e2m1", out_fmt="bf16")
 
 
+def int8_case(M=8192, N=8192, K=8192, seed=10):
+    """Signed 8-bit A (M x K) and B (N x K), uniform over the full range -128 .. 127."""
+    g = generator(seed)
+    A = torch.randint(-128, 128, (M, K), generator=g, dtype=torch.int8)
+    B = torch.randint(-128, 128, (N, K), generator=g, dtype=torch.int8)
+    return dict(A=A, B=B, i8=True, out_fmt="i32")
+
+
 def small_case(M=512, N=512, K=512, seed=0):
     g = generator(seed)
     A = uniform((M, K), g)

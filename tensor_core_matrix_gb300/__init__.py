@@ -34,7 +34,8 @@ EXPORTS = ("tcm_gemm", "tcm_gemm_ex", "tcm_gemm_fused", "tcm_sp_compress", "tcm_
            "tcm_nvfp4_pack_scales",
            "tcm_get_device_status", "tcm_clear_device_status", "tcm_set_timeout_ns",
            "tcm_status_string", "tcm_version", "tcm_set_config_override", "tcm_debug_fail_next_launch",
-           "tcm_set_clock_probe", "tcm_gemm_ex_ws", "tcm_gemm_workspace_bytes", "tcm_gemm_ex_builtin_ws")
+           "tcm_set_clock_probe", "tcm_gemm_ex_ws", "tcm_gemm_workspace_bytes", "tcm_gemm_ex_builtin_ws",
+           "tcm_gemm_i8", "tcm_gemm_i8_workspace_bytes")
 
 
 class TcmError(RuntimeError):
@@ -67,6 +68,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.tcm_gemm_ex_builtin_ws.restype = i32
     lib.tcm_gemm_ex_builtin_ws.argtypes = [i64, i64, i64, i32, vp, i64, i32, vp, i64, vp, i64, vp, i64,
                                            i32, f32, f32, vp, vp, vp, vp]
+    lib.tcm_gemm_i8.restype = i32
+    lib.tcm_gemm_i8.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, vp]
+    lib.tcm_gemm_i8_workspace_bytes.restype = i64
+    lib.tcm_gemm_i8_workspace_bytes.argtypes = [i64, i64, i64]
     lib.tcm_gemm_workspace_bytes.restype = i64
     lib.tcm_gemm_workspace_bytes.argtypes = [i64, i64, i64, i32, i32]
     lib.tcm_gemm_fused.restype = i32
@@ -327,6 +332,38 @@ def tcm_gemm(A, B, D, *, C=None, alpha=1.0, beta=0.0, stream=None):
     st = lib.tcm_gemm(M, N, K, _code(A, "A"), _ptr(A), _ptr(B), _ptr(C), _ptr(D), float(alpha),
                       float(beta), _code(D, "D"), _stream(stream))
     _check(st, "tcm_gemm")
+    return D
+
+
+def tcm_gemm_i8_workspace_bytes(M: int, N: int, K: int) -> int:
+    """Workspace bytes of tcm_gemm_i8 (the bf16 copies of A and B); -1 if the sizes are rejected."""
+    return int(load_library().tcm_gemm_i8_workspace_bytes(int(M), int(N), int(K)))
+
+
+def tcm_gemm_i8(A, B, D, *, C=None, workspace=None, stream=None):
+    """D = satfinite_int32(A @ B_stored.T + C), exact: A int8 (M x K), B int8 (N x K), C and D
+    int32 (M x N).  workspace: a contiguous uint8 CUDA tensor of tcm_gemm_i8_workspace_bytes
+    bytes, allocated here if None."""
+    _mat(A, "A", dtypes=(torch.int8,))
+    M, K = A.shape
+    _mat(B, "B", None, K, (torch.int8,))
+    N = B.shape[0]
+    _mat(D, "D", M, N, (torch.int32,))
+    if C is not None:
+        _mat(C, "C", M, N, (torch.int32,))
+    nbytes = tcm_gemm_i8_workspace_bytes(M, N, K)
+    if nbytes < 0:
+        raise ValueError(f"unsupported sizes {M} x {N} x {K}")
+    if workspace is not None:
+        _bytes(workspace, "workspace", nbytes)
+    _on_device(A=A, B=B, D=D, C=C, workspace=workspace)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=A.device)
+    lib = load_library()
+    st = lib.tcm_gemm_i8(M, N, K, _ptr(A), A.stride(0), _ptr(B), B.stride(0), _ptr(C),
+                         C.stride(0) if C is not None else 0, _ptr(D), D.stride(0), _ptr(workspace),
+                         workspace.numel(), _stream(stream))
+    _check(st, "tcm_gemm_i8")
     return D
 
 

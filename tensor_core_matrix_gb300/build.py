@@ -18,7 +18,8 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libtcm.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
-SOURCES = ["tcm_api.cu", "tcm_gemm.cu", "tcm_gemm_pair.cu", "tcm_gemm_ksplit.cu", "tcm_gemm_mx.cu", "tcm_sparse.cu"]
+SOURCES = ["tcm_api.cu", "tcm_gemm.cu", "tcm_gemm_pair.cu", "tcm_gemm_ksplit.cu", "tcm_gemm_mx.cu", "tcm_sparse.cu",
+           "tcm_gemm_i8.cu"]
 GENCODE = "arch=compute_103a,code=sm_103a"
 
 

@@ -862,6 +862,74 @@ tcm_status tcm_nvfp4_pack_scales(int64_t rows, int64_t K, const uint8_t *scales,
                : TCM_ERR_CUDA;
 }
 
+// INT8: K rounded up to whole 64-element K blocks in the bf16 copies
+static int64_t i8_pitch(int64_t K) { return (K + 63) / 64 * 64; }
+
+int64_t tcm_gemm_i8_workspace_bytes(int64_t M, int64_t N, int64_t K)
+{
+    if (M < 1 || N < 1 || K < 0 || K > 131071) return -1;
+    return (M + N) * i8_pitch(K) * 2;
+}
+
+tcm_status tcm_gemm_i8(int64_t M, int64_t N, int64_t K, const int8_t *A, int64_t lda, const int8_t *B, int64_t ldb,
+                       const int32_t *C, int64_t ldc, int32_t *D, int64_t ldd, void *workspace, int64_t workspace_bytes,
+                       tcm_stream_t stream)
+{
+    if (M < 1 || N < 1 || K < 0) return TCM_ERR_INVALID_ARG;
+    if (K > 131071 || M > INT32_MAX / 2 || N > INT32_MAX / 2) return TCM_ERR_UNSUPPORTED;
+    if (!D || (K > 0 && (!A || !B || !workspace)) || lda < K || ldb < K || ldd < N || (C && ldc < N))
+        return TCM_ERR_INVALID_ARG;
+    if (!aligned16(D) || ldd % 4 || (C && (!aligned16(C) || ldc % 4)) || (workspace && !aligned16(workspace)))
+        return TCM_ERR_MISALIGNED;
+    const int64_t kp = i8_pitch(K);
+    if (K > 0 && workspace_bytes < (M + N) * kp * 2) return TCM_ERR_INVALID_ARG;
+    const int64_t sms = sm_count();
+    if (sms <= 0) return TCM_ERR_CUDA;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t *wa = static_cast<uint8_t *>(workspace);
+    uint8_t *wb = wa ? wa + M * kp * 2 : nullptr;
+
+    CUtensorMap tmA, tmB;
+    std::memset(&tmA, 0, sizeof tmA);
+    std::memset(&tmB, 0, sizeof tmB);
+    if (K > 0) {
+        if (!encode_kmajor(&tmA, wa, 2, static_cast<uint64_t>(kp), static_cast<uint64_t>(M), static_cast<uint64_t>(kp),
+                           128) ||
+            !encode_kmajor(&tmB, wb, 2, static_cast<uint64_t>(kp), static_cast<uint64_t>(N), static_cast<uint64_t>(kp),
+                           128))
+            return TCM_ERR_CUDA;
+    }
+    GemmParams p{};
+    p.kM = static_cast<int>(M);
+    p.kN = static_cast<int>(N);
+    p.K = static_cast<int>(K);
+    p.num_kb = static_cast<int>(kp / 64);
+    p.tiles_m = static_cast<int>((M + 255) / 256);
+    p.tiles_n = static_cast<int>((N + 255) / 256);
+    p.num_tiles = p.tiles_m * p.tiles_n;
+    p.group_m = g_force_group_m.load() > 0 ? g_force_group_m.load() : 16;
+    p.split = 1;
+    p.split_begin = p.num_tiles;
+    p.tile_begin = 0;
+    p.tile_end = p.num_tiles;
+    p.D = D;
+    p.ldd = ldd;
+    p.C = C;
+    p.ldc = ldc;
+    p.idesc = make_idesc(1u, 1u, 256u, 256u); // bf16 x bf16, M = 256 (CTA pair), N = 256
+    p.clock_probe = g_clock_probe.load();
+    p.timeout_ns = timeout_ns();
+    p.status = device_status_ptr();
+    if (!p.status) return TCM_ERR_CUDA;
+    p.fault_inject = g_fault_once.exchange(0);
+    if (K > 0 && (launch_i8_to_bf16(A, M, K, lda, wa, kp, st) != cudaSuccess ||
+                  launch_i8_to_bf16(B, N, K, ldb, wb, kp, st) != cudaSuccess))
+        return TCM_ERR_CUDA;
+    const int64_t clusters = sms / 2;
+    const int grid = static_cast<int>((p.num_tiles < clusters ? p.num_tiles : clusters) * 2);
+    return launch_gemm_i8(tmA, tmB, p, grid, st) == cudaSuccess ? TCM_OK : TCM_ERR_CUDA;
+}
+
 tcm_status tcm_get_device_status(tcm_stream_t stream, int32_t *code, int32_t *site)
 {
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return TCM_ERR_CUDA;

@@ -114,6 +114,12 @@ cudaError_t launch_sp_compress(int64_t M, int64_t K, int elem_bytes, const void 
 cudaError_t launch_sp_decompress(int64_t M, int64_t K, int elem_bytes, const void *Ac, const uint32_t *meta, void *A,
                                  int64_t lda, cudaStream_t stream);
 
+// INT8 GEMM on the bf16 tensor path: int8 -> bf16 rows (zero-padded to ldo), then the chunked pair kernel
+cudaError_t launch_i8_to_bf16(const int8_t *src, int64_t rows, int64_t K, int64_t lds, void *dst, int64_t ldo,
+                              cudaStream_t stream);
+cudaError_t launch_gemm_i8(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmParams &p, int grid,
+                           cudaStream_t stream);
+
 int *device_status_ptr(); // address of this device's status words (per current device)
 
 // Raise a kernel's dynamic shared-memory limit once per device instead of on every
