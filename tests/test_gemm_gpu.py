@@ -94,8 +94,7 @@ def override():
     tcm.tcm_set_config_override(0, 0, 0, 0, 0)
 
 
-@pytest.mark.parametrize("cg,bn,stages", [(1, 256, 0), (1, 128, 0), (1, 64, 0), (1, 32, 0), (2, 256, 0),
-                                          (2, 256, 7)])
+@pytest.mark.parametrize("cg,bn,stages", [(1, 256, 0), (1, 128, 0), (1, 64, 0), (1, 32, 0), (2, 256, 0)])
 @pytest.mark.parametrize("M,N,K", [(256, 256, 64), (512, 768, 320), (300, 520, 136), (1000, 1030, 1024)])
 def test_each_variant_integer_exact(override, cg, bn, stages, M, N, K):
     override.tcm_set_config_override(cg, bn, stages, 3)
@@ -107,7 +106,7 @@ def test_each_variant_integer_exact(override, cg, bn, stages, M, N, K):
     assert np.array_equal(D.double().numpy(), ref)
 
 
-@pytest.mark.parametrize("cg,bn,stages", [(1, 256, 0), (2, 256, 0), (2, 256, 7), (1, 128, 0)])
+@pytest.mark.parametrize("cg,bn,stages", [(1, 256, 0), (2, 256, 0), (1, 128, 0), (1, 64, 0), (1, 32, 0)])
 @pytest.mark.parametrize("fb", ["e4m3", "e5m2"])
 def test_each_variant_fp8_bound(override, cg, bn, stages, fb):
     override.tcm_set_config_override(cg, bn, stages)
