@@ -76,6 +76,10 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-parts", action="store_true", help="skip the per-config parts")
+    ap.add_argument("--no-workspace", action="store_true",
+                    help="dense GEMMs of the step through tcm_gemm_ex without a workspace (no split tail): "
+                         "the same kernels in a non-cooperative launch, for profilers that cannot replay "
+                         "cooperative launches")
     ap.add_argument("--part-iters", type=int, default=20)
     ap.add_argument("--shapes", action="store_true",
                     help="instead of the step, time every configured workload shape (one JSON line each)")
@@ -311,8 +315,9 @@ def step_host_inputs():
     }
 
 
-def make_inputs(device):
-    """Resident device inputs of one step plus their pinned host copies (for the end-to-end leg)."""
+def make_inputs(device, workspace=True):
+    """Resident device inputs of one step plus their pinned host copies (for the end-to-end leg);
+    workspace=False: the dense GEMMs run without one (dev["ws"] is None)."""
     host = step_host_inputs()
     pinned = {k: v.pin_memory() for k, v in host.items()}
     dev = {k: v.to(device) for k, v in host.items()}
@@ -324,7 +329,7 @@ def make_inputs(device):
     import tensor_core_matrix_gb300 as tcm
     ws = max(tcm.tcm_gemm_workspace_bytes(SIZE, SIZE, SIZE, torch.bfloat16),
              tcm.tcm_gemm_workspace_bytes(SIZE, SIZE, SIZE, torch.float8_e4m3fn))
-    dev["ws"] = torch.empty(max(ws, 16), dtype=torch.uint8, device=device)
+    dev["ws"] = torch.empty(max(ws, 16), dtype=torch.uint8, device=device) if workspace else None
     return host, pinned, dev
 
 
@@ -730,11 +735,12 @@ def run_shapes(args, tcm, device, peaks_used):
         del w
 
 
-def config_block(world):
+def config_block(world, workspace=True):
+    route = ("both through tcm_gemm_ex_ws: the last round's tiles split over K" if workspace
+             else "both through tcm_gemm_ex without a workspace: no split tail")
     return {"workload": "GEMM 8192^3 (M=N=K=8192): bf16 x bf16 -> bf16; E4M3 x E4M3 with per-tensor "
-                        "scales + bf16 bias -> bf16 (both through tcm_gemm_ex_ws: the last round's tiles split "
-                        "over K); 2:4-sparse bf16 A (compress + sparse GEMM on canonical metadata) -> bf16; "
-                        "A row-major, B K-major, fp32 accumulate",
+                        f"scales + bf16 bias -> bf16 ({route}); 2:4-sparse bf16 A (compress + sparse GEMM on "
+                        "canonical metadata) -> bf16; A row-major, B K-major, fp32 accumulate",
             "M": SIZE, "N": SIZE, "K": SIZE,
             "value_counts": "2*M*N*K of the bf16 and E4M3 GEMMs per step (the sparse GEMM runs in the step; "
                             "its logical FLOPs are reported in parts.sp24_gemm_bf16 only)",
@@ -778,7 +784,7 @@ def main():
     local_cpus = gpu_local_cpus(local_rank_index(device))
     if local_cpus:
         os.sched_setaffinity(0, local_cpus)
-    host, pinned, dev = make_inputs(device)
+    host, pinned, dev = make_inputs(device, workspace=not args.no_workspace)
     # the end-to-end results' pinned buffers (two sets), first-touched here as well
     outs = [{k: torch.empty((SIZE, SIZE), dtype=torch.bfloat16).pin_memory() for k in ("D", "D8", "Dsp")}
             for _ in range(2)] if args.e2e_steps > 0 else None
@@ -913,7 +919,8 @@ def main():
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16+e4m3", "data": "synthetic", "config": config_block(world),
+            "vs_baseline": None, "dtype": "bf16+e4m3", "data": "synthetic",
+            "config": config_block(world, not args.no_workspace),
             "parts": {
                 "bf16_dense": {"tflops": ach_bf16, "ms": t_bf16, "frac_of_bf16_peak": ach_bf16 / bf16_peak},
                 "e4m3_scaled_bias": {"tflops": ach_fp8, "ms": t_fp8, "frac_of_fp8_peak": ach_fp8 / fp8_peak},
