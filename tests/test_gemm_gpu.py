@@ -146,7 +146,7 @@ def test_pair_tail_k_split_with_epilogue(override, in_fmt):
         A, B = si.normal((M, K), g), si.normal((N, K), g)
         kw = dict(bias=si.normal((N,), g))
     C = si.normal((M, N), g)
-    override.tcm_set_config_override(0, 0, 0, 0, 0, 2)  # split the 28 tail tiles whatever K
+    override.tcm_set_config_override(2, 256, 0, 0, 0, 2)  # 256-column pair tiles, 28 tail tiles split
     out = [run_gemm_ex(A, B, torch.bfloat16, C=C, alpha=0.5, beta=0.25, workspace=ws, **kw) for ws in (False, True)]
     rows, cols = sample_indices(M, N, per_tile=2)
     ref, S = oracle_ref(A, B, C=C, alpha=0.5, beta=0.25, rows=rows, cols=cols, **kw)
@@ -187,7 +187,7 @@ def test_tail_k_split_wait_times_out_and_context_stays_usable(override):
     A = si.integers((M, K), g)
     B = si.integers((N, K), g)
     Ad, Bd = A.to(d), B.to(d)
-    tcm.tcm_set_config_override(0, 0, 0, 0, 0, 2)  # split the 8 tail tiles whatever K
+    tcm.tcm_set_config_override(2, 256, 0, 0, 0, 2)  # 256-column pair tiles, 8 tail tiles split
     ws = torch.empty(tcm.tcm_gemm_workspace_bytes(M, N, K, torch.bfloat16), dtype=torch.uint8, device=d)
     assert ws.numel() > 0
     D = torch.zeros((M, N), dtype=torch.float32, device=d)

@@ -81,7 +81,7 @@ def test_builtin_workspace_integer_exact_twice(lib):
     """Integer inputs (exact sums) on a shape with 8 split tiles, forced split: bit-exact with the
     oracle on every output, twice in a row."""
     import tensor_core_matrix_gb300 as tcm
-    tcm.tcm_set_config_override(0, 0, 0, 0, 0, 2)
+    tcm.tcm_set_config_override(2, 256, 0, 0, 0, 2)  # 256-column pair tiles: 8 tail tiles split
     try:
         d = dev()
         M, N, K = 4096, 2560, 512
