@@ -60,8 +60,11 @@ FP8_OVER_BF16 = 4.5 / 2.25  # nominal dense ratio
 BF16_FLOP_PER_CLK_PER_SM = 8192
 L2_BYTES = 129 * 10 ** 6
 SUSTAINED_AFTER_S = 1.0  # timed regions at least this long are compared with the sustained peak
+# the bf16 kernel and the host code that plans its launch (tile order, split): the recorded
+# DRAM traffic holds only while none of them changed
 KERNEL_SOURCES = ["tensor_core_matrix_gb300/csrc/tcm_gemm_kernel.cuh", "tensor_core_matrix_gb300/csrc/tcm_kernel_common.cuh",
-                  "tensor_core_matrix_gb300/csrc/tcm_ptx.cuh", "tensor_core_matrix_gb300/csrc/tcm_gemm_pair.cu"]
+                  "tensor_core_matrix_gb300/csrc/tcm_ptx.cuh", "tensor_core_matrix_gb300/csrc/tcm_gemm_pair.cu",
+                  "tensor_core_matrix_gb300/csrc/tcm_api.cu"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_kernel_bf16_8192cubed.json")
 SLEEP_CYCLES = 400_000  # ~0.2 ms: lets the host enqueue a launch before its start event
 

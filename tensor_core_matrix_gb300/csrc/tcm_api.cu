@@ -379,7 +379,9 @@ static tcm_status gemm_impl(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, 
     p.tiles_m = static_cast<int>(plan.tiles_m);
     p.tiles_n = static_cast<int>(plan.tiles_n);
     p.num_tiles = static_cast<int>(plan.num_tiles);
-    p.group_m = g_force_group_m.load() > 0 ? g_force_group_m.load() : 16;
+    // raster groups: 8 row blocks for 16-bit operands (bf16 8192^3: 11 % fewer DRAM bytes and
+    // ~1 % faster than 16), 16 for 8-bit ones (E4M3 8192^3: 1.6 % faster than 8)
+    p.group_m = g_force_group_m.load() > 0 ? g_force_group_m.load() : (kind == 0 ? 8 : 16);
     p.split = plan.split;
     p.split_begin = static_cast<int>(plan.split_begin);
     if (plan.split > 1) {
