@@ -144,12 +144,15 @@ __global__ void __launch_bounds__(I8_THREADS, 1)
                         ok = false;
                         break;
                     }
-                    const uint32_t sa = sbase + L::A_OFF + stage * L::A_STAGE;
-                    const uint32_t sb = sbase + L::B_OFF + stage * L::B_STAGE;
-                    if (leader) mbar_arrive_expect_tx(full + stage, STAGE_TX);
-                    const uint32_t fb = full_cluster0 + static_cast<uint32_t>(stage) * 8u;
-                    tma_load_2d_pair(sa, &tmA, fb, kb * 64, a_row);
-                    tma_load_2d_pair(sb, &tmB, fb, kb * 64, b_row);
+                    // test hook: the launch's first stage is never loaded (its waits time out)
+                    if (!(p.fault_inject & FAULT_SKIP_FIRST_LOAD) || issued != 0) {
+                        const uint32_t sa = sbase + L::A_OFF + stage * L::A_STAGE;
+                        const uint32_t sb = sbase + L::B_OFF + stage * L::B_STAGE;
+                        if (leader) mbar_arrive_expect_tx(full + stage, STAGE_TX);
+                        const uint32_t fb = full_cluster0 + static_cast<uint32_t>(stage) * 8u;
+                        tma_load_2d_pair(sa, &tmA, fb, kb * 64, a_row);
+                        tma_load_2d_pair(sb, &tmB, fb, kb * 64, b_row);
+                    }
                     ++issued;
                     if (++stage == STAGES) {
                         stage = 0;

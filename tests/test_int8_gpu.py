@@ -91,3 +91,49 @@ def test_int8_k0_gives_c_and_limits(tcm):
     with pytest.raises(ValueError, match="workspace holds"):
         tcm.tcm_gemm_i8(A, A, torch.empty((128, 128), dtype=torch.int32, device=d),
                         workspace=torch.empty(1024, dtype=torch.uint8, device=d))
+
+
+def test_int8_odd_pitches_and_unaligned_bases(tcm):
+    """A and B may have any row pitch and start at any byte (the conversion reads single bytes):
+    A at a 3-byte offset with pitch K + 13, B at a 1-byte offset with pitch K + 5, K = 777
+    (not a multiple of 8 or 64), ragged M and N; C and D padded to 16-byte pitches."""
+    d = dev()
+    M, N, K = 300, 260, 777
+    g = si.generator(12)
+    A = torch.randint(-128, 128, (M, K), generator=g, dtype=torch.int8)
+    B = torch.randint(-128, 128, (N, K), generator=g, dtype=torch.int8)
+    C = torch.randint(-2 ** 31, 2 ** 31 - 1, (M, N), generator=g, dtype=torch.int64).to(torch.int32)
+    buf_a = torch.zeros((M, K + 13), dtype=torch.int8, device=d)
+    buf_a[:, 3:3 + K] = A.to(d)
+    buf_b = torch.zeros((N, K + 5), dtype=torch.int8, device=d)
+    buf_b[:, 1:1 + K] = B.to(d)
+    D = padded(torch.full((M, N), -7, dtype=torch.int32), d)
+    tcm.tcm_gemm_i8(buf_a[:, 3:3 + K], buf_b[:, 1:1 + K], D, C=padded(C, d))
+    code, site = tcm.tcm_get_device_status()
+    assert code == 0, (code, site)
+    assert np.array_equal(D.cpu().numpy(), oracle.gemm_i8(A.numpy(), B.numpy(), C.numpy()))
+
+
+def test_int8_starved_stage_times_out_and_context_stays_usable(tcm):
+    """The first stage is never loaded (test hook): a bounded wait gives up (MMA issuer, site 2, or
+    epilogue, site 4), the status says so, the kernel returns, and the next launch is exact."""
+    d = dev()
+    M, N, K = 512, 512, 2048
+    g = si.generator(13)
+    A = torch.randint(-128, 128, (M, K), generator=g, dtype=torch.int8)
+    B = torch.randint(-128, 128, (N, K), generator=g, dtype=torch.int8)
+    Ad, Bd = A.to(d), B.to(d)
+    D = torch.zeros((M, N), dtype=torch.int32, device=d)
+    tcm.tcm_clear_device_status()
+    tcm.tcm_set_timeout_ns(50_000_000)
+    try:
+        tcm.tcm_debug_fail_next_launch(1)
+        tcm.tcm_gemm_i8(Ad, Bd, D)
+        code, site = tcm.tcm_get_device_status()
+        assert code == 5 and site in (2, 4)
+    finally:
+        tcm.tcm_set_timeout_ns(0)
+        tcm.tcm_clear_device_status()
+    tcm.tcm_gemm_i8(Ad, Bd, D)
+    assert tcm.tcm_get_device_status() == (0, 0)
+    assert np.array_equal(D.cpu().numpy(), oracle.gemm_i8(A.numpy(), B.numpy()))
