@@ -131,9 +131,11 @@ tcm_status tcm_gemm_ex(int64_t M, int64_t N, int64_t K,
  * 256 x 256 output tiles in rounds; when the last round is only partly filled
  * (e.g. 8192^3: 1024 tiles = 13 rounds of 76 pairs + 36 tiles) and at most half
  * full, and K is long enough for it to pay (at least 64 K blocks of 128 bytes),
- * each of its tiles is split into two halves along K, computed by two pairs
- * at once: the second half stores its fp32 partial sums in the workspace and the
- * first adds them before the epilogue.  Same results as tcm_gemm_ex up to the
+ * each of its tiles is split into two parts along K, computed by two pairs
+ * at once: the second part stores its fp32 partial sums in the workspace and the
+ * first adds them before the epilogue.  The first part takes a few K blocks more
+ * than half (9 when K allows), so that the second part's sums are published by the
+ * time the first part's own products are done.  Same results as tcm_gemm_ex up to the
  * order of the fp32 accumulation (integer-valued sums stay exact).
  *  workspace        DEVICE memory, 16-byte aligned, caller-owned, at least
  *                   tcm_gemm_workspace_bytes(M, N, K, a_dtype, b_dtype) bytes
@@ -473,7 +475,7 @@ void tcm_set_timeout_ns(uint64_t ns);
  *              single-CTA tiles of width 32 or 64, e.g. skinny M)
  *   tail_split tcm_gemm_ex_ws with a workspace: 1 = never split the last round's
  *              CTA-pair tiles over K; 2 = split them whenever every pair then gets
- *              at most one half (automatic: also only when a tile has at least 64
+ *              at most one part (automatic: also only when a tile has at least 64
  *              K blocks of 128 bytes, i.e. K >= 4096 for 16-bit, K >= 8192 for FP8)
  * Combinations the kernels do not provide fall back to the automatic choice.
  * Results are the same either way, up to the order of the fp32 accumulation.

@@ -203,6 +203,7 @@ struct DensePlan {
     int64_t tiles_m, tiles_n, num_tiles;
     int64_t per_cluster, clusters;
     int split;                  // K parts per tile of the last, partly filled round (1: none)
+    int split_kb;               // split 2: K blocks of the owner part (the helper has the rest)
     int64_t split_begin, units;
     int64_t flag_bytes, ws_bytes; // workspace: counters, then fp32 partial slots
 };
@@ -265,13 +266,17 @@ static DensePlan plan_dense(int64_t M, int64_t N, int64_t K, int kind, int64_t s
     d.per_cluster = static_cast<int64_t>(cfg.cta_group) * cfg.ksplit;
     d.clusters = sms / d.per_cluster;
     // Tail K split (CTA-pair tiles, with a workspace): the R tiles of the last, partly
-    // filled round become 2R half-K units when every pair then gets at most one of them
-    // (2R <= clusters).  Handing the second half's partial sums to the first costs
-    // ~6 us (stage, bulk store, counter, bulk load; measured), so only tiles of at least
-    // SPLIT_MIN_KB K blocks are split (measured at 4096^3: bf16, 64 blocks, 2.6 % faster;
-    // E4M3, 32 blocks, 7.6 % slower).  tail_split 2 in the config override lowers the
-    // limit to 2 blocks, 1 turns the split off.
-    constexpr int64_t SPLIT_MIN_KB = 64;
+    // filled round become 2R part-K units when every pair then gets at most one of them
+    // (2R <= clusters).  Handing the helper part's partial sums to the owner part takes
+    // ~6 us (stage, bulk store, counter; measured), so the owner takes SPLIT_SKEW_KB K
+    // blocks more than half -- ~3 us of MMA at ~0.3-0.4 us per block -- and the helper's
+    // sums are published about when the owner's own MMAs end; the owner then only loads
+    // them (~1 us).  Measured (whole builds timed back to back): 4096^3 bf16/fp16 and
+    // 2048 x 8192 x 4096 3.5 % faster than with equal halves.  Only tiles of at least
+    // SPLIT_MIN_KB K blocks are split: with 32 (E4M3 4096^3) the split, skewed or not,
+    // was 7-10 % slower.  tail_split 2 in the config override lowers the limit to 2
+    // blocks, 1 turns the split off.
+    constexpr int64_t SPLIT_MIN_KB = 64, SPLIT_SKEW_KB = 9;
     d.split = 1;
     const int64_t rem = d.num_tiles % d.clusters;
     const int fs = g_force_split.load();
@@ -280,6 +285,8 @@ static DensePlan plan_dense(int64_t M, int64_t N, int64_t K, int kind, int64_t s
         fs != 1)
         d.split = 2;
     d.split_begin = d.split > 1 ? d.num_tiles - rem : d.num_tiles;
+    // owner: half the K blocks plus the skew, leaving the helper at least one
+    d.split_kb = static_cast<int>(kbs / 2 + std::min<int64_t>(SPLIT_SKEW_KB, std::max<int64_t>(kbs / 2 - 1, 0)));
     d.units = d.split_begin + (d.num_tiles - d.split_begin) * d.split;
     if (d.split > 1) {
         const int64_t nsplit = d.num_tiles - d.split_begin;
@@ -384,6 +391,7 @@ static tcm_status gemm_impl(int64_t M, int64_t N, int64_t K, tcm_dtype a_dtype, 
     p.group_m = g_force_group_m.load() > 0 ? g_force_group_m.load() : (kind == 0 ? 8 : 16);
     p.split = plan.split;
     p.split_begin = static_cast<int>(plan.split_begin);
+    p.split_kb = plan.split_kb;
     if (plan.split > 1) {
         p.ws_flag = static_cast<int *>(ws);
         p.ws_part = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + plan.flag_bytes);

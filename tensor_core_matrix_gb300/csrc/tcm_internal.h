@@ -42,6 +42,7 @@ struct GemmParams {
     int split_begin;          // units below are whole tiles (unit = tile index); from here on each
                               // tile of the last, partly filled round is `split` K parts
     int split;                // K parts per tile of that round (1: none)
+    int split_kb;             // split == 2: K blocks of part 0 (the owner); part 1 has the rest
     float *ws_part;           // split > 1: fp32 partial accumulators of parts 1 .. split-1
     int *ws_flag;             // split > 1: per (tail tile, CTA of the pair): epilogue warps done storing
     void *D;

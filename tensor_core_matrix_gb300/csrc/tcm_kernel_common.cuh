@@ -114,9 +114,11 @@ __device__ __forceinline__ void tile_coords(const GemmParams &p, int t, int &mb,
 // Work unit u of a launch: a whole tile (u < split_begin), or part `part` of the `split`
 // K parts of tile split_begin + j of the last, partly filled round (j = (u - split_begin) /
 // split).  Splitting that round over K lets more CTA pairs share it at full tile width:
-// at 8192^3 with 76 pairs, the 36 leftover 256 x 256 tiles become 72 half-K units, so
-// the launch takes 13.5 tile times instead of 14.  Part 0 owns the tile: it adds the
-// other parts' fp32 partial sums (in part order) before its epilogue.
+// at 8192^3 with 76 pairs, the 36 leftover 256 x 256 tiles become 72 part-K units, so
+// the launch takes ~13.6 tile times instead of 14.  Part 0 owns the tile: it adds the
+// other parts' fp32 partial sums (in part order) before its epilogue.  With two parts the
+// owner takes p.split_kb K blocks, more than half: the helper finishes first and its
+// partial sums are published by the time the owner's own MMAs end.
 struct Unit {
     int mb, nb;   // the tile's row and column block
     int kb0, kb1; // K blocks of this unit
@@ -137,8 +139,13 @@ __device__ __forceinline__ Unit unit_coords(const GemmParams &p, int u)
         r.j = q / p.split;
         r.part = q - r.j * p.split;
         t = p.split_begin + r.j;
-        r.kb0 = static_cast<int>((static_cast<long long>(p.num_kb) * r.part) / p.split);
-        r.kb1 = static_cast<int>((static_cast<long long>(p.num_kb) * (r.part + 1)) / p.split);
+        if (p.split == 2) {
+            r.kb0 = r.part == 0 ? 0 : p.split_kb;
+            r.kb1 = r.part == 0 ? p.split_kb : p.num_kb;
+        } else {
+            r.kb0 = static_cast<int>((static_cast<long long>(p.num_kb) * r.part) / p.split);
+            r.kb1 = static_cast<int>((static_cast<long long>(p.num_kb) * (r.part + 1)) / p.split);
+        }
     }
     tile_coords(p, t, r.mb, r.nb);
     return r;
