@@ -208,6 +208,23 @@ def test_tail_k_split_wait_times_out_and_context_stays_usable(override):
     assert np.array_equal(D.cpu().double().numpy(), ref)
 
 
+def test_4096_cubed_with_workspace_skewed_split_exact():
+    """4096^3 through tcm_gemm_ex_ws as the bench times it: the 28 tiles of the last round split
+    automatically, the owner part 41 of the 64 K blocks and the helper 23 (skewed).  Integer inputs,
+    so every sampled output of every 128 x 128 block must equal the oracle exactly."""
+    import tensor_core_matrix_gb300 as tcm
+    M = N = K = 4096
+    g = si.generator(4096)
+    A = si.integers((M, K), g)
+    B = si.integers((N, K), g)
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        assert tcm.tcm_gemm_workspace_bytes(M, N, K, torch.bfloat16) > 0  # the split is used
+    D = run_gemm_ex(A, B, torch.float32, workspace=True)
+    rows, cols = sample_indices(M, N)
+    ref, _ = oracle_ref(A, B, rows=rows, cols=cols)
+    assert np.array_equal(D.double().numpy()[rows, cols], ref)
+
+
 @pytest.mark.parametrize("in_fmt", ["bf16", "e4m3"])
 def test_8192_cubed_with_workspace_sampled(in_fmt):
     """The bench's two dense GEMMs through tcm_gemm_ex_ws at full size (tail tiles split over K),
