@@ -272,6 +272,9 @@ tcm_status tcm_sp_decompress(int64_t M, int64_t K, tcm_dtype dtype,
  * into the sparse MMA's tensor-memory order itself (the order described below
  * for tcm_sp_meta_pack), so no second metadata buffer is needed; the result is
  * bit-identical to tcm_gemm_sp_tc on the packed copy of the same metadata.
+ * When K % 128 == 0 each stage's words (16 bytes of each row) are staged in
+ * shared memory by TMA together with A and B; otherwise the kernel's metadata
+ * threads load them from global memory.
  */
 tcm_status tcm_gemm_sp(int64_t M, int64_t N, int64_t K, tcm_dtype dtype,
                        const void *A_comp, const uint32_t *meta, const void *B,

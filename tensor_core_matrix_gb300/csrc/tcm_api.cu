@@ -594,9 +594,9 @@ tcm_status tcm_sp_meta_pack(int64_t M, int64_t K, const uint32_t *meta, void *me
 } // extern "C"
 
 // 2:4-sparse GEMM on the block-scaled kernel's sparse formats.  canonical: `meta` is the
-// M x K/32-word layout of tcm_sp_compress, which the kernel's writer warps read and
-// reorder themselves; otherwise it is the hardware-ordered layout of tcm_sp_meta_pack,
-// loaded by TMA.
+// M x K/32-word layout of tcm_sp_compress, which the kernel's writer warps reorder
+// themselves (staged by TMA when K % 128 == 0, else loaded from global memory);
+// otherwise it is the hardware-ordered layout of tcm_sp_meta_pack, loaded by TMA.
 static tcm_status sparse_impl(bool canonical, int64_t M, int64_t N, int64_t K, tcm_dtype dtype, const void *A_comp,
                               const void *meta, const void *B, const void *C, void *D, float alpha, float beta,
                               tcm_dtype out_dtype, tcm_stream_t stream)
@@ -618,7 +618,9 @@ static tcm_status sparse_impl(bool canonical, int64_t M, int64_t N, int64_t K, t
     if (sms <= 0) return TCM_ERR_CUDA;
 
     GemmConfig cfg{};
-    cfg.kind = canonical ? 2 : 5;
+    // canonical metadata: staged by TMA when its rows hold whole 16-byte stages (K % 128 == 0),
+    // else loaded by the writer warps
+    cfg.kind = !canonical ? 5 : K % 128 == 0 ? 2 : 7;
     cfg.ksplit = 1;
     cfg.katoms = 1;
     const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
@@ -646,6 +648,20 @@ static tcm_status sparse_impl(bool canonical, int64_t M, int64_t N, int64_t K, t
             const cuuint32_t box[2] = {128, 16};
             const cuuint32_t estr[2] = {1, 1};
             if (!fn || fn(&maps.sa, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(meta), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                return TCM_ERR_CUDA;
+            maps.sb = maps.sa;
+        } else if (cfg.kind == 2) {
+            // library layout: each stage's four words of the tile's 128 rows (16 bytes per row)
+            // as one box of a 2-D map over the M x K/32 words; rows past M read zero, which the
+            // writer warps replace with the fill pattern
+            EncodeTiledFn fn = encode_fn();
+            const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 32), static_cast<cuuint64_t>(M)};
+            const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 32) * 4u};
+            const cuuint32_t box[2] = {4, 128};
+            const cuuint32_t estr[2] = {1, 1};
+            if (!fn || fn(&maps.sa, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(meta), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
                 return TCM_ERR_CUDA;

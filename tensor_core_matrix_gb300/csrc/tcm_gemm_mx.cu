@@ -68,13 +68,19 @@ constexpr int SF_ATOM = 512;                       // scales of 128 rows x one 1
 // Formats of the kernel: MX (MXFP8), NV (NVFP4), SP (2:4-sparse bf16/fp16 A,
 // metadata in the hardware order -- the "side" data of a stage is then the
 // sparse metadata instead of block scales).
-// SPC: 2:4-sparse A with the canonical metadata of tcm_sp_compress, which the writer
-// warps read from global memory and put into the hardware order themselves.
+// SPC: 2:4-sparse A with the canonical metadata of tcm_sp_compress (K % 128 == 0): TMA
+// stages each stage's words of the tile's rows with its A and B, and the writer warps put
+// them into the hardware order.  SPG: the same for any K % 32 == 0, the writer warps loading
+// the words from global memory themselves (a row pitch that is no multiple of 16 bytes
+// admits no tensor map).  The two are separate instantiations: the global-load writer
+// compiled into the TMA-fed kernel cost it 2 %.
 // MXF4: MXFP4, packed E2M1 with one E8M0 scale per 32 (kind::mxf4nvf4.scale_vec::2X).
-enum SideFmt : int { FMT_MX = 0, FMT_NV = 1, FMT_SP = 2, FMT_SPC = 3, FMT_MXF4 = 4 };
-__host__ __device__ constexpr bool is_sparse(int fmt) { return fmt == FMT_SP || fmt == FMT_SPC; }
+enum SideFmt : int { FMT_MX = 0, FMT_NV = 1, FMT_SP = 2, FMT_SPC = 3, FMT_MXF4 = 4, FMT_SPG = 5 };
+__host__ __device__ constexpr bool is_sparse(int fmt) { return fmt == FMT_SP || fmt == FMT_SPC || fmt == FMT_SPG; }
+// sparse formats whose metadata TMA stages in shared memory
+__host__ __device__ constexpr bool meta_by_tma(int fmt) { return fmt == FMT_SP || fmt == FMT_SPC; }
 // Side-data warps per format.  MX, NV: copy warps (lane 0 of each issues the copies e
-// with e % n == its index).  SP, SPC: one writer warp per TMEM lane quadrant (warp % 4).
+// with e % n == its index).  SP, SPC, SPG: one writer warp per TMEM lane quadrant (warp % 4).
 __host__ __device__ constexpr int mx_copy_warps(int fmt)
 {
     return fmt == FMT_NV ? 3 : is_sparse(fmt) ? 4 : fmt == FMT_MXF4 ? 2 : 1;
@@ -91,8 +97,9 @@ constexpr int SP_META_STAGE = 2048; // 128 lanes x 16 bytes: lane L's words for 
 template <int BN_CTA, int BN, int STAGES, int FMT>
 struct MxSmem {
     static constexpr int B_STAGE = BN_CTA * TILE_K_BYTES * (is_sparse(FMT) ? 2 : 1); // 128 logical K = 2 atoms
-    static constexpr int SF_STAGE = FMT == FMT_SPC ? 0 : FMT == FMT_SP ? SP_META_STAGE
-                                                  : SF_ATOM * mx_atoms_per_tile(FMT) * (1 + BN / 128);
+    static constexpr int SF_STAGE = FMT == FMT_SPG         ? 0
+                                    : meta_by_tma(FMT)       ? SP_META_STAGE
+                                                             : SF_ATOM * mx_atoms_per_tile(FMT) * (1 + BN / 128);
     static constexpr int A_OFF = 0;
     static constexpr int B_OFF = STAGES * A_STAGE_BYTES;
     static constexpr int SF_OFF = B_OFF + STAGES * B_STAGE;
@@ -394,7 +401,7 @@ __global__ void __launch_bounds__(mx_threads(FMT), 1)
     if (warp == 0 && lane == 0 && p.num_kb > 0) { // K == 0: the maps are not encoded
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
-        if (FMT != FMT_SPC) tma_prefetch_desc(&tmSA);
+        if (FMT != FMT_SPG) tma_prefetch_desc(&tmSA);
         if (!is_sparse(FMT)) tma_prefetch_desc(&tmSB);
     }
     if (warp == 1) {
@@ -421,6 +428,9 @@ __global__ void __launch_bounds__(mx_threads(FMT), 1)
             const uint32_t full_cluster0 = CG == 2 ? mapa_shared(smem_u32(full), 0) : 0u;
             const uint32_t sfull_cluster0 = CG == 2 ? mapa_shared(smem_u32(sfull), 0) : 0u;
             const int kt = p.num_kb * APT; // scale atoms per 128-row tile along K
+            // sparse metadata by TMA onto this CTA's own side-data barrier: hardware-ordered
+            // blocks (SP) or canonical rows (SPC)
+            constexpr bool meta_tma = meta_by_tma(FMT);
             int stage = 0;
             uint32_t phase = 0;
             long long issued = 0;
@@ -448,21 +458,24 @@ __global__ void __launch_bounds__(mx_threads(FMT), 1)
                         }
                         continue;
                     }
-                    // SP: each CTA's metadata lands on its own side-data barrier (its writer warps
-                    // wait there); scales: both CTAs' atoms on the even CTA's (its copy threads)
-                    if (FMT == FMT_SP) mbar_arrive_expect_tx(sfull + stage, L::SF_STAGE);
-                    else if (FMT != FMT_SPC && (leader || CG == 1)) mbar_arrive_expect_tx(sfull + stage, SIDE_TX);
+                    // sparse: each CTA's metadata lands on its own side-data barrier (its writer
+                    // warps wait there); scales: both CTAs' atoms on the even CTA's (its copy threads)
+                    if (meta_tma) mbar_arrive_expect_tx(sfull + stage, L::SF_STAGE);
+                    else if (!is_sparse(FMT) && (leader || CG == 1)) mbar_arrive_expect_tx(sfull + stage, SIDE_TX);
                     if (leader || CG == 1) mbar_arrive_expect_tx(full + stage, STAGE_TX);
                     // pair: both CTAs' loads complete on the even CTA's barriers (cluster addresses)
                     const uint32_t fb = CG == 2 ? full_cluster0 + static_cast<uint32_t>(stage) * 8u : 0u;
                     const uint32_t sfb = CG == 2 ? sfull_cluster0 + static_cast<uint32_t>(stage) * 8u : 0u;
                     if constexpr (is_sparse(FMT)) {
-                        // SP metadata: the tile's 2 KB block of this stage (16 rows of 128 bytes), onto
-                        // this CTA's own barrier (SPC: the writer warps read it themselves);
+                        // SP metadata: the tile's 2 KB block of this stage (16 rows of 128 bytes);
+                        // SPC: the stage's four canonical words (16 bytes) of the tile's 128 rows
+                        // (SPG: the writer warps load them themselves);
                         // compressed A: 64 kept values (128 bytes) of the stage's 128 logical K;
                         // B: two 64-value atoms
                         if constexpr (FMT == FMT_SP)
                             tma_load_2d(ss, &tmSA, sfull + stage, 0, (a_tile * p.num_kb + kb) * 16);
+                        else if constexpr (FMT == FMT_SPC)
+                            tma_load_2d(ss, &tmSA, sfull + stage, kb * 4, a_row);
                         tma_ld<CG>(sa, &tmA, full + stage, fb, kb * 64, a_row);
                         tma_ld<CG>(sb, &tmB, full + stage, fb, kb * 128, b_row);
                         tma_ld<CG>(sb + BN_CTA * TILE_K_BYTES, &tmB, full + stage, fb, kb * 128 + 64, b_row);
@@ -489,11 +502,11 @@ __global__ void __launch_bounds__(mx_threads(FMT), 1)
                 if (n == 0) continue;
                 const uint32_t last = static_cast<uint32_t>((n - 1) & 1);
                 if (leader) {
-                    if (FMT != FMT_SPC) wait_bar<CG>(sfull + s, last, w, SITE_DRAIN, false);
+                    if (!is_sparse(FMT) || meta_tma) wait_bar<CG>(sfull + s, last, w, SITE_DRAIN, false);
                     wait_bar<CG>(full + s, last, w, SITE_DRAIN, false);
                 } else {
-                    // SP: this CTA's metadata lands on its own side-data barrier
-                    if (FMT == FMT_SP) wait_bar<CG>(sfull + s, last, w, SITE_DRAIN, false);
+                    // sparse: this CTA's metadata lands on its own side-data barrier
+                    if (meta_tma) wait_bar<CG>(sfull + s, last, w, SITE_DRAIN, false);
                     wait_bar<CG>(empty + s, last, w, SITE_DRAIN, false);
                 }
             }
@@ -559,13 +572,61 @@ __global__ void __launch_bounds__(mx_threads(FMT), 1)
             wait_bar<CG>(drain, 0, w, SITE_DRAIN, false);
         }
     } else if (FMT == FMT_SPC && warp >= MX_COPY_WARP) {
-        // Metadata writer for TMEM lane quadrant q = warp % 4 (in both CTAs of a pair): lane l
-        // reads, SPC_PREFETCH stages ahead, the stage's four canonical words of its tile row
-        // 32q + l from global memory, exchanges half-words with lane l ^ 8 -- the sparse MMA
-        // reads, in TMEM lane 16a + 8s + r, bits 16s .. 16s+15 of the words of rows 16a + r
-        // (low half) and 16a + 8 + r (high half) -- and stores word k at column 4k of the
-        // stage's slot.  A slot is rewritten only after its previous readers (the MMAs of
-        // item - STAGES) completed, which the stage's empty barrier records.
+        // Metadata writer for TMEM lane quadrant q = warp % 4 (in both CTAs of a pair).  The sparse
+        // MMA reads, in TMEM lane 16a + 8s + r, bits 16s .. 16s+15 of the stage's words of tile
+        // rows 16a + r (low half) and 16a + 8 + r (high half); word k goes to column 4k of the
+        // stage's slot.  The stage's four canonical words of the tile's 128 rows landed in shared
+        // memory with its A and B (16 bytes per row, rows past M zero), so lane L = 32q + l takes
+        // rows L & ~8 and L | 8 from there; rows past M become the fill code.  The slot's
+        // previous readers (the MMAs of item - STAGES) completed before the producer could
+        // refill the stage.
+        const int quad = warp & 3;
+        const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+        const uint32_t sfready0 = CG == 2 ? mapa_shared(smem_u32(sfready), 0) : smem_u32(sfready);
+        const int my_tiles = first_tile < p.tile_end ? (p.tile_end - 1 - first_tile) / step + 1 : 0;
+        const long long items = static_cast<long long>(my_tiles) * p.num_kb;
+        const int row_lo = (quad * 32 + lane) & ~8, row_hi = (quad * 32 + lane) | 8;
+        const uint32_t sel = (lane & 8) ? 0x7632u : 0x5410u; // half s of the low row, then of the high row
+        int t = first_tile, kb = 0, rows_left = 0;
+        int stage = 0;
+        uint32_t phase = 0;
+        for (long long item = 0; item < items; ++item) {
+            if (kb == 0) {
+                int mb, nb;
+                tile_coords(p, t, mb, nb);
+                rows_left = p.kM - (mb * CG + static_cast<int>(rank)) * BM;
+            }
+            if (!wait_bar<CG>(sfull + stage, phase, w, SITE_MMA_FULL, true)) break;
+            tc_fence_after();
+            const uint8_t *ss = smem + L::SF_OFF + stage * L::SF_STAGE;
+            uint4 lo = *reinterpret_cast<const uint4 *>(ss + row_lo * 16);
+            uint4 hi = *reinterpret_cast<const uint4 *>(ss + row_hi * 16);
+            if (row_lo >= rows_left) lo = make_uint4(SP_META_FILL, SP_META_FILL, SP_META_FILL, SP_META_FILL);
+            if (row_hi >= rows_left) hi = make_uint4(SP_META_FILL, SP_META_FILL, SP_META_FILL, SP_META_FILL);
+            const uint32_t t0 = tmem_base + lane_base + SF_COL + static_cast<uint32_t>(stage) * SF_STAGE_COLS;
+            tmem_st_32x32b_x1(t0, __byte_perm(lo.x, hi.x, sel));
+            tmem_st_32x32b_x1(t0 + 4u, __byte_perm(lo.y, hi.y, sel));
+            tmem_st_32x32b_x1(t0 + 8u, __byte_perm(lo.z, hi.z, sel));
+            tmem_st_32x32b_x1(t0 + 12u, __byte_perm(lo.w, hi.w, sel));
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (CG == 2) mbar_arrive_cluster(sfready0 + static_cast<uint32_t>(stage) * 8u);
+                else mbar_arrive(sfready + stage);
+            }
+            if (++kb == p.num_kb) kb = 0, t += step;
+            if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    } else if (FMT == FMT_SPG && warp >= MX_COPY_WARP) {
+        // Metadata writer as for SPC, the words from global memory: lane l loads, SPC_PREFETCH
+        // stages ahead, the stage's four canonical words of its own tile row 32q + l and
+        // exchanges half-words with lane l ^ 8 (the same TMEM words as above).  A slot is
+        // rewritten only after its previous readers (the MMAs of item - STAGES) completed,
+        // which the stage's empty barrier records.
         constexpr int SPC_PREFETCH = 4;
         const int quad = warp & 3;
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
@@ -831,13 +892,22 @@ cudaError_t launch_gemm_mx(const GemmConfig &cfg, const MxMaps &maps, const Gemm
         if (cfg.bn == 128) return launch_mx_one<128, 4, 2, 1, FMT_SP>(maps, p, grid, stream);
         return cudaErrorInvalidValue;
     }
-    if (cfg.kind == 2) { // 2:4-sparse A with canonical metadata (read by the writer warps)
+    if (cfg.kind == 2) { // 2:4-sparse A with canonical metadata, K % 128 == 0 (staged by TMA)
         if (cfg.cta_group == 2) {
             if (cfg.bn == 256) return launch_mx_one<256, 4, 1, 2, FMT_SPC>(maps, p, grid, stream);
             if (cfg.bn == 128) return launch_mx_one<128, 5, 2, 2, FMT_SPC>(maps, p, grid, stream);
             return cudaErrorInvalidValue;
         }
         if (cfg.bn == 128) return launch_mx_one<128, 4, 2, 1, FMT_SPC>(maps, p, grid, stream);
+        return cudaErrorInvalidValue;
+    }
+    if (cfg.kind == 7) { // 2:4-sparse A with canonical metadata, any K % 32 == 0 (global loads)
+        if (cfg.cta_group == 2) {
+            if (cfg.bn == 256) return launch_mx_one<256, 4, 1, 2, FMT_SPG>(maps, p, grid, stream);
+            if (cfg.bn == 128) return launch_mx_one<128, 5, 2, 2, FMT_SPG>(maps, p, grid, stream);
+            return cudaErrorInvalidValue;
+        }
+        if (cfg.bn == 128) return launch_mx_one<128, 4, 2, 1, FMT_SPG>(maps, p, grid, stream);
         return cudaErrorInvalidValue;
     }
     if (cfg.kind == 6) { // MXFP4

@@ -164,9 +164,11 @@ def test_meta_pack_bit_exact(tcm, M, K):
     assert np.array_equal(got, oracle.sp_meta_pack(meta.numpy().view(np.uint32), K))
 
 
-def test_sparse_tc_identical_to_canonical_path(tcm):
-    """Same MMAs in the same order: the two metadata paths give bit-identical D."""
-    case = si.sparse_case(1024, 768, 2048, seed=13)
+@pytest.mark.parametrize("M,N,K", [(1024, 768, 2048), (520, 384, 1184)])
+def test_sparse_tc_identical_to_canonical_path(tcm, M, N, K):
+    """Same MMAs in the same order: the two metadata paths give bit-identical D, with the
+    canonical words staged by TMA (K % 128 == 0) and loaded by the writer warps (otherwise)."""
+    case = si.sparse_case(M, N, K, seed=13)
     D1, _, _ = run_sparse(tcm, case["A_logical"], case["B"], torch.float32, tc=False)
     D2, _, _ = run_sparse(tcm, case["A_logical"], case["B"], torch.float32, tc=True)
     assert torch.equal(D1, D2)

@@ -12,7 +12,7 @@ pytestmark = pytest.mark.gpu
 
 # 2: the MMA issuer or a side-data thread waiting for data; 4: the epilogue waiting for the
 # tile; 6: the MMA issuer waiting for the stage's scales or metadata in tensor memory;
-# 7: a metadata writer waiting for a stage's previous MMAs (canonical sparse path)
+# 7: a metadata writer waiting for a stage's previous MMAs (canonical sparse path, K % 128 != 0)
 SITES = (2, 4, 6, 7)
 
 
@@ -93,11 +93,12 @@ def test_sparse_tc_starved_stage(tcm, cg, bn):
     starve_then_recover(tcm, lambda: tcm.tcm_gemm_sp_tc(Ac, meta_tc, B, D), D)
 
 
+@pytest.mark.parametrize("K", [512, 160])  # metadata staged by TMA; loaded by the writer warps
 @pytest.mark.parametrize("cg,bn", [(2, 256), (1, 128)])
-def test_sparse_canonical_starved_stage(tcm, cg, bn):
+def test_sparse_canonical_starved_stage(tcm, cg, bn, K):
     tcm.tcm_set_config_override(cg, bn, 0, 0, 0)
     d = dev()
-    s = si.sparse_case(512, 512, 512, seed=93)
+    s = si.sparse_case(512, 512, K, seed=93)
     Ac, meta = tcm.tcm_sp_compress(s["A_logical"].to(d))
     B = s["B"].to(d)
     D = torch.empty((512, 512), dtype=torch.bfloat16, device=d)
