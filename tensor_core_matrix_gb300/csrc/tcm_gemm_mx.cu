@@ -583,42 +583,44 @@ __global__ void __launch_bounds__(mx_threads(FMT), 1)
         const int quad = warp & 3;
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
         const uint32_t sfready0 = CG == 2 ? mapa_shared(smem_u32(sfready), 0) : smem_u32(sfready);
-        const int my_tiles = first_tile < p.tile_end ? (p.tile_end - 1 - first_tile) / step + 1 : 0;
-        const long long items = static_cast<long long>(my_tiles) * p.num_kb;
         const int row_lo = (quad * 32 + lane) & ~8, row_hi = (quad * 32 + lane) | 8;
         const uint32_t sel = (lane & 8) ? 0x7632u : 0x5410u; // half s of the low row, then of the high row
-        int t = first_tile, kb = 0, rows_left = 0;
         int stage = 0;
         uint32_t phase = 0;
-        for (long long item = 0; item < items; ++item) {
-            if (kb == 0) {
-                int mb, nb;
-                tile_coords(p, t, mb, nb);
-                rows_left = p.kM - (mb * CG + static_cast<int>(rank)) * BM;
-            }
-            if (!wait_bar<CG>(sfull + stage, phase, w, SITE_MMA_FULL, true)) break;
-            tc_fence_after();
-            const uint8_t *ss = smem + L::SF_OFF + stage * L::SF_STAGE;
-            uint4 lo = *reinterpret_cast<const uint4 *>(ss + row_lo * 16);
-            uint4 hi = *reinterpret_cast<const uint4 *>(ss + row_hi * 16);
-            if (row_lo >= rows_left) lo = make_uint4(SP_META_FILL, SP_META_FILL, SP_META_FILL, SP_META_FILL);
-            if (row_hi >= rows_left) hi = make_uint4(SP_META_FILL, SP_META_FILL, SP_META_FILL, SP_META_FILL);
-            const uint32_t t0 = tmem_base + lane_base + SF_COL + static_cast<uint32_t>(stage) * SF_STAGE_COLS;
-            tmem_st_32x32b_x1(t0, __byte_perm(lo.x, hi.x, sel));
-            tmem_st_32x32b_x1(t0 + 4u, __byte_perm(lo.y, hi.y, sel));
-            tmem_st_32x32b_x1(t0 + 8u, __byte_perm(lo.z, hi.z, sel));
-            tmem_st_32x32b_x1(t0 + 12u, __byte_perm(lo.w, hi.w, sel));
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                if (CG == 2) mbar_arrive_cluster(sfready0 + static_cast<uint32_t>(stage) * 8u);
-                else mbar_arrive(sfready + stage);
-            }
-            if (++kb == p.num_kb) kb = 0, t += step;
-            if (++stage == STAGES) {
-                stage = 0;
-                phase ^= 1u;
+        bool ok = true;
+        for (int t = first_tile; ok && t < p.tile_end; t += step) {
+            int mb, nb;
+            tile_coords(p, t, mb, nb);
+            const int rows_left = p.kM - (mb * CG + static_cast<int>(rank)) * BM;
+            for (int kb = 0; kb < p.num_kb; ++kb) {
+                if (!wait_bar<CG>(sfull + stage, phase, w, SITE_MMA_FULL, true)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint8_t *ss = smem + L::SF_OFF + stage * L::SF_STAGE;
+                uint4 lo = *reinterpret_cast<const uint4 *>(ss + row_lo * 16);
+                uint4 hi = *reinterpret_cast<const uint4 *>(ss + row_hi * 16);
+                if (rows_left < BM) { // the last row tile: rows past M take the fill code
+                    if (row_lo >= rows_left) lo = make_uint4(SP_META_FILL, SP_META_FILL, SP_META_FILL, SP_META_FILL);
+                    if (row_hi >= rows_left) hi = make_uint4(SP_META_FILL, SP_META_FILL, SP_META_FILL, SP_META_FILL);
+                }
+                const uint32_t t0 = tmem_base + lane_base + SF_COL + static_cast<uint32_t>(stage) * SF_STAGE_COLS;
+                tmem_st_32x32b_x1(t0, __byte_perm(lo.x, hi.x, sel));
+                tmem_st_32x32b_x1(t0 + 4u, __byte_perm(lo.y, hi.y, sel));
+                tmem_st_32x32b_x1(t0 + 8u, __byte_perm(lo.z, hi.z, sel));
+                tmem_st_32x32b_x1(t0 + 12u, __byte_perm(lo.w, hi.w, sel));
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if (CG == 2) mbar_arrive_cluster(sfready0 + static_cast<uint32_t>(stage) * 8u);
+                    else mbar_arrive(sfready + stage);
+                }
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
             }
         }
     } else if (FMT == FMT_SPG && warp >= MX_COPY_WARP) {
