@@ -292,6 +292,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             red_full_cluster0 = mapa_shared(smem_u32(red_full), 0);
         }
 
+        if (p.prefetch_c && (KS == 1 || krank == 0) && first_tile < p.tile_end) {
+            // one unit per CTA: pull this lane's C row segment into L2 while the MMAs run
+            const Unit u = unit_coords(p, first_tile);
+            const int row = u.mb * (BM * CG) + static_cast<int>(rank) * BM + row_in_tile;
+            const int col0 = u.nb * BN;
+            if (u.part == 0 && row < p.kM && col0 < p.kN) {
+                const int es = p.out_fmt == OUT_F32 ? 4 : (p.out_fmt == OUT_BF16 || p.out_fmt == OUT_F16) ? 2 : 1;
+                const int bytes = min(BN, p.kN - col0) * es;
+                const char *c = static_cast<const char *>(p.C) + (static_cast<long long>(row) * p.ldc + col0) * es;
+                for (int off = 0; off < bytes; off += 128) prefetch_l2(c + off);
+                prefetch_l2(c + bytes - 1);
+            }
+        }
         int local = 0;
         float amax_local = 0.f; // max |y| of this lane's outputs (when p.amax is set)
         for (int t = first_tile; t < p.tile_end; t += num_clusters, ++local) {

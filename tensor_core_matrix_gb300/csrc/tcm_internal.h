@@ -59,6 +59,7 @@ struct GemmParams {
     const float *d_scale;     // FP8 output: dequantisation factor of D (D = y / d_scale); null = 1
     float *amax;              // if set: max |y| over the launch, max-combined as fp32 bits
     int swap_ab;
+    int prefetch_c;           // one round of tiles with C: the epilogue pulls its C rows into L2 first
     uint32_t stage_tx;        // bytes a stage's TMA loads complete (all CTAs of a pair); 0 = from the tile sizes
     unsigned long long *clock_probe; // if set: CTA 0 adds its SM cycles, global-timer ns and 1 to [0..2]
     uint32_t idesc;

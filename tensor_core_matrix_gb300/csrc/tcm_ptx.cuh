@@ -109,6 +109,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
 
 // ------------------------------------------------------------ TMA
 
+// Bring the line holding `addr` into L2 (no register result, no ordering).
+__device__ __forceinline__ void prefetch_l2(const void *addr)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(addr)));
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const void *tmap)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
