@@ -78,8 +78,10 @@ enum FaultBits : int {
 
 // Which kernel variant a launch uses.
 struct GemmConfig {
-    int kind;      // 0 = kind::f16, 1 = kind::f8f6f4, 2 = sparse kind::f16 (canonical metadata),
-                   // 3 = MXFP8, 4 = NVFP4, 5 = sparse kind::f16 (hardware-ordered metadata)
+    int kind;      // 0 = kind::f16, 1 = kind::f8f6f4, 2 = sparse kind::f16 (canonical metadata
+                   // staged by TMA, K % 128 == 0), 3 = MXFP8, 4 = NVFP4, 5 = sparse kind::f16
+                   // (hardware-ordered metadata), 6 = MXFP4, 7 = sparse kind::f16 (canonical
+                   // metadata loaded by the writer warps, any K % 32 == 0)
     int bn;        // N tile (columns of the accumulator)
     int cta_group; // 1 = one CTA per 128-row tile, 2 = CTA pair per 256-row tile
     int stages;    // 0 = the variant's default ring depth
