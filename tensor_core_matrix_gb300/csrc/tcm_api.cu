@@ -263,6 +263,7 @@ static DensePlan plan_dense(int64_t M, int64_t N, int64_t K, int kind, int64_t s
     // two 128-byte K atoms per stage for 32-wide single-CTA tiles (the skinny,
     // HBM-bound shapes): longer contiguous reads of each weight row
     cfg.katoms = (cfg.cta_group == 1 && cfg.bn == 32 && cfg.ksplit <= 2) ? 2 : 1;
+    if (cfg.cta_group == 2) cfg.katoms = 2; // CTA pairs: stages of two K atoms
 
     d.tiles_m = (kM + 128 * cfg.cta_group - 1) / (128 * cfg.cta_group);
     d.tiles_n = (kN + cfg.bn - 1) / cfg.bn;
@@ -273,7 +274,8 @@ static DensePlan plan_dense(int64_t M, int64_t N, int64_t K, int kind, int64_t s
     // filled round become 2R part-K units when every pair then gets at most one of them
     // (2R <= clusters).  Handing the helper part's partial sums to the owner part takes
     // ~6 us (stage, bulk store, counter; measured), so the owner takes SPLIT_SKEW_KB K
-    // blocks more than half -- ~3 us of MMA at ~0.3-0.4 us per block -- and the helper's
+    // blocks more than half (rounded to whole stages of cfg.katoms blocks) -- ~3 us of MMA
+    // at ~0.3-0.4 us per block -- and the helper's
     // sums are published about when the owner's own MMAs end; the owner then only loads
     // them (~1 us).  Measured (whole builds timed back to back): 4096^3 bf16/fp16 and
     // 2048 x 8192 x 4096 3.5 % faster than with equal halves.  Only tiles of at least
@@ -285,12 +287,15 @@ static DensePlan plan_dense(int64_t M, int64_t N, int64_t K, int kind, int64_t s
     const int64_t rem = d.num_tiles % d.clusters;
     const int fs = g_force_split.load();
     const int64_t min_kb = fs == 2 ? 2 : SPLIT_MIN_KB;
+    // the parts are whole stages (cfg.katoms K blocks each)
+    const int64_t stages = (kbs + cfg.katoms - 1) / cfg.katoms;
     if (allow_split && cfg.cta_group == 2 && cfg.ksplit == 1 && rem > 0 && 2 * rem <= d.clusters && kbs >= min_kb &&
-        fs != 1)
+        stages >= 2 && fs != 1)
         d.split = 2;
     d.split_begin = d.split > 1 ? d.num_tiles - rem : d.num_tiles;
-    // owner: half the K blocks plus the skew, leaving the helper at least one
-    d.split_kb = static_cast<int>(kbs / 2 + std::min<int64_t>(SPLIT_SKEW_KB, std::max<int64_t>(kbs / 2 - 1, 0)));
+    // owner: half the stages plus the skew (rounded to stages), leaving the helper at least one
+    const int64_t skew = (SPLIT_SKEW_KB + cfg.katoms / 2) / cfg.katoms;
+    d.split_kb = static_cast<int>(stages / 2 + std::min<int64_t>(skew, std::max<int64_t>(stages / 2 - 1, 0)));
     d.units = d.split_begin + (d.num_tiles - d.split_begin) * d.split;
     if (d.split > 1) {
         const int64_t nsplit = d.num_tiles - d.split_begin;

@@ -65,8 +65,9 @@ __device__ __forceinline__ float *part_slot(const GemmParams &p, int j, uint32_t
 // and CTA 0 adds them in rank order (a fixed order, so results do not depend
 // on timing) before the epilogue.  This keeps every SM streaming when a
 // problem has fewer tiles than the GPU has SMs (skinny M after the swap).
-// KATOMS: 128-byte K atoms per stage; more than one gives each weight row
-// a longer contiguous run per stage (skinny, HBM-bound shapes).
+// KATOMS: 128-byte K atoms per stage.  Single-CTA tiles of width 32 use two (each weight
+// row a longer contiguous run per stage: skinny, HBM-bound shapes); CTA pairs use two (eight
+// MMAs per barrier wait and commit: 0.5-2 % faster than one atom per stage, same ring bytes).
 // Work units (unit_coords): whole tiles, and -- when p.split == 2 -- the two K halves
 // of each tile of the last, partly filled round (CTA pairs only).  That round is each
 // CTA's last unit, so its shared-memory ring is idle by then: the helper half stages its
@@ -86,7 +87,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     using L = Smem<BN / CG, STAGES, (KS - 1) * RED_SLOT, KATOMS>;
     static_assert(CG == 1 || CG == 2, "CTA group of 1 or 2");
     static_assert(KS == 1 || (CG == 1 && (KS == 2 || KS == 4)), "K split of 2 or 4 CTAs, single-CTA tiles only");
-    static_assert(KATOMS == 1 || CG == 1, "multi-atom stages for single-CTA tiles only");
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN must be a multiple of 32 in [32, 256]");
     static_assert(L::ALLOC <= 227 * 1024, "shared memory ring too large");
     constexpr uint32_t TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
@@ -190,8 +190,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         if (CG == 2) {
                             if (leader) mbar_arrive_expect_tx(full + stage, stage_tx);
                             const uint32_t fb = full_cluster0 + static_cast<uint32_t>(stage) * 8u;
-                            tma_load_2d_pair(sa, &tmA, fb, kb * KB_ELEMS, a_row);
-                            tma_load_2d_pair(sb, &tmB, fb, kb * KB_ELEMS, b_row);
+#pragma unroll
+                            for (int a = 0; a < KATOMS; ++a) {
+                                tma_load_2d_pair(sa + a * A_STAGE_BYTES, &tmA, fb, (kb * KATOMS + a) * KB_ELEMS, a_row);
+                                tma_load_2d_pair(sb + a * BN_CTA * TILE_K_BYTES, &tmB, fb, (kb * KATOMS + a) * KB_ELEMS,
+                                                 b_row);
+                            }
                         } else {
                             mbar_arrive_expect_tx(full + stage, stage_tx);
 #pragma unroll

@@ -35,14 +35,14 @@ enum WaitSite : int {
 // operand; with swap_ab the kernel computes D^T (kernel row = D column).
 struct GemmParams {
     int kM, kN, K;            // kernel-space problem (K = logical K)
-    int num_kb;               // number of K blocks of the tile loop
+    int num_kb;               // stages of the tile loop (K blocks of 128 bytes x katoms)
     int tiles_m, tiles_n, num_tiles;
     int group_m;              // rasterisation: tiles of this many row blocks share B in L2
     int tile_begin, tile_end; // the range of work units this launch covers (see split_begin)
     int split_begin;          // units below are whole tiles (unit = tile index); from here on each
                               // tile of the last, partly filled round is `split` K parts
     int split;                // K parts per tile of that round (1: none)
-    int split_kb;             // split == 2: K blocks of part 0 (the owner); part 1 has the rest
+    int split_kb;             // split == 2: stages of part 0 (the owner); part 1 has the rest
     float *ws_part;           // split > 1: fp32 partial accumulators of parts 1 .. split-1
     int *ws_flag;             // split > 1: per (tail tile, CTA of the pair): epilogue warps done storing
     void *D;

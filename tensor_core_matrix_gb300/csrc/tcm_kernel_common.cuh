@@ -117,11 +117,11 @@ __device__ __forceinline__ void tile_coords(const GemmParams &p, int t, int &mb,
 // at 8192^3 with 76 pairs, the 36 leftover 256 x 256 tiles become 72 part-K units, so
 // the launch takes ~13.6 tile times instead of 14.  Part 0 owns the tile: it adds the
 // other parts' fp32 partial sums (in part order) before its epilogue.  With two parts the
-// owner takes p.split_kb K blocks, more than half: the helper finishes first and its
+// owner takes p.split_kb stages, more than half: the helper finishes first and its
 // partial sums are published by the time the owner's own MMAs end.
 struct Unit {
     int mb, nb;   // the tile's row and column block
-    int kb0, kb1; // K blocks of this unit
+    int kb0, kb1; // stages (K blocks x katoms) of this unit
     int part;     // 0: whole tile or owner of a split tile; 1 .. split-1: helper
     int j;        // index of a split tile among the split ones; -1 for a whole tile
 };
