@@ -937,7 +937,7 @@ def main():
             },
             "roofline": {"bound": "tensor", "achieved": ach_bf16, "peak": bf16_peak, "unit": "TFLOP/s",
                          "frac": ach_bf16 / bf16_peak, "traffic": recorded_traffic(),
-                         "kernel": "gemm_kernel<kind::f16, 256x256 CTA-pair tile, 3 stages of 2 K atoms> bf16 8192^3",
+                         "kernel": "gemm_kernel<kind::f16, 256x256 CTA-pair tile, 6 stages> bf16 8192^3",
                          "peak_source": peak_label, "timed_region_s": region_s,
                          "algorithmic_flop_per_launch": FLOP_PER_GEMM},
             "gpu_launches": KERNELS_PER_STEP * args.steps,

@@ -134,8 +134,8 @@ tcm_status tcm_gemm_ex(int64_t M, int64_t N, int64_t K,
  * each of its tiles is split into two parts along K, computed by two pairs
  * at once: the second part stores its fp32 partial sums in the workspace and the
  * first adds them before the epilogue.  The first part takes a few K blocks more
- * than half (10 when K allows: 5 stages of two 128-byte blocks), so that the
- * second part's sums are published by the
+ * than half (9 when K allows; 10 for 8-bit operands, whose stages hold two
+ * 128-byte blocks), so that the second part's sums are published by the
  * time the first part's own products are done.  Same results as tcm_gemm_ex up to the
  * order of the fp32 accumulation (integer-valued sums stay exact).
  *  workspace        DEVICE memory, 16-byte aligned, caller-owned, at least

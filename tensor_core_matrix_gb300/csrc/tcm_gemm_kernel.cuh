@@ -66,8 +66,8 @@ __device__ __forceinline__ float *part_slot(const GemmParams &p, int j, uint32_t
 // on timing) before the epilogue.  This keeps every SM streaming when a
 // problem has fewer tiles than the GPU has SMs (skinny M after the swap).
 // KATOMS: 128-byte K atoms per stage.  Single-CTA tiles of width 32 use two (each weight
-// row a longer contiguous run per stage: skinny, HBM-bound shapes); CTA pairs use two (eight
-// MMAs per barrier wait and commit: 0.5-2 % faster than one atom per stage, same ring bytes).
+// row a longer contiguous run per stage: skinny, HBM-bound shapes); CTA pairs with 8-bit
+// operands use two (eight MMAs per barrier wait and commit, same ring bytes).
 // Work units (unit_coords): whole tiles, and -- when p.split == 2 -- the two K halves
 // of each tile of the last, partly filled round (CTA pairs only).  That round is each
 // CTA's last unit, so its shared-memory ring is idle by then: the helper half stages its

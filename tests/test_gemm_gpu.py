@@ -210,7 +210,7 @@ def test_tail_k_split_wait_times_out_and_context_stays_usable(override):
 
 def test_4096_cubed_with_workspace_skewed_split_exact():
     """4096^3 through tcm_gemm_ex_ws as the bench times it: the 28 tiles of the last round split
-    automatically, the owner part 21 of the 32 stages (of two K blocks) and the helper 11 (skewed).  Integer inputs,
+    automatically, the owner part 41 of the 64 K blocks and the helper 23 (skewed).  Integer inputs,
     so every sampled output of every 128 x 128 block must equal the oracle exactly."""
     import tensor_core_matrix_gb300 as tcm
     M = N = K = 4096
