@@ -85,6 +85,21 @@ def test_fp4_each_variant_exact(tcm, cg, bn, ks, order):
     assert np.array_equal(D.double().numpy(), ref)
 
 
+@pytest.mark.parametrize("K", [128, 384, 640])
+@pytest.mark.parametrize("order", [("e4m3", "e2m1"), ("e2m1", "e2m1")])
+def test_fp4_pair_tiles_with_a_half_filled_last_stage(tcm, order, K):
+    """CTA-pair tiles of 8-bit kinds take two 128-value K atoms per stage: with K an odd number
+    of atoms the last stage's second atom lies past K (zero-filled by TMA, still counted on
+    the stage's barrier)."""
+    tcm.tcm_set_config_override(2, 256, 0, 0, 0)
+    g = si.generator(K + 7)
+    A, B = operands(order, 512, 768, K, g)
+    fa, fb = order
+    D = run(tcm, A, B, a_fmt="e2m1" if fa == "e2m1" else None, b_fmt="e2m1" if fb == "e2m1" else None)
+    ref, _ = ref_of(A, B, fa, fb)
+    assert np.array_equal(D.double().numpy(), ref)
+
+
 @pytest.mark.parametrize("ks", [0, 2, 4])
 @pytest.mark.parametrize("M", [1, 16, 48])
 def test_fp4_skinny_swapped_and_k_split_exact(tcm, ks, M):

@@ -116,6 +116,19 @@ def test_each_variant_fp8_bound(override, cg, bn, stages, fb):
     assert ratio(D, ref, S, scale=case["sa"] * case["sb"]) <= 1.0
 
 
+@pytest.mark.parametrize("K", [128, 384, 1152])
+def test_fp8_pair_tiles_with_a_half_filled_last_stage(override, K):
+    """E4M3 CTA-pair tiles take two 128-value K atoms per stage: with K an odd number of atoms
+    the last stage's second atom lies past K (zero-filled by TMA, counted on the barrier)."""
+    override.tcm_set_config_override(2, 256, 0, 0, 0)
+    g = si.generator(K + 3)
+    A = si.integers((512, K), g, -8, 8, dtype="e4m3")
+    B = si.integers((768, K), g, -8, 8, dtype="e4m3")
+    D = run_gemm_ex(A, B, torch.float32)
+    ref, _ = oracle_ref(A, B)
+    assert np.array_equal(D.double().numpy(), ref)
+
+
 @pytest.mark.parametrize("split", [1, 2])
 @pytest.mark.parametrize("M,N,K", [(512, 768, 320), (300, 520, 136), (4096, 2560, 256), (4000, 2600, 200),
                                    (1024, 1024, 1000)])
